@@ -1,0 +1,31 @@
+"""Plain, slow fp64 CPU oracle for linear-logprob scoring and the three-way compare.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product path (the CUDA library and its Python binding) never imports, links or
+executes anything here, and this package imports nothing from the product.
+
+It shares no code with the CUDA path: the only common dependency is the seeded
+input generator ``synth`` (data only, none of the method's arithmetic).
+
+Modules
+-------
+``oracle.logprob``  the plain definition  logprob = log_softmax(z / tau)[x]
+                    with z = bf16(RMSNorm(h)) . W^T, plus lse and top-1.
+``oracle.compare``  per-sequence A/B/C mismatch statistics, k3, TIS weights,
+                    and the single-pair ``compare`` summary.
+
+Every function cites the page passage it follows.  Pins that tie this oracle to
+something other than itself live in ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_mutations.py``.  Parity status: every function is pinned
+(see those tests); none is "parity unpinned".
+"""
+from .logprob import (  # noqa: F401
+    widen_bf16, round_to_bf16, rmsnorm, logits, lse_stats, oracle_logprob,
+    oracle_log_softmax_rows,
+)
+from .compare import (  # noqa: F401
+    OracleError, FLAG_EMPTY, FLAG_BAD_MASK, FLAG_NONFINITE, FLAG_BAD_OFFSETS,
+    FLAG_K3_OVERFLOW, PAIRS, oracle_compare, oracle_compare_lenient, compare_summary,
+    compare_bitwise,
+)

@@ -1,0 +1,571 @@
+"""Pins that tie the fp64 oracle to something other than itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees with a
+value the pages print, a closed form, an invariant, a library routine the
+oracle does not call, or a brute-force evaluation.  ``test_oracle_pins.py``
+runs them against the oracle as it stands; ``test_oracle_mutations.py`` plants
+plausible mistakes in the oracle and checks that some pin catches each one.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# bf16 helpers built independently of the oracle (for constructing inputs)
+
+def _all_finite_bf16():
+    """Every finite bf16 value as (sorted fp64 values, their uint16 patterns)."""
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):
+        vals = (pats.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ok = np.isfinite(vals)
+    pats, vals = pats[ok], vals[ok]
+    # keep one zero (+0) so the table is strictly increasing
+    keep = ~((vals == 0) & (pats != 0))
+    pats, vals = pats[keep], vals[keep]
+    order = np.argsort(vals, kind="stable")
+    return vals[order], pats[order]
+
+
+_BF16_TABLE = None
+
+
+def brute_nearest_bf16(x: np.ndarray) -> np.ndarray:
+    """Nearest finite bf16 by exhaustive table search; exact ties go to the even pattern."""
+    global _BF16_TABLE
+    if _BF16_TABLE is None:
+        _BF16_TABLE = _all_finite_bf16()
+    vals, pats = _BF16_TABLE
+    x = np.asarray(x, dtype=np.float64)
+    hi = np.clip(np.searchsorted(vals, x, side="left"), 1, vals.size - 1)
+    lo = hi - 1
+    dlo = np.abs(x - vals[lo])
+    dhi = np.abs(vals[hi] - x)
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (pats[hi] % 2 == 0))
+    return np.where(pick_hi, vals[hi], vals[lo])
+
+
+def trunc_bf16_bits(x: float) -> int:
+    """bf16 pattern of x truncated toward zero (via float32)."""
+    return int(np.float32(x).view(np.uint32) >> np.uint32(16))
+
+
+def bits_value(b: int) -> float:
+    return float(np.uint32(b << 16).view(np.float32))
+
+
+def exact_logit_head(z_rows, n_limbs: int = 7):
+    """A d=8 head whose logits equal the given fp64 targets to ~1e-16.
+
+    hidden = 1 everywhere and eps = 0 give rstd = 1, so y = gamma exactly with
+    gamma_i = 2^(-8 i).  Each W row holds the target split into truncated bf16
+    limbs: z_v = sum_i W_vi 2^(-8 i).  Returns (hidden_bits [1,8], gamma_bits,
+    W_bits [V,8], exact z as Fractions).
+    """
+    z_rows = [float(v) for v in z_rows]
+    V = len(z_rows)
+    d = 8
+    gamma_bits = np.array([trunc_bf16_bits(2.0 ** (-8 * i)) for i in range(d)], dtype=np.uint16)
+    W = np.zeros((V, d), dtype=np.uint16)
+    z_exact = []
+    for v, target in enumerate(z_rows):
+        r = Fraction(target)
+        tot = Fraction(0)
+        for i in range(n_limbs):
+            scaled = r * (2 ** (8 * i))
+            b = trunc_bf16_bits(float(scaled))
+            W[v, i] = b
+            limb = Fraction(bits_value(b)) / (2 ** (8 * i))
+            tot += limb
+            r -= limb
+        z_exact.append(tot)
+    hidden = np.full((1, d), trunc_bf16_bits(1.0), dtype=np.uint16)
+    return hidden, gamma_bits, W, z_exact
+
+
+def _score(z_targets, x, tau):
+    h, g, W, zx = exact_logit_head(z_targets)
+    out = oracle.oracle_logprob(h, g, W, np.array([x], dtype=np.int32), tau, 0.0)
+    return out, zx
+
+
+# ---------------------------------------------------------------------------
+# logprob pins
+
+def pin_widen():
+    v = oracle.widen_bf16(np.array([0x3F80, 0xC000, 0x7F80, 0x0001, 0x8000], dtype=np.uint16))
+    assert v[0] == 1.0 and v[1] == -2.0 and v[2] == np.inf
+    assert v[3] == 2.0 ** -133 and v[4] == 0.0 and math.copysign(1, v[4]) < 0
+
+
+def pin_round_to_bf16_brute():
+    g = np.random.default_rng(123)
+    x = np.concatenate([
+        g.standard_normal(20000) * 3.0,
+        g.standard_normal(2000) * 1e-38,           # bf16 subnormal range
+        np.ldexp(g.random(2000) + 0.5, g.integers(-120, 120, 2000)),
+    ])
+    vals, _ = _all_finite_bf16()
+    mid = (vals[1000:30000:7] + vals[1001:30001:7]) / 2.0   # exact midpoints -> ties
+    x = np.concatenate([x, mid, -mid])
+    got = oracle.round_to_bf16(x)
+    want = brute_nearest_bf16(x)
+    assert np.array_equal(got, want), "round_to_bf16 disagrees with exhaustive nearest-even search"
+
+
+def pin_v8_uniform():
+    """All logits equal: logprob = -ln 8 for every token, top-1 = 0 (lowest id on ties)."""
+    for x in (0, 3, 7):
+        out, _ = _score([0.0] * 8, x, 1.0)
+        assert abs(out["logprob"][0] - (-math.log(8))) < 1e-15
+        assert abs(out["logprob"][0] - (-2.0794415416798357)) < 1e-15
+        assert out["top1"][0] == 0
+
+
+def pin_v8_page_probabilities():
+    """p = 0.10 vs 0.12 for the scored token (Debugging page, What a Logprob Difference Means)."""
+    gd = golden("logprob_difference_example.json")
+    p1 = [0.10, 0.30, 0.20, 0.10, 0.10, 0.10, 0.05, 0.05]
+    p2 = [0.12, 0.28, 0.20, 0.10, 0.10, 0.10, 0.05, 0.05]
+    o1, _ = _score([math.log(p) for p in p1], 0, 1.0)
+    o2, _ = _score([math.log(p) for p in p2], 0, 1.0)
+    l1, l2 = o1["logprob"][0], o2["logprob"][0]
+    assert abs(l1 - math.log(0.10)) < 1e-12 and abs(l2 - math.log(0.12)) < 1e-12
+    assert round(l1, 4) == gd["logprob_rollout"] and round(l2, 4) == gd["logprob_train"]
+    assert round(l2 - l1, 4) == gd["train_minus_rollout"]
+    assert abs((l2 - l1) - 0.1823215568) < 1e-9
+    assert round(math.exp(l2 - l1), 2) == gd["ratio"]
+    assert o1["top1"][0] == 1 and o2["top1"][0] == 1
+    assert abs(o1["gap"][0] - (math.log(0.30) - math.log(0.20))) < 1e-12
+
+
+def pin_v8_temperature():
+    """tau = 0.5 on z = 0..7: log_softmax(z/tau), not log_softmax(z)/tau (Debugging page,
+    'How this differs from a real temperature mismatch')."""
+    tau = 0.5
+    lse_scaled = math.log((math.exp(16) - 1) / (math.exp(2) - 1))      # ln sum_k e^{2k}
+    lse_raw = math.log((math.exp(8) - 1) / (math.exp(1) - 1))          # ln sum_k e^{k}
+    for x in (0, 5, 7):
+        out, _ = _score([float(k) for k in range(8)], x, tau)
+        want = 2 * x - lse_scaled
+        wrong = (x - lse_raw) / tau
+        assert abs(out["logprob"][0] - want) < 1e-12
+        assert abs(out["lse"][0] - lse_scaled) < 1e-12
+        assert abs(want - wrong) > 0.05
+        assert out["top1"][0] == 7
+
+
+def pin_large_logits():
+    """Logits near 800 must not overflow the normaliser (max shift)."""
+    z = [800.0 - k for k in range(8)]
+    out, _ = _score(z, 2, 1.0)
+    want = -2.0 - math.log(sum(math.exp(-k) for k in range(8)))
+    assert math.isfinite(out["logprob"][0]) and abs(out["logprob"][0] - want) < 1e-12
+    assert abs(out["lse"][0] - (800.0 + math.log(sum(math.exp(-k) for k in range(8))))) < 1e-11
+
+
+def pin_rmsnorm_closed_form():
+    """Constant rows: y = bf16(c / sqrt(c^2 + eps) * gamma); scale invariance at eps = 0."""
+    for c, eps in ((2.0, 0.25), (0.5, 1e-6), (3.0, 1.0)):
+        h = np.full((1, 16), c)
+        gam = np.ones(16)
+        y = oracle.rmsnorm(h, gam, eps)
+        want = brute_nearest_bf16(np.array([c / math.sqrt(c * c + eps)]))[0]
+        assert np.all(y == want), (c, eps, y[0, 0], want)
+    g = np.random.default_rng(5)
+    hb = synth.f32_to_bf16_bits(g.standard_normal((4, 64)).astype(np.float32))
+    h = oracle.widen_bf16(hb)
+    gam = oracle.widen_bf16(synth.f32_to_bf16_bits((1 + 0.2 * g.standard_normal(64)).astype(np.float32)))
+    assert np.array_equal(oracle.rmsnorm(h, gam, 0.0), oracle.rmsnorm(4.0 * h, gam, 0.0))
+
+
+def pin_rmsnorm_library():
+    """fp64 torch rms_norm (not used by the oracle) then nearest-even bf16 matches."""
+    import torch
+    b = synth.make_custom(T=16, d=256, V=64, eps=1e-5, tag="rmslib")
+    h = oracle.widen_bf16(b.hidden_gen)
+    gam = oracle.widen_bf16(b.head.gamma)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(h), (h.shape[1],), torch.from_numpy(gam),
+                                       eps=b.eps).numpy()
+    want = brute_nearest_bf16(ref)
+    got = oracle.rmsnorm(h, gam, b.eps)
+    diff = got != want
+    # fp64 rounding order may move a value across a bf16 rounding midpoint only if it sits
+    # within ~1e-15 relative of it: allow at most a handful of such elements, each 1 bf16 step.
+    assert diff.sum() <= 2
+    if diff.any():
+        assert np.all(np.abs(got[diff] - want[diff]) <= np.abs(want[diff]) * 2.0 ** -7)
+
+
+def pin_library_log_softmax():
+    """At tau = 1 torch.log_softmax + gather (the trainer extraction of the Debugging page's
+    trainer_scores) reproduces the oracle's lse / logprob / argmax on the same logits;
+    at tau != 1 torch.logsumexp(z / tau) does."""
+    import torch
+    b = synth.make_custom(T=24, d=128, V=333, tag="lsm")
+    y = oracle.rmsnorm(oracle.widen_bf16(b.hidden_gen), oracle.widen_bf16(b.head.gamma), b.eps)
+    z = oracle.logits(y, b.head.W)
+    for tau in (1.0, 0.7):
+        out = oracle.oracle_logprob(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, tau, b.eps)
+        zt = torch.from_numpy(z)
+        ls = torch.log_softmax(zt / tau, dim=-1)
+        lp = ls.gather(1, torch.from_numpy(b.token_ids.astype(np.int64))[:, None])[:, 0].numpy()
+        assert np.max(np.abs(lp - out["logprob"])) < 1e-12
+        lse = torch.logsumexp(zt / tau, dim=-1).numpy()
+        assert np.max(np.abs(lse - out["lse"])) < 1e-12
+        assert np.array_equal(torch.argmax(zt, dim=-1).numpy(), out["top1"])
+
+
+def pin_sum_exp_one():
+    """exp(log_softmax) sums to 1 within 1e-12 on full rows."""
+    b = synth.make_tiny()
+    for tau in (1.0, 0.7):
+        rows = oracle.oracle_log_softmax_rows(b.hidden_gen, b.head.gamma, b.head.W, tau, b.eps)
+        for r in rows:
+            assert abs(math.fsum(np.exp(r)) - 1.0) < 1e-12
+
+
+def pin_invariants():
+    """logprob <= 0, lse >= max s, the top-1 token has the highest logprob, gap >= 0."""
+    b = synth.make_tiny()
+    tau = 0.7
+    out = oracle.oracle_logprob(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, tau, b.eps)
+    rows = oracle.oracle_log_softmax_rows(b.hidden_gen, b.head.gamma, b.head.W, tau, b.eps)
+    assert np.all(out["logprob"] <= 0)
+    assert np.all(out["lse"] >= out["zmax"] / tau)
+    assert np.array_equal(np.argmax(rows, axis=1), out["top1"])
+    assert np.all(out["gap"] >= 0)
+    assert np.allclose(rows[np.arange(b.T), b.token_ids], out["logprob"], atol=1e-12, rtol=0)
+
+
+def _mp_nearest_bf16(x_mp):
+    import mpmath
+    return brute_nearest_bf16(np.array([float(x_mp)]))[0] if abs(float(x_mp)) > 0 else 0.0
+
+
+def pin_brute_force_mpmath():
+    """Small rows evaluated end to end at 50 digits (mpmath), including the bf16 rounding of y
+    by exhaustive search; the oracle must agree to 1e-12."""
+    import mpmath
+    mpmath.mp.dps = 50
+    b = synth.make_custom(T=3, d=16, V=40, temperature=0.7, eps=1e-6, tag="mp")
+    out = oracle.oracle_logprob(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 0.7, 1e-6)
+    hb = oracle.widen_bf16(b.hidden_gen)  # exact widening (pinned by pin_widen)
+    gb = oracle.widen_bf16(b.head.gamma)
+    Wb = oracle.widen_bf16(b.head.W)
+    for t in range(b.T):
+        h = [mpmath.mpf(float(v)) for v in hb[t]]
+        ms = mpmath.fsum(v * v for v in h) / len(h)
+        rstd = 1 / mpmath.sqrt(ms + mpmath.mpf(1e-6))
+        y = []
+        for i, v in enumerate(h):
+            pre = v * rstd * mpmath.mpf(float(gb[i]))
+            # exact nearest bf16 of the 50-digit value: fp64 conversion first is safe unless
+            # the value lies within 1e-16 relative of a bf16 midpoint (not the case here)
+            y.append(mpmath.mpf(_mp_nearest_bf16(pre)))
+        z = [mpmath.fsum(y[i] * mpmath.mpf(float(Wb[v, i])) for i in range(len(y))) for v in range(b.V)]
+        s = [zz / mpmath.mpf(0.7) for zz in z]
+        lse = mpmath.log(mpmath.fsum(mpmath.exp(v) for v in s))
+        x = int(b.token_ids[t])
+        lp = s[x] - lse
+        assert abs(float(lp) - out["logprob"][t]) < 1e-12
+        assert abs(float(lse) - out["lse"][t]) < 1e-12
+        zf = [float(v) for v in z]
+        assert out["top1"][t] == int(np.argmax(zf))
+
+
+def pin_bad_token():
+    b = synth.make_custom(T=4, d=64, V=50, tag="badtok")
+    ids = b.token_ids.copy()
+    ids[1] = 50
+    ids[2] = -1
+    out = oracle.oracle_logprob(b.hidden_gen, b.head.gamma, b.head.W, ids, 1.0, b.eps)
+    assert np.isnan(out["logprob"][1]) and np.isnan(out["logprob"][2])
+    assert np.all(np.isfinite(out["lse"])) and np.isfinite(out["logprob"][0])
+    assert list(out["bad_token"]) == [False, True, True, False]
+
+
+# ---------------------------------------------------------------------------
+# compare pins
+
+def _one_seq(A, B, C, mask=None, cap=2.0):
+    A = np.asarray(A, dtype=np.float32)
+    n = A.shape[0]
+    mask = np.ones(n, dtype=np.uint8) if mask is None else np.asarray(mask, dtype=np.uint8)
+    st, w = oracle.oracle_compare(A, np.asarray(B, np.float32), np.asarray(C, np.float32),
+                                  np.array([0, n], dtype=np.int64), mask, cap)
+    return st[0], w
+
+
+def pin_recorded_token_summary():
+    """The Case 1 outlier token: compare() summaries reproduce the printed differences."""
+    gd = golden("recorded_token_case1.json")
+    s = gd["scores"]
+    for label, want in gd["signed_differences_6dp"].items():
+        l, r = label.split("-")
+        res = oracle.compare_summary([s[l]], [s[r]], [1])
+        assert res["count"] == 1
+        assert round(res["signed_mean"], 6) == want, (label, res["signed_mean"], want)
+        assert round(res["mae"], 6) == abs(want)
+        assert res["maximum"] == res["p95"] == res["p99"] == res["mae"]
+
+
+def pin_recorded_token_bitwise():
+    """B0, B1, C0, C1 are float32 values: B1 and C0 differ by one float32 step (about
+    1.19e-7 nat), C0 and C1 are bitwise equal."""
+    gd = golden("recorded_token_case1.json")
+    s = {k: np.float32(v) for k, v in gd["scores"].items() if k != "A"}
+    for k, v in gd["scores"].items():
+        if k != "A":
+            assert float(s[k]) == v, "page value is not a float32"
+    st, _ = _one_seq([s["B0"]], [s["B1"]], [s["C0"]])
+    # pairs: (A,B)=(B0,B1), (B,C)=(B1,C0), (A,C)=(B0,C0)
+    assert st["pair"][0]["mismatch_count"] == 1 and st["pair"][0]["first_div"] == 0
+    assert st["pair"][1]["max_abs_diff"] == 2.0 ** -23
+    assert abs(st["pair"][1]["max_abs_diff"] - gd["B1_minus_C0_about"]) < 0.01e-7
+    assert round(st["pair"][0]["signed_mean"], 6) == gd["signed_differences_6dp"]["B0-B1"]
+    st2, _ = _one_seq([s["C0"]], [s["C1"]], [s["C1"]])
+    assert st2["pair"][0]["mismatch_count"] == 0 and st2["pair"][0]["max_abs_diff"] == 0.0
+
+
+def pin_case3_outlier():
+    gd = golden("case3_stale_outlier.json")
+    s = gd["scores"]
+    st, _ = _one_seq([s["A"]], [s["B0"]], [s["C0"]])
+    assert st["pair"][0]["mismatch_count"] == 0 and st["pair"][0]["max_abs_diff"] == 0.0
+    assert abs(st["pair"][1]["max_abs_diff"] - gd["differences_9dp"]["B0-C0"]) < 5e-10
+    assert abs(st["pair"][1]["signed_mean"] - gd["differences_9dp"]["B0-C0"]) < 5e-10
+    assert st["pair"][1]["first_div"] == 0 and st["pair"][1]["longest_run"] == 1
+
+
+def pin_fig1_split():
+    """Eq. (1) with the Figure 1 numbers: C - A = (C - B) + (B - A); w = 1.05, r = 1.20."""
+    gd = golden("fig1_ratio_split.json")
+    A = np.float32(math.log(gd["q_v"]))
+    B = np.float32(math.log(gd["p_v"]))
+    C = np.float32(math.log(gd["p_k"]))
+    st, _ = _one_seq([A], [B], [C], cap=2.0)
+    tol = 4e-7   # float32 rounding of the three inputs
+    assert abs(st["mean_log_ratio"] - gd["log_pk_over_qv"]) < tol
+    assert round(math.log(gd["p_k"] / gd["q_v"]), 10) == gd["log_pk_over_qv"]
+    assert abs(st["mean_weight_move"] - math.log(gd["r"])) < tol
+    assert abs(st["mean_same_version"] - math.log(gd["w"])) < tol
+    assert st["mean_log_ratio"] == st["mean_weight_move"] + st["mean_same_version"]
+    # token TIS weight with the historical trainer as anchor: w = pi0 / q = 0.21 / 0.20
+    st2, w2 = _one_seq([A], [A], [B], cap=2.0)
+    assert abs(st2["tis_mean"] - gd["w"]) < 1e-6 and abs(float(w2[0]) - gd["w"]) < 1e-6
+    assert st2["tis_clipped"] == 0
+    # movement ratio r = p_k / pi0 read through the same statistic
+    st3, _ = _one_seq([B], [B], [C], cap=2.0)
+    assert abs(st3["tis_mean"] - gd["r"]) < 1e-6
+
+
+def pin_tii_example():
+    gd = golden("tii_weight_example.json")
+    A = np.float32(math.log(gd["q_v"]))
+    C = np.float32(math.log(gd["p_k"]))
+    st, w = _one_seq([A], [A], [C], cap=2.0)
+    assert st["pair"][0]["mismatch_count"] == 0 and st["mean_same_version"] == 0.0
+    assert abs(st["tis_mean"] - gd["weight"]) < 1e-6
+
+
+def pin_eq1_exact_per_token():
+    """Per token, (C - B) + (B - A) equals C - A exactly (rational arithmetic on float32
+    inputs), and the per-sequence means obey the split to 1e-12 relative."""
+    g = np.random.default_rng(7)
+    A = (g.standard_normal(500) * 3 - 5).astype(np.float32)
+    B = (A + g.standard_normal(500).astype(np.float32) * np.float32(0.01)).astype(np.float32)
+    C = (B + g.standard_normal(500).astype(np.float32) * np.float32(0.3)).astype(np.float32)
+    for a, b, c in zip(A[:50], B[:50], C[:50]):
+        fa, fb, fc = Fraction(float(a)), Fraction(float(b)), Fraction(float(c))
+        assert (fc - fb) + (fb - fa) == fc - fa
+        assert Fraction(float(np.float64(c) - np.float64(a))) == fc - fa
+    st, _ = _one_seq(A, B, C)
+    lhs = st["mean_log_ratio"]
+    rhs = st["mean_weight_move"] + st["mean_same_version"]
+    assert abs(lhs - rhs) <= 1e-12 * max(1.0, abs(lhs))
+    want = float(sum(Fraction(float(c)) - Fraction(float(a)) for a, c in zip(A, C)) / len(A))
+    assert abs(lhs - want) <= 1e-12 * abs(want)
+
+
+def pin_identical_inputs():
+    g = np.random.default_rng(3)
+    A = (g.standard_normal(300) - 4).astype(np.float32)
+    mask = (g.random(300) < 0.7).astype(np.uint8)
+    mask[0] = 1
+    st, w = _one_seq(A, A.copy(), A.copy(), mask)
+    for p in st["pair"]:
+        assert p["mismatch_count"] == 0 and p["first_div"] == -1 and p["longest_run"] == 0
+        assert p["max_abs_diff"] == 0.0 and p["signed_mean"] == 0.0 and p["mae"] == 0.0
+    assert st["k3_mean"] == 0.0 and st["tis_mean"] == 1.0 and st["tis_clipped"] == 0
+    assert st["n_valid"] == int(mask.sum())
+    assert np.all(w[mask == 1] == 1.0) and np.all(w[mask == 0] == 0.0)
+
+
+def pin_k3_closed_form():
+    """k3 = exp(d) - 1 - d: d = ln 2 gives 1 - ln 2, d = -1 gives 1/e (up to the float32
+    rounding of the inputs); tiny d gives d^2/2 + d^3/6 + ... to 1e-8 relative, which an
+    evaluation as exp(d) - 1 - d would miss by cancellation."""
+    a = np.float32(-3.0)
+    for d, closed in ((math.log(2.0), 1 - math.log(2.0)), (-1.0, math.exp(-1.0))):
+        c = np.float32(a + np.float32(d))
+        dd = float(np.float64(c) - np.float64(a))
+        st, _ = _one_seq([a], [a], [c])
+        assert abs(st["k3_mean"] - closed) < 1e-6
+        assert abs(st["k3_mean"] - (math.exp(dd) - 1 - dd)) < 1e-12
+    a = np.float32(-1.0)
+    c = np.nextafter(a, np.float32(0))  # d = one float32 step = 2^-24
+    dd = float(np.float64(c) - np.float64(a))
+    st, _ = _one_seq([a], [a], [c])
+    series = dd * dd / 2 + dd ** 3 / 6 + dd ** 4 / 24
+    assert abs(st["k3_mean"] - series) <= 1e-8 * series
+
+
+def pin_k3_overflow_flag():
+    st, _ = _one_seq([np.float32(-900.0)], [np.float32(-900.0)], [np.float32(-50.0)])
+    assert not math.isfinite(st["k3_mean"])
+    assert st["flags"] & oracle.FLAG_K3_OVERFLOW
+    assert st["tis_mean"] == 2.0 and st["tis_clipped"] == 1
+
+
+def pin_tis_clip():
+    A = np.float32(-5.0)
+    for d, w_want, clip in ((math.log(3.0), 2.0, 1), (math.log(1.5), 1.5, 0), (-1.0, math.exp(-1.0), 0)):
+        C = np.float32(A + np.float32(d))
+        st, w = _one_seq([A], [A], [C], cap=2.0)
+        assert st["tis_clipped"] == clip
+        assert abs(st["tis_mean"] - w_want) < 2e-6 * w_want
+    st, w = _one_seq([A, A], [A, A], [np.float32(0.0), A], mask=[1, 0], cap=2.0)
+    assert w[1] == 0.0 and w[0] == 2.0
+
+
+def pin_active_ordinals():
+    """first divergence and longest run count active tokens only; a masked gap does not break
+    a run of differences ("Fault localization ...", Per-sequence observation patterns)."""
+    mask = np.array([1, 1, 0, 1, 1, 1, 0, 1], dtype=np.uint8)
+    A = np.full(8, -1.0, dtype=np.float32)
+    B = A.copy()
+    for pos in (1, 3, 4, 7, 6):  # 6 is masked
+        B[pos] = np.float32(-1.5)
+    st, _ = _one_seq(A, B, B, mask)
+    p = st["pair"][0]
+    assert p["mismatch_count"] == 4 and p["first_div"] == 1 and p["longest_run"] == 3
+    assert st["n_valid"] == 6
+    assert abs(p["mae"] - 4 * 0.5 / 6) < 1e-15 and abs(p["signed_mean"] - 4 * 0.5 / 6) < 1e-15
+    assert p["max_abs_diff"] == 0.5
+
+
+def pin_signed_zero_and_nan():
+    """+0.0 and -0.0 differ bitwise but not in value; NaN on an active token is an error."""
+    st, _ = _one_seq([np.float32(0.0)], [np.float32(-0.0)], [np.float32(0.0)])
+    assert st["pair"][0]["mismatch_count"] == 1 and st["pair"][0]["max_abs_diff"] == 0.0
+    assert st["pair"][2]["mismatch_count"] == 0
+    try:
+        _one_seq([np.float32(np.nan), np.float32(-1)], [np.float32(-1)] * 2, [np.float32(-1)] * 2)
+    except oracle.OracleError as e:
+        assert e.code == "NONFINITE"
+    else:
+        raise AssertionError("NaN on an active token must raise")
+    st, _ = _one_seq([np.float32(np.nan), np.float32(-1)], [np.float32(-1)] * 2,
+                     [np.float32(-1)] * 2, mask=[0, 1])
+    assert st["n_valid"] == 1
+
+
+def pin_error_contract():
+    ok = np.zeros(8, np.float32)
+    offs = np.array([0, 4, 8], dtype=np.int64)
+    m = np.ones(8, np.uint8)
+    cases = [
+        ("SHAPE", (ok, ok[:7], ok, offs, m, 2.0)),
+        ("BAD_MASK", (ok, ok, ok, offs, np.array([1, 2, 1, 1, 1, 1, 1, 1], np.uint8), 2.0)),
+        ("EMPTY_SEQUENCE", (ok, ok, ok, offs, np.array([1, 1, 1, 1, 0, 0, 0, 0], np.uint8), 2.0)),
+        ("INVALID_ARG", (ok, ok, ok, np.array([0, 5, 4], np.int64), m, 2.0)),
+        ("INVALID_ARG", (ok, ok, ok, np.array([0, 4, 9], np.int64), m, 2.0)),
+        ("INVALID_ARG", (ok, ok, ok, offs, m, 0.0)),
+    ]
+    for code, args in cases:
+        try:
+            oracle.oracle_compare(*args)
+        except oracle.OracleError as e:
+            assert e.code == code, (code, e.code)
+        else:
+            raise AssertionError(f"expected {code}")
+    for bad in (([1.0], [1.0, 2.0], [1, 1]), ([1.0, 2.0], [1.0, 2.0], [0, 0]),
+                ([1.0, 2.0], [1.0, 2.0], [1, 2]), ([np.inf, 2.0], [1.0, 2.0], [1, 1])):
+        try:
+            oracle.compare_summary(*bad)
+        except oracle.OracleError:
+            pass
+        else:
+            raise AssertionError("compare_summary must reject " + repr(bad))
+
+
+def pin_bitwise_requests():
+    """compare_logprobs semantics: request sets and masks must match; tokens, mismatched,
+    first (request, ordinal), max_abs."""
+    x1 = np.array([-1.0, -2.0, -3.0], np.float32)
+    y1 = np.array([-1.0, -2.5, -3.0], np.float32)
+    m1 = np.array([True, True, True])
+    x2 = np.array([-0.5, -0.25], np.float32)
+    m2 = np.array([False, True])
+    res = oracle.compare_bitwise({"r1": (x1, m1), "r2": (x2, m2)}, {"r1": (y1, m1), "r2": (x2, m2)})
+    assert res == dict(tokens=4, mismatched=1, first=("r1", 1), max_abs=0.5)
+    for a, b in (({"r1": (x1, m1)}, {"r2": (x1, m1)}),
+                 ({"r1": (x1, m1)}, {"r1": (x1, np.array([True, False, True]))})):
+        try:
+            oracle.compare_bitwise(a, b)
+        except oracle.OracleError:
+            pass
+        else:
+            raise AssertionError("must raise")
+
+
+def pin_shift_fault_detected():
+    """Scoring with token ids shifted by one inside each sequence is detected: every active
+    token whose shifted id differs mismatches (Fault localization page: +-1 offsets)."""
+    b = synth.make_tiny()
+    A = oracle.oracle_logprob(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 1.0, b.eps)["logprob"]
+    ids_s = b.token_ids.copy()
+    for j in range(b.n_seq):
+        a0, a1 = b.seq_offsets[j], b.seq_offsets[j + 1]
+        ids_s[a0:a1] = np.roll(b.token_ids[a0:a1], -1)
+    C = oracle.oracle_logprob(b.hidden_gen, b.head.gamma, b.head.W, ids_s, 1.0, b.eps)["logprob"]
+    A32, C32 = A.astype(np.float32), C.astype(np.float32)
+    stats, _ = oracle.oracle_compare(A32, A32, C32, b.seq_offsets, b.mask, 2.0)
+    for j, st in enumerate(stats):
+        a0, a1 = b.seq_offsets[j], b.seq_offsets[j + 1]
+        act = np.flatnonzero(b.mask[a0:a1]) + a0
+        changed = int(np.sum(ids_s[act] != b.token_ids[act]))
+        assert st["pair"][2]["mismatch_count"] == changed
+        assert changed >= st["n_valid"] - 2
+        assert st["pair"][2]["mae"] > 0.5
+        assert st["pair"][0]["mismatch_count"] == 0
+
+
+def pin_topk_renorm_example():
+    """The page's k=2 renormalisation (used as a fixture check of the golden file only)."""
+    gd = golden("topk_renormalisation.json")
+    p = np.array(gd["probs"])
+    keep = np.argsort(-p)[:gd["k"]]
+    q = np.zeros_like(p)
+    q[keep] = p[keep] / p[keep].sum()
+    assert np.allclose(q, gd["renormalised"], atol=1e-15)
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -1,0 +1,152 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins catch each.
+
+A mutation that no pin catches would mean the oracle's correctness rests on
+itself for that step.  Each case names the pins expected to fail.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.compare as oc
+import oracle.logprob as ol
+import oracle_pins as P
+
+
+def _lse_after_softmax(z, temperature):
+    # log_softmax(z) / tau instead of log_softmax(z / tau)
+    m = np.max(z, axis=1)
+    lse = m + np.log(np.sum(np.exp(z - m[:, None]), axis=1))
+    return z / temperature, lse / temperature
+
+
+def _lse_no_shift(z, temperature):
+    s = z / temperature
+    with np.errstate(over="ignore"):
+        return s, np.log(np.sum(np.exp(s), axis=1))
+
+
+def _rms_eps_outside(h, gamma, eps):
+    ms = np.mean(h * h, axis=1)
+    rstd = 1.0 / np.sqrt(ms) + eps
+    return ol.round_to_bf16(h * rstd[:, None] * gamma[None, :])
+
+
+def _rms_no_round(h, gamma, eps):
+    ms = np.mean(h * h, axis=1)
+    return h * (1.0 / np.sqrt(ms + eps))[:, None] * gamma[None, :]
+
+
+def _rms_sum_not_mean(h, gamma, eps):
+    ms = np.sum(h * h, axis=1) / (h.shape[1] - 1)
+    return ol.round_to_bf16(h * (1.0 / np.sqrt(ms + eps))[:, None] * gamma[None, :])
+
+
+def _logits_reversed_features(y, W_bits, vocab_block=8192):
+    return y @ ol.widen_bf16(W_bits[:, ::-1]).T
+
+
+def _round_truncate(x):
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    q = np.ldexp(np.ones_like(x), np.maximum(e, -125) - 8)
+    return np.trunc(x / q) * q
+
+
+_orig_oracle_logprob = ol.oracle_logprob
+
+
+def _gather_next_id(hidden_bits, gamma_bits, W_bits, token_ids, temperature, eps, row_block=128):
+    ids = (np.asarray(token_ids, dtype=np.int64) + 1) % W_bits.shape[0]
+    return _orig_oracle_logprob(hidden_bits, gamma_bits, W_bits, ids, temperature, eps, row_block)
+
+
+def _top1_last(hidden_bits, gamma_bits, W_bits, token_ids, temperature, eps, row_block=128):
+    out = _orig_oracle_logprob(hidden_bits, gamma_bits, W_bits, token_ids, temperature, eps, row_block)
+    rows = ol.oracle_log_softmax_rows(hidden_bits, gamma_bits, W_bits, temperature, eps)
+    out["top1"] = rows.shape[1] - 1 - np.argmax(rows[:, ::-1], axis=1)
+    return out
+
+
+_orig_pair = oc._pair_stats
+
+
+def _pair_reversed(x, y):
+    return _orig_pair(y, x)
+
+
+def _differ_by_value(x, y):
+    return x != y
+
+
+def _run_plus_one(b):
+    if b.size == 0 or not b.any():
+        return 0
+    edges = np.diff(np.concatenate(([0], b.astype(np.int8), [0])))
+    return int(np.max(np.flatnonzero(edges == -1) - np.flatnonzero(edges == 1))) + 1
+
+
+def _active_all_rows(m, start):
+    return np.arange(m.shape[0]) + start
+
+
+def _k3_exp_plus(d):
+    with np.errstate(over="ignore", invalid="ignore"):
+        return np.exp(d) - 1 + d
+
+
+def _k3_naive(d):
+    with np.errstate(over="ignore", invalid="ignore"):
+        return np.exp(d) - 1 - d
+
+
+_orig_tis = oc._tis_weights
+
+
+def _tis_reversed(d, cap):
+    return _orig_tis(-d, cap)
+
+
+def _tis_no_clip(d, cap):
+    with np.errstate(over="ignore"):
+        w = np.exp(d)
+    return w, np.zeros(d.shape, dtype=bool)
+
+
+MUTATIONS = [
+    ("temperature after softmax", ol, "lse_stats", _lse_after_softmax, ["pin_v8_temperature"]),
+    ("no max shift", ol, "lse_stats", _lse_no_shift, ["pin_large_logits"]),
+    ("eps outside sqrt", ol, "rmsnorm", _rms_eps_outside, ["pin_rmsnorm_closed_form"]),
+    ("y not rounded to bf16", ol, "rmsnorm", _rms_no_round, ["pin_brute_force_mpmath"]),
+    ("sum/(d-1) instead of mean", ol, "rmsnorm", _rms_sum_not_mean, ["pin_rmsnorm_closed_form"]),
+    ("W features reversed", ol, "logits", _logits_reversed_features, ["pin_brute_force_mpmath"]),
+    ("bf16 truncation not nearest-even", ol, "round_to_bf16", _round_truncate,
+     ["pin_round_to_bf16_brute"]),
+    ("gather the next id", ol, "oracle_logprob", _gather_next_id, ["pin_v8_page_probabilities"]),
+    ("top-1 picks last on ties", ol, "oracle_logprob", _top1_last, ["pin_v8_uniform"]),
+    ("pair subtraction reversed", oc, "_pair_stats", _pair_reversed, ["pin_recorded_token_summary",
+                                                                      "pin_case3_outlier"]),
+    ("value compare instead of bitwise", oc, "_differ", _differ_by_value, ["pin_signed_zero_and_nan"]),
+    ("longest run off by one", oc, "_longest_true_run", _run_plus_one, ["pin_active_ordinals"]),
+    ("mask ignored (positions, not active ordinals)", oc, "_active_rows", _active_all_rows,
+     ["pin_active_ordinals"]),
+    ("k3 sign of d flipped", oc, "_k3_terms", _k3_exp_plus, ["pin_k3_closed_form"]),
+    ("k3 by exp(d)-1-d (cancellation)", oc, "_k3_terms", _k3_naive, ["pin_k3_closed_form"]),
+    ("TIS ratio inverted (A - C)", oc, "_tis_weights", _tis_reversed, ["pin_fig1_split"]),
+    ("TIS without the cap", oc, "_tis_weights", _tis_no_clip, ["pin_tis_clip"]),
+]
+
+
+@pytest.mark.parametrize("name,mod,attr,fn,pins", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_mutation_is_caught(monkeypatch, name, mod, attr, fn, pins):
+    monkeypatch.setattr(mod, attr, fn)
+    if hasattr(oracle, attr):   # names re-exported by the package
+        monkeypatch.setattr(oracle, attr, fn)
+    caught = []
+    for pin_name in pins:
+        try:
+            getattr(P, pin_name)()
+        except (AssertionError, oracle.OracleError, FloatingPointError):
+            caught.append(pin_name)
+    assert caught, f"mutation '{name}' passed every pin in {pins}"
