@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark: scored tokens/s of the fused linear logprob on the Qwen3-8B-shaped head.
+
+One step = one pass of the whole scoring path over one batch of synthetic input:
+RMSNorm -> LM-head GEMM with fused per-vocab-tile softmax statistics -> fixed-order
+merge (logprob, lse, top-1) for T = 32768 rows (8 samples x 4096 tokens, d = 4096,
+V = 151936, temperature 0.7), followed by the three-way compare of that batch's
+generation / replay / trainer scores (8 sequences, TIS cap 2.0).  The step scores
+the trainer set (C); A and B are recorded before the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints ONE JSON line on rank 0.  N > 1 runs under torchrun: every rank scores its
+own batch (weak scaling, no data-path collective); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "scored tokens/s, fused logprob at d=4096,V=151936; % of bf16 tensor peak"
+WORKLOAD = ("Qwen3-8B-shaped head: T=32768 rows (8 samples x 4096: 1024 shared prompt + 3072 "
+            "response), d=4096, V=151936, temperature 0.7, three-way compare with TIS cap 2.0")
+L2_NOTE = "inputs larger than L2 (W 1.245 GB + hidden 268 MB per step vs 129 MB L2)"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--cpu-rows", type=int, default=128,
+                   help="rows of the workload the oracle scores for the CPU baseline")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return dict(hbm_gbs=pk["hbm_gbs"], bf16=pk["bf16_tflops"],
+                    bf16_sustained=pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        self.out = os.path.join("/tmp", f"tim_clocks_{os.getpid()}.csv")
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if gpu_id:
+                cmd += ["-i", gpu_id]
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.out) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                     power=float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else 0.0,
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+                except ValueError:
+                    continue
+        os.remove(self.out)
+        if not rows:
+            return None
+        load = [r for r in rows if r["power"] > 0.5 * max(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(r["sm"] for r in load),
+                    sm_max_mhz=max(r["smax"] for r in load), reasons=sorted(reasons),
+                    samples=len(rows), samples_under_load=len(load),
+                    power_w_max=max(r["power"] for r in rows))
+
+
+def gpu_uuid(torch):
+    try:
+        return str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------------------ distributed
+
+def dist_setup(n):
+    if n <= 1 and "WORLD_SIZE" not in os.environ:
+        return 0, 1, 0, None
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    backend = "nccl" if os.environ.get("TIM_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+    dist.init_process_group(backend=backend)
+    return rank, world, local, dist
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device):
+    if dist is None:
+        return
+    import torch
+    if dist.get_backend() == "nccl":
+        dist.barrier(device_ids=[torch.cuda.current_device()])
+    else:
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(b, rows):
+    """fp64 oracle on ``rows`` of the workload (trainer set) + the compare of those rows."""
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    out = oracle.oracle_logprob(b.hidden_train[rows], b.head.gamma, b.head.W, b.token_ids[rows],
+                                b.temperature, b.eps)
+    lp = out["logprob"].astype(np.float32)
+    oracle.oracle_compare(lp, lp, lp, np.array([0, len(rows)], dtype=np.int64),
+                          np.ones(len(rows), np.uint8), b.tis_cap)
+    return time.perf_counter() - t0
+
+
+def reference_arm(args):
+    """--impl reference: the fp64 CPU oracle on this workload, bounded per step."""
+    import numpy as np
+    import synth
+    rank = int(os.environ.get("RANK", 0))
+    if rank != 0:
+        return 0
+    b = synth.make_qwen3_8b()
+    rows_per_step = 16
+    g = np.random.default_rng(77)
+    for _ in range(args.warmup):
+        time_oracle(b, np.sort(g.choice(b.T, rows_per_step, replace=False)))
+    total = 0.0
+    for _ in range(args.steps):
+        total += time_oracle(b, np.sort(g.choice(b.T, rows_per_step, replace=False)))
+    value = rows_per_step * args.steps / total
+    sample = (f"{rows_per_step} seeded rows of the workload per step, scored by the fp64 oracle "
+              f"(RMSNorm, bf16 rounding, fp64 GEMM over V=151936, log-sum-exp) plus the compare")
+    line = dict(impl="reference", metric=METRIC, value=value, unit="tokens/s", n_gpus=args.gpus,
+                steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * total / args.steps,
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic", config=dict(workload=WORKLOAD, T=b.T, d=b.d, V=b.V,
+                                              temperature=b.temperature, l2=L2_NOTE),
+                cpu_baseline=dict(value=value, unit="tokens/s", cores=cpu_cores(), kind="oracle",
+                                  sample=sample),
+                e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+                gpu_launches=0)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return reference_arm(args)
+    import numpy as np
+    import torch
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    import rollout_logprob_consistency_gb300 as tim
+
+    peaks = load_peaks()
+    b = synth.make_qwen3_8b(seed=rank)
+    T, d, V = b.T, b.d, b.V
+    tau, eps = b.temperature, b.eps
+    stream = torch.cuda.current_stream()
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    W = bf16(b.head.W)
+    gam = bf16(b.head.gamma)
+    hid_gen = bf16(b.hidden_gen)
+    hid_train = bf16(b.hidden_train)
+    ids = torch.from_numpy(b.token_ids).to(dev)
+    offs = torch.from_numpy(b.seq_offsets).to(dev)
+    mask = torch.from_numpy(b.mask).to(dev)
+    ws = tim.Workspace(tim.logprob_workspace_size(T, d, V), dev)
+    cws = tim.Workspace(tim.compare_workspace_size(T, b.n_seq), dev)
+
+    def new_out():
+        return (torch.empty(T, dtype=torch.float32, device=dev),
+                torch.empty(T, dtype=torch.float32, device=dev),
+                torch.empty(T, dtype=torch.int32, device=dev))
+
+    A = new_out()
+    Bo = new_out()
+    C = new_out()
+    tim.logprob(hid_gen, gam, W, ids, tau, eps, out=A, workspace=ws)
+    tim.logprob(hid_gen, gam, W, ids, tau, eps, out=Bo, workspace=ws)
+    stats_buf = torch.empty(b.n_seq * tim.SEQ_STATS_DTYPE.itemsize, dtype=torch.uint8, device=dev)
+    tis_w = torch.empty(T, dtype=torch.float32, device=dev)
+
+    def step(evs=None):
+        tim.logprob_stages(hid_train, gam, W, ids, tau, eps, C, ws, stream, events=evs)
+        tim.compare(A[0], Bo[0], C[0], offs, mask, b.tis_cap, out_stats=stats_buf,
+                    out_tis_w=tis_w, workspace=cws, check=False, to_host=False)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    ws.check("warmup")
+    cws.check("warmup compare")
+
+    ev_all = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(gpu_uuid(torch)) if rank == 0 else None
+    barrier(dist, dev)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        step(ev_all[k])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    clk = clocks.stop() if clocks is not None else None
+    ws.check("timed steps")
+    cws.check("timed compare")
+    total_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
+    gemm_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev_all)
+    norm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev_all)
+    fin_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev_all)
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    flops = 2.0 * T * d * V
+    achieved_tflops = flops / (gemm_ms / 1e3) / 1e12
+    peak = peaks["bf16_sustained"]
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_hid = pin(b.hidden_train.view(np.int16))
+    h_ids = pin(b.token_ids)
+    h_A = A[0].cpu().pin_memory()
+    h_B = Bo[0].cpu().pin_memory()
+    h_mask = pin(b.mask)
+    h_offs = pin(b.seq_offsets)
+    h_out = [torch.empty(T, dtype=torch.float32).pin_memory(),
+             torch.empty(T, dtype=torch.float32).pin_memory(),
+             torch.empty(T, dtype=torch.int32).pin_memory(),
+             torch.empty(stats_buf.numel(), dtype=torch.uint8).pin_memory()]
+    d_hid = torch.empty(T, d, dtype=torch.int16, device=dev)
+    d_ids = torch.empty(T, dtype=torch.int32, device=dev)
+    d_A = torch.empty(T, dtype=torch.float32, device=dev)
+    d_B = torch.empty(T, dtype=torch.float32, device=dev)
+    d_mask = torch.empty(T, dtype=torch.uint8, device=dev)
+    d_offs = torch.empty(b.n_seq + 1, dtype=torch.int64, device=dev)
+    h2d = sum(x.numel() * x.element_size() for x in (h_hid, h_ids, h_A, h_B, h_mask, h_offs))
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+
+    def e2e_step():
+        for dst, src in ((d_hid, h_hid), (d_ids, h_ids), (d_A, h_A), (d_B, h_B), (d_mask, h_mask),
+                         (d_offs, h_offs)):
+            dst.copy_(src, non_blocking=True)
+        tim.logprob(d_hid.view(torch.bfloat16), gam, W, d_ids, tau, eps, out=C, workspace=ws,
+                    check=False)
+        tim.compare(d_A, d_B, C[0], d_offs, d_mask, b.tis_cap, out_stats=stats_buf,
+                    out_tis_w=tis_w, workspace=cws, check=False, to_host=False)
+        for dst, src in zip(h_out, (C[0], C[1], C[2], stats_buf)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, args.steps // 2)
+    barrier(dist, dev)
+    start.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, dev)
+    ws.check("e2e")
+    e2e_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
+    e2e_value = world * T * e2e_steps / (e2e_ms / 1e3)
+
+    # ---------------------------------------------------------------- decode-shaped rows (HBM bound)
+    decode = None
+    if not args.no_decode and rank == 0:
+        decode = {}
+        for M in (1, 7, 64):
+            wsm = tim.Workspace(tim.logprob_workspace_size(M, d, V), dev)
+            outm = (torch.empty(M, device=dev), torch.empty(M, device=dev),
+                    torch.empty(M, dtype=torch.int32, device=dev))
+            hm, im = hid_gen[:M].contiguous(), ids[:M].contiguous()
+            for _ in range(5):
+                tim.logprob_stages(hm, gam, W, im, tau, eps, outm, wsm, stream)
+            iters = 50
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(iters)]
+            for it in range(iters):
+                tim.logprob_stages(hm, gam, W, im, tau, eps, outm, wsm, stream, events=evs[it])
+            torch.cuda.synchronize()
+            wsm.check(f"decode M={M}")
+            call_us = 1e3 * statistics.median(e[0].elapsed_time(e[3]) for e in evs)
+            gemm_us = 1e3 * statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+            nbytes = 2.0 * V * d + 2.0 * M * d
+            decode[f"M{M}"] = dict(call_us=round(call_us, 2), gemm_us=round(gemm_us, 2),
+                                   call_GBps=round(nbytes / call_us / 1e3, 1),
+                                   gemm_GBps=round(nbytes / gemm_us / 1e3, 1),
+                                   gemm_frac_of_hbm=round(nbytes / gemm_us / 1e3 / peaks["hbm_gbs"], 3),
+                                   call_frac_of_hbm=round(nbytes / call_us / 1e3 / peaks["hbm_gbs"], 3))
+
+    # ---------------------------------------------------------------- CPU baseline (oracle)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rows = np.sort(np.random.default_rng(99).choice(T, args.cpu_rows, replace=False))
+        dt = time_oracle(b, rows)
+        cpu = dict(value=args.cpu_rows / dt, unit="tokens/s", cores=cpu_cores(), kind="oracle",
+                   sample=f"{args.cpu_rows} seeded rows of this workload (trainer set) scored by "
+                          f"the fp64 numpy oracle plus their compare; {dt:.1f} s")
+
+    if rank == 0:
+        line = dict(
+            metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
+            warmup=max(args.warmup, 3), ms_per_step=ms_per_step, higher_is_better=True,
+            scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
+            config=dict(workload=WORKLOAD, T=T, d=d, V=V, temperature=tau, l2=L2_NOTE,
+                        parallelism=f"dp{world} (independent row batches per GPU)"),
+            roofline=dict(bound="tensor", achieved=achieved_tflops, peak=peak, unit="TFLOP/s",
+                          frac=achieved_tflops / peak, traffic=None,
+                          kernel="lmhead_lse_kernel",
+                          peak_source=f"{peaks['source']} bf16 sustained",
+                          frac_of_burst=achieved_tflops / peaks["bf16"],
+                          step_frac=(value / world) * 2.0 * d * V / 1e12 / peak),
+            stage_ms=dict(rmsnorm=norm_ms, lmhead_lse=gemm_ms, finalize=fin_ms,
+                          compare=ms_per_step - norm_ms - gemm_ms - fin_ms),
+            cpu_baseline=cpu,
+            e2e=dict(value=e2e_value, unit="tokens/s", h2d_bytes_per_step=h2d,
+                     d2h_bytes_per_step=d2h, steps=e2e_steps),
+            gpu_launches=4 * args.steps,
+            clocks=clk,
+            decode_shapes=decode,
+        )
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,245 @@
+/*
+ * tim.h -- batch-invariant linear logprob and three-way score comparison on
+ * one GB300 (sm_103a).  Plain C ABI: raw pointers and sizes only.
+ *
+ * The operations are defined by these passages:
+ *
+ *  - selected-token logprob l_t = z_t[x_t] - log sum_v exp z_t[v] in nats,
+ *    temperature applied to the logits before the softmax:
+ *      "Debugging Logprob Mismatches in LLM Reinforcement Learning",
+ *      Case 2: A and B Stay Close; C Changes (the l_t equation);
+ *      What a Logprob Difference Means (natural log, nats);
+ *      Make Sure Both Scores Describe the Same Probability (score-definition
+ *      table) and "How this differs from a real temperature mismatch".
+ *  - the "linear logprob" of the strict path: final RMSNorm (fixed reduction
+ *    domain and epsilon), LM-head GEMM with a fixed K-dimension reduction,
+ *    normaliser over the true vocabulary range merged across vocabulary chunks
+ *    in a fixed order:
+ *      "Training and rollout stop disagreeing: vime and RL-Kernel hold
+ *      logprobs bitwise identical for 200 steps on AMD MI300X", Interpretation.
+ *  - no batch-size dependent GEMM path:
+ *      "Rollout-Training Mismatch in LLM RL", section 5.2 (table: remove
+ *      small-batch backend switches, batch-invariant accumulation).
+ *  - the per-sequence comparison of generation (A), replay (B) and trainer (C)
+ *    scores: "Fault localization and mismatch bisect", Per-sequence
+ *    observation patterns, Metric measurement basis and Compare per-token
+ *    logprobs; "Debugging Logprob Mismatches ...", Check Whether the Pattern
+ *    Extends Across the Response; eq. (1) of "Rollout-Training Mismatch in
+ *    LLM RL" (section 1.2); token TIS of "Diagnosing Training Inference
+ *    Mismatch in LLM Reinforcement Learning", 3. TIS.
+ *
+ * Conventions for every entry point
+ *  - All data pointers are DEVICE pointers owned by the caller (the library
+ *    allocates nothing per call and keeps no per-call global state).
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  Nothing is synchronised unless stated.
+ *  - Argument errors (null pointers, bad sizes, bad alignment, workspace too
+ *    small, wrong GPU) are returned immediately and nothing is enqueued.
+ *  - Data-dependent errors found by the kernels (token id out of range,
+ *    non-finite values, empty sequence, bad mask, bad offsets, a bounded wait
+ *    that timed out) are recorded in a status word inside the workspace; the
+ *    first recorded error is kept.  tim_status_sync() returns and clears it.
+ *    Once an error is reported, the numbers of that call are not to be trusted.
+ *  - A workspace must be zero-initialised once (tim_workspace_init) before its
+ *    first use; it may then be reused by any number of calls on one stream.
+ *    Calls that share a workspace must not overlap in time.
+ *
+ * Only sm_103 devices (GB300) are supported.
+ */
+#ifndef TIM_H_
+#define TIM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle type, declared here without CUDA headers. */
+typedef struct CUstream_st *tim_stream_t;
+
+typedef enum tim_status {
+  TIM_OK = 0,
+  TIM_ERR_INVALID_ARG = 1,         /* null pointer, bad size/scalar, bad offsets */
+  TIM_ERR_SHAPE = 2,               /* d not a multiple of 64, d/V/T out of range */
+  TIM_ERR_TOKEN_RANGE = 3,         /* a token id outside [0, V) (row -> NaN)     */
+  TIM_ERR_NONFINITE = 4,           /* non-finite hidden value, lse or score      */
+  TIM_ERR_EMPTY_SEQUENCE = 5,      /* a sequence with no active token            */
+  TIM_ERR_BAD_MASK = 6,            /* a mask byte that is neither 0 nor 1        */
+  TIM_ERR_WORKSPACE = 7,           /* workspace pointer/size insufficient        */
+  TIM_ERR_CUDA = 8,                /* a CUDA runtime/driver call failed          */
+  TIM_ERR_TIMEOUT = 9,             /* a bounded device-side wait gave up         */
+  TIM_ERR_UNSUPPORTED_DEVICE = 10  /* current device is not sm_103               */
+} tim_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *tim_status_string(tim_status s);
+
+/* ABI version of this header (bumped on any signature or struct change). */
+int32_t tim_abi_version(void);
+#define TIM_ABI_VERSION 1
+
+/* Zero the status word of a workspace (enqueued on `stream`).  Call once
+ * after allocating a workspace, before its first use. */
+tim_status tim_workspace_init(void *workspace, size_t workspace_bytes, tim_stream_t stream);
+
+/* Synchronise `stream`, then return the first data-dependent error recorded
+ * in `workspace` since the last tim_status_sync / tim_workspace_init and
+ * clear it.  Returns TIM_ERR_CUDA if a CUDA call failed. */
+tim_status tim_status_sync(void *workspace, tim_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Linear logprob.
+ *
+ * For every row t in [0, T) (rows are pre-aligned: hidden row t predicts
+ * token_ids[t]):
+ *   rstd_t      = 1 / sqrt(mean_i(h_ti^2) + eps)              (fp32)
+ *   y_ti        = bf16_round_nearest_even(h_ti * rstd_t * gamma_i)
+ *   z_tv        = sum_i y_ti * W_vi                           (fp32 accumulation)
+ *   s_tv        = z_tv / temperature
+ *   out_lse[t]  = ln sum_{v<V} exp(s_tv)                      (nats)
+ *   out_logprob[t] = s_t[token_ids[t]] - out_lse[t]
+ *   out_top1[t] = smallest v with z_tv maximal (unscaled logits)
+ * The [T, V] logits are never written to memory.
+ *
+ * Batch invariance: the bits of every output of row t depend only on row t's
+ * inputs (hidden row, token id), W, gamma, V, d, temperature and eps -- not on
+ * T, on the other rows, on the row's position, or on the number of SMs.
+ *
+ * Arguments
+ *   hidden      bf16 [T, d] row-major (row stride d elements), 16-byte aligned.
+ *   gamma       bf16 [d], 16-byte aligned.
+ *   W           bf16 [V, d] row-major (nn.Linear weight layout), 16-byte aligned.
+ *   token_ids   int32 [T].
+ *   T           rows, 1 <= T <= 2^31 - 1.
+ *   d           hidden size, a multiple of 64, 64 <= d <= 65536.
+ *   V           vocabulary size, 1 <= V <= 2^31 - 256.
+ *   temperature finite and > 0 (1.0 gives the raw-model score).
+ *   eps         finite and >= 0.
+ *   out_logprob float32 [T]; NaN where the token id is out of range.
+ *   out_lse     float32 [T].
+ *   out_top1    int32 [T].
+ *   workspace   device buffer of at least tim_logprob_workspace_size(T, d, V)
+ *               bytes, 256-byte aligned, zero-initialised once.
+ * Errors: TIM_ERR_INVALID_ARG, TIM_ERR_SHAPE, TIM_ERR_WORKSPACE,
+ *   TIM_ERR_UNSUPPORTED_DEVICE, TIM_ERR_CUDA (immediate); TIM_ERR_TOKEN_RANGE,
+ *   TIM_ERR_NONFINITE, TIM_ERR_TIMEOUT (via tim_status_sync).
+ * ------------------------------------------------------------------------ */
+size_t tim_logprob_workspace_size(int64_t T, int32_t d, int32_t V);
+
+tim_status tim_logprob(const void *hidden, const void *gamma, const void *W,
+                       const int32_t *token_ids, int64_t T, int32_t d, int32_t V,
+                       float temperature, float eps, float *out_logprob, float *out_lse,
+                       int32_t *out_top1, void *workspace, size_t workspace_bytes,
+                       tim_stream_t stream);
+
+/* The three stages of tim_logprob, exposed so that callers can time or
+ * overlap them.  tim_logprob is exactly these three calls in this order on
+ * the same workspace; the arguments mean the same as above and must be the
+ * same (T, d, V, temperature) across the three calls.
+ *
+ * Stage 1, RMSNorm: writes y (bf16 [T, d]) into the workspace.
+ * Stage 2, LM head + per-vocabulary-tile softmax statistics: reads y and W,
+ *          writes one (max, sum of exponentials, best logit, best id) record
+ *          per (row, 256-column vocabulary tile) and the target logit of each
+ *          row into the workspace.
+ * Stage 3, finalize: merges each row's tile records in a fixed order and
+ *          writes out_logprob, out_lse and out_top1. */
+tim_status tim_rmsnorm_rows(const void *hidden, const void *gamma, int64_t T, int32_t d,
+                            int32_t V, float eps, void *workspace, size_t workspace_bytes,
+                            tim_stream_t stream);
+tim_status tim_lmhead_lse(const void *W, const int32_t *token_ids, int64_t T, int32_t d,
+                          int32_t V, float temperature, void *workspace,
+                          size_t workspace_bytes, tim_stream_t stream);
+tim_status tim_lse_finalize(const int32_t *token_ids, int64_t T, int32_t d, int32_t V,
+                            float temperature, float *out_logprob, float *out_lse,
+                            int32_t *out_top1, void *workspace, size_t workspace_bytes,
+                            tim_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Three-way compare.
+ *
+ * Score sets for the same saved tokens: A = lp_gen (generation), B =
+ * lp_replay (rollout prefill replay), C = lp_train (frozen trainer forward).
+ * Sequence j covers rows [seq_offsets[j], seq_offsets[j+1]); its active
+ * tokens are the rows with mask == 1, numbered 0, 1, ... in row order.
+ *
+ * For each pair p (0: A-B, 1: B-C, 2: A-C; left minus right):
+ *   mismatch_count  active tokens whose float32 bit patterns differ
+ *                   (+0.0 and -0.0 differ);
+ *   first_div       ordinal of the first such token, -1 if none;
+ *   longest_run     longest run of consecutive active ordinals that differ;
+ *   max_abs_diff    max |double(x) - double(y)|  (exact);
+ *   signed_mean     mean of double(x) - double(y);
+ *   mae             mean of |double(x) - double(y)|.
+ * With d = double(C) - double(A) per active token:
+ *   mean_log_ratio = mean(C - A) = mean_weight_move + mean_same_version,
+ *   mean_weight_move = mean(C - B), mean_same_version = mean(B - A)  (eq. 1),
+ *   k3_mean = mean(expm1(d) - d)  (Schulman k3; not clipped: overflow gives
+ *             +inf and sets TIM_SEQ_K3_OVERFLOW),
+ *   token TIS weight w = cap if d > ln(cap) else exp(d);
+ *   tis_mean = mean(w), tis_clipped = number of tokens with d > ln(cap).
+ * out_tis_w[t] = float(w) for active rows, 0 for inactive rows of a
+ * sequence; rows outside every sequence are not written.
+ * Means are fp64 sums in a fixed order divided by n_valid.
+ *
+ * Arguments
+ *   lp_gen, lp_replay, lp_train  float32 [T] (any alignment; 16-byte aligned
+ *                                arrays take the 128-bit load path).
+ *   seq_offsets  int64 [n_seq + 1]; each sequence needs
+ *                0 <= seq_offsets[j] <= seq_offsets[j+1] <= T.
+ *   n_seq        >= 1.
+ *   mask         uint8 [T], values 0 or 1.
+ *   T            >= 1.
+ *   tis_cap      finite and > 0.
+ *   out_stats    tim_seq_stats [n_seq] (device memory).
+ *   out_tis_w    float32 [T] or NULL.
+ *   workspace    >= tim_compare_workspace_size(T, n_seq) bytes, zero-initialised once.
+ * Per-sequence problems set bits in tim_seq_stats.flags and the status word:
+ *   bad offsets -> TIM_SEQ_BAD_OFFSETS / TIM_ERR_INVALID_ARG (stats zeroed),
+ *   mask byte not 0/1 -> TIM_SEQ_BAD_MASK / TIM_ERR_BAD_MASK (stats zeroed),
+ *   no active token -> TIM_SEQ_EMPTY / TIM_ERR_EMPTY_SEQUENCE,
+ *   non-finite active score -> TIM_SEQ_NONFINITE / TIM_ERR_NONFINITE.
+ * out_tis_w rows of a sequence flagged BAD_OFFSETS or BAD_MASK are unspecified.
+ * ------------------------------------------------------------------------ */
+typedef struct tim_pair_stats {
+  int64_t mismatch_count;
+  int64_t first_div;
+  int64_t longest_run;
+  double max_abs_diff;
+  double signed_mean;
+  double mae;
+} tim_pair_stats;
+
+typedef struct tim_seq_stats {
+  int64_t n_valid;
+  tim_pair_stats pair[3]; /* 0: A-B, 1: B-C, 2: A-C */
+  double mean_log_ratio;    /* C - A */
+  double mean_weight_move;  /* C - B */
+  double mean_same_version; /* B - A */
+  double k3_mean;
+  double tis_mean;
+  int64_t tis_clipped;
+  int32_t flags;
+  int32_t reserved;
+} tim_seq_stats;
+
+#define TIM_SEQ_EMPTY 1
+#define TIM_SEQ_BAD_MASK 2
+#define TIM_SEQ_NONFINITE 4
+#define TIM_SEQ_BAD_OFFSETS 8
+#define TIM_SEQ_K3_OVERFLOW 16
+
+size_t tim_compare_workspace_size(int64_t T, int32_t n_seq);
+
+tim_status tim_compare(const float *lp_gen, const float *lp_replay, const float *lp_train,
+                       const int64_t *seq_offsets, int32_t n_seq, const uint8_t *mask,
+                       int64_t T, float tis_cap, tim_seq_stats *out_stats, float *out_tis_w,
+                       void *workspace, size_t workspace_bytes, tim_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TIM_H_ */

@@ -1,0 +1,10 @@
+"""Batch-invariant linear logprob and three-way score comparison for GB300 (sm_103a).
+
+The compute runs in ``libtim.so`` (hand-written CUDA for sm_103a, C ABI in
+``include/tim.h``); ``binding`` marshals torch tensors into it.  Build with
+``rollout_logprob_consistency_gb300.build.build()``.
+"""
+from .binding import (  # noqa: F401
+    TimError, Workspace, compare, compare_workspace_size, lib, logprob, logprob_stages,
+    logprob_workspace_size, stats_to_dicts, SEQ_STATS_DTYPE, STATUS, STATUS_NAMES,
+)

@@ -1,0 +1,282 @@
+"""Thin ctypes binding over libtim.so (argument marshalling only).
+
+Every step of the scoring and comparison runs in the CUDA library; this module
+only checks tensor dtypes/devices, passes raw device pointers and sizes through
+the C ABI declared in include/tim.h, and converts the status codes to
+exceptions.  PyTorch supplies device memory and streams.  There is no CPU
+fallback: if libtim.so is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtim.so")
+
+STATUS_NAMES = {
+    0: "TIM_OK", 1: "TIM_ERR_INVALID_ARG", 2: "TIM_ERR_SHAPE", 3: "TIM_ERR_TOKEN_RANGE",
+    4: "TIM_ERR_NONFINITE", 5: "TIM_ERR_EMPTY_SEQUENCE", 6: "TIM_ERR_BAD_MASK",
+    7: "TIM_ERR_WORKSPACE", 8: "TIM_ERR_CUDA", 9: "TIM_ERR_TIMEOUT",
+    10: "TIM_ERR_UNSUPPORTED_DEVICE",
+}
+STATUS = {v: k for k, v in STATUS_NAMES.items()}
+
+SEQ_EMPTY, SEQ_BAD_MASK, SEQ_NONFINITE, SEQ_BAD_OFFSETS, SEQ_K3_OVERFLOW = 1, 2, 4, 8, 16
+
+# numpy mirror of struct tim_seq_stats (208 bytes)
+PAIR_DTYPE = np.dtype([("mismatch_count", "<i8"), ("first_div", "<i8"), ("longest_run", "<i8"),
+                       ("max_abs_diff", "<f8"), ("signed_mean", "<f8"), ("mae", "<f8")])
+SEQ_STATS_DTYPE = np.dtype([("n_valid", "<i8"), ("pair", PAIR_DTYPE, (3,)),
+                            ("mean_log_ratio", "<f8"), ("mean_weight_move", "<f8"),
+                            ("mean_same_version", "<f8"), ("k3_mean", "<f8"), ("tis_mean", "<f8"),
+                            ("tis_clipped", "<i8"), ("flags", "<i4"), ("reserved", "<i4")])
+assert SEQ_STATS_DTYPE.itemsize == 208
+
+
+class TimError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        self.name = STATUS_NAMES.get(int(code), f"code {code}")
+        super().__init__(f"{where}: {self.name}")
+
+
+_c = ctypes
+_vp, _i64, _i32, _f32, _sz = _c.c_void_p, _c.c_int64, _c.c_int32, _c.c_float, _c.c_size_t
+
+_SIGNATURES = {
+    "tim_status_string": (_c.c_char_p, [_c.c_int]),
+    "tim_abi_version": (_i32, []),
+    "tim_workspace_init": (_c.c_int, [_vp, _sz, _vp]),
+    "tim_status_sync": (_c.c_int, [_vp, _vp]),
+    "tim_logprob_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "tim_logprob": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _vp, _vp, _vp,
+                               _vp, _sz, _vp]),
+    "tim_rmsnorm_rows": (_c.c_int, [_vp, _vp, _i64, _i32, _i32, _f32, _vp, _sz, _vp]),
+    "tim_lmhead_lse": (_c.c_int, [_vp, _vp, _i64, _i32, _i32, _f32, _vp, _sz, _vp]),
+    "tim_lse_finalize": (_c.c_int, [_vp, _i64, _i32, _i32, _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "tim_compare_workspace_size": (_sz, [_i64, _i32]),
+    "tim_compare": (_c.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i64, _f32, _vp, _vp, _vp, _sz,
+                               _vp]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libtim.so (built in-tree by ``build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libtim.so not found at {LIB_PATH}: run __graft_entry__.build() "
+                               "(there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().tim_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise TimError(code, where)
+
+
+# ----------------------------------------------------------------------------- torch helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+def _ptr(t) -> int:
+    return t.data_ptr()
+
+
+def _need(t, dtype, name, ndim=None, cuda=True):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D")
+
+
+class Workspace:
+    """A device workspace (torch uint8 buffer) with its status word zeroed once."""
+
+    def __init__(self, nbytes: int, device=None, stream=None):
+        torch = _torch()
+        self.nbytes = int(max(nbytes, 1024))
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        if self.buf.data_ptr() % 256:
+            raise RuntimeError("workspace is not 256-byte aligned")
+        _check(lib().tim_workspace_init(self.ptr, self.nbytes, _stream_ptr(stream)),
+               "tim_workspace_init")
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def sync_status(self, stream=None) -> int:
+        return int(lib().tim_status_sync(self.ptr, _stream_ptr(stream)))
+
+    def check(self, where: str = "kernel", stream=None):
+        code = self.sync_status(stream)
+        if code != 0:
+            raise TimError(code, where)
+
+
+def logprob_workspace_size(T: int, d: int, V: int) -> int:
+    return int(lib().tim_logprob_workspace_size(int(T), int(d), int(V)))
+
+
+def compare_workspace_size(T: int, n_seq: int) -> int:
+    return int(lib().tim_compare_workspace_size(int(T), int(n_seq)))
+
+
+def _as_bf16(t, name):
+    """Accept bf16 tensors or 16-bit integer views of bf16 bit patterns."""
+    torch = _torch()
+    if t.dtype == torch.int16 or t.dtype == getattr(torch, "uint16", torch.int16):
+        t = t.view(torch.bfloat16)
+    _need(t, torch.bfloat16, name)
+    return t
+
+
+def logprob(hidden, gamma, W, token_ids, temperature: float, eps: float, *, out=None,
+            workspace: Optional[Workspace] = None, stream=None, check: bool = True):
+    """Score rows with tim_logprob.  Returns (logprob f32 [T], lse f32 [T], top1 i32 [T]).
+
+    hidden bf16 [T, d], gamma bf16 [d], W bf16 [V, d], token_ids int32 [T] (CUDA tensors;
+    int16 views of bf16 bits are accepted).  ``check`` synchronises and raises on a
+    data-dependent error.
+    """
+    torch = _torch()
+    hidden = _as_bf16(hidden, "hidden")
+    gamma = _as_bf16(gamma, "gamma")
+    W = _as_bf16(W, "W")
+    _need(token_ids, torch.int32, "token_ids", 1)
+    T, d = hidden.shape
+    V = W.shape[0]
+    if W.shape[1] != d or gamma.shape != (d,) or token_ids.shape[0] != T:
+        raise ValueError("shape mismatch between hidden, gamma, W and token_ids")
+    if out is None:
+        out = (torch.empty(T, dtype=torch.float32, device=hidden.device),
+               torch.empty(T, dtype=torch.float32, device=hidden.device),
+               torch.empty(T, dtype=torch.int32, device=hidden.device))
+    lp, lse, top1 = out
+    if workspace is None:
+        workspace = Workspace(logprob_workspace_size(T, d, V), hidden.device, stream)
+    code = lib().tim_logprob(_ptr(hidden), _ptr(gamma), _ptr(W), _ptr(token_ids), T, d, V,
+                             float(temperature), float(eps), _ptr(lp), _ptr(lse), _ptr(top1),
+                             workspace.ptr, workspace.nbytes, _stream_ptr(stream))
+    _check(code, "tim_logprob")
+    if check:
+        workspace.check("tim_logprob", stream)
+    return lp, lse, top1
+
+
+def logprob_stages(hidden, gamma, W, token_ids, temperature: float, eps: float, out,
+                   workspace: Workspace, stream=None, events=None):
+    """The three stages of tim_logprob as separate C-ABI calls (same work, same order).
+
+    ``events`` = optional list of 4 torch.cuda.Event recorded before stage 1, between the
+    stages and after stage 3 on ``stream``.
+    """
+    T, d = hidden.shape
+    V = W.shape[0]
+    lp, lse, top1 = out
+    sp = _stream_ptr(stream)
+    L = lib()
+    ev = events or [None] * 4
+    if ev[0] is not None:
+        ev[0].record(stream)
+    _check(L.tim_rmsnorm_rows(_ptr(hidden), _ptr(gamma), T, d, V, float(eps), workspace.ptr,
+                              workspace.nbytes, sp), "tim_rmsnorm_rows")
+    if ev[1] is not None:
+        ev[1].record(stream)
+    _check(L.tim_lmhead_lse(_ptr(W), _ptr(token_ids), T, d, V, float(temperature), workspace.ptr,
+                            workspace.nbytes, sp), "tim_lmhead_lse")
+    if ev[2] is not None:
+        ev[2].record(stream)
+    _check(L.tim_lse_finalize(_ptr(token_ids), T, d, V, float(temperature), _ptr(lp), _ptr(lse),
+                              _ptr(top1), workspace.ptr, workspace.nbytes, sp), "tim_lse_finalize")
+    if ev[3] is not None:
+        ev[3].record(stream)
+
+
+def compare(lp_gen, lp_replay, lp_train, seq_offsets, mask, tis_cap: float, *, out_stats=None,
+            out_tis_w=None, want_tis_w: bool = True, workspace: Optional[Workspace] = None,
+            stream=None, check: bool = True, to_host: bool = True):
+    """Per-sequence A/B/C statistics with tim_compare.
+
+    lp_* float32 [T], seq_offsets int64 [S+1], mask uint8 [T] (CUDA tensors).
+    Returns (stats, tis_w): stats is a numpy structured array (SEQ_STATS_DTYPE) when
+    ``to_host`` else the raw device uint8 buffer.
+    """
+    torch = _torch()
+    for t, n in ((lp_gen, "lp_gen"), (lp_replay, "lp_replay"), (lp_train, "lp_train")):
+        _need(t, torch.float32, n, 1)
+    _need(seq_offsets, torch.int64, "seq_offsets", 1)
+    _need(mask, torch.uint8, "mask", 1)
+    T = lp_gen.shape[0]
+    S = seq_offsets.shape[0] - 1
+    if lp_replay.shape[0] != T or lp_train.shape[0] != T or mask.shape[0] != T or S < 1:
+        raise ValueError("shape mismatch")
+    dev = lp_gen.device
+    if out_stats is None:
+        out_stats = torch.empty(S * SEQ_STATS_DTYPE.itemsize, dtype=torch.uint8, device=dev)
+    if out_tis_w is None and want_tis_w:
+        out_tis_w = torch.empty(T, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = Workspace(compare_workspace_size(T, S), dev, stream)
+    code = lib().tim_compare(_ptr(lp_gen), _ptr(lp_replay), _ptr(lp_train), _ptr(seq_offsets), S,
+                             _ptr(mask), T, float(tis_cap), _ptr(out_stats),
+                             _ptr(out_tis_w) if out_tis_w is not None else None,
+                             workspace.ptr, workspace.nbytes, _stream_ptr(stream))
+    _check(code, "tim_compare")
+    if check:
+        workspace.check("tim_compare", stream)
+    if to_host:
+        host = out_stats.cpu().numpy().view(SEQ_STATS_DTYPE)
+        return host, out_tis_w
+    return out_stats, out_tis_w
+
+
+def stats_to_dicts(arr) -> list:
+    """Structured stats array -> list of dicts shaped like the oracle's."""
+    out = []
+    for r in arr:
+        out.append(dict(
+            n_valid=int(r["n_valid"]),
+            pair=[dict(mismatch_count=int(p["mismatch_count"]), first_div=int(p["first_div"]),
+                       longest_run=int(p["longest_run"]), max_abs_diff=float(p["max_abs_diff"]),
+                       signed_mean=float(p["signed_mean"]), mae=float(p["mae"]))
+                  for p in r["pair"]],
+            mean_log_ratio=float(r["mean_log_ratio"]), mean_weight_move=float(r["mean_weight_move"]),
+            mean_same_version=float(r["mean_same_version"]), k3_mean=float(r["k3_mean"]),
+            tis_mean=float(r["tis_mean"]), tis_clipped=int(r["tis_clipped"]),
+            flags=int(r["flags"])))
+    return out

@@ -1,0 +1,237 @@
+// C ABI of libtim: argument validation, workspace layout, status handling and
+// kernel launches on the caller's stream.  See include/tim.h for the contract.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "tim_common.cuh"
+
+namespace tim {
+cudaError_t launch_rmsnorm_rows(const void* hidden, const void* gamma, int64_t T, int d, float eps,
+                                void* y, int* status, cudaStream_t stream);
+cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T, int d,
+                              int V, float temperature, void* part, float* tgt, int* status,
+                              cudaStream_t stream, int num_sms);
+cudaError_t launch_lse_finalize(const void* part, const float* tgt, const int32_t* ids, int64_t T,
+                                int V, float* out_lp, float* out_lse, int32_t* out_top1,
+                                int* status, cudaStream_t stream);
+cudaError_t launch_seg_compare(const float* A, const float* B, const float* C,
+                               const int64_t* offs, int n_seq, const uint8_t* mask, int64_t T,
+                               float tis_cap, tim_seq_stats* out, float* tis_w, int* status,
+                               cudaStream_t stream);
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+tim_status check_shape(int64_t T, int32_t d, int32_t V) {
+  if (T < 1 || T > INT32_MAX) return TIM_ERR_SHAPE;
+  if (d < 64 || d > 65536 || (d % 64) != 0) return TIM_ERR_SHAPE;
+  if (V < 1 || V > INT32_MAX - 256) return TIM_ERR_SHAPE;
+  return TIM_OK;
+}
+
+tim_status check_scalars(float temperature, float eps) {
+  if (!(std::isfinite(temperature) && temperature > 0.f)) return TIM_ERR_INVALID_ARG;
+  if (!(std::isfinite(eps) && eps >= 0.f)) return TIM_ERR_INVALID_ARG;
+  return TIM_OK;
+}
+
+tim_status check_workspace(const void* ws, size_t bytes, size_t need) {
+  if (ws == nullptr || !aligned(ws, 256) || bytes < need) return TIM_ERR_WORKSPACE;
+  return TIM_OK;
+}
+
+// The current device must be an sm_103 part.  Returns its SM count.
+tim_status check_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return TIM_ERR_CUDA;
+  }
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return TIM_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return TIM_ERR_UNSUPPORTED_DEVICE;
+  if (num_sms != nullptr) *num_sms = sms;
+  return TIM_OK;
+}
+
+inline tim_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TIM_OK : TIM_ERR_CUDA; }
+
+struct Ptrs {
+  int* status;
+  void* y;
+  void* part;
+  float* tgt;
+};
+
+Ptrs logprob_ptrs(void* ws, int64_t T, int32_t d, int32_t V) {
+  const WsLayout L = logprob_layout(T, d, V);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  return Ptrs{reinterpret_cast<int*>(b + L.status_off), b + L.y_off, b + L.part_off,
+              reinterpret_cast<float*>(b + L.tgt_off)};
+}
+
+tim_status validate_logprob_common(int64_t T, int32_t d, int32_t V, float temperature,
+                                   float eps, const void* ws, size_t ws_bytes) {
+  tim_status s = check_shape(T, d, V);
+  if (s != TIM_OK) return s;
+  if ((s = check_scalars(temperature, eps)) != TIM_OK) return s;
+  return check_workspace(ws, ws_bytes, logprob_layout(T, d, V).total);
+}
+
+}  // namespace
+}  // namespace tim
+
+using namespace tim;
+
+extern "C" {
+
+const char* tim_status_string(tim_status s) {
+  switch (s) {
+    case TIM_OK: return "TIM_OK";
+    case TIM_ERR_INVALID_ARG: return "TIM_ERR_INVALID_ARG";
+    case TIM_ERR_SHAPE: return "TIM_ERR_SHAPE";
+    case TIM_ERR_TOKEN_RANGE: return "TIM_ERR_TOKEN_RANGE";
+    case TIM_ERR_NONFINITE: return "TIM_ERR_NONFINITE";
+    case TIM_ERR_EMPTY_SEQUENCE: return "TIM_ERR_EMPTY_SEQUENCE";
+    case TIM_ERR_BAD_MASK: return "TIM_ERR_BAD_MASK";
+    case TIM_ERR_WORKSPACE: return "TIM_ERR_WORKSPACE";
+    case TIM_ERR_CUDA: return "TIM_ERR_CUDA";
+    case TIM_ERR_TIMEOUT: return "TIM_ERR_TIMEOUT";
+    case TIM_ERR_UNSUPPORTED_DEVICE: return "TIM_ERR_UNSUPPORTED_DEVICE";
+  }
+  return "TIM_ERR_UNKNOWN";
+}
+
+int32_t tim_abi_version(void) { return TIM_ABI_VERSION; }
+
+tim_status tim_workspace_init(void* workspace, size_t workspace_bytes, tim_stream_t stream) {
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < 256)
+    return TIM_ERR_WORKSPACE;
+  return from_cuda(cudaMemsetAsync(workspace, 0, 256, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tim_status tim_status_sync(void* workspace, tim_stream_t stream) {
+  if (workspace == nullptr) return TIM_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TIM_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TIM_ERR_CUDA;
+  if (v != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return TIM_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return TIM_ERR_CUDA;
+  }
+  return static_cast<tim_status>(v);
+}
+
+size_t tim_logprob_workspace_size(int64_t T, int32_t d, int32_t V) {
+  if (check_shape(T, d, V) != TIM_OK) return 0;
+  return logprob_layout(T, d, V).total;
+}
+
+tim_status tim_rmsnorm_rows(const void* hidden, const void* gamma, int64_t T, int32_t d,
+                            int32_t V, float eps, void* workspace, size_t workspace_bytes,
+                            tim_stream_t stream) {
+  if (hidden == nullptr || gamma == nullptr) return TIM_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(gamma, 16)) return TIM_ERR_INVALID_ARG;
+  tim_status s = validate_logprob_common(T, d, V, 1.0f, eps, workspace, workspace_bytes);
+  if (s != TIM_OK) return s;
+  if ((s = check_device(nullptr)) != TIM_OK) return s;
+  const Ptrs p = logprob_ptrs(workspace, T, d, V);
+  return from_cuda(launch_rmsnorm_rows(hidden, gamma, T, d, eps, p.y, p.status,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tim_status tim_lmhead_lse(const void* W, const int32_t* token_ids, int64_t T, int32_t d,
+                          int32_t V, float temperature, void* workspace, size_t workspace_bytes,
+                          tim_stream_t stream) {
+  if (W == nullptr || token_ids == nullptr) return TIM_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(token_ids, 4)) return TIM_ERR_INVALID_ARG;
+  tim_status s = validate_logprob_common(T, d, V, temperature, 0.f, workspace, workspace_bytes);
+  if (s != TIM_OK) return s;
+  int sms = 0;
+  if ((s = check_device(&sms)) != TIM_OK) return s;
+  const Ptrs p = logprob_ptrs(workspace, T, d, V);
+  return from_cuda(launch_lmhead_lse(p.y, W, token_ids, T, d, V, temperature, p.part, p.tgt,
+                                     p.status, reinterpret_cast<cudaStream_t>(stream), sms));
+}
+
+tim_status tim_lse_finalize(const int32_t* token_ids, int64_t T, int32_t d, int32_t V,
+                            float temperature, float* out_logprob, float* out_lse,
+                            int32_t* out_top1, void* workspace, size_t workspace_bytes,
+                            tim_stream_t stream) {
+  if (token_ids == nullptr || out_logprob == nullptr || out_lse == nullptr || out_top1 == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!aligned(token_ids, 4) || !aligned(out_logprob, 4) || !aligned(out_lse, 4) ||
+      !aligned(out_top1, 4))
+    return TIM_ERR_INVALID_ARG;
+  tim_status s = validate_logprob_common(T, d, V, temperature, 0.f, workspace, workspace_bytes);
+  if (s != TIM_OK) return s;
+  if ((s = check_device(nullptr)) != TIM_OK) return s;
+  const Ptrs p = logprob_ptrs(workspace, T, d, V);
+  return from_cuda(launch_lse_finalize(p.part, p.tgt, token_ids, T, V, out_logprob, out_lse,
+                                       out_top1, p.status,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tim_status tim_logprob(const void* hidden, const void* gamma, const void* W,
+                       const int32_t* token_ids, int64_t T, int32_t d, int32_t V,
+                       float temperature, float eps, float* out_logprob, float* out_lse,
+                       int32_t* out_top1, void* workspace, size_t workspace_bytes,
+                       tim_stream_t stream) {
+  if (hidden == nullptr || gamma == nullptr || W == nullptr || token_ids == nullptr ||
+      out_logprob == nullptr || out_lse == nullptr || out_top1 == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(gamma, 16) || !aligned(W, 16) || !aligned(token_ids, 4) ||
+      !aligned(out_logprob, 4) || !aligned(out_lse, 4) || !aligned(out_top1, 4))
+    return TIM_ERR_INVALID_ARG;
+  tim_status s = validate_logprob_common(T, d, V, temperature, eps, workspace, workspace_bytes);
+  if (s != TIM_OK) return s;
+  if ((s = tim_rmsnorm_rows(hidden, gamma, T, d, V, eps, workspace, workspace_bytes, stream)) !=
+      TIM_OK)
+    return s;
+  if ((s = tim_lmhead_lse(W, token_ids, T, d, V, temperature, workspace, workspace_bytes,
+                          stream)) != TIM_OK)
+    return s;
+  return tim_lse_finalize(token_ids, T, d, V, temperature, out_logprob, out_lse, out_top1,
+                          workspace, workspace_bytes, stream);
+}
+
+size_t tim_compare_workspace_size(int64_t T, int32_t n_seq) {
+  if (T < 1 || n_seq < 1) return 0;
+  return 1024;
+}
+
+tim_status tim_compare(const float* lp_gen, const float* lp_replay, const float* lp_train,
+                       const int64_t* seq_offsets, int32_t n_seq, const uint8_t* mask, int64_t T,
+                       float tis_cap, tim_seq_stats* out_stats, float* out_tis_w,
+                       void* workspace, size_t workspace_bytes, tim_stream_t stream) {
+  if (lp_gen == nullptr || lp_replay == nullptr || lp_train == nullptr || seq_offsets == nullptr ||
+      mask == nullptr || out_stats == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!aligned(lp_gen, 4) || !aligned(lp_replay, 4) || !aligned(lp_train, 4) ||
+      !aligned(seq_offsets, 8) || !aligned(out_stats, 8) ||
+      (out_tis_w != nullptr && !aligned(out_tis_w, 4)))
+    return TIM_ERR_INVALID_ARG;
+  if (T < 1 || n_seq < 1) return TIM_ERR_SHAPE;
+  if (!(std::isfinite(tis_cap) && tis_cap > 0.f)) return TIM_ERR_INVALID_ARG;
+  tim_status s = check_workspace(workspace, workspace_bytes, tim_compare_workspace_size(T, n_seq));
+  if (s != TIM_OK) return s;
+  if ((s = check_device(nullptr)) != TIM_OK) return s;
+  int* status = static_cast<int*>(workspace);
+  return from_cuda(launch_seg_compare(lp_gen, lp_replay, lp_train, seq_offsets, n_seq, mask, T,
+                                      tis_cap, out_stats, out_tis_w, status,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,384 @@
+// Stage 2 of the linear logprob: LM-head GEMM z = y . W^T on the tcgen05 tensor
+// cores, with a fused epilogue that reduces every 256-column vocabulary tile of
+// every row to softmax statistics, so the [T, V] logits never reach memory.
+//
+// Sources: "Debugging Logprob Mismatches in LLM Reinforcement Learning", Case 2
+// (selected-token logprob = chosen logit minus the log of the summed
+// exponentials over the whole vocabulary) and "How this differs from a real
+// temperature mismatch" (temperature scales the logits before the softmax);
+// "Training and rollout stop disagreeing: vime and RL-Kernel ...",
+// Interpretation (GEMM K-dimension reduction and accumulation precision fixed;
+// linear logprob over the true vocabulary range); "Rollout-Training Mismatch in
+// LLM RL", section 5.2 (no small-batch backend switch; batch-invariant
+// accumulation).
+//
+// Design (one CTA per SM, persistent over (row-tile, vocab-tile) work items):
+//   warp 0       TMA producer: y tile [128 x 64] and W tile [256 x 64] per
+//                stage, 128-byte swizzle, 4-stage mbarrier ring.
+//   warp 1       allocates 512 TMEM columns; one thread issues
+//                tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16; bf16
+//                in, fp32 accumulate) 4x per stage into one of two 256-column
+//                accumulators, then tcgen05.commit.
+//   warps 2..5   epilogue, one thread per TMEM lane = one row: reads 32 columns
+//                at a time (tcgen05.ld 32x32b.x32), keeps an online max / sum of
+//                2^(z*log2e/tau - max), the arg-max of the raw logits and the
+//                target's logit, and writes one 16-byte record per (row, tile).
+//   Double-buffered accumulators let the epilogue of tile i overlap the MMAs of
+//   tile i+1.
+//
+// Batch invariance: every logit is the same sequence of MMAs (k-blocks in
+// order, 4 K=16 steps each) whatever T is; rows past T are zero-filled by the
+// TMA and never touch other rows; the epilogue arithmetic of a (row, tile) pair
+// is fixed.  Which CTA computes a tile does not matter.
+//
+// Every mbarrier wait is bounded (2 s); on timeout the kernel records
+// TIM_ERR_TIMEOUT, raises a CTA-wide abort flag, waits (bounded) for its own
+// TMA copies and MMAs still in flight, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+
+#include "tim_common.cuh"
+
+namespace tim {
+
+struct GemmArgs {
+  int64_t T;
+  int V;
+  int d;
+  int num_m;
+  int num_n;
+  int num_kb;
+  int group_m;
+  int64_t num_tiles;
+  float k2;        // log2(e) / temperature
+  float inv_temp;  // 1 / temperature
+  const int32_t* ids;
+  float4* part;
+  float* tgt;
+  int* status;
+};
+
+constexpr size_t kGemmSmemBytes =
+    1024 /* alignment slack */ + kStages * (kABytes + kBBytes) + 256 /* barriers, flags */;
+
+__device__ __forceinline__ void tile_coords(int64_t tile, const GemmArgs& a, int& m, int& n) {
+  const int64_t per_group = static_cast<int64_t>(a.group_m) * a.num_n;
+  const int64_t g = tile / per_group;
+  const int64_t r = tile - g * per_group;
+  const int m0 = static_cast<int>(g * a.group_m);
+  const int gm = min(a.group_m, a.num_m - m0);
+  m = m0 + static_cast<int>(r % gm);
+  n = static_cast<int>(r / gm);
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag, int* status) {
+  set_status(status, TIM_ERR_TIMEOUT);
+  *abort_flag = 1;
+  __threadfence_block();
+}
+
+// Bounded wait that ignores the abort flag (used while winding down).
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// One 32-column chunk of one row: update the running (max, sum) in the base-2
+// domain, the arg-max of the raw logits (first occurrence), and pick the
+// target's logit if it lies in this chunk.
+template <bool kPartial>
+__device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], int nvalid, int col0,
+                                               int rel_c, float k2, float& m2, float& sum,
+                                               float& bz, int& bi, float& zt) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    v[j] = __uint_as_float(r[j]);
+    if (kPartial) v[j] = (j < nvalid) ? v[j] : -INFINITY;
+  }
+  float cmax = v[0];
+  int cidx = 0;
+#pragma unroll
+  for (int j = 1; j < 32; ++j) {
+    if (v[j] > cmax) {
+      cmax = v[j];
+      cidx = j;
+    }
+  }
+  const float mnew = fmaxf(m2, cmax * k2);
+  float cs = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) cs += ex2_approx(fmaf(v[j], k2, -mnew));
+  sum = sum * ex2_approx(m2 - mnew) + cs;
+  m2 = mnew;
+  if (cmax > bz) {
+    bz = cmax;
+    bi = col0 + cidx;
+  }
+  if (static_cast<unsigned>(rel_c) < 32u) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j == rel_c) zt = v[j];
+  }
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    lmhead_lse_kernel(const __grid_constant__ CUtensorMap tmap_y,
+                      const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  uint32_t* last_parity = reinterpret_cast<uint32_t*>(tmem_holder + 2);  // [kStages], producer
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      last_parity[s] = 0xFFFFFFFFu;  // no load issued into this stage yet
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    prefetch_tmap(&tmap_y);
+    prefetch_tmap(&tmap_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+        int m, n;
+        tile_coords(tile, a, m, n);
+        for (int kb = 0; kb < a.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
+          tma_load_2d(sA + stage * kABytes, &tmap_y, kb * kBK, m * kBM, &full[stage]);
+          tma_load_2d(sB + stage * kBBytes, &tmap_w, kb * kBK, n * kBN, &full[stage]);
+          last_parity[stage] = ph;
+          if (++stage == kStages) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) raise_abort(abort_flag, a.status);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16_f32(kBM, kBN);
+      int stage = 0;
+      uint32_t ph = 0;
+      uint32_t acc = 0, acc_ph = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int kb = 0; kb < a.num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], ph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            umma_bf16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
+                      idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[acc]);
+        acc ^= 1u;
+        if (acc == 0) acc_ph ^= 1u;
+      }
+      if (!ok) raise_abort(abort_flag, a.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    uint32_t acc = 0, acc_ph = 0;
+    for (int64_t tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+      int m, n;
+      tile_coords(tile, a, m, n);
+      const int64_t row = static_cast<int64_t>(m) * kBM + q * 32 + lane;
+      const int x = (row < a.T) ? __ldg(a.ids + row) : -1;
+      const int col_base = n * kBN;
+      const int rel = x - col_base;
+
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_ph, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) raise_abort(abort_flag, a.status);
+        break;
+      }
+      tc_fence_after();
+      __syncwarp();
+
+      float m2 = -INFINITY, sum = 0.f, bz = -INFINITY, zt = 0.f;
+      int bi = col_base;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int col0 = col_base + c * 32;
+        if (col0 >= a.V) break;  // warp-uniform
+        uint32_t r[32];
+        tmem_ld32(tbase + c * 32, r);
+        const int nvalid = min(32, a.V - col0);
+        if (nvalid == 32)
+          epilogue_chunk<false>(r, 32, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
+        else
+          epilogue_chunk<true>(r, nvalid, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+
+      if (row < a.T) {
+        a.part[((row >> 5) * a.num_n + n) * 32 + (row & 31)] =
+            make_float4(m2, sum, bz, __int_as_float(bi));
+        if (static_cast<unsigned>(rel) < static_cast<unsigned>(kBN)) a.tgt[row] = zt * a.inv_temp;
+      }
+      acc ^= 1u;
+      if (acc == 0) acc_ph ^= 1u;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (warp == 0 && lane == 0) {
+      // wait for TMA copies still landing in shared memory
+      for (int s = 0; s < kStages; ++s)
+        if (last_parity[s] != 0xFFFFFFFFu) mbar_wait_drain(&full[s], last_parity[s]);
+    }
+    if (warp == 1 && lane == 0) {
+      // wait for MMAs still reading shared memory / writing TMEM
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 [rows, d] row-major, box = [box_rows x 64] with 128-byte swizzle,
+// out-of-range rows read as zeros.
+static bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t d,
+                            uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {d, rows};
+  const cuuint64_t strides[1] = {d * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T,
+                              int d, int V, float temperature, void* part, float* tgt,
+                              int* status, cudaStream_t stream, int num_sms) {
+  CUtensorMap map_y, map_w;
+  if (!make_kmajor_map(&map_y, y, static_cast<uint64_t>(T), static_cast<uint64_t>(d), kBM) ||
+      !make_kmajor_map(&map_w, W, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN))
+    return cudaErrorInvalidValue;
+
+  GemmArgs a;
+  a.T = T;
+  a.V = V;
+  a.d = d;
+  a.num_m = static_cast<int>((T + kBM - 1) / kBM);
+  a.num_n = (V + kBN - 1) / kBN;
+  a.num_kb = d / kBK;
+  a.group_m = 16;
+  a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
+  a.k2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  a.inv_temp = static_cast<float>(1.0 / static_cast<double>(temperature));
+  a.ids = ids;
+  a.part = static_cast<float4*>(part);
+  a.tgt = tgt;
+  a.status = status;
+
+  cudaError_t e = cudaFuncSetAttribute(lmhead_lse_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kGemmSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int64_t grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
+  lmhead_lse_kernel<<<static_cast<unsigned>(grid), kGemmThreads, kGemmSmemBytes, stream>>>(
+      map_y, map_w, a);
+  return cudaGetLastError();
+}
+
+}  // namespace tim
