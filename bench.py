@@ -31,16 +31,38 @@ WORKLOAD = ("Qwen3-8B-shaped head: T=32768 rows (8 samples x 4096: 1024 shared p
             "response), d=4096, V=151936, temperature 0.7, three-way compare with TIS cap 2.0")
 L2_NOTE = "inputs larger than L2 (W 1.245 GB + hidden 268 MB per step vs 129 MB L2)"
 
+# DRAM bytes per lmhead_lse launch from the committed ncu capture
+# (profiles/lmhead_lse_T4096_d4096_V151936.md): a T=4096 launch moved 2.523 GB read +
+# 0.041 GB written; traffic grows with the number of 2048-row groups, so a T=32768
+# launch moves 8x that.  Valid only for the kernel sources hashed here.
+TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "79720eb612350054",
+                                "tim_common.cuh": "eaad5d12289b6619"},
+                       T=4096, bytes=2.523109e9 + 41.117696e6)
+
+
+def traffic_per_launch(T):
+    import hashlib
+    csrc = os.path.join(ROOT, "rollout_logprob_consistency_gb300", "csrc")
+    for name, h in TRAFFIC_CAPTURE["sources"].items():
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != h:
+                return None   # the kernel changed since the counters were taken
+    return TRAFFIC_CAPTURE["bytes"] * T / TRAFFIC_CAPTURE["T"]
+
 
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=40)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true")
-    p.add_argument("--cpu-rows", type=int, default=128,
+    p.add_argument("--profile-shape", default=None,
+                   help="T,d,V: only run --profile-iters tim_logprob calls of this shape "
+                        "(small case for ncu captures), print nothing")
+    p.add_argument("--profile-iters", type=int, default=3)
+    p.add_argument("--cpu-rows", type=int, default=1024,
                    help="rows of the workload the oracle scores for the CPU baseline")
     return p.parse_args()
 
@@ -65,18 +87,35 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id):
+    def __init__(self, gpu_uuid):
         self.proc = None
         self.out = os.path.join("/tmp", f"tim_clocks_{os.getpid()}.csv")
+        index = self._index_of(gpu_uuid)
         try:
             cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                    "-lms", "200"]
-            if gpu_id:
-                cmd += ["-i", gpu_id]
+            if index is not None:
+                cmd += ["-i", str(index)]
             self.fh = open(self.out, "w")
             self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    @staticmethod
+    def _index_of(gpu_uuid):
+        """nvidia-smi index of the GPU this process uses (matched by UUID)."""
+        try:
+            r = subprocess.run(["nvidia-smi", "--query-gpu=index,uuid", "--format=csv,noheader"],
+                               capture_output=True, text=True, timeout=20)
+        except (OSError, subprocess.TimeoutExpired):
+            return None
+        rows = [ln.split(",") for ln in r.stdout.strip().splitlines() if "," in ln]
+        if gpu_uuid:
+            key = gpu_uuid.lower().replace("gpu-", "")
+            for idx, uuid in rows:
+                if uuid.strip().lower().replace("gpu-", "") == key:
+                    return int(idx)
+        return int(rows[0][0]) if len(rows) == 1 else None
 
     def stop(self):
         if self.proc is None:
@@ -211,10 +250,38 @@ def reference_arm(args):
 
 # ------------------------------------------------------------------------------ GPU arm
 
+def profile_case(args):
+    """A few tim_logprob calls of one shape, for ncu captures of the kernels."""
+    import numpy as np
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    import rollout_logprob_consistency_gb300 as tim
+    T, d, V = (int(x) for x in args.profile_shape.split(","))
+    b = synth.make_custom(T=T, d=d, V=V, temperature=0.7, tag="prof")
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    hid, gam, W = bf16(b.hidden_gen), bf16(b.head.gamma), bf16(b.head.W)
+    ids = torch.from_numpy(b.token_ids).cuda()
+    ws = tim.Workspace(tim.logprob_workspace_size(T, d, V))
+    out = (torch.empty(T, device="cuda"), torch.empty(T, device="cuda"),
+           torch.empty(T, dtype=torch.int32, device="cuda"))
+    for _ in range(args.profile_iters):
+        tim.logprob(hid, gam, W, ids, 0.7, b.eps, out=out, workspace=ws, check=False)
+    ws.check("profile case")
+    torch.cuda.synchronize()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return reference_arm(args)
+    if args.profile_shape:
+        return profile_case(args)
     import numpy as np
     import torch
 
@@ -383,7 +450,9 @@ def main():
             config=dict(workload=WORKLOAD, T=T, d=d, V=V, temperature=tau, l2=L2_NOTE,
                         parallelism=f"dp{world} (independent row batches per GPU)"),
             roofline=dict(bound="tensor", achieved=achieved_tflops, peak=peak, unit="TFLOP/s",
-                          frac=achieved_tflops / peak, traffic=None,
+                          frac=achieved_tflops / peak, traffic=traffic_per_launch(T),
+                          traffic_unit="bytes per launch (scaled from the T=4096 ncu capture)",
+                          algorithmic_bytes=2.0 * V * d + 2.0 * T * d,
                           kernel="lmhead_lse_kernel",
                           peak_source=f"{peaks['source']} bf16 sustained",
                           frac_of_burst=achieved_tflops / peaks["bf16"],
