@@ -238,6 +238,44 @@ tim_status tim_compare(const float *lp_gen, const float *lp_replay, const float 
                        int64_t T, float tis_cap, tim_seq_stats *out_stats, float *out_tis_w,
                        void *workspace, size_t workspace_bytes, tim_stream_t stream);
 
+/* ------------------------------------------------------------------------ *
+ * tim_logprob without a caller-supplied workspace.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory: for example a scoring hook inside a
+ * rollout or serving engine that has already claimed nearly all free device
+ * memory for its own caches and pools (so cudaMalloc fails, and the engine's
+ * allocator is not reachable from C), or latency-sensitive code that must not
+ * call cudaMalloc/cudaFree because they can synchronise the device.
+ *
+ * Computes exactly what tim_logprob computes, with the same kernels, but keeps
+ * its scratch (y, the per-vocabulary-tile records, the target logits and the
+ * status word) in one 8 MiB device array owned by the library.  Every GPU
+ * that loads the library holds that array until the process exits.  It
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *
+ * Limit: tim_logprob_workspace_size(T, d, V) must not exceed 8 MiB (8388608
+ * bytes) -- e.g. up to 466 rows at d = 4096 or 416 rows at d = 5120 with
+ * V = 151936; larger sizes return TIM_ERR_WORKSPACE with nothing enqueued.
+ *
+ * Arguments are those of tim_logprob (device pointers, same layouts and
+ * alignment), plus out_status: a device int32 that receives this call's first
+ * data-dependent error code (0 = none; TIM_ERR_TOKEN_RANGE, TIM_ERR_NONFINITE,
+ * TIM_ERR_TIMEOUT), or NULL to skip it.
+ *
+ * The first call on each device performs a one-time set-up (it looks up the
+ * device address of the array with that device current); make that first call
+ * before any stream capture.  All calls on a device share the one array and it
+ * keeps the previous call's contents (each call clears the status word it
+ * needs zeroed): calls whose work overlaps on the GPU -- on different streams,
+ * or from different threads -- race on the array and must be serialised by the
+ * caller, for instance by issuing them on one stream.
+ * ------------------------------------------------------------------------ */
+tim_status tim_logprob_noalloc(const void *hidden, const void *gamma, const void *W,
+                               const int32_t *token_ids, int64_t T, int32_t d, int32_t V,
+                               float temperature, float eps, float *out_logprob, float *out_lse,
+                               int32_t *out_top1, int32_t *out_status, tim_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
