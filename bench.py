@@ -407,6 +407,23 @@ def main():
     e2e_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
     e2e_value = world * T * e2e_steps / (e2e_ms / 1e3)
 
+    # ---------------------------------------------------------------- compare alone
+    c_a, c_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        tim.compare(A[0], Bo[0], C[0], offs, mask, b.tis_cap, out_stats=stats_buf, out_tis_w=tis_w,
+                    workspace=cws, check=False, to_host=False)
+    c_a.record(stream)
+    for _ in range(50):
+        tim.compare(A[0], Bo[0], C[0], offs, mask, b.tis_cap, out_stats=stats_buf, out_tis_w=tis_w,
+                    workspace=cws, check=False, to_host=False)
+    c_b.record(stream)
+    torch.cuda.synchronize()
+    cws.check("compare timing")
+    cmp_us = 1e3 * c_a.elapsed_time(c_b) / 50
+    cmp_bytes = T * (3 * 4 + 1 + 4) + (b.n_seq + 1) * 8 + b.n_seq * tim.SEQ_STATS_DTYPE.itemsize
+    compare_info = dict(us=round(cmp_us, 2), bytes=cmp_bytes,
+                        GBps=round(cmp_bytes / cmp_us / 1e3, 1), sequences=b.n_seq)
+
     # ---------------------------------------------------------------- decode-shaped rows (HBM bound)
     decode = None
     if not args.no_decode and rank == 0:
@@ -419,12 +436,19 @@ def main():
             for _ in range(5):
                 tim.logprob_stages(hm, gam, W, im, tau, eps, outm, wsm, stream)
             iters = 50
+            # whole tim_logprob calls back to back (no events between the stages)
+            t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t_a.record(stream)
+            for it in range(iters):
+                tim.logprob(hm, gam, W, im, tau, eps, out=outm, workspace=wsm, check=False)
+            t_b.record(stream)
+            # the same calls stage by stage with events, for the GEMM kernel alone
             evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(iters)]
             for it in range(iters):
                 tim.logprob_stages(hm, gam, W, im, tau, eps, outm, wsm, stream, events=evs[it])
             torch.cuda.synchronize()
             wsm.check(f"decode M={M}")
-            call_us = 1e3 * statistics.median(e[0].elapsed_time(e[3]) for e in evs)
+            call_us = 1e3 * t_a.elapsed_time(t_b) / iters
             gemm_us = 1e3 * statistics.median(e[1].elapsed_time(e[2]) for e in evs)
             nbytes = 2.0 * V * d + 2.0 * M * d
             decode[f"M{M}"] = dict(call_us=round(call_us, 2), gemm_us=round(gemm_us, 2),
@@ -464,6 +488,7 @@ def main():
                      d2h_bytes_per_step=d2h, steps=e2e_steps),
             gpu_launches=4 * args.steps,
             clocks=clk,
+            compare=compare_info,
             decode_shapes=decode,
         )
         print(json.dumps(line), flush=True)

@@ -42,7 +42,10 @@
  *    Once an error is reported, the numbers of that call are not to be trusted.
  *  - A workspace must be zero-initialised once (tim_workspace_init) before its
  *    first use; it may then be reused by any number of calls on one stream.
- *    Calls that share a workspace must not overlap in time.
+ *    Calls that share a workspace must not overlap in time.  A workspace
+ *    serves one family of calls: either the tim_logprob family or tim_compare
+ *    (tim_compare keeps per-sequence counters in its workspace that must be
+ *    zero between calls; it leaves them zero itself).
  *
  * Only sm_103 devices (GB300) are supported.
  */
@@ -80,8 +83,8 @@ const char *tim_status_string(tim_status s);
 int32_t tim_abi_version(void);
 #define TIM_ABI_VERSION 1
 
-/* Zero the status word of a workspace (enqueued on `stream`).  Call once
- * after allocating a workspace, before its first use. */
+/* Zero a whole workspace, status word included (enqueued on `stream`).  Call
+ * once after allocating a workspace, before its first use. */
 tim_status tim_workspace_init(void *workspace, size_t workspace_bytes, tim_stream_t stream);
 
 /* Synchronise `stream`, then return the first data-dependent error recorded
@@ -255,7 +258,7 @@ tim_status tim_compare(const float *lp_gen, const float *lp_replay, const float 
  * allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *
  * Limit: tim_logprob_workspace_size(T, d, V) must not exceed 8 MiB (8388608
- * bytes) -- e.g. up to 466 rows at d = 4096 or 416 rows at d = 5120 with
+ * bytes) -- e.g. up to 416 rows at d = 4096 or 384 rows at d = 5120 with
  * V = 151936; larger sizes return TIM_ERR_WORKSPACE with nothing enqueued.
  *
  * Arguments are those of tim_logprob (device pointers, same layouts and

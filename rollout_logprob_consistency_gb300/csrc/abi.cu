@@ -17,8 +17,9 @@ cudaError_t launch_lse_finalize(const void* part, const float* tgt, const int32_
                                 int* status, cudaStream_t stream);
 cudaError_t launch_seg_compare(const float* A, const float* B, const float* C,
                                const int64_t* offs, int n_seq, const uint8_t* mask, int64_t T,
-                               float tis_cap, tim_seq_stats* out, float* tis_w, int* status,
+                               float tis_cap, tim_seq_stats* out, float* tis_w, void* workspace,
                                cudaStream_t stream);
+size_t compare_workspace_bytes(int64_t T, int n_seq);
 
 namespace {
 
@@ -116,7 +117,8 @@ int32_t tim_abi_version(void) { return TIM_ABI_VERSION; }
 tim_status tim_workspace_init(void* workspace, size_t workspace_bytes, tim_stream_t stream) {
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < 256)
     return TIM_ERR_WORKSPACE;
-  return from_cuda(cudaMemsetAsync(workspace, 0, 256, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(
+      cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 tim_status tim_status_sync(void* workspace, tim_stream_t stream) {
@@ -209,7 +211,7 @@ tim_status tim_logprob(const void* hidden, const void* gamma, const void* W,
 
 size_t tim_compare_workspace_size(int64_t T, int32_t n_seq) {
   if (T < 1 || n_seq < 1) return 0;
-  return 1024;
+  return compare_workspace_bytes(T, n_seq);
 }
 
 tim_status tim_compare(const float* lp_gen, const float* lp_replay, const float* lp_train,
@@ -228,9 +230,8 @@ tim_status tim_compare(const float* lp_gen, const float* lp_replay, const float*
   tim_status s = check_workspace(workspace, workspace_bytes, tim_compare_workspace_size(T, n_seq));
   if (s != TIM_OK) return s;
   if ((s = check_device(nullptr)) != TIM_OK) return s;
-  int* status = static_cast<int*>(workspace);
   return from_cuda(launch_seg_compare(lp_gen, lp_replay, lp_train, seq_offsets, n_seq, mask, T,
-                                      tis_cap, out_stats, out_tis_w, status,
+                                      tis_cap, out_stats, out_tis_w, workspace,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -1,4 +1,4 @@
-// Three-way score comparison, one CTA per sequence (segmented reduction).
+// Three-way score comparison: a segmented reduction over sequences.
 //
 // Definitions (left minus right for the pairs A-B, B-C, A-C; A = generation,
 // B = rollout replay, C = trainer forward):
@@ -18,22 +18,28 @@
 //    Mismatch in LLM RL", section 2.1, and "Diagnosing Training Inference
 //    Mismatch in LLM Reinforcement Learning", 3. TIS.
 //
-// Each thread owns a 4-token vector (a 128-bit load of each score array when
-// the arrays are 16-byte aligned) and walks its tokens in order.  Runs of
-// differing tokens are combined with an ordered monoid
+// Work split: sequence j is cut into P contiguous parts (P depends only on T
+// and the number of sequences); CTA (j, p) reduces part p to a 256-byte
+// partial, and the last CTA of sequence j to finish (an atomic ticket) merges
+// the P partials in part order and writes the sequence's statistics.  Inside a
+// CTA each thread owns a 4-token vector (128-bit loads of each score array when
+// the arrays are 16-byte aligned) and walks its tokens in order; runs of
+// differing tokens are combined with the ordered monoid
 //   (n, ndiff, first, prefix_run, suffix_run, best_run)
-// by a warp shuffle tree (lane i with lane i+o, o = 1, 2, 4, 8, 16) and then
-// across the 8 warps in warp order, 1024 tokens at a time; counts, first
-// position, runs and maxima are therefore exact, and the fp64 sums are taken in
-// a fixed order.
+// through a warp shuffle tree (lane i with lane i+o, o = 1, 2, 4, 8, 16) and
+// then across warps in warp order.  Counts, first positions, runs and maxima
+// are exact; the fp64 sums are taken in a fixed order.
 #include <cmath>
+#include <cstring>
 
 #include "tim_common.cuh"
 
 namespace tim {
 
-constexpr int kCmpThreads = 256;
+constexpr int kCmpThreads = 64;
 constexpr int kCmpWarps = kCmpThreads / 32;
+constexpr int kCmpTokensPerPart = 256;
+constexpr int kCmpMaxParts = 256;
 
 template <typename I>
 struct Runs {
@@ -79,10 +85,42 @@ __device__ __forceinline__ Runs<int> warp_runs_reduce(Runs<int> r, int lane) {
   return r;
 }
 
-// Per-thread fp64 accumulators (fixed order within a thread).
+// One part's reduction (256 bytes, written by CTA (j, p) to the workspace).
+// v[]: sgn[3], abs[3], max[3], k3, tis.
+struct alignas(16) CmpPart {
+  Runs<long long> runs[3];
+  double v[11];
+  long long clipped;
+  int flags;
+  int pad;
+  int pad2[2];
+};
+static_assert(sizeof(CmpPart) == 256, "compare partial is 256 bytes");
+
+__host__ __device__ inline int compare_parts(int64_t T, int n_seq) {
+  const int64_t avg = (T + n_seq - 1) / n_seq;
+  int64_t P = (avg + kCmpTokensPerPart - 1) / kCmpTokensPerPart;
+  if (P < 1) P = 1;
+  if (P > kCmpMaxParts) P = kCmpMaxParts;
+  return static_cast<int>(P);
+}
+
+// Compare workspace: status word | per-sequence tickets int32 [S] | parts [S][P].
+struct CmpLayout {
+  size_t cnt_off, part_off, total;
+};
+__host__ inline CmpLayout compare_layout(int64_t T, int n_seq) {
+  CmpLayout L;
+  L.cnt_off = 256;
+  L.part_off = align_up(L.cnt_off + static_cast<size_t>(n_seq) * 4, 256);
+  L.total = align_up(L.part_off + static_cast<size_t>(n_seq) * compare_parts(T, n_seq) *
+                                      sizeof(CmpPart),
+                     1024);
+  return L;
+}
+
 struct Acc {
-  double sgn[3], abs_[3], mx[3];
-  double k3, tis;
+  double v[11];
   long long clipped;
   int flags;
 };
@@ -98,12 +136,12 @@ __device__ __forceinline__ void token(Acc& acc, Runs<int> (&runs)[3], float a, f
   const double x[3] = {da - db, db - dc, da - dc};
 #pragma unroll
   for (int p = 0; p < 3; ++p) {
-    acc.sgn[p] += x[p];
-    acc.abs_[p] += fabs(x[p]);
-    acc.mx[p] = fmax(acc.mx[p], fabs(x[p]));
+    acc.v[p] += x[p];
+    acc.v[3 + p] += fabs(x[p]);
+    acc.v[6 + p] = fmax(acc.v[6 + p], fabs(x[p]));
   }
   const double d = dc - da;
-  acc.k3 += expm1(d) - d;
+  acc.v[9] += expm1(d) - d;
   double w;
   if (d > ln_cap) {
     w = cap;
@@ -111,46 +149,52 @@ __device__ __forceinline__ void token(Acc& acc, Runs<int> (&runs)[3], float a, f
   } else {
     w = exp(d);
   }
-  acc.tis += w;
+  acc.v[10] += w;
   if (tis_w != nullptr) tis_w[t] = static_cast<float>(w);
 }
+
+__device__ __forceinline__ bool is_max_slot(int i) { return i >= 6 && i < 9; }
 
 template <bool kVec>
 __global__ void __launch_bounds__(kCmpThreads)
     seg_compare_kernel(const float* __restrict__ A, const float* __restrict__ B,
                        const float* __restrict__ C, const int64_t* __restrict__ offs,
-                       const uint8_t* __restrict__ mask, int64_t T, double cap, double ln_cap,
-                       tim_seq_stats* __restrict__ out, float* __restrict__ tis_w, int* status) {
+                       const uint8_t* __restrict__ mask, int64_t T, int P, double cap,
+                       double ln_cap, tim_seq_stats* __restrict__ out, float* __restrict__ tis_w,
+                       int* status, int* cnt, CmpPart* parts) {
   __shared__ Runs<int> s_runs[kCmpWarps][3];
   __shared__ double s_red[kCmpWarps][11];
   __shared__ long long s_clip[kCmpWarps];
   __shared__ int s_flags[kCmpWarps];
+  __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j = blockIdx.x;
+  const int p = blockIdx.y;
   const int64_t s = offs[j], e = offs[j + 1];
-  tim_seq_stats st;
   if (!(s >= 0 && s <= e && e <= T)) {
-    if (tid == 0) {
+    if (tid == 0 && p == 0) {
+      tim_seq_stats st;
       memset(&st, 0, sizeof(st));
-      for (int p = 0; p < 3; ++p) st.pair[p].first_div = -1;
+      for (int q = 0; q < 3; ++q) st.pair[q].first_div = -1;
       st.flags = TIM_SEQ_BAD_OFFSETS;
       out[j] = st;
       set_status(status, TIM_ERR_INVALID_ARG);
     }
     return;
   }
+  const int64_t len = e - s;
+  const int64_t ps = s + len * p / P, pe = s + len * (p + 1) / P;   // this CTA's part
 
   Acc acc;
 #pragma unroll
-  for (int p = 0; p < 3; ++p) acc.sgn[p] = acc.abs_[p] = acc.mx[p] = 0.0;
-  acc.k3 = acc.tis = 0.0;
+  for (int i = 0; i < 11; ++i) acc.v[i] = 0.0;
   acc.clipped = 0;
   acc.flags = 0;
   Runs<long long> total[3] = {runs_identity<long long>(), runs_identity<long long>(),
                               runs_identity<long long>()};
 
-  const int64_t vbeg = s >> 2, vend = (e + 3) >> 2;
+  const int64_t vbeg = ps >> 2, vend = (pe + 3) >> 2;
   for (int64_t base = vbeg; base < vend; base += kCmpThreads) {
     Runs<int> runs[3] = {runs_identity<int>(), runs_identity<int>(), runs_identity<int>()};
     const int64_t v = base + tid;
@@ -172,7 +216,7 @@ __global__ void __launch_bounds__(kCmpThreads)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int64_t t = t0 + k;
-          const bool in = (t >= s && t < e);
+          const bool in = (t >= ps && t < pe);
           av[k] = in ? __ldg(A + t) : 0.f;
           bv[k] = in ? __ldg(B + t) : 0.f;
           cv[k] = in ? __ldg(C + t) : 0.f;
@@ -182,7 +226,7 @@ __global__ void __launch_bounds__(kCmpThreads)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int64_t t = t0 + k;
-        if (t < s || t >= e) continue;
+        if (t < ps || t >= pe) continue;
         if (mv[k] > 1) acc.flags |= TIM_SEQ_BAD_MASK;
         if (mv[k] != 1) {
           if (tis_w != nullptr) tis_w[t] = 0.f;
@@ -192,25 +236,26 @@ __global__ void __launch_bounds__(kCmpThreads)
       }
     }
 #pragma unroll
-    for (int p = 0; p < 3; ++p) {
-      runs[p] = warp_runs_reduce(runs[p], lane);
-      if (lane == 0) s_runs[warp][p] = runs[p];
+    for (int q = 0; q < 3; ++q) {
+      runs[q] = warp_runs_reduce(runs[q], lane);
+      if (lane == 0) s_runs[warp][q] = runs[q];
     }
     __syncthreads();
     if (tid == 0) {
 #pragma unroll
-      for (int p = 0; p < 3; ++p) {
+      for (int q = 0; q < 3; ++q) {
         Runs<int> chunk = runs_identity<int>();
-        for (int w = 0; w < kCmpWarps; ++w) chunk = runs_combine(chunk, s_runs[w][p]);
-        total[p] = runs_combine(total[p], chunk);
+        for (int w = 0; w < kCmpWarps; ++w) chunk = runs_combine(chunk, s_runs[w][q]);
+        total[q] = runs_combine(total[q], chunk);
       }
     }
     __syncthreads();
   }
 
-  // fixed-order block reduction of the fp64 sums
-  double v[11] = {acc.sgn[0], acc.sgn[1], acc.sgn[2], acc.abs_[0], acc.abs_[1], acc.abs_[2],
-                  acc.mx[0],  acc.mx[1],  acc.mx[2],  acc.k3,      acc.tis};
+  // fixed-order block reduction of the per-thread accumulators
+  double v[11];
+#pragma unroll
+  for (int i = 0; i < 11; ++i) v[i] = acc.v[i];
   long long clip = acc.clipped;
   int flags = acc.flags;
 #pragma unroll
@@ -218,7 +263,7 @@ __global__ void __launch_bounds__(kCmpThreads)
 #pragma unroll
     for (int i = 0; i < 11; ++i) {
       const double other = __shfl_xor_sync(0xFFFFFFFFu, v[i], o);
-      v[i] = (i >= 6 && i < 9) ? fmax(v[i], other) : v[i] + other;
+      v[i] = is_max_slot(i) ? fmax(v[i], other) : v[i] + other;
     }
     clip += __shfl_xor_sync(0xFFFFFFFFu, clip, o);
     flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, o);
@@ -230,24 +275,62 @@ __global__ void __launch_bounds__(kCmpThreads)
     s_flags[warp] = flags;
   }
   __syncthreads();
-  if (tid != 0) return;
-  for (int i = 0; i < 11; ++i) {
-    double r = s_red[0][i];
-    for (int w = 1; w < kCmpWarps; ++w)
-      r = (i >= 6 && i < 9) ? fmax(r, s_red[w][i]) : r + s_red[w][i];
-    v[i] = r;
+  if (tid == 0) {
+    CmpPart part;
+    memset(&part, 0, sizeof(part));
+    for (int i = 0; i < 11; ++i) {
+      double r = s_red[0][i];
+      for (int w = 1; w < kCmpWarps; ++w) r = is_max_slot(i) ? fmax(r, s_red[w][i]) : r + s_red[w][i];
+      part.v[i] = r;
+    }
+    for (int w = 0; w < kCmpWarps; ++w) {
+      part.clipped += s_clip[w];
+      part.flags |= s_flags[w];
+    }
+    for (int q = 0; q < 3; ++q) part.runs[q] = total[q];
+    parts[static_cast<int64_t>(j) * P + p] = part;
+    __threadfence();
+    const int ticket = atomicAdd(&cnt[j], 1);
+    s_last = (ticket == P - 1) ? 1 : 0;
   }
-  clip = 0;
-  flags = 0;
-  for (int w = 0; w < kCmpWarps; ++w) {
-    clip += s_clip[w];
-    flags |= s_flags[w];
-  }
+  __syncthreads();
+  if (!s_last || tid != 0) return;
 
+  // last CTA of sequence j: merge the P partials in part order
+  __threadfence();
+  const CmpPart* pj = parts + static_cast<int64_t>(j) * P;
+  Runs<long long> R[3] = {runs_identity<long long>(), runs_identity<long long>(),
+                          runs_identity<long long>()};
+  double tot[11];
+  for (int i = 0; i < 11; ++i) tot[i] = 0.0;
+  long long clipped = 0;
+  int fl = 0;
+  for (int q = 0; q < P; ++q) {
+    const CmpPart* pp = pj + q;
+    for (int r = 0; r < 3; ++r) {
+      Runs<long long> x;
+      x.n = __ldcg(&pp->runs[r].n);
+      x.ndiff = __ldcg(&pp->runs[r].ndiff);
+      x.first = __ldcg(&pp->runs[r].first);
+      x.pre = __ldcg(&pp->runs[r].pre);
+      x.suf = __ldcg(&pp->runs[r].suf);
+      x.best = __ldcg(&pp->runs[r].best);
+      R[r] = runs_combine(R[r], x);
+    }
+    for (int i = 0; i < 11; ++i) {
+      const double x = __ldcg(&pp->v[i]);
+      tot[i] = is_max_slot(i) ? fmax(tot[i], x) : tot[i] + x;
+    }
+    clipped += __ldcg(&pp->clipped);
+    fl |= __ldcg(&pp->flags);
+  }
+  cnt[j] = 0;  // ready for the next call on this workspace
+
+  tim_seq_stats st;
   memset(&st, 0, sizeof(st));
-  for (int p = 0; p < 3; ++p) st.pair[p].first_div = -1;
-  const long long n = total[0].n;
-  if (flags & TIM_SEQ_BAD_MASK) {
+  for (int q = 0; q < 3; ++q) st.pair[q].first_div = -1;
+  const long long n = R[0].n;
+  if (fl & TIM_SEQ_BAD_MASK) {
     st.flags = TIM_SEQ_BAD_MASK;
     set_status(status, TIM_ERR_BAD_MASK);
   } else if (n == 0) {
@@ -256,42 +339,51 @@ __global__ void __launch_bounds__(kCmpThreads)
   } else {
     const double dn = static_cast<double>(n);
     st.n_valid = n;
-    for (int p = 0; p < 3; ++p) {
-      st.pair[p].mismatch_count = total[p].ndiff;
-      st.pair[p].first_div = total[p].first;
-      st.pair[p].longest_run = total[p].best;
-      st.pair[p].max_abs_diff = v[6 + p];
-      st.pair[p].signed_mean = v[p] / dn;
-      st.pair[p].mae = v[3 + p] / dn;
+    for (int q = 0; q < 3; ++q) {
+      st.pair[q].mismatch_count = R[q].ndiff;
+      st.pair[q].first_div = R[q].first;
+      st.pair[q].longest_run = R[q].best;
+      st.pair[q].max_abs_diff = tot[6 + q];
+      st.pair[q].signed_mean = tot[q] / dn;
+      st.pair[q].mae = tot[3 + q] / dn;
     }
-    st.mean_log_ratio = -v[2] / dn;
-    st.mean_weight_move = -v[1] / dn;
-    st.mean_same_version = -v[0] / dn;
-    st.k3_mean = v[9] / dn;
-    st.tis_mean = v[10] / dn;
-    st.tis_clipped = clip;
-    st.flags = flags;
+    st.mean_log_ratio = -tot[2] / dn;
+    st.mean_weight_move = -tot[1] / dn;
+    st.mean_same_version = -tot[0] / dn;
+    st.k3_mean = tot[9] / dn;
+    st.tis_mean = tot[10] / dn;
+    st.tis_clipped = clipped;
+    st.flags = fl;
     if (!isfinite(st.k3_mean)) st.flags |= TIM_SEQ_K3_OVERFLOW;
-    if (flags & TIM_SEQ_NONFINITE) set_status(status, TIM_ERR_NONFINITE);
+    if (fl & TIM_SEQ_NONFINITE) set_status(status, TIM_ERR_NONFINITE);
   }
   out[j] = st;
 }
 
+size_t compare_workspace_bytes(int64_t T, int n_seq) { return compare_layout(T, n_seq).total; }
+
 cudaError_t launch_seg_compare(const float* A, const float* B, const float* C,
                                const int64_t* offs, int n_seq, const uint8_t* mask, int64_t T,
-                               float tis_cap, tim_seq_stats* out, float* tis_w, int* status,
+                               float tis_cap, tim_seq_stats* out, float* tis_w, void* workspace,
                                cudaStream_t stream) {
   const double cap = static_cast<double>(tis_cap);
   const double ln_cap = std::log(cap);
+  const CmpLayout L = compare_layout(T, n_seq);
+  const int P = compare_parts(T, n_seq);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  int* cnt = reinterpret_cast<int*>(ws + L.cnt_off);
+  CmpPart* parts = reinterpret_cast<CmpPart*>(ws + L.part_off);
   const bool vec = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
                      reinterpret_cast<uintptr_t>(C)) & 15u) == 0 &&
                    (reinterpret_cast<uintptr_t>(mask) & 3u) == 0;
+  const dim3 grid(static_cast<unsigned>(n_seq), static_cast<unsigned>(P));
   if (vec)
-    seg_compare_kernel<true><<<n_seq, kCmpThreads, 0, stream>>>(A, B, C, offs, mask, T, cap,
-                                                                ln_cap, out, tis_w, status);
+    seg_compare_kernel<true><<<grid, kCmpThreads, 0, stream>>>(
+        A, B, C, offs, mask, T, P, cap, ln_cap, out, tis_w, status, cnt, parts);
   else
-    seg_compare_kernel<false><<<n_seq, kCmpThreads, 0, stream>>>(A, B, C, offs, mask, T, cap,
-                                                                 ln_cap, out, tis_w, status);
+    seg_compare_kernel<false><<<grid, kCmpThreads, 0, stream>>>(
+        A, B, C, offs, mask, T, P, cap, ln_cap, out, tis_w, status, cnt, parts);
   return cudaGetLastError();
 }
 

@@ -64,8 +64,18 @@ __global__ void __launch_bounds__(32 * kFinWarps)
   const float4* p = part + group * static_cast<int64_t>(n_tiles) * 32 + lane;
 
   if (t0 < t1) {
+    // fold the range left to right; records are fetched 8 at a time so the
+    // loads overlap (the merge order is unchanged)
     Rec acc = load_rec(p + static_cast<int64_t>(t0) * 32);
-    for (int t = t0 + 1; t < t1; ++t) acc = merge(acc, load_rec(p + static_cast<int64_t>(t) * 32));
+    for (int t = t0 + 1; t < t1; t += 8) {
+      Rec buf[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (t + i < t1) buf[i] = load_rec(p + static_cast<int64_t>(t + i) * 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (t + i < t1) acc = merge(acc, buf[i]);
+    }
     red[warp][lane] = acc;
   }
   __syncthreads();

@@ -27,9 +27,13 @@
 //   tile i+1.
 //
 // Batch invariance: every logit is the same sequence of MMAs (k-blocks in
-// order, 4 K=16 steps each) whatever T is; rows past T are zero-filled by the
-// TMA and never touch other rows; the epilogue arithmetic of a (row, tile) pair
+// order, 4 K=16 steps each) whatever T is; rows past T (zeros written by the
+// RMSNorm kernel up to the next 128-row boundary) never touch other rows; the epilogue arithmetic of a (row, tile) pair
 // is fixed.  Which CTA computes a tile does not matter.
+//
+// Launched with programmatic stream serialisation: the producer streams its
+// first W stages, then waits (griddepcontrol.wait) for the RMSNorm kernel
+// before the first load of y.
 //
 // Every mbarrier wait is bounded (2 s); on timeout the kernel records
 // TIM_ERR_TIMEOUT, raises a CTA-wide abort flag, waits (bounded) for its own
@@ -178,10 +182,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
+      bool first = true;
       for (int64_t tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
         int m, n;
         tile_coords(tile, a, m, n);
-        for (int kb = 0; kb < a.num_kb; ++kb) {
+        int kb0 = 0;
+        if (first) {
+          // W does not depend on the RMSNorm kernel that precedes this one in the
+          // stream: stream the first stages of W before waiting for y to be ready.
+          const int pre = min(kStages, a.num_kb);
+          for (int s = 0; s < pre; ++s) {
+            mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
+            tma_load_2d(sB + s * kBBytes, &tmap_w, s * kBK, n * kBN, &full[s]);
+          }
+          pdl_wait();
+          for (int s = 0; s < pre; ++s) {
+            tma_load_2d(sA + s * kABytes, &tmap_y, s * kBK, m * kBM, &full[s]);
+            last_parity[s] = 0;
+          }
+          stage = pre % kStages;
+          ph = (pre == kStages) ? 1u : 0u;
+          kb0 = pre;
+          first = false;
+        }
+        for (int kb = kb0; kb < a.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -351,7 +375,8 @@ cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, 
                               int d, int V, float temperature, void* part, float* tgt,
                               int* status, cudaStream_t stream, int num_sms) {
   CUtensorMap map_y, map_w;
-  if (!make_kmajor_map(&map_y, y, static_cast<uint64_t>(T), static_cast<uint64_t>(d), kBM) ||
+  if (!make_kmajor_map(&map_y, y, static_cast<uint64_t>(rows_padded(T)),
+                       static_cast<uint64_t>(d), kBM) ||
       !make_kmajor_map(&map_w, W, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN))
     return cudaErrorInvalidValue;
 
@@ -376,9 +401,20 @@ cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, 
                                        static_cast<int>(kGemmSmemBytes));
   if (e != cudaSuccess) return e;
   const int64_t grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
-  lmhead_lse_kernel<<<static_cast<unsigned>(grid), kGemmThreads, kGemmSmemBytes, stream>>>(
-      map_y, map_w, a);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the kernel's prologue and its first W loads
+  // may overlap the tail of the RMSNorm kernel; y is read only after
+  // griddepcontrol.wait.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lmhead_lse_kernel, map_y, map_w, a);
 }
 
 }  // namespace tim

@@ -9,7 +9,9 @@
 //   (offsets 16, 8, 4, 2, 1).
 // Every lane ends with the same bits (IEEE addition is commutative), and the
 // result depends only on the row's own values: the kernel is batch-invariant.
-// y = bf16_rn((h * rstd) * gamma) in fp32, written for the LM-head GEMM.
+// y = bf16_rn((h * rstd) * gamma) in fp32, written for the LM-head GEMM; rows
+// from T up to the next multiple of 128 are written as zeros (the GEMM reads
+// whole 128-row tiles).
 #include <cuda_bf16.h>
 
 #include "tim_common.cuh"
@@ -29,14 +31,20 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
 
 __global__ void __launch_bounds__(32 * kNormRowsPerBlock)
     rmsnorm_rows_kernel(const uint4* __restrict__ hidden, const uint4* __restrict__ gamma,
-                        int64_t T, int d, float eps, uint4* __restrict__ y, int* status) {
+                        int64_t T, int64_t T_pad, int d, float eps, uint4* __restrict__ y,
+                        int* status) {
+  pdl_launch_dependents();  // the LM-head kernel may start streaming W now
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kNormRowsPerBlock + warp;
-  if (row >= T) return;
+  if (row >= T_pad) return;
   const int nvec = d >> 3;
-  const uint4* h = hidden + row * nvec;
   uint4* out = y + row * nvec;
+  if (row >= T) {
+    for (int c = lane; c < nvec; c += 32) out[c] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const uint4* h = hidden + row * nvec;
 
   float ss = 0.f;
   for (int c = lane; c < nvec; c += 32) {
@@ -71,9 +79,10 @@ __global__ void __launch_bounds__(32 * kNormRowsPerBlock)
 
 cudaError_t launch_rmsnorm_rows(const void* hidden, const void* gamma, int64_t T, int d,
                                 float eps, void* y, int* status, cudaStream_t stream) {
-  const int64_t blocks = (T + kNormRowsPerBlock - 1) / kNormRowsPerBlock;
+  const int64_t T_pad = rows_padded(T);
+  const int64_t blocks = (T_pad + kNormRowsPerBlock - 1) / kNormRowsPerBlock;
   rmsnorm_rows_kernel<<<static_cast<unsigned>(blocks), 32 * kNormRowsPerBlock, 0, stream>>>(
-      static_cast<const uint4*>(hidden), static_cast<const uint4*>(gamma), T, d, eps,
+      static_cast<const uint4*>(hidden), static_cast<const uint4*>(gamma), T, T_pad, d, eps,
       static_cast<uint4*>(y), status);
   return cudaGetLastError();
 }

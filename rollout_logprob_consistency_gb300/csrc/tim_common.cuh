@@ -36,7 +36,7 @@ constexpr int kRowGroup = 32;            // rows per partial-record group
 // Workspace layout (all offsets 1024-byte aligned).
 struct WsLayout {
   size_t status_off;   // int32 status word (+ padding)
-  size_t y_off;        // bf16 [T, d]
+  size_t y_off;        // bf16 [rows_padded(T), d]; rows >= T are zero
   size_t part_off;     // float4 [ceil(T/32)][n_tiles][32]
   size_t tgt_off;      // float32 [T]
   size_t total;
@@ -44,13 +44,17 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// y is stored with whole 128-row tiles (zero rows past T) so the LM-head TMA
+// never reads outside the tensor.
+__host__ __device__ inline int64_t rows_padded(int64_t T) { return (T + kBM - 1) / kBM * kBM; }
+
 __host__ inline WsLayout logprob_layout(int64_t T, int32_t d, int32_t V) {
   WsLayout L;
   const size_t n_tiles = ((size_t)V + kBN - 1) / kBN;
   const size_t groups = ((size_t)T + kRowGroup - 1) / kRowGroup;
   L.status_off = 0;
   L.y_off = 1024;
-  L.part_off = align_up(L.y_off + (size_t)T * (size_t)d * 2, 1024);
+  L.part_off = align_up(L.y_off + (size_t)rows_padded(T) * (size_t)d * 2, 1024);
   L.tgt_off = align_up(L.part_off + groups * n_tiles * kRowGroup * 16, 1024);
   L.total = align_up(L.tgt_off + (size_t)T * 4, 1024);
   return L;
@@ -227,6 +231,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue now / wait until the previous kernel's memory is visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // 2^x with the hardware approximation (MUFU.EX2), flush-to-zero.
 __device__ __forceinline__ float ex2_approx(float x) {
