@@ -35,9 +35,9 @@ L2_NOTE = "inputs larger than L2 (W 1.245 GB + hidden 268 MB per step vs 129 MB 
 # (profiles/lmhead_lse_T4096_d4096_V151936.md): a T=4096 launch moved 2.523 GB read +
 # 0.041 GB written; traffic grows with the number of 2048-row groups, so a T=32768
 # launch moves 8x that.  Valid only for the kernel sources hashed here.
-TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "79720eb612350054",
-                                "tim_common.cuh": "eaad5d12289b6619"},
-                       T=4096, bytes=2.523109e9 + 41.117696e6)
+TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "425b375ce460ba2a",
+                                "tim_common.cuh": "a255a6e438eba7fa"},
+                       T=4096, bytes=2.523121e9 + 40.945152e6)
 
 
 def traffic_per_launch(T):
@@ -272,6 +272,15 @@ def profile_case(args):
     for _ in range(args.profile_iters):
         tim.logprob(hid, gam, W, ids, 0.7, b.eps, out=out, workspace=ws, check=False)
     ws.check("profile case")
+    # the three-way compare of the scored rows as 8 equal sequences (all tokens active)
+    S = 8 if T >= 8 else 1
+    offs = torch.from_numpy(np.linspace(0, T, S + 1).astype(np.int64)).cuda()
+    mask = torch.ones(T, dtype=torch.uint8, device="cuda")
+    cws = tim.Workspace(tim.compare_workspace_size(T, S))
+    for _ in range(args.profile_iters):
+        tim.compare(out[0], out[0], out[0], offs, mask, 2.0, workspace=cws, check=False,
+                    to_host=False)
+    cws.check("profile compare")
     torch.cuda.synchronize()
     return 0
 
