@@ -14,6 +14,9 @@ Modules
                     with z = bf16(RMSNorm(h)) . W^T, plus lse and top-1.
 ``oracle.compare``  per-sequence A/B/C mismatch statistics, k3, TIS weights,
                     and the single-pair ``compare`` summary.
+``oracle.diag``     extended per-sequence diagnostics: |delta| quantiles,
+                    probability MAE, top-1 flips, sequence TIS, K1/K3 sums,
+                    ratio error, MIS weights, mean w^2.
 
 Every function cites the page passage it follows.  Pins that tie this oracle to
 something other than itself live in ``tests/test_oracle_pins.py`` and
@@ -28,4 +31,8 @@ from .compare import (  # noqa: F401
     OracleError, FLAG_EMPTY, FLAG_BAD_MASK, FLAG_NONFINITE, FLAG_BAD_OFFSETS,
     FLAG_K3_OVERFLOW, PAIRS, oracle_compare, oracle_compare_lenient, compare_summary,
     compare_bitwise,
+)
+from .diag import (  # noqa: F401
+    FLAG_QUANTILE_SKIPPED, QUANTILE_MAX_TOKENS, QUANTILES, oracle_diag, oracle_diag_lenient,
+    quantile_linear,
 )

@@ -568,4 +568,106 @@ def pin_topk_renorm_example():
     assert np.allclose(q, gd["renormalised"], atol=1e-15)
 
 
+# ---------------------------------------------------------------------------
+# extended diagnostics pins
+
+def _diag1(A, B, C, mask=None, cap=2.0, lo=0.5, hi=1.5, top1=(None, None, None)):
+    A = np.asarray(A, dtype=np.float32)
+    n = A.shape[0]
+    mask = np.ones(n, dtype=np.uint8) if mask is None else np.asarray(mask, dtype=np.uint8)
+    return oracle.oracle_diag(A, np.asarray(B, np.float32), np.asarray(C, np.float32),
+                              np.array([0, n], dtype=np.int64), mask, cap, lo, hi, top1)[0]
+
+
+def pin_quantile_definition():
+    """Type-7 quantiles: closed form on 0..99 and numpy's 'linear' method (a library routine
+    the oracle does not call) on random data."""
+    x = np.arange(100, dtype=np.float64)[::-1].copy()
+    assert oracle.quantile_linear(x, 0.5) == 49.5
+    assert abs(oracle.quantile_linear(x, 0.95) - 94.05) < 1e-12
+    assert abs(oracle.quantile_linear(x, 0.99) - 98.01) < 1e-12
+    g = np.random.default_rng(11)
+    for n in (1, 2, 3, 7, 100, 1001):
+        v = np.abs(g.standard_normal(n)) * 0.3
+        for q in oracle.QUANTILES:
+            ref = float(np.quantile(v, q, method="linear"))
+            assert abs(oracle.quantile_linear(v, q) - ref) <= 1e-15 * max(1.0, abs(ref))
+
+
+def pin_diag_quantiles_in_sequence():
+    """|A - B| = 0.01 k on 101 active tokens (masked tokens interleaved) -> p50 = 0.5, p95 = 0.95,
+    p99 = 0.99 (up to float32 rounding of the inputs)."""
+    k = np.arange(101)
+    A = np.full(202, -2.0, np.float32)
+    B = A.copy()
+    mask = np.zeros(202, np.uint8)
+    mask[::2] = 1
+    B[::2] = (A[::2].astype(np.float64) - 0.01 * k).astype(np.float32)
+    B[1::2] = np.float32(-50.0)                   # masked: must not count
+    st = _diag1(A, B, B, mask)
+    assert st["n_valid"] == 101
+    assert abs(st["abs_q50"][0] - 0.50) < 1e-6 and abs(st["abs_q95"][0] - 0.95) < 1e-6
+    assert abs(st["abs_q99"][0] - 0.99) < 1e-6 and st["abs_q50"][1] == 0.0
+
+
+def pin_diag_page_probability_mae():
+    """p = 0.10 vs 0.12 (Debugging page, What a Logprob Difference Means): probability MAE 0.02
+    while the logprob difference is 0.1823."""
+    A = np.float32(math.log(0.10))
+    C = np.float32(math.log(0.12))
+    st = _diag1([A], [A], [C])
+    assert abs(st["prob_mae"][2] - 0.02) < 1e-8 and st["prob_mae"][0] == 0.0
+    assert abs(st["abs_q99"][2] - 0.1823215568) < 1e-6
+
+
+def pin_diag_fig1_sequence():
+    """Two tokens with the Figure 1 ratio w = 0.21 / 0.20 each: sequence ratio 1.1025, k1 sum
+    -2 ln 1.05, k3 sum 2 (0.05 - ln 1.05), ratio error 0.05, mean w^2 1.1025."""
+    A = np.float32(math.log(0.20))
+    C = np.float32(math.log(0.21))
+    st = _diag1([A, A], [A, A], [C, C], cap=2.0)
+    d = float(np.float64(C) - np.float64(A))
+    assert abs(d - math.log(1.05)) < 4e-7
+    assert abs(st["log_ratio_sum"] - 2 * math.log(1.05)) < 1e-6
+    assert abs(st["seq_tis"] - 1.1025) < 2e-6
+    assert abs(st["k1_sum"] + 2 * math.log(1.05)) < 1e-6
+    assert abs(st["k3_sum"] - 2 * (0.05 - math.log(1.05))) < 1e-7
+    assert abs(st["ratio_err_mean"] - 0.05) < 1e-6
+    assert abs(st["w2_mean"] - 1.1025) < 2e-6
+    capped = _diag1([A, A], [A, A], [C, C], cap=1.1)
+    assert capped["seq_tis"] == 1.1
+
+
+def pin_diag_mis_and_flips():
+    A = np.full(3, -4.0, np.float32)
+    C = np.array([-4.0 + math.log(1.05), -4.0 + math.log(2.0), -4.0 - math.log(4.0)], np.float32)
+    t_a = np.array([5, 6, 7])
+    t_c = np.array([5, 9, 8])
+    st = _diag1(A, A, C, lo=0.5, hi=1.5, top1=(t_a, t_a, t_c))
+    assert st["mis_kept"] == 1
+    assert abs(st["mis_mean"] - 1.05 / 3) < 1e-6
+    assert st["top1_flips"] == [0, 2, 2]
+    st2 = _diag1(A, A, C, lo=0.5, hi=1.5)
+    assert st2["top1_flips"] == [-1, -1, -1]
+
+
+def pin_diag_recorded_token():
+    """One active token: every quantile equals its |difference| (the page's note that p95, p99
+    and the maximum coincide for a single token)."""
+    gd = golden("recorded_token_case1.json")
+    s = {k: np.float32(v) for k, v in gd["scores"].items() if k != "A"}
+    st = _diag1([s["B0"]], [s["B1"]], [s["C0"]])
+    want = abs(float(np.float64(s["B0"]) - np.float64(s["B1"])))
+    assert st["abs_q50"][0] == st["abs_q95"][0] == st["abs_q99"][0] == want
+    assert round(want, 6) == gd["signed_differences_6dp"]["B0-B1"]
+
+
+def pin_diag_quantile_limit():
+    n = oracle.QUANTILE_MAX_TOKENS + 1
+    A = np.zeros(n, np.float32)
+    st = _diag1(A, A, A)
+    assert st["flags"] & oracle.FLAG_QUANTILE_SKIPPED and math.isnan(st["abs_q50"][0])
+    assert st["n_valid"] == n and st["k3_sum"] == 0.0
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -114,6 +114,34 @@ def _tis_no_clip(d, cap):
     return w, np.zeros(d.shape, dtype=bool)
 
 
+import oracle.diag as od
+
+
+def _quantile_nearest(x, q):
+    xs = np.sort(np.asarray(x, dtype=np.float64))
+    return float(xs[int(round((xs.shape[0] - 1) * q))])
+
+
+def _quantile_n_not_n_minus_1(x, q):
+    xs = np.sort(np.asarray(x, dtype=np.float64))
+    h = xs.shape[0] * q
+    lo = min(int(math.floor(h)), xs.shape[0] - 1)
+    hi = min(lo + 1, xs.shape[0] - 1)
+    return float(xs[lo] + (h - lo) * (xs[hi] - xs[lo]))
+
+
+def _prob_mae_in_logs(left, right):
+    return float(np.mean(np.abs(left - right)))
+
+
+def _seq_tis_mean_not_sum(log_ratio_sum, cap):
+    return min(math.exp(log_ratio_sum / 2.0), cap)
+
+
+def _mis_keeps_everything(d, lo, hi):
+    return float(np.sum(np.exp(d))), int(d.shape[0])
+
+
 MUTATIONS = [
     ("temperature after softmax", ol, "lse_stats", _lse_after_softmax, ["pin_v8_temperature"]),
     ("no max shift", ol, "lse_stats", _lse_no_shift, ["pin_large_logits"]),
@@ -135,6 +163,14 @@ MUTATIONS = [
     ("k3 by exp(d)-1-d (cancellation)", oc, "_k3_terms", _k3_naive, ["pin_k3_closed_form"]),
     ("TIS ratio inverted (A - C)", oc, "_tis_weights", _tis_reversed, ["pin_fig1_split"]),
     ("TIS without the cap", oc, "_tis_weights", _tis_no_clip, ["pin_tis_clip"]),
+    ("quantile by nearest rank", od, "quantile_linear", _quantile_nearest,
+     ["pin_quantile_definition", "pin_diag_quantiles_in_sequence"]),
+    ("quantile index n q", od, "quantile_linear", _quantile_n_not_n_minus_1,
+     ["pin_quantile_definition"]),
+    ("probability MAE on logprobs", od, "_prob_mae", _prob_mae_in_logs,
+     ["pin_diag_page_probability_mae"]),
+    ("sequence TIS from a mean", od, "_seq_tis", _seq_tis_mean_not_sum, ["pin_diag_fig1_sequence"]),
+    ("MIS keeps every token", od, "_mis", _mis_keeps_everything, ["pin_diag_mis_and_flips"]),
 ]
 
 
