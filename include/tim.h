@@ -242,6 +242,69 @@ tim_status tim_compare(const float *lp_gen, const float *lp_replay, const float 
                        void *workspace, size_t workspace_bytes, tim_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * Extended per-sequence diagnostics.
+ *
+ * Same score sets, sequences, masks and pair order as tim_compare.  With
+ * d = double(C) - double(A) per active token, each sequence gets:
+ *   abs_q50/abs_q95/abs_q99[p]  quantiles of |left - right| for pair p,
+ *       linear interpolation between order statistics: h = (n-1) q,
+ *       Q = x[floor h] + (h - floor h) (x[floor h + 1] - x[floor h])
+ *       ("Diagnosing Training Inference Mismatch in LLM Reinforcement Learning",
+ *       5. practical indicators: abs(delta_logprob) p50/p95/p99/max);
+ *   prob_mae[p]     mean |exp(left) - exp(right)| ("Fault localization and
+ *       mismatch bisect", Metric measurement basis: probability_mae);
+ *   top1_flips[p]   active tokens whose top-1 ids differ (practical indicators:
+ *       top-1 flip rate), -1 unless both top-1 arrays of the pair are given;
+ *   log_ratio_sum = sum d, k1_sum = -sum d, k3_sum = sum(expm1(d) - d)
+ *       (sequence rejection by sum_t K1 / K3 of the correction ratio,
+ *       "Diagnosing ...", 3. TIS);
+ *   seq_tis = cap if sum d > ln(cap) else exp(sum d) (sequence TIS, same section);
+ *   ratio_err_mean = mean |exp(d) - 1| (practical indicators: PPO ratio error);
+ *   mis_mean = mean of w 1[mis_lo <= w <= mis_hi] with w = exp(d), the interval
+ *       test taken as ln(mis_lo) <= d <= ln(mis_hi); mis_kept = tokens inside
+ *       ("Rollout-Training Mismatch in LLM RL", section 2.1, w_MIS);
+ *   w2_mean = mean exp(2 d) (E_q[w^2] = exp D_2(p||q), same page, section 5.3).
+ * Quantiles need at most TIM_DIAG_QUANTILE_MAX_TOKENS active tokens in a
+ * sequence; longer sequences get NaN quantiles and TIM_SEQ_QUANTILE_SKIPPED.
+ * Flags and errors as for tim_compare.
+ *
+ * Arguments: those of tim_compare, plus top1_gen / top1_replay / top1_train
+ * (int32 [T] device arrays or NULL), mis_lo / mis_hi (finite,
+ * 0 < mis_lo <= mis_hi), out_diag (tim_seq_diag [n_seq], device memory).
+ * The workspace holds only the status word (tim_compare_diag_workspace_size).
+ * ------------------------------------------------------------------------ */
+#define TIM_SEQ_QUANTILE_SKIPPED 32
+#define TIM_DIAG_QUANTILE_MAX_TOKENS 16384
+
+typedef struct tim_seq_diag {
+  int64_t n_valid;
+  double abs_q50[3];
+  double abs_q95[3];
+  double abs_q99[3];
+  double prob_mae[3];
+  int64_t top1_flips[3];
+  double log_ratio_sum;
+  double k1_sum;
+  double k3_sum;
+  double seq_tis;
+  double ratio_err_mean;
+  double mis_mean;
+  int64_t mis_kept;
+  double w2_mean;
+  int32_t flags;
+  int32_t reserved;
+} tim_seq_diag;
+
+size_t tim_compare_diag_workspace_size(int64_t T, int32_t n_seq);
+
+tim_status tim_compare_diag(const float *lp_gen, const float *lp_replay, const float *lp_train,
+                            const int32_t *top1_gen, const int32_t *top1_replay,
+                            const int32_t *top1_train, const int64_t *seq_offsets,
+                            int32_t n_seq, const uint8_t *mask, int64_t T, float tis_cap,
+                            float mis_lo, float mis_hi, tim_seq_diag *out_diag, void *workspace,
+                            size_t workspace_bytes, tim_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * tim_logprob without a caller-supplied workspace.
  *
  * The pages have no counterpart to this entry point; it exists for callers

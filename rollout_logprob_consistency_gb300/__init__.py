@@ -5,6 +5,7 @@ The compute runs in ``libtim.so`` (hand-written CUDA for sm_103a, C ABI in
 ``rollout_logprob_consistency_gb300.build.build()``.
 """
 from .binding import (  # noqa: F401
-    TimError, Workspace, compare, compare_workspace_size, lib, logprob, logprob_stages,
-    logprob_workspace_size, stats_to_dicts, SEQ_STATS_DTYPE, STATUS, STATUS_NAMES,
+    TimError, Workspace, compare, compare_diag, compare_workspace_size, diag_to_dicts, lib,
+    logprob, logprob_stages, logprob_workspace_size, stats_to_dicts, SEQ_DIAG_DTYPE,
+    SEQ_STATS_DTYPE, STATUS, STATUS_NAMES,
 )

@@ -36,6 +36,16 @@ SEQ_STATS_DTYPE = np.dtype([("n_valid", "<i8"), ("pair", PAIR_DTYPE, (3,)),
                             ("tis_clipped", "<i8"), ("flags", "<i4"), ("reserved", "<i4")])
 assert SEQ_STATS_DTYPE.itemsize == 208
 
+SEQ_QUANTILE_SKIPPED = 32
+# numpy mirror of struct tim_seq_diag (200 bytes)
+SEQ_DIAG_DTYPE = np.dtype([("n_valid", "<i8"), ("abs_q50", "<f8", (3,)), ("abs_q95", "<f8", (3,)),
+                           ("abs_q99", "<f8", (3,)), ("prob_mae", "<f8", (3,)),
+                           ("top1_flips", "<i8", (3,)), ("log_ratio_sum", "<f8"),
+                           ("k1_sum", "<f8"), ("k3_sum", "<f8"), ("seq_tis", "<f8"),
+                           ("ratio_err_mean", "<f8"), ("mis_mean", "<f8"), ("mis_kept", "<i8"),
+                           ("w2_mean", "<f8"), ("flags", "<i4"), ("reserved", "<i4")])
+assert SEQ_DIAG_DTYPE.itemsize == 200
+
 
 class TimError(RuntimeError):
     def __init__(self, code: int, where: str):
@@ -61,6 +71,9 @@ _SIGNATURES = {
     "tim_compare_workspace_size": (_sz, [_i64, _i32]),
     "tim_compare": (_c.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i64, _f32, _vp, _vp, _vp, _sz,
                                _vp]),
+    "tim_compare_diag_workspace_size": (_sz, [_i64, _i32]),
+    "tim_compare_diag": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i64, _f32,
+                                    _f32, _f32, _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -263,6 +276,64 @@ def compare(lp_gen, lp_replay, lp_train, seq_offsets, mask, tis_cap: float, *, o
         host = out_stats.cpu().numpy().view(SEQ_STATS_DTYPE)
         return host, out_tis_w
     return out_stats, out_tis_w
+
+
+def compare_diag(lp_gen, lp_replay, lp_train, seq_offsets, mask, tis_cap: float,
+                 mis_lo: float, mis_hi: float, top1=(None, None, None), *, out=None,
+                 workspace: Optional[Workspace] = None, stream=None, check: bool = True,
+                 to_host: bool = True):
+    """Extended per-sequence diagnostics with tim_compare_diag.
+
+    top1 = (top1_gen, top1_replay, top1_train), each an int32 [T] CUDA tensor or None.
+    Returns a numpy structured array (SEQ_DIAG_DTYPE) when ``to_host`` else the raw
+    device buffer.
+    """
+    torch = _torch()
+    for t, n in ((lp_gen, "lp_gen"), (lp_replay, "lp_replay"), (lp_train, "lp_train")):
+        _need(t, torch.float32, n, 1)
+    _need(seq_offsets, torch.int64, "seq_offsets", 1)
+    _need(mask, torch.uint8, "mask", 1)
+    tops = []
+    for t, n in zip(top1, ("top1_gen", "top1_replay", "top1_train")):
+        if t is not None:
+            _need(t, torch.int32, n, 1)
+        tops.append(None if t is None else _ptr(t))
+    T = lp_gen.shape[0]
+    S = seq_offsets.shape[0] - 1
+    if lp_replay.shape[0] != T or lp_train.shape[0] != T or mask.shape[0] != T or S < 1:
+        raise ValueError("shape mismatch")
+    dev = lp_gen.device
+    if out is None:
+        out = torch.empty(S * SEQ_DIAG_DTYPE.itemsize, dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = Workspace(int(lib().tim_compare_diag_workspace_size(T, S)), dev, stream)
+    code = lib().tim_compare_diag(_ptr(lp_gen), _ptr(lp_replay), _ptr(lp_train), tops[0], tops[1],
+                                  tops[2], _ptr(seq_offsets), S, _ptr(mask), T, float(tis_cap),
+                                  float(mis_lo), float(mis_hi), _ptr(out), workspace.ptr,
+                                  workspace.nbytes, _stream_ptr(stream))
+    _check(code, "tim_compare_diag")
+    if check:
+        workspace.check("tim_compare_diag", stream)
+    if to_host:
+        return out.cpu().numpy().view(SEQ_DIAG_DTYPE)
+    return out
+
+
+def diag_to_dicts(arr) -> list:
+    """Structured diag array -> list of dicts shaped like the oracle's."""
+    keys3 = ("abs_q50", "abs_q95", "abs_q99", "prob_mae")
+    out = []
+    for r in arr:
+        dct = {k: [float(v) for v in r[k]] for k in keys3}
+        dct["top1_flips"] = [int(v) for v in r["top1_flips"]]
+        for k in ("log_ratio_sum", "k1_sum", "k3_sum", "seq_tis", "ratio_err_mean", "mis_mean",
+                  "w2_mean"):
+            dct[k] = float(r[k])
+        dct["n_valid"] = int(r["n_valid"])
+        dct["mis_kept"] = int(r["mis_kept"])
+        dct["flags"] = int(r["flags"])
+        out.append(dct)
+    return out
 
 
 def stats_to_dicts(arr) -> list:

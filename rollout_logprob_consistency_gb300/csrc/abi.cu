@@ -20,6 +20,10 @@ cudaError_t launch_seg_compare(const float* A, const float* B, const float* C,
                                float tis_cap, tim_seq_stats* out, float* tis_w, void* workspace,
                                cudaStream_t stream);
 size_t compare_workspace_bytes(int64_t T, int n_seq);
+cudaError_t launch_seg_diag(const float* A, const float* B, const float* C, const int32_t* tA,
+                            const int32_t* tB, const int32_t* tC, const int64_t* offs, int n_seq,
+                            const uint8_t* mask, int64_t T, float tis_cap, float mis_lo,
+                            float mis_hi, tim_seq_diag* out, int* status, cudaStream_t stream);
 
 namespace {
 
@@ -233,6 +237,40 @@ tim_status tim_compare(const float* lp_gen, const float* lp_replay, const float*
   return from_cuda(launch_seg_compare(lp_gen, lp_replay, lp_train, seq_offsets, n_seq, mask, T,
                                       tis_cap, out_stats, out_tis_w, workspace,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t tim_compare_diag_workspace_size(int64_t T, int32_t n_seq) {
+  if (T < 1 || n_seq < 1) return 0;
+  return 1024;
+}
+
+tim_status tim_compare_diag(const float* lp_gen, const float* lp_replay, const float* lp_train,
+                            const int32_t* top1_gen, const int32_t* top1_replay,
+                            const int32_t* top1_train, const int64_t* seq_offsets, int32_t n_seq,
+                            const uint8_t* mask, int64_t T, float tis_cap, float mis_lo,
+                            float mis_hi, tim_seq_diag* out_diag, void* workspace,
+                            size_t workspace_bytes, tim_stream_t stream) {
+  if (lp_gen == nullptr || lp_replay == nullptr || lp_train == nullptr || seq_offsets == nullptr ||
+      mask == nullptr || out_diag == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!aligned(lp_gen, 4) || !aligned(lp_replay, 4) || !aligned(lp_train, 4) ||
+      !aligned(seq_offsets, 8) || !aligned(out_diag, 8) ||
+      (top1_gen != nullptr && !aligned(top1_gen, 4)) ||
+      (top1_replay != nullptr && !aligned(top1_replay, 4)) ||
+      (top1_train != nullptr && !aligned(top1_train, 4)))
+    return TIM_ERR_INVALID_ARG;
+  if (T < 1 || n_seq < 1) return TIM_ERR_SHAPE;
+  if (!(std::isfinite(tis_cap) && tis_cap > 0.f)) return TIM_ERR_INVALID_ARG;
+  if (!(std::isfinite(mis_lo) && std::isfinite(mis_hi) && mis_lo > 0.f && mis_lo <= mis_hi))
+    return TIM_ERR_INVALID_ARG;
+  tim_status s =
+      check_workspace(workspace, workspace_bytes, tim_compare_diag_workspace_size(T, n_seq));
+  if (s != TIM_OK) return s;
+  if ((s = check_device(nullptr)) != TIM_OK) return s;
+  return from_cuda(launch_seg_diag(lp_gen, lp_replay, lp_train, top1_gen, top1_replay, top1_train,
+                                   seq_offsets, n_seq, mask, T, tis_cap, mis_lo, mis_hi, out_diag,
+                                   static_cast<int*>(workspace),
+                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -78,6 +78,15 @@ def three_way(tim, b, W_train_bits=None, oracle_rows=N_ORACLE_ROWS):
     r, rw = oracle.oracle_compare(A[0], B[0], C[0], b.seq_offsets, b.mask, b.tis_cap)
     assert_compare_parity(gs, r, what=b.name)
     assert_tis_parity(w.cpu().numpy(), rw, covered_rows(b.seq_offsets, b.T))
+    # extended diagnostics on the same arrays, with the top-1 ids of each score set
+    from test_gpu_diag import assert_diag_parity, d_abs
+    tops = (cuda_tensor(A[2]), cuda_tensor(B[2]), cuda_tensor(C[2]))
+    gd = tim.diag_to_dicts(tim.compare_diag(
+        cuda_tensor(A[0]), cuda_tensor(B[0]), cuda_tensor(C[0]), cuda_tensor(b.seq_offsets),
+        cuda_tensor(b.mask), b.tis_cap, 0.5, 2.0, top1=tops))
+    rd = oracle.oracle_diag(A[0], B[0], C[0], b.seq_offsets, b.mask, b.tis_cap, 0.5, 2.0,
+                            (A[2], B[2], C[2]))
+    assert_diag_parity(gd, rd, d_abs(A[0], C[0], b.seq_offsets, b.mask), what=b.name)
     for st in gs:  # A and B agree bitwise: same-version term is exactly zero
         assert st["pair"][0]["mismatch_count"] == 0 and st["mean_same_version"] == 0.0
         lhs = st["mean_log_ratio"]
