@@ -242,6 +242,49 @@ tim_status tim_compare(const float *lp_gen, const float *lp_replay, const float 
                        void *workspace, size_t workspace_bytes, tim_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * Vocabulary-parallel linear logprob.
+ *
+ * "Debugging Logprob Mismatches in LLM Reinforcement Learning", Collect A/B
+ * and C in Your Own Run: with a vocabulary-parallel LM head the normaliser
+ * must run over all shards together; "Training and rollout stop disagreeing:
+ * vime and RL-Kernel ...", Interpretation: cross-rank LSE merge, fixed rank
+ * reduction order.
+ *
+ * The vocabulary is split over G ranks (G = 1, 2, 4, 8 or 16) along the 16
+ * fixed merge ranges of tim_lse_finalize: rank g owns global ids
+ * [v0, v0 + v_len) from tim_vocab_shard (whole 256-column tiles; the last
+ * shards may be empty for small V).  Rank g calls tim_logprob_shard with its
+ * W rows; the callers all-gather the per-row records (16 bytes) and target
+ * logits (4 bytes) into [G][T] arrays in rank order; every rank then calls
+ * tim_logprob_merge_shards.  The outputs are bitwise identical to
+ * tim_logprob's on the full W for every G.
+ *
+ * tim_logprob_shard arguments: hidden, gamma, token_ids, T, d, temperature and
+ *   eps as for tim_logprob; V = the FULL vocabulary size; W_shard = bf16
+ *   [v_len, d] rows v0 .. v0+v_len-1 of W (may be NULL when v_len = 0, in
+ *   which case nothing is enqueued); out_rec = 16-byte records [T] (16-byte
+ *   aligned); out_tgt = float32 [T] (the target's scaled logit, meaningful on
+ *   the rank that owns the target id); workspace of
+ *   tim_logprob_shard_workspace_size bytes.
+ * tim_logprob_merge_shards arguments: recs = [G][T] records, tgts = [G][T]
+ *   float32, token_ids [T], T, V (full), G; outputs as tim_logprob; workspace
+ *   of tim_logprob_merge_workspace_size bytes (status word: token range,
+ *   non-finite lse).
+ * ------------------------------------------------------------------------ */
+tim_status tim_vocab_shard(int32_t V, int32_t G, int32_t g, int32_t *v0, int32_t *v_len);
+size_t tim_logprob_shard_workspace_size(int64_t T, int32_t d, int32_t V, int32_t G, int32_t g);
+tim_status tim_logprob_shard(const void *hidden, const void *gamma, const void *W_shard,
+                             const int32_t *token_ids, int64_t T, int32_t d, int32_t V,
+                             int32_t G, int32_t g, float temperature, float eps, void *out_rec,
+                             float *out_tgt, void *workspace, size_t workspace_bytes,
+                             tim_stream_t stream);
+size_t tim_logprob_merge_workspace_size(int64_t T);
+tim_status tim_logprob_merge_shards(const void *recs, const float *tgts, const int32_t *token_ids,
+                                    int64_t T, int32_t V, int32_t G, float *out_logprob,
+                                    float *out_lse, int32_t *out_top1, void *workspace,
+                                    size_t workspace_bytes, tim_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * Extended per-sequence diagnostics.
  *
  * Same score sets, sequences, masks and pair order as tim_compare.  With

@@ -7,5 +7,6 @@ The compute runs in ``libtim.so`` (hand-written CUDA for sm_103a, C ABI in
 from .binding import (  # noqa: F401
     TimError, Workspace, compare, compare_diag, compare_workspace_size, diag_to_dicts, lib,
     logprob, logprob_stages, logprob_workspace_size, stats_to_dicts, SEQ_DIAG_DTYPE,
-    SEQ_STATS_DTYPE, STATUS, STATUS_NAMES,
+    SEQ_STATS_DTYPE, STATUS, STATUS_NAMES, vocab_shard, logprob_shard, logprob_merge_shards,
+    gather_shard_records, logprob_vocab_parallel, logprob_vocab_parallel_emulated,
 )

@@ -72,6 +72,13 @@ _SIGNATURES = {
     "tim_compare": (_c.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i64, _f32, _vp, _vp, _vp, _sz,
                                _vp]),
     "tim_compare_diag_workspace_size": (_sz, [_i64, _i32]),
+    "tim_vocab_shard": (_c.c_int, [_i32, _i32, _i32, _c.POINTER(_i32), _c.POINTER(_i32)]),
+    "tim_logprob_shard_workspace_size": (_sz, [_i64, _i32, _i32, _i32, _i32]),
+    "tim_logprob_shard": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _f32, _f32,
+                                     _vp, _vp, _vp, _sz, _vp]),
+    "tim_logprob_merge_workspace_size": (_sz, [_i64]),
+    "tim_logprob_merge_shards": (_c.c_int, [_vp, _vp, _vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp,
+                                            _sz, _vp]),
     "tim_compare_diag": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i64, _f32,
                                     _f32, _f32, _vp, _vp, _sz, _vp]),
 }
@@ -334,6 +341,110 @@ def diag_to_dicts(arr) -> list:
         dct["flags"] = int(r["flags"])
         out.append(dct)
     return out
+
+
+# ----------------------------------------------------------------------------- vocab-parallel
+
+def vocab_shard(V: int, G: int, g: int):
+    """(v0, v_len) of rank g's vocabulary ids when V is split over G ranks."""
+    v0, n = _c.c_int32(0), _c.c_int32(0)
+    _check(lib().tim_vocab_shard(int(V), int(G), int(g), _c.byref(v0), _c.byref(n)),
+           "tim_vocab_shard")
+    return int(v0.value), int(n.value)
+
+
+def logprob_shard(hidden, gamma, W_shard, token_ids, V: int, G: int, g: int, temperature: float,
+                  eps: float, *, workspace: Optional[Workspace] = None, stream=None,
+                  check: bool = True):
+    """Rank g's part of the vocabulary-parallel score: returns (records float32 [T, 4],
+    target logits float32 [T]) for the all-gather."""
+    torch = _torch()
+    hidden = _as_bf16(hidden, "hidden")
+    gamma = _as_bf16(gamma, "gamma")
+    if W_shard is not None:
+        W_shard = _as_bf16(W_shard, "W_shard")
+    _need(token_ids, torch.int32, "token_ids", 1)
+    T, d = hidden.shape
+    dev = hidden.device
+    rec = torch.empty(T, 4, dtype=torch.float32, device=dev)
+    tgt = torch.empty(T, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = Workspace(int(lib().tim_logprob_shard_workspace_size(T, d, V, G, g)), dev,
+                              stream)
+    code = lib().tim_logprob_shard(_ptr(hidden), _ptr(gamma),
+                                   None if W_shard is None else _ptr(W_shard), _ptr(token_ids), T,
+                                   d, int(V), int(G), int(g), float(temperature), float(eps),
+                                   _ptr(rec), _ptr(tgt), workspace.ptr, workspace.nbytes,
+                                   _stream_ptr(stream))
+    _check(code, "tim_logprob_shard")
+    if check:
+        workspace.check("tim_logprob_shard", stream)
+    return rec, tgt
+
+
+def logprob_merge_shards(recs, tgts, token_ids, V: int, *, out=None,
+                         workspace: Optional[Workspace] = None, stream=None, check: bool = True):
+    """Merge [G, T, 4] records and [G, T] target logits (rank order) into
+    (logprob, lse, top1)."""
+    torch = _torch()
+    _need(recs, torch.float32, "recs", 3)
+    _need(tgts, torch.float32, "tgts", 2)
+    _need(token_ids, torch.int32, "token_ids", 1)
+    G, T, _ = recs.shape
+    dev = recs.device
+    if out is None:
+        out = (torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = Workspace(int(lib().tim_logprob_merge_workspace_size(T)), dev, stream)
+    code = lib().tim_logprob_merge_shards(_ptr(recs), _ptr(tgts), _ptr(token_ids), T, int(V),
+                                          int(G), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                                          workspace.ptr, workspace.nbytes, _stream_ptr(stream))
+    _check(code, "tim_logprob_merge_shards")
+    if check:
+        workspace.check("tim_logprob_merge_shards", stream)
+    return out
+
+
+def gather_shard_records(rec, tgt, group=None):
+    """All-gather every rank's (records [T, 4], targets [T]) into [G, T, 4] and [G, T] in
+    rank order (the one exchange step of the vocabulary-parallel path)."""
+    import torch.distributed as dist
+    G = dist.get_world_size(group)
+    recs = [rec.new_empty(rec.shape) for _ in range(G)]
+    tgts = [tgt.new_empty(tgt.shape) for _ in range(G)]
+    dist.all_gather(recs, rec.contiguous(), group=group)
+    dist.all_gather(tgts, tgt.contiguous(), group=group)
+    torch = _torch()
+    return torch.stack(recs), torch.stack(tgts)
+
+
+def logprob_vocab_parallel(hidden, gamma, W_shard, token_ids, V: int, temperature: float,
+                           eps: float, group=None):
+    """Vocabulary-parallel tim_logprob across the ranks of ``group`` (one GPU per rank,
+    rank g holding W rows vocab_shard(V, G, g)); returns the same bits as tim_logprob."""
+    import torch.distributed as dist
+    G, g = dist.get_world_size(group), dist.get_rank(group)
+    rec, tgt = logprob_shard(hidden, gamma, W_shard, token_ids, V, G, g, temperature, eps)
+    recs, tgts = gather_shard_records(rec, tgt, group)
+    return logprob_merge_shards(recs, tgts, token_ids, V)
+
+
+def logprob_vocab_parallel_emulated(hidden, gamma, W, token_ids, G: int, temperature: float,
+                                    eps: float):
+    """The vocabulary-parallel path with G shards run one after another on this GPU."""
+    torch = _torch()
+    W = _as_bf16(W, "W")
+    V = W.shape[0]
+    recs, tgts = [], []
+    for g in range(G):
+        v0, n = vocab_shard(V, G, g)
+        rec, tgt = logprob_shard(hidden, gamma, W[v0:v0 + n] if n else None, token_ids, V, G, g,
+                                 temperature, eps)
+        recs.append(rec)
+        tgts.append(tgt)
+    return logprob_merge_shards(torch.stack(recs), torch.stack(tgts), token_ids, V)
 
 
 def stats_to_dicts(arr) -> list:

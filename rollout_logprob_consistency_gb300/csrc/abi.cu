@@ -20,6 +20,15 @@ cudaError_t launch_seg_compare(const float* A, const float* B, const float* C,
                                float tis_cap, tim_seq_stats* out, float* tis_w, void* workspace,
                                cudaStream_t stream);
 size_t compare_workspace_bytes(int64_t T, int n_seq);
+cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t* ids, int64_t T,
+                                    int d, int V, int v0, float temperature, void* part,
+                                    float* tgt, int* status, cudaStream_t stream, int num_sms);
+void vocab_shard_range(int V, int G, int g, int* v0, int* v_len);
+cudaError_t launch_shard_reduce(const void* part, const float* tgt, int64_t T, int V, int G, int g,
+                                int v_len, void* out_rec, float* out_tgt, cudaStream_t stream);
+cudaError_t launch_merge_shards(const void* recs, const float* tgts, const int32_t* ids, int64_t T,
+                                int V, int G, float* out_lp, float* out_lse, int32_t* out_top1,
+                                int* status, cudaStream_t stream);
 cudaError_t launch_seg_diag(const float* A, const float* B, const float* C, const int32_t* tA,
                             const int32_t* tB, const int32_t* tC, const int64_t* offs, int n_seq,
                             const uint8_t* mask, int64_t T, float tis_cap, float mis_lo,
@@ -90,6 +99,10 @@ tim_status validate_logprob_common(int64_t T, int32_t d, int32_t V, float temper
   if (s != TIM_OK) return s;
   if ((s = check_scalars(temperature, eps)) != TIM_OK) return s;
   return check_workspace(ws, ws_bytes, logprob_layout(T, d, V).total);
+}
+
+bool valid_shard(int32_t G, int32_t g) {
+  return (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) && g >= 0 && g < G;
 }
 
 }  // namespace
@@ -237,6 +250,79 @@ tim_status tim_compare(const float* lp_gen, const float* lp_replay, const float*
   return from_cuda(launch_seg_compare(lp_gen, lp_replay, lp_train, seq_offsets, n_seq, mask, T,
                                       tis_cap, out_stats, out_tis_w, workspace,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tim_status tim_vocab_shard(int32_t V, int32_t G, int32_t g, int32_t* v0, int32_t* v_len) {
+  if (v0 == nullptr || v_len == nullptr || !valid_shard(G, g)) return TIM_ERR_INVALID_ARG;
+  if (V < 1 || V > INT32_MAX - 256) return TIM_ERR_SHAPE;
+  int a = 0, n = 0;
+  vocab_shard_range(V, G, g, &a, &n);
+  *v0 = a;
+  *v_len = n;
+  return TIM_OK;
+}
+
+size_t tim_logprob_shard_workspace_size(int64_t T, int32_t d, int32_t V, int32_t G, int32_t g) {
+  if (check_shape(T, d, V) != TIM_OK || !valid_shard(G, g)) return 0;
+  int v0 = 0, v_len = 0;
+  vocab_shard_range(V, G, g, &v0, &v_len);
+  return logprob_layout(T, d, v_len > 0 ? v_len : 1).total;
+}
+
+tim_status tim_logprob_shard(const void* hidden, const void* gamma, const void* W_shard,
+                             const int32_t* token_ids, int64_t T, int32_t d, int32_t V,
+                             int32_t G, int32_t g, float temperature, float eps, void* out_rec,
+                             float* out_tgt, void* workspace, size_t workspace_bytes,
+                             tim_stream_t stream) {
+  if (hidden == nullptr || gamma == nullptr || token_ids == nullptr || out_rec == nullptr ||
+      out_tgt == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!valid_shard(G, g)) return TIM_ERR_INVALID_ARG;
+  tim_status s = check_shape(T, d, V);
+  if (s != TIM_OK) return s;
+  if ((s = check_scalars(temperature, eps)) != TIM_OK) return s;
+  int v0 = 0, v_len = 0;
+  vocab_shard_range(V, G, g, &v0, &v_len);
+  if (v_len > 0 && W_shard == nullptr) return TIM_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(gamma, 16) || (W_shard != nullptr && !aligned(W_shard, 16)) ||
+      !aligned(token_ids, 4) || !aligned(out_rec, 16) || !aligned(out_tgt, 4))
+    return TIM_ERR_INVALID_ARG;
+  if ((s = check_workspace(workspace, workspace_bytes,
+                           tim_logprob_shard_workspace_size(T, d, V, G, g))) != TIM_OK)
+    return s;
+  int sms = 0;
+  if ((s = check_device(&sms)) != TIM_OK) return s;
+  if (v_len == 0) return TIM_OK;  // this rank owns no vocabulary: its records are never read
+  const Ptrs p = logprob_ptrs(workspace, T, d, v_len);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_rmsnorm_rows(hidden, gamma, T, d, eps, p.y, p.status, st) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  if (launch_lmhead_lse_shard(p.y, W_shard, token_ids, T, d, v_len, v0, temperature, p.part,
+                              p.tgt, p.status, st, sms) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  return from_cuda(launch_shard_reduce(p.part, p.tgt, T, V, G, g, v_len, out_rec, out_tgt, st));
+}
+
+size_t tim_logprob_merge_workspace_size(int64_t T) { return T < 1 ? 0 : 1024; }
+
+tim_status tim_logprob_merge_shards(const void* recs, const float* tgts, const int32_t* token_ids,
+                                    int64_t T, int32_t V, int32_t G, float* out_logprob,
+                                    float* out_lse, int32_t* out_top1, void* workspace,
+                                    size_t workspace_bytes, tim_stream_t stream) {
+  if (recs == nullptr || tgts == nullptr || token_ids == nullptr || out_logprob == nullptr ||
+      out_lse == nullptr || out_top1 == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!valid_shard(G, 0)) return TIM_ERR_INVALID_ARG;
+  if (!aligned(recs, 16) || !aligned(tgts, 4) || !aligned(token_ids, 4) ||
+      !aligned(out_logprob, 4) || !aligned(out_lse, 4) || !aligned(out_top1, 4))
+    return TIM_ERR_INVALID_ARG;
+  if (T < 1 || T > INT32_MAX || V < 1 || V > INT32_MAX - 256) return TIM_ERR_SHAPE;
+  tim_status s = check_workspace(workspace, workspace_bytes, tim_logprob_merge_workspace_size(T));
+  if (s != TIM_OK) return s;
+  if ((s = check_device(nullptr)) != TIM_OK) return s;
+  return from_cuda(launch_merge_shards(recs, tgts, token_ids, T, V, G, out_logprob, out_lse,
+                                       out_top1, static_cast<int*>(workspace),
+                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t tim_compare_diag_workspace_size(int64_t T, int32_t n_seq) {

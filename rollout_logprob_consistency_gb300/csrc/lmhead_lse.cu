@@ -49,7 +49,8 @@ namespace tim {
 
 struct GemmArgs {
   int64_t T;
-  int V;
+  int v0;     // global vocabulary id of W row 0 (0 unless W is a vocabulary shard)
+  int v_end;  // global end (exclusive) of the vocabulary columns this launch scores
   int d;
   int num_m;
   int num_n;
@@ -274,7 +275,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tile_coords(tile, a, m, n);
       const int64_t row = static_cast<int64_t>(m) * kBM + q * 32 + lane;
       const int x = (row < a.T) ? __ldg(a.ids + row) : -1;
-      const int col_base = n * kBN;
+      const int col_base = a.v0 + n * kBN;  // global vocabulary id of the tile's column 0
       const int rel = x - col_base;
 
       int ok = 1;
@@ -293,10 +294,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < kBN / 32; ++c) {
         const int col0 = col_base + c * 32;
-        if (col0 >= a.V) break;  // warp-uniform
+        if (col0 >= a.v_end) break;  // warp-uniform
         uint32_t r[32];
         tmem_ld32(tbase + c * 32, r);
-        const int nvalid = min(32, a.V - col0);
+        const int nvalid = min(32, a.v_end - col0);
         if (nvalid == 32)
           epilogue_chunk<false>(r, 32, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
         else
@@ -371,9 +372,11 @@ static bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t rows, u
   return r == CUDA_SUCCESS;
 }
 
-cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T,
-                              int d, int V, float temperature, void* part, float* tgt,
-                              int* status, cudaStream_t stream, int num_sms) {
+// W holds V vocabulary rows whose global ids start at v0 (a vocabulary shard when
+// v0 > 0 or V is not the whole vocabulary); records are written per local tile.
+cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t* ids, int64_t T,
+                                    int d, int V, int v0, float temperature, void* part,
+                                    float* tgt, int* status, cudaStream_t stream, int num_sms) {
   CUtensorMap map_y, map_w;
   if (!make_kmajor_map(&map_y, y, static_cast<uint64_t>(rows_padded(T)),
                        static_cast<uint64_t>(d), kBM) ||
@@ -382,7 +385,8 @@ cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, 
 
   GemmArgs a;
   a.T = T;
-  a.V = V;
+  a.v0 = v0;
+  a.v_end = v0 + V;
   a.d = d;
   a.num_m = static_cast<int>((T + kBM - 1) / kBM);
   a.num_n = (V + kBN - 1) / kBN;
@@ -415,6 +419,13 @@ cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, lmhead_lse_kernel, map_y, map_w, a);
+}
+
+cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T,
+                              int d, int V, float temperature, void* part, float* tgt,
+                              int* status, cudaStream_t stream, int num_sms) {
+  return launch_lmhead_lse_shard(y, W, ids, T, d, V, 0, temperature, part, tgt, status, stream,
+                                 num_sms);
 }
 
 }  // namespace tim
