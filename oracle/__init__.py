@@ -14,6 +14,7 @@ Modules
                     with z = bf16(RMSNorm(h)) . W^T, plus lse and top-1.
 ``oracle.compare``  per-sequence A/B/C mismatch statistics, k3, TIS weights,
                     and the single-pair ``compare`` summary.
+``oracle.processed`` the processed (top-k, then top-p) selected-token logprob.
 ``oracle.diag``     extended per-sequence diagnostics: |delta| quantiles,
                     probability MAE, top-1 flips, sequence TIS, K1/K3 sums,
                     ratio error, MIS weights, mean w^2.
@@ -32,6 +33,7 @@ from .compare import (  # noqa: F401
     FLAG_K3_OVERFLOW, PAIRS, oracle_compare, oracle_compare_lenient, compare_summary,
     compare_bitwise,
 )
+from .processed import oracle_processed_logprob, process_row  # noqa: F401
 from .diag import (  # noqa: F401
     FLAG_QUANTILE_SKIPPED, QUANTILE_MAX_TOKENS, QUANTILES, oracle_diag, oracle_diag_lenient,
     quantile_linear,

@@ -670,4 +670,78 @@ def pin_diag_quantile_limit():
     assert st["n_valid"] == n and st["k3_sum"] == 0.0
 
 
+# ---------------------------------------------------------------------------
+# processed (top-k / top-p) logprob pins
+
+def _proc(z_targets, x, tau, k, p):
+    h, g, W, _ = exact_logit_head(z_targets)
+    return oracle.oracle_processed_logprob(h, g, W, np.array([x], np.int32), tau, 0.0, k, p)
+
+
+def pin_processed_page_topk():
+    """Top-k with k = 2 turns (0.50, 0.30, 0.20) into (0.625, 0.375, 0) (Debugging page,
+    Make Sure Both Scores Describe the Same Probability)."""
+    gd = golden("topk_renormalisation.json")
+    z = [math.log(v) for v in gd["probs"]]
+    for x, want in enumerate(gd["renormalised"]):
+        out = _proc(z, x, 1.0, gd["k"], 1.0)
+        if want == 0.0:
+            assert out["logprob"][0] == -math.inf
+        else:
+            assert abs(out["logprob"][0] - math.log(want)) < 1e-12
+        assert out["kept"][0] == 2
+    assert abs(_proc(z, 0, 1.0, 2, 1.0)["lse_kept"][0] - math.log(0.8)) < 1e-12
+
+
+def pin_processed_top_p_boundary():
+    """Top-p on (0.5, 0.3, 0.2): p = 0.7 keeps {0, 1} (the prefix reaching 0.8 >= 0.7),
+    p = 0.81 keeps all three, p = 0.4 keeps only token 0."""
+    z = [math.log(0.5), math.log(0.3), math.log(0.2)]
+    o = _proc(z, 1, 1.0, 3, 0.7)
+    assert o["kept"][0] == 2 and abs(o["logprob"][0] - math.log(0.375)) < 1e-12
+    assert _proc(z, 2, 1.0, 3, 0.7)["logprob"][0] == -math.inf
+    o = _proc(z, 2, 1.0, 3, 0.81)
+    assert o["kept"][0] == 3 and abs(o["logprob"][0] - math.log(0.2)) < 1e-12
+    o = _proc(z, 0, 1.0, 3, 0.4)
+    assert o["kept"][0] == 1 and o["logprob"][0] == 0.0
+
+
+def pin_processed_ties_and_temperature():
+    """Equal logits at the top-k cut keep the lower ids; temperature is applied before
+    filtering: on z = (0, 1, 2, 3) with tau = 0.5, k = 2 the kept scores are 6 - lse, 4 - lse
+    with lse = ln(e^6 + e^4)."""
+    o = _proc([1.0, 1.0, 1.0, 0.0], 1, 1.0, 2, 1.0)
+    assert abs(o["logprob"][0] - math.log(0.5)) < 1e-12
+    assert _proc([1.0, 1.0, 1.0, 0.0], 2, 1.0, 2, 1.0)["logprob"][0] == -math.inf
+    lse = math.log(math.exp(6.0) + math.exp(4.0))
+    o = _proc([0.0, 1.0, 2.0, 3.0], 2, 0.5, 2, 1.0)
+    assert abs(o["logprob"][0] - (4.0 - lse)) < 1e-12
+    assert abs(o["lse_kept"][0] - lse) < 1e-12
+
+
+def pin_processed_reduces_to_raw():
+    """k = V and p = 1 keep the whole vocabulary: the processed score is the raw score."""
+    b = synth.make_custom(T=12, d=64, V=90, temperature=0.8, tag="proc_raw")
+    raw = oracle.oracle_logprob(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 0.8, b.eps)
+    pr = oracle.oracle_processed_logprob(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 0.8,
+                                         b.eps, 90, 1.0)
+    assert np.max(np.abs(raw["logprob"] - pr["logprob"])) < 1e-12
+    assert np.all(pr["kept"] == 90)
+
+
+def pin_processed_library_topk():
+    """torch.topk + log_softmax on the kept logits (library routines the oracle does not call)."""
+    import torch
+    b = synth.make_custom(T=10, d=128, V=300, temperature=0.7, tag="proc_lib")
+    y = oracle.rmsnorm(oracle.widen_bf16(b.hidden_gen), oracle.widen_bf16(b.head.gamma), b.eps)
+    z = torch.from_numpy(oracle.logits(y, b.head.W))
+    k = 17
+    vals, idx = torch.topk(z, k, dim=1)
+    ls = torch.log_softmax(vals / 0.7, dim=1)
+    ids = idx[:, 3].numpy().astype(np.int32)              # a kept target in every row
+    pr = oracle.oracle_processed_logprob(b.hidden_gen, b.head.gamma, b.head.W, ids, 0.7, b.eps,
+                                         k, 1.0)
+    assert np.max(np.abs(pr["logprob"] - ls[:, 3].numpy())) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -142,6 +142,38 @@ def _mis_keeps_everything(d, lo, hi):
     return float(np.sum(np.exp(d))), int(d.shape[0])
 
 
+import oracle.processed as opr
+
+_orig_process_row = opr.process_row
+
+
+def _proc_cum_inclusive(z, x, temperature, top_k, top_p):
+    V = z.shape[0]
+    order = np.lexsort((np.arange(V), -z))
+    top = order[:min(top_k, V)]
+    s = z[top] / temperature
+    q = np.exp(s - s[0]) / np.sum(np.exp(s - s[0]))
+    keep = np.cumsum(q) < top_p
+    keep[0] = True
+    kept = top[keep]
+    lse = s[0] + math.log(float(np.sum(np.exp(s[keep] - s[0]))))
+    lp = float(z[x] / temperature - lse) if x in set(kept.tolist()) else -math.inf
+    return lp, lse, int(kept.shape[0]), 0.0, 0.0
+
+
+def _proc_no_renorm(z, x, temperature, top_k, top_p):
+    lp, lse, kept, g, m = _orig_process_row(z, x, temperature, top_k, top_p)
+    s = z / temperature
+    full = float(np.max(s) + np.log(np.sum(np.exp(s - np.max(s)))))
+    return (lp if lp == -math.inf else float(s[x] - full)), full, kept, g, m
+
+
+def _proc_ties_high_id(z, x, temperature, top_k, top_p):
+    V = z.shape[0]
+    zz = z.copy()
+    return _orig_process_row(zz[::-1].copy(), V - 1 - x, temperature, top_k, top_p)
+
+
 MUTATIONS = [
     ("temperature after softmax", ol, "lse_stats", _lse_after_softmax, ["pin_v8_temperature"]),
     ("no max shift", ol, "lse_stats", _lse_no_shift, ["pin_large_logits"]),
@@ -171,6 +203,12 @@ MUTATIONS = [
      ["pin_diag_page_probability_mae"]),
     ("sequence TIS from a mean", od, "_seq_tis", _seq_tis_mean_not_sum, ["pin_diag_fig1_sequence"]),
     ("MIS keeps every token", od, "_mis", _mis_keeps_everything, ["pin_diag_mis_and_flips"]),
+    ("top-p cut on inclusive cumulative mass", opr, "process_row", _proc_cum_inclusive,
+     ["pin_processed_top_p_boundary"]),
+    ("processed score not renormalised", opr, "process_row", _proc_no_renorm,
+     ["pin_processed_page_topk"]),
+    ("top-k ties keep the higher ids", opr, "process_row", _proc_ties_high_id,
+     ["pin_processed_ties_and_temperature"]),
 ]
 
 
