@@ -73,7 +73,8 @@ typedef enum tim_status {
   TIM_ERR_WORKSPACE = 7,           /* workspace pointer/size insufficient        */
   TIM_ERR_CUDA = 8,                /* a CUDA runtime/driver call failed          */
   TIM_ERR_TIMEOUT = 9,             /* a bounded device-side wait gave up         */
-  TIM_ERR_UNSUPPORTED_DEVICE = 10  /* current device is not sm_103               */
+  TIM_ERR_UNSUPPORTED_DEVICE = 10, /* current device is not sm_103               */
+  TIM_ERR_CAPACITY = 11            /* a row had more top-k candidates than fit   */
 } tim_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -240,6 +241,43 @@ tim_status tim_compare(const float *lp_gen, const float *lp_replay, const float 
                        const int64_t *seq_offsets, int32_t n_seq, const uint8_t *mask,
                        int64_t T, float tis_cap, tim_seq_stats *out_stats, float *out_tis_w,
                        void *workspace, size_t workspace_bytes, tim_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Processed (top-k, then top-p) selected-token logprob.
+ *
+ * "Debugging Logprob Mismatches in LLM Reinforcement Learning", Make Sure
+ * Both Scores Describe the Same Probability: the sampling score is taken on
+ * the distribution left after the sampler's filters, renormalised (top-k with
+ * k = 2 turns (0.50, 0.30, 0.20) into (0.625, 0.375, 0)).
+ *
+ * With s_v = z_v / temperature (z as in tim_logprob):
+ *   top-k set K = the top_k tokens by z (equal logits: lower id first);
+ *   q = softmax of s over K; walking K in that order, a token is kept when the
+ *   q-mass of the tokens before it is < top_p (the first is always kept);
+ *   out_lse_kept[t] = ln sum_{v kept} exp(s_v);
+ *   out_logprob[t]  = s_x - out_lse_kept[t] if the target x is kept, else -inf;
+ *   out_kept[t]     = number of kept tokens.
+ * Cost: the LM-head GEMM runs twice (the second pass collects, per row, the
+ * logits at or above the k-th largest 256-column-tile maximum, a bound that
+ * every top-k logit meets).  Results are batch-invariant like tim_logprob's.
+ *
+ * Limits: 1 <= top_k <= TIM_PROCESSED_MAX_K, 0 < top_p <= 1, at most 2048
+ * vocabulary tiles (V <= 524288), and either V >= 256 * top_k or
+ * V <= TIM_PROCESSED_CAPACITY.  A row with more than TIM_PROCESSED_CAPACITY
+ * candidates (many logits tied near the top) reports TIM_ERR_CAPACITY and NaN.
+ * Other arguments and errors as tim_logprob; the workspace is
+ * tim_processed_logprob_workspace_size bytes.
+ * ------------------------------------------------------------------------ */
+#define TIM_PROCESSED_MAX_K 64
+#define TIM_PROCESSED_CAPACITY 2048
+
+size_t tim_processed_logprob_workspace_size(int64_t T, int32_t d, int32_t V);
+
+tim_status tim_processed_logprob(const void *hidden, const void *gamma, const void *W,
+                                 const int32_t *token_ids, int64_t T, int32_t d, int32_t V,
+                                 float temperature, float eps, int32_t top_k, float top_p,
+                                 float *out_logprob, float *out_lse_kept, int32_t *out_kept,
+                                 void *workspace, size_t workspace_bytes, tim_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * Vocabulary-parallel linear logprob.

@@ -21,7 +21,7 @@ STATUS_NAMES = {
     0: "TIM_OK", 1: "TIM_ERR_INVALID_ARG", 2: "TIM_ERR_SHAPE", 3: "TIM_ERR_TOKEN_RANGE",
     4: "TIM_ERR_NONFINITE", 5: "TIM_ERR_EMPTY_SEQUENCE", 6: "TIM_ERR_BAD_MASK",
     7: "TIM_ERR_WORKSPACE", 8: "TIM_ERR_CUDA", 9: "TIM_ERR_TIMEOUT",
-    10: "TIM_ERR_UNSUPPORTED_DEVICE",
+    10: "TIM_ERR_UNSUPPORTED_DEVICE", 11: "TIM_ERR_CAPACITY",
 }
 STATUS = {v: k for k, v in STATUS_NAMES.items()}
 
@@ -72,6 +72,9 @@ _SIGNATURES = {
     "tim_compare": (_c.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i64, _f32, _vp, _vp, _vp, _sz,
                                _vp]),
     "tim_compare_diag_workspace_size": (_sz, [_i64, _i32]),
+    "tim_processed_logprob_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "tim_processed_logprob": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _i32,
+                                         _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "tim_vocab_shard": (_c.c_int, [_i32, _i32, _i32, _c.POINTER(_i32), _c.POINTER(_i32)]),
     "tim_logprob_shard_workspace_size": (_sz, [_i64, _i32, _i32, _i32, _i32]),
     "tim_logprob_shard": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _f32, _f32,
@@ -340,6 +343,35 @@ def diag_to_dicts(arr) -> list:
         dct["mis_kept"] = int(r["mis_kept"])
         dct["flags"] = int(r["flags"])
         out.append(dct)
+    return out
+
+
+def processed_logprob(hidden, gamma, W, token_ids, temperature: float, eps: float, top_k: int,
+                      top_p: float = 1.0, *, out=None, workspace: Optional[Workspace] = None,
+                      stream=None, check: bool = True):
+    """Top-k / top-p processed score with tim_processed_logprob.
+    Returns (logprob f32 [T] (-inf if filtered out), lse_kept f32 [T], kept i32 [T])."""
+    torch = _torch()
+    hidden = _as_bf16(hidden, "hidden")
+    gamma = _as_bf16(gamma, "gamma")
+    W = _as_bf16(W, "W")
+    _need(token_ids, torch.int32, "token_ids", 1)
+    T, d = hidden.shape
+    V = W.shape[0]
+    dev = hidden.device
+    if out is None:
+        out = (torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = Workspace(int(lib().tim_processed_logprob_workspace_size(T, d, V)), dev, stream)
+    code = lib().tim_processed_logprob(_ptr(hidden), _ptr(gamma), _ptr(W), _ptr(token_ids), T, d,
+                                       V, float(temperature), float(eps), int(top_k), float(top_p),
+                                       _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), workspace.ptr,
+                                       workspace.nbytes, _stream_ptr(stream))
+    _check(code, "tim_processed_logprob")
+    if check:
+        workspace.check("tim_processed_logprob", stream)
     return out
 
 

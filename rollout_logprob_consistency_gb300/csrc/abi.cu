@@ -24,6 +24,16 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
                                     int d, int V, int v0, float temperature, void* part,
                                     float* tgt, int* status, cudaStream_t stream, int num_sms);
 void vocab_shard_range(int V, int G, int g, int* v0, int* v_len);
+cudaError_t launch_lmhead_collect(const void* y, const void* W, const int32_t* ids, int64_t T,
+                                  int d, int V, float temperature, const float* thr, int* cnt,
+                                  void* cand, int cap, int* status, cudaStream_t stream,
+                                  int num_sms);
+cudaError_t launch_topk_threshold(const void* part, int64_t T, int V, int k, float* thr, int* cnt,
+                                  cudaStream_t stream);
+cudaError_t launch_topk_finalize(const void* cand, const int* cnt, const int32_t* ids, int64_t T,
+                                 int V, int k, float top_p, float temperature, int cap,
+                                 float* out_lp, float* out_lse, int32_t* out_kept, int* status,
+                                 cudaStream_t stream);
 cudaError_t launch_shard_reduce(const void* part, const float* tgt, int64_t T, int V, int G, int g,
                                 int v_len, void* out_rec, float* out_tgt, cudaStream_t stream);
 cudaError_t launch_merge_shards(const void* recs, const float* tgts, const int32_t* ids, int64_t T,
@@ -101,6 +111,22 @@ tim_status validate_logprob_common(int64_t T, int32_t d, int32_t V, float temper
   return check_workspace(ws, ws_bytes, logprob_layout(T, d, V).total);
 }
 
+// Processed-score workspace: the scoring workspace, then thresholds [T],
+// candidate counters [T] and candidate slots [T][TIM_PROCESSED_CAPACITY].
+struct ProcLayout {
+  WsLayout base;
+  size_t thr_off, cnt_off, cand_off, total;
+};
+ProcLayout processed_layout(int64_t T, int32_t d, int32_t V) {
+  ProcLayout P;
+  P.base = logprob_layout(T, d, V);
+  P.thr_off = align_up(P.base.total, 1024);
+  P.cnt_off = align_up(P.thr_off + static_cast<size_t>(T) * 4, 1024);
+  P.cand_off = align_up(P.cnt_off + static_cast<size_t>(T) * 4, 1024);
+  P.total = align_up(P.cand_off + static_cast<size_t>(T) * TIM_PROCESSED_CAPACITY * 8, 1024);
+  return P;
+}
+
 bool valid_shard(int32_t G, int32_t g) {
   return (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) && g >= 0 && g < G;
 }
@@ -125,6 +151,7 @@ const char* tim_status_string(tim_status s) {
     case TIM_ERR_CUDA: return "TIM_ERR_CUDA";
     case TIM_ERR_TIMEOUT: return "TIM_ERR_TIMEOUT";
     case TIM_ERR_UNSUPPORTED_DEVICE: return "TIM_ERR_UNSUPPORTED_DEVICE";
+    case TIM_ERR_CAPACITY: return "TIM_ERR_CAPACITY";
   }
   return "TIM_ERR_UNKNOWN";
 }
@@ -250,6 +277,57 @@ tim_status tim_compare(const float* lp_gen, const float* lp_replay, const float*
   return from_cuda(launch_seg_compare(lp_gen, lp_replay, lp_train, seq_offsets, n_seq, mask, T,
                                       tis_cap, out_stats, out_tis_w, workspace,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t tim_processed_logprob_workspace_size(int64_t T, int32_t d, int32_t V) {
+  if (check_shape(T, d, V) != TIM_OK) return 0;
+  return processed_layout(T, d, V).total;
+}
+
+tim_status tim_processed_logprob(const void* hidden, const void* gamma, const void* W,
+                                 const int32_t* token_ids, int64_t T, int32_t d, int32_t V,
+                                 float temperature, float eps, int32_t top_k, float top_p,
+                                 float* out_logprob, float* out_lse_kept, int32_t* out_kept,
+                                 void* workspace, size_t workspace_bytes, tim_stream_t stream) {
+  if (hidden == nullptr || gamma == nullptr || W == nullptr || token_ids == nullptr ||
+      out_logprob == nullptr || out_lse_kept == nullptr || out_kept == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(gamma, 16) || !aligned(W, 16) || !aligned(token_ids, 4) ||
+      !aligned(out_logprob, 4) || !aligned(out_lse_kept, 4) || !aligned(out_kept, 4))
+    return TIM_ERR_INVALID_ARG;
+  tim_status s = check_shape(T, d, V);
+  if (s != TIM_OK) return s;
+  if ((s = check_scalars(temperature, eps)) != TIM_OK) return s;
+  if (top_k < 1 || top_k > TIM_PROCESSED_MAX_K) return TIM_ERR_INVALID_ARG;
+  if (!(std::isfinite(top_p) && top_p > 0.f && top_p <= 1.f)) return TIM_ERR_INVALID_ARG;
+  const int n_tiles = (V + kBN - 1) / kBN;
+  if (n_tiles > TIM_PROCESSED_CAPACITY) return TIM_ERR_SHAPE;
+  if (n_tiles < top_k && V > TIM_PROCESSED_CAPACITY) return TIM_ERR_SHAPE;
+  const ProcLayout P = processed_layout(T, d, V);
+  if ((s = check_workspace(workspace, workspace_bytes, P.total)) != TIM_OK) return s;
+  int sms = 0;
+  if ((s = check_device(&sms)) != TIM_OK) return s;
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(b + P.base.status_off);
+  void* y = b + P.base.y_off;
+  void* part = b + P.base.part_off;
+  float* tgt = reinterpret_cast<float*>(b + P.base.tgt_off);
+  float* thr = reinterpret_cast<float*>(b + P.thr_off);
+  int* cnt = reinterpret_cast<int*>(b + P.cnt_off);
+  void* cand = b + P.cand_off;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_rmsnorm_rows(hidden, gamma, T, d, eps, y, status, st) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  if (launch_lmhead_lse(y, W, token_ids, T, d, V, temperature, part, tgt, status, st, sms) !=
+      cudaSuccess)
+    return TIM_ERR_CUDA;
+  if (launch_topk_threshold(part, T, V, top_k, thr, cnt, st) != cudaSuccess) return TIM_ERR_CUDA;
+  if (launch_lmhead_collect(y, W, token_ids, T, d, V, temperature, thr, cnt, cand,
+                            TIM_PROCESSED_CAPACITY, status, st, sms) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  return from_cuda(launch_topk_finalize(cand, cnt, token_ids, T, V, top_k, top_p, temperature,
+                                        TIM_PROCESSED_CAPACITY, out_logprob, out_lse_kept,
+                                        out_kept, status, st));
 }
 
 tim_status tim_vocab_shard(int32_t V, int32_t G, int32_t g, int32_t* v0, int32_t* v_len) {

@@ -63,6 +63,12 @@ struct GemmArgs {
   float4* part;
   float* tgt;
   int* status;
+  // collect mode only: per-row logit threshold, candidate counters, candidate
+  // slots (logit bits, vocabulary id) [T][cap]
+  const float* thr;
+  int* cnt;
+  uint2* cand;
+  int cap;
 };
 
 constexpr size_t kGemmSmemBytes =
@@ -131,6 +137,11 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], int nval
   }
 }
 
+// kMode 0: per-(row, tile) softmax records and the target logit (the scoring path).
+// kMode 1: candidate collection -- every logit >= the row's threshold is appended
+//          (in no particular order) to the row's candidate slots; used by the
+//          processed (top-k / top-p) score, which sorts the candidates afterwards.
+template <int kMode>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     lmhead_lse_kernel(const __grid_constant__ CUtensorMap tmap_y,
                       const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
@@ -291,23 +302,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       float m2 = -INFINITY, sum = 0.f, bz = -INFINITY, zt = 0.f;
       int bi = col_base;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+      if constexpr (kMode == 0) {
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        const int col0 = col_base + c * 32;
-        if (col0 >= a.v_end) break;  // warp-uniform
-        uint32_t r[32];
-        tmem_ld32(tbase + c * 32, r);
-        const int nvalid = min(32, a.v_end - col0);
-        if (nvalid == 32)
-          epilogue_chunk<false>(r, 32, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
-        else
-          epilogue_chunk<true>(r, nvalid, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
+        for (int c = 0; c < kBN / 32; ++c) {
+          const int col0 = col_base + c * 32;
+          if (col0 >= a.v_end) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          const int nvalid = min(32, a.v_end - col0);
+          if (nvalid == 32)
+            epilogue_chunk<false>(r, 32, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
+          else
+            epilogue_chunk<true>(r, nvalid, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
+        }
+      } else {
+        const float thr = (row < a.T) ? __ldcg(a.thr + row) : INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          const int col0 = col_base + c * 32;
+          if (col0 >= a.v_end) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          const int nvalid = min(32, a.v_end - col0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < nvalid && __uint_as_float(r[j]) >= thr) {
+              const int slot = atomicAdd(a.cnt + row, 1);
+              if (slot < a.cap) a.cand[row * a.cap + slot] = make_uint2(r[j], col0 + j);
+            }
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
 
-      if (row < a.T) {
+      if (kMode == 0 && row < a.T) {
         a.part[((row >> 5) * a.num_n + n) * 32 + (row & 31)] =
             make_float4(m2, sum, bz, __int_as_float(bi));
         if (static_cast<unsigned>(rel) < static_cast<unsigned>(kBN)) a.tgt[row] = zt * a.inv_temp;
@@ -372,35 +402,11 @@ static bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t rows, u
   return r == CUDA_SUCCESS;
 }
 
-// W holds V vocabulary rows whose global ids start at v0 (a vocabulary shard when
-// v0 > 0 or V is not the whole vocabulary); records are written per local tile.
-cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t* ids, int64_t T,
-                                    int d, int V, int v0, float temperature, void* part,
-                                    float* tgt, int* status, cudaStream_t stream, int num_sms) {
-  CUtensorMap map_y, map_w;
-  if (!make_kmajor_map(&map_y, y, static_cast<uint64_t>(rows_padded(T)),
-                       static_cast<uint64_t>(d), kBM) ||
-      !make_kmajor_map(&map_w, W, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN))
-    return cudaErrorInvalidValue;
-
-  GemmArgs a;
-  a.T = T;
-  a.v0 = v0;
-  a.v_end = v0 + V;
-  a.d = d;
-  a.num_m = static_cast<int>((T + kBM - 1) / kBM);
-  a.num_n = (V + kBN - 1) / kBN;
-  a.num_kb = d / kBK;
-  a.group_m = 16;
-  a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
-  a.k2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
-  a.inv_temp = static_cast<float>(1.0 / static_cast<double>(temperature));
-  a.ids = ids;
-  a.part = static_cast<float4*>(part);
-  a.tgt = tgt;
-  a.status = status;
-
-  cudaError_t e = cudaFuncSetAttribute(lmhead_lse_kernel,
+template <int kMode>
+static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_w,
+                               const GemmArgs& a, cudaStream_t stream, int num_sms,
+                               bool programmatic) {
+  cudaError_t e = cudaFuncSetAttribute(lmhead_lse_kernel<kMode>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kGemmSmemBytes));
   if (e != cudaSuccess) return e;
@@ -417,8 +423,70 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lmhead_lse_kernel, map_y, map_w, a);
+  cfg.numAttrs = programmatic ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, lmhead_lse_kernel<kMode>, map_y, map_w, a);
+}
+
+static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w, const void* y,
+                             const void* W, const int32_t* ids, int64_t T, int d, int V, int v0,
+                             float temperature, int* status) {
+  if (!make_kmajor_map(&map_y, y, static_cast<uint64_t>(rows_padded(T)),
+                       static_cast<uint64_t>(d), kBM) ||
+      !make_kmajor_map(&map_w, W, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN))
+    return cudaErrorInvalidValue;
+  a.T = T;
+  a.v0 = v0;
+  a.v_end = v0 + V;
+  a.d = d;
+  a.num_m = static_cast<int>((T + kBM - 1) / kBM);
+  a.num_n = (V + kBN - 1) / kBN;
+  a.num_kb = d / kBK;
+  a.group_m = 16;
+  a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
+  a.k2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  a.inv_temp = static_cast<float>(1.0 / static_cast<double>(temperature));
+  a.ids = ids;
+  a.part = nullptr;
+  a.tgt = nullptr;
+  a.status = status;
+  a.thr = nullptr;
+  a.cnt = nullptr;
+  a.cand = nullptr;
+  a.cap = 0;
+  return cudaSuccess;
+}
+
+// W holds V vocabulary rows whose global ids start at v0 (a vocabulary shard when
+// v0 > 0 or V is not the whole vocabulary); records are written per local tile.
+cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t* ids, int64_t T,
+                                    int d, int V, int v0, float temperature, void* part,
+                                    float* tgt, int* status, cudaStream_t stream, int num_sms) {
+  CUtensorMap map_y, map_w;
+  GemmArgs a;
+  cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, v0, temperature, status);
+  if (e != cudaSuccess) return e;
+  a.part = static_cast<float4*>(part);
+  a.tgt = tgt;
+  return launch_gemm<0>(map_y, map_w, a, stream, num_sms, true);
+}
+
+// Candidate collection pass of the processed score: logits >= thr[row] are
+// appended to cand[row][0 .. cap) with cnt[row] counting them (counts above cap
+// mean the row overflowed).  Launched without programmatic overlap: the
+// thresholds and zeroed counters come from the kernel just before it.
+cudaError_t launch_lmhead_collect(const void* y, const void* W, const int32_t* ids, int64_t T,
+                                  int d, int V, float temperature, const float* thr, int* cnt,
+                                  void* cand, int cap, int* status, cudaStream_t stream,
+                                  int num_sms) {
+  CUtensorMap map_y, map_w;
+  GemmArgs a;
+  cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, 0, temperature, status);
+  if (e != cudaSuccess) return e;
+  a.thr = thr;
+  a.cnt = cnt;
+  a.cand = static_cast<uint2*>(cand);
+  a.cap = cap;
+  return launch_gemm<1>(map_y, map_w, a, stream, num_sms, false);
 }
 
 cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T,

@@ -1,0 +1,194 @@
+// Processed (top-k, then top-p) selected-token logprob.
+//
+// "Debugging Logprob Mismatches in LLM Reinforcement Learning", Make Sure Both
+// Scores Describe the Same Probability: a sampler's score is taken on the
+// distribution left after its filters, renormalised (top-k with k = 2 turns
+// (0.50, 0.30, 0.20) into (0.625, 0.375, 0)).  Order: temperature, top-k (ties
+// keep the lower token id), top-p on the renormalised top-k distribution
+// (keep tokens whose preceding cumulative probability is < p).  A filtered-out
+// target scores -inf.
+//
+// Three steps after the scoring kernels have produced per-(row, 256-column
+// tile) records:
+//  1. topk_threshold_kernel: per row, thr = the k-th largest tile maximum.  The
+//     k largest tile maxima are k distinct logits, so the k-th largest logit of
+//     the row is >= thr: every top-k logit is >= thr.  (Rows of a vocabulary
+//     with fewer than k tiles use thr = -inf.)
+//  2. the LM-head kernel again, in candidate mode: logits >= thr are appended
+//     to the row's candidate slots.
+//  3. topk_finalize_kernel: per row, the candidates are sorted by (logit
+//     descending, id ascending) with a warp bitonic sort; the first k form the
+//     top-k set; top-p and the score are evaluated in fp64.
+#include <cmath>
+
+#include "tim_common.cuh"
+
+namespace tim {
+
+constexpr int kProcWarps = 4;
+constexpr int kProcSortMax = TIM_PROCESSED_CAPACITY;  // elements per warp sort
+
+// Bitonic sort of n2 (power of two) 64-bit keys, descending, by one warp.
+__device__ __forceinline__ void warp_sort_desc_u64(unsigned long long* b, int n2, int lane) {
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = lane; i < n2; i += 32) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long x = b[i], y = b[ixj];
+          const bool down = (i & k) == 0;
+          if ((x < y) == down) {
+            b[i] = y;
+            b[ixj] = x;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// Monotone map of float bits to unsigned (larger float -> larger key).
+__device__ __forceinline__ uint32_t ordered_bits(uint32_t f) {
+  return (f & 0x80000000u) ? ~f : (f | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(32 * kProcWarps)
+    topk_threshold_kernel(const float4* __restrict__ part, int64_t T, int n_tiles, int k,
+                          float* __restrict__ thr, int* __restrict__ cnt) {
+  extern __shared__ unsigned long long sbuf[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kProcWarps + warp;
+  if (row >= T) return;
+  if (n_tiles < k) {
+    if (lane == 0) {
+      thr[row] = -INFINITY;
+      cnt[row] = 0;
+    }
+    return;
+  }
+  unsigned long long* b = sbuf + warp * kProcSortMax;
+  int n2 = 1;
+  while (n2 < n_tiles) n2 <<= 1;
+  const float4* p = part + (row >> 5) * static_cast<int64_t>(n_tiles) * 32 + (row & 31);
+  for (int i = lane; i < n2; i += 32) {
+    const uint32_t zb = (i < n_tiles) ? __float_as_uint(__ldg(p + static_cast<int64_t>(i) * 32).z)
+                                      : __float_as_uint(-INFINITY);
+    b[i] = static_cast<unsigned long long>(ordered_bits(zb)) << 32;
+  }
+  __syncwarp();
+  warp_sort_desc_u64(b, n2, lane);
+  if (lane == 0) {
+    const uint32_t key = static_cast<uint32_t>(b[k - 1] >> 32);
+    const uint32_t fb = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+    thr[row] = __uint_as_float(fb);
+    cnt[row] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(32 * kProcWarps)
+    topk_finalize_kernel(const uint2* __restrict__ cand, const int* __restrict__ cnt,
+                         const int32_t* __restrict__ ids, int64_t T, int V, int k, double top_p,
+                         double temperature, int cap, float* __restrict__ out_lp,
+                         float* __restrict__ out_lse, int32_t* __restrict__ out_kept,
+                         int* status) {
+  extern __shared__ unsigned long long sbuf[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kProcWarps + warp;
+  if (row >= T) return;
+  const int n = __ldcg(cnt + row);
+  const int x = __ldg(ids + row);
+  if (n > cap || n < 1) {
+    if (lane == 0) {
+      set_status(status, n > cap ? TIM_ERR_CAPACITY : TIM_ERR_NONFINITE);
+      out_lp[row] = __int_as_float(0x7FC00000);
+      out_lse[row] = __int_as_float(0x7FC00000);
+      out_kept[row] = 0;
+    }
+    return;
+  }
+  unsigned long long* b = sbuf + warp * kProcSortMax;
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  const uint2* c = cand + row * cap;
+  for (int i = lane; i < n2; i += 32) {
+    if (i < n) {
+      const uint2 v = __ldcg(c + i);
+      b[i] = (static_cast<unsigned long long>(ordered_bits(v.x)) << 32) |
+             static_cast<unsigned long long>(0xFFFFFFFFu - v.y);
+    } else {
+      b[i] = 0ull;
+    }
+  }
+  __syncwarp();
+  warp_sort_desc_u64(b, n2, lane);
+  if (lane != 0) return;
+
+  const int kk = k < n ? k : n;
+  double s[TIM_PROCESSED_MAX_K];
+  int idv[TIM_PROCESSED_MAX_K];
+  for (int i = 0; i < kk; ++i) {
+    const uint32_t key = static_cast<uint32_t>(b[i] >> 32);
+    const uint32_t fb = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+    s[i] = static_cast<double>(__uint_as_float(fb)) / temperature;
+    idv[i] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(b[i] & 0xFFFFFFFFull));
+  }
+  const double m = s[0];
+  double total = 0.0;
+  for (int i = 0; i < kk; ++i) total += exp(s[i] - m);
+  // top-p on the renormalised top-k distribution
+  int kept = 0;
+  double before = 0.0, kept_sum = 0.0;
+  for (int i = 0; i < kk; ++i) {
+    const double e = exp(s[i] - m);
+    if (i > 0 && !(before < top_p * total)) break;
+    kept_sum += e;
+    before += e;
+    ++kept;
+  }
+  const double lse = m + log(kept_sum);
+  double lp = -INFINITY;
+  if (x < 0 || x >= V) {
+    lp = NAN;
+    set_status(status, TIM_ERR_TOKEN_RANGE);
+  } else {
+    for (int i = 0; i < kept; ++i)
+      if (idv[i] == x) lp = s[i] - lse;
+  }
+  if (!isfinite(lse)) set_status(status, TIM_ERR_NONFINITE);
+  out_lp[row] = static_cast<float>(lp);
+  out_lse[row] = static_cast<float>(lse);
+  out_kept[row] = kept;
+}
+
+cudaError_t launch_topk_threshold(const void* part, int64_t T, int V, int k, float* thr, int* cnt,
+                                  cudaStream_t stream) {
+  const int n_tiles = (V + kBN - 1) / kBN;
+  const size_t smem = static_cast<size_t>(kProcWarps) * kProcSortMax * 8;
+  cudaError_t e = cudaFuncSetAttribute(topk_threshold_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = (T + kProcWarps - 1) / kProcWarps;
+  topk_threshold_kernel<<<static_cast<unsigned>(blocks), 32 * kProcWarps, smem, stream>>>(
+      static_cast<const float4*>(part), T, n_tiles, k, thr, cnt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_finalize(const void* cand, const int* cnt, const int32_t* ids, int64_t T,
+                                 int V, int k, float top_p, float temperature, int cap,
+                                 float* out_lp, float* out_lse, int32_t* out_kept, int* status,
+                                 cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(kProcWarps) * kProcSortMax * 8;
+  cudaError_t e = cudaFuncSetAttribute(topk_finalize_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = (T + kProcWarps - 1) / kProcWarps;
+  topk_finalize_kernel<<<static_cast<unsigned>(blocks), 32 * kProcWarps, smem, stream>>>(
+      static_cast<const uint2*>(cand), cnt, ids, T, V, k, static_cast<double>(top_p),
+      static_cast<double>(temperature), cap, out_lp, out_lse, out_kept, status);
+  return cudaGetLastError();
+}
+
+}  // namespace tim
