@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int nvalid = min(32, a.v_end - col0);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (j < nvalid && __uint_as_float(r[j]) >= thr) {
+            if (j < nvalid && row < a.T && __uint_as_float(r[j]) >= thr) {
               const int slot = atomicAdd(a.cnt + row, 1);
               if (slot < a.cap) a.cand[row * a.cap + slot] = make_uint2(r[j], col0 + j);
             }
