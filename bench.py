@@ -35,9 +35,9 @@ L2_NOTE = "inputs larger than L2 (W 1.245 GB + hidden 268 MB per step vs 129 MB 
 # (profiles/lmhead_lse_T4096_d4096_V151936.md): a T=4096 launch moved 2.523 GB read +
 # 0.041 GB written; traffic grows with the number of 2048-row groups, so a T=32768
 # launch moves 8x that.  Valid only for the kernel sources hashed here.
-TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "425b375ce460ba2a",
+TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "3d9bca03781fc298",
                                 "tim_common.cuh": "a255a6e438eba7fa"},
-                       T=4096, bytes=2.523121e9 + 40.945152e6)
+                       T=4096, bytes=2.523426e9 + 41.295104e6)
 
 
 def traffic_per_launch(T):
@@ -58,6 +58,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-extras", action="store_true")
     p.add_argument("--profile-shape", default=None,
                    help="T,d,V: only run --profile-iters tim_logprob calls of this shape "
                         "(small case for ncu captures), print nothing")
@@ -381,34 +382,49 @@ def main():
              torch.empty(T, dtype=torch.float32).pin_memory(),
              torch.empty(T, dtype=torch.int32).pin_memory(),
              torch.empty(stats_buf.numel(), dtype=torch.uint8).pin_memory()]
-    d_hid = torch.empty(T, d, dtype=torch.int16, device=dev)
-    d_ids = torch.empty(T, dtype=torch.int32, device=dev)
-    d_A = torch.empty(T, dtype=torch.float32, device=dev)
-    d_B = torch.empty(T, dtype=torch.float32, device=dev)
-    d_mask = torch.empty(T, dtype=torch.uint8, device=dev)
-    d_offs = torch.empty(b.n_seq + 1, dtype=torch.int64, device=dev)
+    # two device input slots: the host->device copies of step k+1 run on a copy stream
+    # while step k computes (inputs are still copied every step, inside the timed region)
+    slots = []
+    for _ in range(2):
+        slots.append(dict(
+            hid=torch.empty(T, d, dtype=torch.int16, device=dev),
+            ids=torch.empty(T, dtype=torch.int32, device=dev),
+            A=torch.empty(T, dtype=torch.float32, device=dev),
+            B=torch.empty(T, dtype=torch.float32, device=dev),
+            mask=torch.empty(T, dtype=torch.uint8, device=dev),
+            offs=torch.empty(b.n_seq + 1, dtype=torch.int64, device=dev),
+            ev_in=torch.cuda.Event(), ev_done=torch.cuda.Event()))
+    copy_stream = torch.cuda.Stream(device=dev)
     h2d = sum(x.numel() * x.element_size() for x in (h_hid, h_ids, h_A, h_B, h_mask, h_offs))
     d2h = sum(x.numel() * x.element_size() for x in h_out)
 
-    def e2e_step():
-        for dst, src in ((d_hid, h_hid), (d_ids, h_ids), (d_A, h_A), (d_B, h_B), (d_mask, h_mask),
-                         (d_offs, h_offs)):
-            dst.copy_(src, non_blocking=True)
-        tim.logprob(d_hid.view(torch.bfloat16), gam, W, d_ids, tau, eps, out=C, workspace=ws,
-                    check=False)
-        tim.compare(d_A, d_B, C[0], d_offs, d_mask, b.tis_cap, out_stats=stats_buf,
-                    out_tis_w=tis_w, workspace=cws, check=False, to_host=False)
+    def e2e_step(k):
+        sl = slots[k % 2]
+        copy_stream.wait_event(sl["ev_done"])          # step k-2 finished with this slot
+        with torch.cuda.stream(copy_stream):
+            for key, src in (("hid", h_hid), ("ids", h_ids), ("A", h_A), ("B", h_B),
+                             ("mask", h_mask), ("offs", h_offs)):
+                sl[key].copy_(src, non_blocking=True)
+            sl["ev_in"].record(copy_stream)
+        stream.wait_event(sl["ev_in"])
+        tim.logprob(sl["hid"].view(torch.bfloat16), gam, W, sl["ids"], tau, eps, out=C,
+                    workspace=ws, check=False)
+        tim.compare(sl["A"], sl["B"], C[0], sl["offs"], sl["mask"], b.tis_cap,
+                    out_stats=stats_buf, out_tis_w=tis_w, workspace=cws, check=False,
+                    to_host=False)
         for dst, src in zip(h_out, (C[0], C[1], C[2], stats_buf)):
             dst.copy_(src, non_blocking=True)
+        sl["ev_done"].record(stream)
 
-    for _ in range(3):
-        e2e_step()
+    for k in range(3):
+        e2e_step(k)
     torch.cuda.synchronize()
     e2e_steps = max(3, args.steps // 2)
     barrier(dist, dev)
     start.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    copy_stream.wait_event(start)
+    for k in range(e2e_steps):
+        e2e_step(k)
     stop.record(stream)
     torch.cuda.synchronize()
     barrier(dist, dev)
@@ -432,6 +448,51 @@ def main():
     cmp_bytes = T * (3 * 4 + 1 + 4) + (b.n_seq + 1) * 8 + b.n_seq * tim.SEQ_STATS_DTYPE.itemsize
     compare_info = dict(us=round(cmp_us, 2), bytes=cmp_bytes,
                         GBps=round(cmp_bytes / cmp_us / 1e3, 1), sequences=b.n_seq)
+
+    # ---------------------------------------------------------------- next-row paths on this workload
+    extras = None
+    if rank == 0 and not args.no_extras:
+        extras = {}
+        pout = (torch.empty(T, device=dev), torch.empty(T, device=dev),
+                torch.empty(T, dtype=torch.int32, device=dev))
+        pws = tim.Workspace(int(tim.lib().tim_processed_logprob_workspace_size(T, d, V)), dev)
+        e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tim.processed_logprob(hid_train, gam, W, ids, tau, eps, 50, 0.95, out=pout,
+                              workspace=pws, check=False)
+        e_a.record(stream)
+        for _ in range(3):
+            tim.processed_logprob(hid_train, gam, W, ids, tau, eps, 50, 0.95, out=pout,
+                                  workspace=pws, check=False)
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        pws.check("processed")
+        pms = e_a.elapsed_time(e_b) / 3
+        extras["processed_topk50_topp0.95"] = dict(ms=round(pms, 3),
+                                                   tokens_per_s=round(T / (pms / 1e3), 1))
+        del pws
+        dws = tim.Workspace(int(tim.lib().tim_compare_diag_workspace_size(T, b.n_seq)), dev)
+        dout = torch.empty(b.n_seq * tim.SEQ_DIAG_DTYPE.itemsize, dtype=torch.uint8, device=dev)
+        tops = (A[2], Bo[2], C[2])
+        tim.compare_diag(A[0], Bo[0], C[0], offs, mask, b.tis_cap, 0.5, 2.0, top1=tops, out=dout,
+                         workspace=dws, check=False, to_host=False)
+        e_a.record(stream)
+        for _ in range(10):
+            tim.compare_diag(A[0], Bo[0], C[0], offs, mask, b.tis_cap, 0.5, 2.0, top1=tops,
+                             out=dout, workspace=dws, check=False, to_host=False)
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        dws.check("diag")
+        extras["compare_diag_us"] = round(1e3 * e_a.elapsed_time(e_b) / 10, 2)
+        G = 8
+        e_a.record(stream)
+        for _ in range(2):
+            tim.logprob_vocab_parallel_emulated(hid_train, gam, W, ids, G, tau, eps)
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        vms = e_a.elapsed_time(e_b) / 2
+        extras["vocab_parallel_G8_emulated_on_1_gpu"] = dict(
+            ms=round(vms, 3), note="the 8 shards run one after another on one GPU; on 8 GPUs "
+            "each rank would run one shard plus the merge")
 
     # ---------------------------------------------------------------- decode-shaped rows (HBM bound)
     decode = None
@@ -494,11 +555,13 @@ def main():
                           compare=ms_per_step - norm_ms - gemm_ms - fin_ms),
             cpu_baseline=cpu,
             e2e=dict(value=e2e_value, unit="tokens/s", h2d_bytes_per_step=h2d,
-                     d2h_bytes_per_step=d2h, steps=e2e_steps),
+                     d2h_bytes_per_step=d2h, steps=e2e_steps,
+                     note="pinned host buffers; the copies of step k+1 overlap step k"),
             gpu_launches=4 * args.steps,
             clocks=clk,
             compare=compare_info,
             decode_shapes=decode,
+            next_rows=extras,
         )
         print(json.dumps(line), flush=True)
     if dist is not None:
