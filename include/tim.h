@@ -402,7 +402,7 @@ tim_status tim_compare_diag(const float *lp_gen, const float *lp_replay, const f
  * allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *
  * Limit: tim_logprob_workspace_size(T, d, V) must not exceed 8 MiB (8388608
- * bytes) -- e.g. up to 416 rows at d = 4096 or 320 rows at d = 5120 with
+ * bytes) -- e.g. up to 416 rows at d = 4096 or 384 rows at d = 5120 with
  * V = 151936; larger sizes return TIM_ERR_WORKSPACE with nothing enqueued.
  *
  * Arguments are those of tim_logprob (device pointers, same layouts and

@@ -151,10 +151,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
-  uint64_t* full = bars;                    // leader: both CTAs' bytes of a stage
-  uint64_t* empty = bars + kStages;         // each CTA: its stage may be refilled
-  uint64_t* acc_full = bars + 2 * kStages;  // each CTA: accumulator ready
-  uint64_t* acc_empty = acc_full + 2;       // leader: both CTAs' epilogues done
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* acc_full = bars + 2 * kStages;
+  uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -162,10 +162,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the pair MMAs), 1 = peer
-  const bool leader = rank == 0;
-  const int64_t cluster = blockIdx.x >> 1;
-  const int64_t nclusters = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -175,7 +171,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 2 * kEpiWarps);
+      mbar_init(&acc_empty[b], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -184,42 +180,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     prefetch_tmap(&tmap_w);
   }
   if (warp == 1) {
-    tmem_alloc_pair(tmem_holder, kTmemCols);
-    tmem_relinquish_pair();
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
   }
   tc_fence_before();
-  cluster_sync_all();  // barrier inits and the allocation are visible to both CTAs
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer (both CTAs)
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
       bool first = true;
-      const int row_off = static_cast<int>(rank) * kBM;      // this CTA's rows of the pair tile
-      const int col_off = static_cast<int>(rank) * (kBN / 2);  // this CTA's half of the W tile
-      for (int64_t tile = cluster; tile < a.num_tiles && ok; tile += nclusters) {
+      for (int64_t tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
         int m, n;
         tile_coords(tile, a, m, n);
-        const int ya = m * kPairRows + row_off;
-        const int wb = n * kBN + col_off;
         int kb0 = 0;
         if (first) {
           // W does not depend on the RMSNorm kernel that precedes this one in the
           // stream: stream the first stages of W before waiting for y to be ready.
           const int pre = min(kStages, a.num_kb);
           for (int s = 0; s < pre; ++s) {
-            if (leader) mbar_arrive_expect_tx(&full[s], 2 * (kABytes + kBBytes));
-            tma_load_2d_pair(sB + s * kBBytes, &tmap_w, s * kBK, wb,
-                             mapa_shared(smem_u32(&full[s]), 0));
+            mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
+            tma_load_2d(sB + s * kBBytes, &tmap_w, s * kBK, n * kBN, &full[s]);
           }
           pdl_wait();
           for (int s = 0; s < pre; ++s) {
-            tma_load_2d_pair(sA + s * kABytes, &tmap_y, s * kBK, ya,
-                             mapa_shared(smem_u32(&full[s]), 0));
+            tma_load_2d(sA + s * kABytes, &tmap_y, s * kBK, m * kBM, &full[s]);
             last_parity[s] = 0;
           }
           stage = pre % kStages;
@@ -232,10 +222,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
-          const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kABytes + kBBytes));
-          tma_load_2d_pair(sA + stage * kABytes, &tmap_y, kb * kBK, ya, fb);
-          tma_load_2d_pair(sB + stage * kBBytes, &tmap_w, kb * kBK, wb, fb);
+          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
+          tma_load_2d(sA + stage * kABytes, &tmap_y, kb * kBK, m * kBM, &full[stage]);
+          tma_load_2d(sB + stage * kBBytes, &tmap_w, kb * kBK, n * kBN, &full[stage]);
           last_parity[stage] = ph;
           if (++stage == kStages) {
             stage = 0;
@@ -247,22 +236,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (leader only)
-    if (leader && lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16_f32(kPairRows, kBN);
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16_f32(kBM, kBN);
       int stage = 0;
       uint32_t ph = 0;
       uint32_t acc = 0, acc_ph = 0;
       bool ok = true;
-      for (int64_t tile = cluster; tile < a.num_tiles && ok; tile += nclusters) {
-        if (!mbar_wait_cluster(&acc_empty[acc], acc_ph ^ 1u, abort_flag)) {
+      for (int64_t tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
         for (int kb = 0; kb < a.num_kb; ++kb) {
-          if (!mbar_wait_cluster(&full[stage], ph, abort_flag)) {
+          if (!mbar_wait(&full[stage], ph, abort_flag)) {
             ok = false;
             break;
           }
@@ -271,17 +260,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t b0 = smem_u32(sB + stage * kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
-            umma_bf16_pair(d_tmem, sw128_kmajor_desc(a0 + k * 32),
-                           sw128_kmajor_desc(b0 + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
+                      idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit_pair_multicast(&empty[stage], 0x3);
+          umma_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             ph ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit_pair_multicast(&acc_full[acc], 0x3);
+        umma_commit(&acc_full[acc]);
         acc ^= 1u;
         if (acc == 0) acc_ph ^= 1u;
       }
@@ -289,15 +278,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (both CTAs)
+    // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&acc_empty[0]), 0);
-    const uint32_t acc_empty_leader1 = mapa_shared(smem_u32(&acc_empty[1]), 0);
     uint32_t acc = 0, acc_ph = 0;
-    for (int64_t tile = cluster; tile < a.num_tiles; tile += nclusters) {
+    for (int64_t tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
       int m, n;
       tile_coords(tile, a, m, n);
-      const int64_t row = static_cast<int64_t>(m) * kPairRows + rank * kBM + q * 32 + lane;
+      const int64_t row = static_cast<int64_t>(m) * kBM + q * 32 + lane;
       const int x = (row < a.T) ? __ldg(a.ids + row) : -1;
       const int col_base = a.v0 + n * kBN;  // global vocabulary id of the tile's column 0
       const int rel = x - col_base;
@@ -348,7 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc == 0 ? acc_empty_leader0 : acc_empty_leader1);
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
 
       if (kMode == 0 && row < a.T) {
         a.part[((row >> 5) * a.num_n + n) * 32 + (row & 31)] =
@@ -365,28 +352,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   if (*abort_flag) {
     if (warp == 0 && lane == 0) {
-      // give this CTA's TMA copies time to land (their completion is counted on
-      // the leader's barriers, which the peer cannot wait on)
-      if (leader) {
-        for (int s = 0; s < kStages; ++s)
-          if (last_parity[s] != 0xFFFFFFFFu) mbar_wait_drain(&full[s], last_parity[s]);
-      } else {
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 100000ull) {
-        }
-      }
+      // wait for TMA copies still landing in shared memory
+      for (int s = 0; s < kStages; ++s)
+        if (last_parity[s] != 0xFFFFFFFFu) mbar_wait_drain(&full[s], last_parity[s]);
     }
-    if (warp == 1 && lane == 0 && leader) {
-      // wait for MMAs still reading shared memory / writing tensor memory
-      umma_commit_pair(drain);
+    if (warp == 1 && lane == 0) {
+      // wait for MMAs still reading shared memory / writing TMEM
+      umma_commit(drain);
       mbar_wait_drain(drain, 0);
     }
   }
-  tc_fence_before();
-  cluster_sync_all();  // neither CTA leaves while the pair may still touch its memory
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
-    tmem_dealloc_pair(tmem_base, kTmemCols);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -423,34 +402,6 @@ static bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t rows, u
   return r == CUDA_SUCCESS;
 }
 
-// Number of CTA pairs of lmhead_lse_kernel<kMode> that fit on the device at once
-// (queried once per device and mode).
-template <int kMode>
-static int max_resident_pairs(int num_sms) {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
-  if (cached[dev] > 0) return cached[dev];
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
-  cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = kGemmSmemBytes;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, lmhead_lse_kernel<kMode>, &cfg) != cudaSuccess || n < 1) {
-    cudaGetLastError();
-    n = num_sms / 2;
-  }
-  cached[dev] = n;
-  return n;
-}
-
 template <int kMode>
 static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_w,
                                const GemmArgs& a, cudaStream_t stream, int num_sms,
@@ -459,28 +410,20 @@ static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kGemmSmemBytes));
   if (e != cudaSuccess) return e;
-  // persistent CTA pairs (clusters of 2): as many as can be resident at once
-  // (a pair needs two SMs of one GPC), at most one per tile
-  const int max_pairs = max_resident_pairs<kMode>(num_sms);
-  if (max_pairs < 1) return cudaErrorLaunchOutOfResources;
-  const int64_t pairs = a.num_tiles < max_pairs ? a.num_tiles : max_pairs;
+  const int64_t grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
   // Programmatic dependent launch: the kernel's prologue and its first W loads
   // may overlap the tail of the RMSNorm kernel; y is read only after
   // griddepcontrol.wait.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = kGemmSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = programmatic ? 2 : 1;
+  cfg.numAttrs = programmatic ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, lmhead_lse_kernel<kMode>, map_y, map_w, a);
 }
 
@@ -489,16 +432,16 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
                              float temperature, int* status) {
   if (!make_kmajor_map(&map_y, y, static_cast<uint64_t>(rows_padded(T)),
                        static_cast<uint64_t>(d), kBM) ||
-      !make_kmajor_map(&map_w, W, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN / 2))
+      !make_kmajor_map(&map_w, W, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN))
     return cudaErrorInvalidValue;
   a.T = T;
   a.v0 = v0;
   a.v_end = v0 + V;
   a.d = d;
-  a.num_m = static_cast<int>((T + kPairRows - 1) / kPairRows);
+  a.num_m = static_cast<int>((T + kBM - 1) / kBM);
   a.num_n = (V + kBN - 1) / kBN;
   a.num_kb = d / kBK;
-  a.group_m = 8;
+  a.group_m = 16;
   a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
   a.k2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   a.inv_temp = static_cast<float>(1.0 / static_cast<double>(temperature));

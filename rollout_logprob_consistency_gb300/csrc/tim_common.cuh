@@ -14,14 +14,13 @@ namespace tim {
 // ---------------------------------------------------------------------------
 // Tiling of the LM-head GEMM.  One shape for every T: the K-reduction order of
 // a logit never depends on the batch.
-constexpr int kBM = 128;          // rows (tokens) per CTA tile (a CTA pair covers 2 x kBM)
-constexpr int kPairRows = 2 * kBM;  // rows per CTA-pair tile = UMMA M of cta_group::2
+constexpr int kBM = 128;          // rows (tokens) per tile = UMMA M
 constexpr int kBN = 256;          // vocabulary columns per tile = UMMA N = leaf tile width
 constexpr int kBK = 64;           // K elements per stage (= one 128-byte swizzle row of bf16)
 constexpr int kUmmaK = 16;        // K per tcgen05.mma (kind::f16)
-constexpr int kStages = 6;        // smem pipeline depth
-constexpr int kABytes = kBM * kBK * 2;         // 16 KiB: this CTA's 128 rows of y
-constexpr int kBBytes = (kBN / 2) * kBK * 2;   // 16 KiB: this CTA's half of the W tile
+constexpr int kStages = 4;        // smem pipeline depth
+constexpr int kABytes = kBM * kBK * 2;   // 16 KiB
+constexpr int kBBytes = kBN * kBK * 2;   // 32 KiB
 constexpr int kEpiWarps = 4;             // one epilogue warp per TMEM lane quadrant
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;           // two 256-column fp32 accumulators
@@ -45,11 +44,9 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// y is stored with whole 256-row pair tiles (zero rows past T) so the LM-head
-// TMA never reads outside the tensor.
-__host__ __device__ inline int64_t rows_padded(int64_t T) {
-  return (T + kPairRows - 1) / kPairRows * kPairRows;
-}
+// y is stored with whole 128-row tiles (zero rows past T) so the LM-head TMA
+// never reads outside the tensor.
+__host__ __device__ inline int64_t rows_padded(int64_t T) { return (T + kBM - 1) / kBM * kBM; }
 
 __host__ inline WsLayout logprob_layout(int64_t T, int32_t d, int32_t V) {
   WsLayout L;
@@ -241,113 +238,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-// ---------------------------------------------------------------------------
-// Thread-block clusters (a CTA pair shares one 2-SM MMA)
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
-// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t cta_addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(cta_addr), "r"(rank));
-  return r;
-}
-
-// arrive (release, cluster scope) on an mbarrier given by its shared::cluster address
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// try_wait with acquire at cluster scope (arrivals may come from the peer CTA)
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
-                                                  const volatile int* abort_flag) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 31u) == 0u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-  }
-}
-
-// TMA load into this CTA's shared memory whose completion is counted on an
-// mbarrier of the leader CTA of the pair (shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap, int32_t x,
-                                                 int32_t y, uint32_t mbar_cluster_addr) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(mbar_cluster_addr)
-      : "memory");
-}
-
-// Tensor memory for a CTA pair: executed by one warp in each CTA of the pair.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* holder_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(holder_smem)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-// 2-SM MMA issued by one thread of the leader CTA: D (in both CTAs' tensor memory,
-// 128 rows each) += A (each CTA's 128 rows) * B (N columns, half from each CTA).
-__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                               uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive once on the mbarrier at this shared-memory offset in every CTA of
-// cta_mask when the pair MMAs issued so far are done.
-__device__ __forceinline__ void umma_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
 
 // 2^x with the hardware approximation (MUFU.EX2), flush-to-zero.
 __device__ __forceinline__ float ex2_approx(float x) {
