@@ -152,7 +152,8 @@ class ClockSampler:
         return dict(sm_mhz=statistics.median(r["sm"] for r in load),
                     sm_max_mhz=max(r["smax"] for r in load), reasons=sorted(reasons),
                     samples=len(rows), samples_under_load=len(load),
-                    power_w_max=max(r["power"] for r in rows))
+                    power_w_max=max(r["power"] for r in rows),
+                    power_w_median=statistics.median(r["power"] for r in load))
 
 
 def gpu_uuid(torch):
