@@ -441,7 +441,7 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   a.num_m = static_cast<int>((T + kBM - 1) / kBM);
   a.num_n = (V + kBN - 1) / kBN;
   a.num_kb = d / kBK;
-  a.group_m = 16;
+  a.group_m = 48;
   a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
   a.k2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   a.inv_temp = static_cast<float>(1.0 / static_cast<double>(temperature));
