@@ -31,13 +31,13 @@ WORKLOAD = ("Qwen3-8B-shaped head: T=32768 rows (8 samples x 4096: 1024 shared p
             "response), d=4096, V=151936, temperature 0.7, three-way compare with TIS cap 2.0")
 L2_NOTE = "inputs larger than L2 (W 1.245 GB + hidden 268 MB per step vs 129 MB L2)"
 
-# DRAM bytes per lmhead_lse launch from the committed ncu capture
-# (profiles/lmhead_lse_T4096_d4096_V151936.md): a T=4096 launch moved 2.523 GB read +
-# 0.041 GB written; traffic grows with the number of 2048-row groups, so a T=32768
-# launch moves 8x that.  Valid only for the kernel sources hashed here.
-TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "3d9bca03781fc298",
-                                "tim_common.cuh": "a255a6e438eba7fa"},
-                       T=4096, bytes=2.523426e9 + 41.295104e6)
+# DRAM bytes per lmhead_lse launch of this workload (T=32768, d=4096, V=151936),
+# measured by a one-pass ncu capture of the full-size launch
+# (profiles/lmhead_lse_T32768_dram.md): 8.91 GB read + 0.315 GB written.  Valid
+# only for the kernel sources hashed here and for T = 32768.
+TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "5a6f7f7bd965944a",
+                                "tim_common.cuh": "8142ccafdf0e09d8"},
+                       T=32768, bytes=8.91e9 + 315.06e6)
 
 
 def traffic_per_launch(T):
@@ -47,7 +47,7 @@ def traffic_per_launch(T):
         with open(os.path.join(csrc, name), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest()[:16] != h:
                 return None   # the kernel changed since the counters were taken
-    return TRAFFIC_CAPTURE["bytes"] * T / TRAFFIC_CAPTURE["T"]
+    return TRAFFIC_CAPTURE["bytes"] if T == TRAFFIC_CAPTURE["T"] else None
 
 
 def parse():
@@ -546,7 +546,7 @@ def main():
                         parallelism=f"dp{world} (independent row batches per GPU)"),
             roofline=dict(bound="tensor", achieved=achieved_tflops, peak=peak, unit="TFLOP/s",
                           frac=achieved_tflops / peak, traffic=traffic_per_launch(T),
-                          traffic_unit="bytes per launch (scaled from the T=4096 ncu capture)",
+                          traffic_unit="DRAM bytes per launch (one-pass ncu capture of this launch)",
                           algorithmic_bytes=2.0 * V * d + 2.0 * T * d,
                           kernel="lmhead_lse_kernel",
                           peak_source=f"{peaks['source']} bf16 sustained",
