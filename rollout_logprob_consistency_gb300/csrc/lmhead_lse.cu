@@ -31,8 +31,9 @@
 // RMSNorm kernel up to the next 128-row boundary) never touch other rows; the epilogue arithmetic of a (row, tile) pair
 // is fixed.  Which CTA computes a tile does not matter.
 //
-// Launched with programmatic stream serialisation: the producer streams its
-// first W stages, then waits (griddepcontrol.wait) for the RMSNorm kernel
+// Launched with programmatic stream serialisation when the batch fits one
+// raster group: the producer streams its first W stages, then waits
+// (griddepcontrol.wait, a no-op for an ordinary launch) for the RMSNorm kernel
 // before the first load of y.
 //
 // Every mbarrier wait is bounded (2 s); on timeout the kernel records
@@ -467,7 +468,13 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
   if (e != cudaSuccess) return e;
   a.part = static_cast<float4*>(part);
   a.tgt = tgt;
-  return launch_gemm<0>(map_y, map_w, a, stream, num_sms, true);
+  // Programmatic overlap with the RMSNorm kernel pays off while all row tiles
+  // fit one raster group (decode-sized and mid-sized batches: measured 10-200 us
+  // faster up to 4096 rows); beyond that the early-launched grid ran slower
+  // (3 ms at 32768 rows), so larger batches are launched in stream order.  The
+  // arithmetic is identical either way.
+  const bool programmatic = a.num_m <= a.group_m;
+  return launch_gemm<0>(map_y, map_w, a, stream, num_sms, programmatic);
 }
 
 // Candidate collection pass of the processed score: logits >= thr[row] are
