@@ -744,4 +744,100 @@ def pin_processed_library_topk():
     assert np.max(np.abs(pr["logprob"] - ls[:, 3].numpy())) < 1e-12
 
 
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) head pins
+
+def _e4m3_table():
+    """All finite e4m3 values decoded from the bit layout (1 sign, 4 exponent bits with
+    bias 7, 3 mantissa bits; code 0x7F / 0xFF is NaN), with their codes."""
+    vals, codes = [], []
+    for c in range(256):
+        s, e, m = c >> 7, (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            continue
+        v = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        vals.append(-v if s else v)
+        codes.append(c)
+    vals, codes = np.array(vals), np.array(codes)
+    keep = ~((vals == 0) & (codes == 0x80))
+    vals, codes = vals[keep], codes[keep]
+    o = np.argsort(vals, kind="stable")
+    return vals[o], codes[o]
+
+
+def pin_e4m3_rounding_exhaustive():
+    """Nearest-even e4m3 rounding against an exhaustive search of the 253 finite values,
+    including exact ties; torch's float8_e4m3fn conversion (a library routine) agrees."""
+    import torch
+    vals, codes = _e4m3_table()
+    assert vals.max() == 448.0 and vals[vals > 0].min() == 2.0 ** -9
+    g = np.random.default_rng(17)
+    x = np.concatenate([g.uniform(-448, 448, 20000), g.standard_normal(5000) * 0.01,
+                        (vals[:-1] + vals[1:]) / 2.0])
+    hi = np.clip(np.searchsorted(vals, x, side="left"), 1, vals.size - 1)
+    lo = hi - 1
+    dlo, dhi = np.abs(x - vals[lo]), np.abs(vals[hi] - x)
+    pick = (dhi < dlo) | ((dhi == dlo) & (codes[hi] % 2 == 0))
+    want = np.where(pick, vals[hi], vals[lo])
+    got = oracle.e4m3_round(x)
+    assert np.array_equal(got, want)
+    tq = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(tq, want)
+    assert oracle.e4m3_round(np.array([1.0625]))[0] == 1.0       # tie -> even mantissa
+    assert oracle.e4m3_round(np.array([1.1875]))[0] == 1.25
+
+
+def pin_fp8_scale_rule():
+    """The scale is the smallest power of two s with max|row| / s <= 448."""
+    for amax, s in ((448.0, 1.0), (449.0, 2.0), (224.0, 0.5), (1.0, 2.0 ** -8), (0.0, 1.0),
+                    (448.0 * 2 ** -20, 2.0 ** -20), (900.0, 4.0)):
+        assert oracle.fp8_scale(amax) == s, (amax, s)
+    g = np.random.default_rng(3)
+    for amax in np.abs(g.standard_normal(200)) * 10 ** g.uniform(-3, 3, 200):
+        s = oracle.fp8_scale(float(amax))
+        assert amax / s <= 448 < amax / (s / 2)
+        assert math.frexp(s)[0] == 0.5
+
+
+def pin_fp8_exact_head():
+    """When y and W are already e4m3 values with unit scales, the FP8 oracle equals the bf16
+    oracle; a scale applied to a whole W row cancels exactly in the dequantised logits."""
+    z = [1.0, 2.0, 0.5, -1.5, 3.0, 0.0, -0.25, 1.75]
+    h = np.full((1, 8), trunc_bf16_bits(1.0), dtype=np.uint16)
+    g = np.full(8, trunc_bf16_bits(0.0), dtype=np.uint16)
+    g[0] = trunc_bf16_bits(1.0)                     # y = (1, 0, ..., 0): an e4m3 value
+    W = np.zeros((8, 8), dtype=np.uint16)
+    W[:, 0] = [trunc_bf16_bits(v) for v in z]       # every logit is an e4m3 value
+    for x in range(8):
+        a = oracle.oracle_logprob(h, g, W, np.array([x], np.int32), 0.9, 0.0)
+        b = oracle.oracle_logprob_fp8(h, g, W, np.array([x], np.int32), 0.9, 0.0)
+        assert a["logprob"][0] == b["logprob"][0] and a["top1"][0] == b["top1"][0]
+    W2 = W.copy()
+    W2[:, 0] = [trunc_bf16_bits(v * 8.0) for v in z]  # same row, 8x larger: scale absorbs it
+    b2 = oracle.oracle_logprob_fp8(h, g, W2, np.array([4], np.int32), 1.0, 0.0)
+    lse = math.log(sum(math.exp(8.0 * v) for v in z))
+    assert abs(b2["logprob"][0] - (8.0 * 3.0 - lse)) < 1e-12
+
+
+def pin_fp8_quantized_dot_product():
+    """Random rows: z_fp8 = (Q(y) s_y) . (Q(W) s_W) written out term by term in exact rational
+    arithmetic matches the oracle's logits to 1e-12."""
+    b = synth.make_custom(T=2, d=64, V=12, tag="fp8dot")
+    y = oracle.rmsnorm(oracle.widen_bf16(b.hidden_gen), oracle.widen_bf16(b.head.gamma), b.eps)
+    Wf = oracle.widen_bf16(b.head.W)
+    out = oracle.oracle_logprob_fp8(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 1.0, b.eps)
+    for t in range(2):
+        sy = oracle.fp8_scale(float(np.max(np.abs(y[t]))))
+        qy = [Fraction(float(v)) * Fraction(sy) for v in oracle.e4m3_round(y[t] / sy)]
+        zs = []
+        for v in range(12):
+            sw = oracle.fp8_scale(float(np.max(np.abs(Wf[v]))))
+            qw = [Fraction(float(u)) * Fraction(sw) for u in oracle.e4m3_round(Wf[v] / sw)]
+            zs.append(float(sum(a * c for a, c in zip(qy, qw))))
+        m = max(zs)
+        lse = m + math.log(sum(math.exp(v - m) for v in zs))
+        assert abs(out["lse"][t] - lse) < 1e-12
+        assert abs(out["logprob"][t] - (zs[b.token_ids[t]] - lse)) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

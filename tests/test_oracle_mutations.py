@@ -174,6 +174,27 @@ def _proc_ties_high_id(z, x, temperature, top_k, top_p):
     return _orig_process_row(zz[::-1].copy(), V - 1 - x, temperature, top_k, top_p)
 
 
+import oracle.fp8 as of8
+
+
+def _e4m3_truncate(x):
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    q = np.ldexp(np.ones_like(x), np.maximum(e - 1, -6) - 3)
+    return np.clip(np.trunc(x / q) * q, -448.0, 448.0)
+
+
+def _e4m3_two_mantissa_bits(x):
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    q = np.ldexp(np.ones_like(x), np.maximum(e - 1, -6) - 2)
+    return np.clip(np.rint(x / q) * q, -448.0, 448.0)
+
+
+def _scale_max_over_448(amax):
+    return amax / 448.0 if amax else 1.0
+
+
 MUTATIONS = [
     ("temperature after softmax", ol, "lse_stats", _lse_after_softmax, ["pin_v8_temperature"]),
     ("no max shift", ol, "lse_stats", _lse_no_shift, ["pin_large_logits"]),
@@ -209,6 +230,10 @@ MUTATIONS = [
      ["pin_processed_page_topk"]),
     ("top-k ties keep the higher ids", opr, "process_row", _proc_ties_high_id,
      ["pin_processed_ties_and_temperature"]),
+    ("e4m3 truncation", of8, "e4m3_round", _e4m3_truncate, ["pin_e4m3_rounding_exhaustive"]),
+    ("e4m3 with two mantissa bits", of8, "e4m3_round", _e4m3_two_mantissa_bits,
+     ["pin_e4m3_rounding_exhaustive"]),
+    ("non-power-of-two scale", of8, "fp8_scale", _scale_max_over_448, ["pin_fp8_scale_rule"]),
 ]
 
 
