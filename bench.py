@@ -484,6 +484,25 @@ def main():
         torch.cuda.synchronize()
         dws.check("diag")
         extras["compare_diag_us"] = round(1e3 * e_a.elapsed_time(e_b) / 10, 2)
+        # FP8 (e4m3) head: W quantised once per weight version (untimed), then whole calls
+        W8, sW8 = tim.quantize_fp8_rows(W)
+        fws = tim.Workspace(int(tim.lib().tim_logprob_fp8_workspace_size(T, d, V)), dev)
+        tim.logprob_fp8(hid_train, gam, W8, sW8, ids, tau, eps, out=pout, workspace=fws,
+                        check=False)
+        e_a.record(stream)
+        for _ in range(5):
+            tim.logprob_fp8(hid_train, gam, W8, sW8, ids, tau, eps, out=pout, workspace=fws,
+                            check=False)
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        fws.check("fp8 head")
+        fms = e_a.elapsed_time(e_b) / 5
+        fp8_peak = 2.0 * peaks["bf16_sustained"] if peaks.get("bf16_sustained") else None
+        extras["fp8_e4m3_head"] = dict(
+            ms=round(fms, 3), tokens_per_s=round(T / (fms / 1e3), 1),
+            call_TFLOPs=round(2.0 * T * d * V / (fms / 1e3) / 1e12, 1),
+            peak_TFLOPs=fp8_peak, peak_note="2 x measured sustained bf16 (nominal fp8:bf16 ratio)")
+        del fws, W8, sW8
         G = 8
         e_a.record(stream)
         for _ in range(2):

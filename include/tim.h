@@ -243,6 +243,39 @@ tim_status tim_compare(const float *lp_gen, const float *lp_replay, const float 
                        void *workspace, size_t workspace_bytes, tim_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * FP8 (e4m3) variant of the linear logprob.
+ *
+ * "Rollout-Training Mismatch in LLM RL", section 3 (Unified FP8 table): FP8
+ * quantize-dequantize forward values, and native FP8 GEMMs consuming codes and
+ * scales.  Quantisation here: one power-of-two scale per row, the smallest s
+ * with max|row| / s <= 448 (1 for an all-zero row); code = e4m3(x / s), round
+ * to nearest-even, saturating.  W is quantised by vocabulary row (once, with
+ * tim_quantize_fp8_rows); y (the bf16 output of the final RMSNorm, exactly as
+ * in tim_logprob) by token row inside tim_logprob_fp8.  The LM head runs on
+ * the e4m3 codes (tcgen05 kind::f8f6f4, fp32 accumulation) and multiplies each
+ * logit by s_y[t] * s_W[v]; because the scales are powers of two this equals
+ * the GEMM of the quantize-dequantize operands.  Everything after the logits is
+ * the tim_logprob path.  Batch-invariant like tim_logprob.
+ *
+ * tim_quantize_fp8_rows: x = bf16 [rows, K] (16-byte aligned, K a multiple of
+ *   16) -> codes = e4m3 bytes [rows, K] (8-byte aligned), scales = float32
+ *   [rows].  Asynchronous on `stream`; needs no workspace.
+ * tim_logprob_fp8: as tim_logprob, with W_codes = e4m3 [V, d] and W_scales =
+ *   float32 [V] from tim_quantize_fp8_rows, d a multiple of 128, and a
+ *   workspace of tim_logprob_fp8_workspace_size bytes.
+ * ------------------------------------------------------------------------ */
+tim_status tim_quantize_fp8_rows(const void *x, int64_t rows, int32_t K, void *codes,
+                                 float *scales, tim_stream_t stream);
+
+size_t tim_logprob_fp8_workspace_size(int64_t T, int32_t d, int32_t V);
+
+tim_status tim_logprob_fp8(const void *hidden, const void *gamma, const void *W_codes,
+                           const float *W_scales, const int32_t *token_ids, int64_t T, int32_t d,
+                           int32_t V, float temperature, float eps, float *out_logprob,
+                           float *out_lse, int32_t *out_top1, void *workspace,
+                           size_t workspace_bytes, tim_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * Processed (top-k, then top-p) selected-token logprob.
  *
  * "Debugging Logprob Mismatches in LLM Reinforcement Learning", Make Sure

@@ -35,7 +35,8 @@ from .compare import (  # noqa: F401
     compare_bitwise,
 )
 from .processed import oracle_processed_logprob, process_row  # noqa: F401
-from .fp8 import e4m3_round, fp8_scale, oracle_logprob_fp8, quantize_rows  # noqa: F401
+from .fp8 import (e4m3_round, fp8_scale, oracle_logprob_fp8, quantize_rows,  # noqa: F401
+                  rmsnorm_fp32)
 from .diag import (  # noqa: F401
     FLAG_QUANTILE_SKIPPED, QUANTILE_MAX_TOKENS, QUANTILES, oracle_diag, oracle_diag_lenient,
     quantile_linear,

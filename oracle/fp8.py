@@ -18,6 +18,27 @@ nor the scaling granularity; the readings taken here:
 * logits z = sum_i DQ(y)_i DQ(W)_vi -- the same value native FP8 MMA produces
   from the codes when both scales are applied after accumulation -- then the
   same softmax definition as ``oracle.logprob``.
+
+Precision of y.  The e4m3 code of an element of y is an integer decided from
+y's bf16 value; one bf16 step of y moves that code across an e4m3 rounding
+boundary with probability about 1/16, and one code step moves a logit by up to
+~1e-2.  An fp64 RMSNorm and an fp32 one round a few y values per million to
+different bf16 neighbours, so the code decision is taken here in fp32, the
+precision the scoring kernel takes it in, with the RMSNorm reduction order
+fixed and stated ("Training and rollout stop disagreeing: vime and RL-Kernel
+...", Interpretation: the strict path pins the RMSNorm reduction domain, and a
+fixed order is what makes a reduction batch-invariant):
+
+* 32 partial sums; partial l adds h_i^2 for the 8-element chunks l, l+32,
+  l+64, ... of the row in increasing order (each square is exact in fp32: a
+  bf16 value has 8 significant bits), every addition rounded to fp32;
+* the partials combine by the butterfly s_l <- s_l + s_(l xor o) for
+  o = 16, 8, 4, 2, 1, rounded to fp32 (every partial ends equal);
+* rstd = 1 / sqrt(s / d + eps) and y = bf16((h * rstd) * gamma), each
+  operation rounded to fp32 (round to nearest even), then to bf16.
+
+``rmsnorm_fp32`` is that computation; ``oracle_logprob_fp8(...,
+y_precision="fp64")`` uses the fp64 RMSNorm of ``oracle.logprob`` instead.
 """
 from __future__ import annotations
 
@@ -25,7 +46,7 @@ import math
 
 import numpy as np
 
-from .logprob import lse_stats, rmsnorm, widen_bf16, _top2_gap
+from .logprob import lse_stats, rmsnorm, round_to_bf16, widen_bf16, _top2_gap
 
 E4M3_MAX = 448.0
 
@@ -57,9 +78,40 @@ def quantize_rows(x: np.ndarray):
     return codes, scales
 
 
+def rmsnorm_fp32(h: np.ndarray, gamma: np.ndarray, eps: float, return_rstd: bool = False):
+    """y = bf16((h * rstd) * gamma) with every step in fp32 and the reduction order stated
+    in the module docstring.  h, gamma: fp64 arrays holding bf16 values.  Returns y as fp64
+    (and the fp32 rstd of each row with ``return_rstd``)."""
+    f32 = np.float32
+    h = np.asarray(h, dtype=np.float64)
+    T, d = h.shape
+    nvec = -(-d // 8)
+    nchunk = -(-nvec // 32)
+    hp = np.zeros((T, nchunk * 32 * 8))
+    hp[:, :d] = h
+    hp = hp.reshape(T, nchunk, 32, 8)            # [row, round, partial, element]
+    part = np.zeros((T, 32), dtype=f32)
+    for c in range(nchunk):
+        for i in range(8):
+            sq = hp[:, c, :, i] ** 2                 # exact
+            part = (part.astype(np.float64) + sq).astype(f32)
+    lanes = np.arange(32)
+    for o in (16, 8, 4, 2, 1):
+        part = part + part[:, lanes ^ o]             # fp32 additions
+    ss = part[:, 0]
+    rstd = f32(1.0) / np.sqrt(ss / f32(d) + f32(eps))
+    y32 = (h.astype(f32) * rstd[:, None]) * np.asarray(gamma, dtype=np.float64).astype(f32)[None, :]
+    y = round_to_bf16(y32.astype(np.float64))
+    return (y, rstd) if return_rstd else y
+
+
 def oracle_logprob_fp8(hidden_bits, gamma_bits, W_bits, token_ids, temperature: float,
-                       eps: float, row_block: int = 128, vocab_block: int = 8192):
+                       eps: float, row_block: int = 128, vocab_block: int = 8192,
+                       y_precision: str = "fp32"):
     """Scores with FP8-quantised y and W.  Same output dict as oracle_logprob."""
+    if y_precision not in ("fp32", "fp64"):
+        raise ValueError("y_precision must be 'fp32' or 'fp64'")
+    norm = rmsnorm_fp32 if y_precision == "fp32" else rmsnorm
     hidden_bits = np.asarray(hidden_bits, dtype=np.uint16)
     T = hidden_bits.shape[0]
     V = W_bits.shape[0]
@@ -75,7 +127,7 @@ def oracle_logprob_fp8(hidden_bits, gamma_bits, W_bits, token_ids, temperature: 
                nonfinite=np.zeros(T, dtype=bool))
     for r0 in range(0, T, row_block):
         r1 = min(T, r0 + row_block)
-        y = rmsnorm(widen_bf16(hidden_bits[r0:r1]), gamma, eps)
+        y = norm(widen_bf16(hidden_bits[r0:r1]), gamma, eps)
         cy, sy = quantize_rows(y)
         z = (cy * sy[:, None]) @ Wq.T
         s, lse = lse_stats(z, temperature)

@@ -72,6 +72,10 @@ _SIGNATURES = {
     "tim_compare": (_c.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _i64, _f32, _vp, _vp, _vp, _sz,
                                _vp]),
     "tim_compare_diag_workspace_size": (_sz, [_i64, _i32]),
+    "tim_quantize_fp8_rows": (_c.c_int, [_vp, _i64, _i32, _vp, _vp, _vp]),
+    "tim_logprob_fp8_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "tim_logprob_fp8": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _vp, _vp,
+                                   _vp, _vp, _sz, _vp]),
     "tim_processed_logprob_workspace_size": (_sz, [_i64, _i32, _i32]),
     "tim_processed_logprob": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _i32,
                                          _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -343,6 +347,48 @@ def diag_to_dicts(arr) -> list:
         dct["mis_kept"] = int(r["mis_kept"])
         dct["flags"] = int(r["flags"])
         out.append(dct)
+    return out
+
+
+def quantize_fp8_rows(x, *, stream=None):
+    """Per-row e4m3 quantisation of a bf16 [rows, K] CUDA tensor: returns (codes uint8
+    [rows, K], scales float32 [rows]) (tim_quantize_fp8_rows)."""
+    torch = _torch()
+    x = _as_bf16(x, "x")
+    rows, K = x.shape
+    codes = torch.empty(rows, K, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check(lib().tim_quantize_fp8_rows(_ptr(x), rows, K, _ptr(codes), _ptr(scales),
+                                       _stream_ptr(stream)), "tim_quantize_fp8_rows")
+    return codes, scales
+
+
+def logprob_fp8(hidden, gamma, W_codes, W_scales, token_ids, temperature: float, eps: float, *,
+                out=None, workspace: Optional[Workspace] = None, stream=None, check: bool = True):
+    """FP8-head score (tim_logprob_fp8) with W quantised by quantize_fp8_rows.
+    Returns (logprob, lse, top1) like ``logprob``."""
+    torch = _torch()
+    hidden = _as_bf16(hidden, "hidden")
+    gamma = _as_bf16(gamma, "gamma")
+    _need(W_codes, torch.uint8, "W_codes", 2)
+    _need(W_scales, torch.float32, "W_scales", 1)
+    _need(token_ids, torch.int32, "token_ids", 1)
+    T, d = hidden.shape
+    V = W_codes.shape[0]
+    dev = hidden.device
+    if out is None:
+        out = (torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = Workspace(int(lib().tim_logprob_fp8_workspace_size(T, d, V)), dev, stream)
+    code = lib().tim_logprob_fp8(_ptr(hidden), _ptr(gamma), _ptr(W_codes), _ptr(W_scales),
+                                 _ptr(token_ids), T, d, V, float(temperature), float(eps),
+                                 _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), workspace.ptr,
+                                 workspace.nbytes, _stream_ptr(stream))
+    _check(code, "tim_logprob_fp8")
+    if check:
+        workspace.check("tim_logprob_fp8", stream)
     return out
 
 

@@ -24,6 +24,12 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
                                     int d, int V, int v0, float temperature, void* part,
                                     float* tgt, int* status, cudaStream_t stream, int num_sms);
 void vocab_shard_range(int V, int G, int g, int* v0, int* v_len);
+cudaError_t launch_quantize_rows_e4m3(const void* x, int64_t rows, int K, void* codes,
+                                      float* scales, cudaStream_t stream);
+cudaError_t launch_lmhead_lse_fp8(const void* y8, const float* sy, const void* W8,
+                                  const float* sw, const int32_t* ids, int64_t T, int d, int V,
+                                  float temperature, void* part, float* tgt, int* status,
+                                  cudaStream_t stream, int num_sms);
 cudaError_t launch_lmhead_collect(const void* y, const void* W, const int32_t* ids, int64_t T,
                                   int d, int V, float temperature, const float* thr, int* cnt,
                                   void* cand, int cap, int* status, cudaStream_t stream,
@@ -125,6 +131,22 @@ ProcLayout processed_layout(int64_t T, int32_t d, int32_t V) {
   P.cand_off = align_up(P.cnt_off + static_cast<size_t>(T) * 4, 1024);
   P.total = align_up(P.cand_off + static_cast<size_t>(T) * TIM_PROCESSED_CAPACITY * 8, 1024);
   return P;
+}
+
+// FP8 workspace: the scoring workspace, then y codes [rows_padded(T), d] and
+// their per-row scales [rows_padded(T)].
+struct Fp8Layout {
+  WsLayout base;
+  size_t y8_off, sy_off, total;
+};
+Fp8Layout fp8_layout(int64_t T, int32_t d, int32_t V) {
+  Fp8Layout F;
+  F.base = logprob_layout(T, d, V);
+  const size_t rows = static_cast<size_t>(rows_padded(T));
+  F.y8_off = align_up(F.base.total, 1024);
+  F.sy_off = align_up(F.y8_off + rows * static_cast<size_t>(d), 1024);
+  F.total = align_up(F.sy_off + rows * 4, 1024);
+  return F;
 }
 
 bool valid_shard(int32_t G, int32_t g) {
@@ -277,6 +299,62 @@ tim_status tim_compare(const float* lp_gen, const float* lp_replay, const float*
   return from_cuda(launch_seg_compare(lp_gen, lp_replay, lp_train, seq_offsets, n_seq, mask, T,
                                       tis_cap, out_stats, out_tis_w, workspace,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+tim_status tim_quantize_fp8_rows(const void* x, int64_t rows, int32_t K, void* codes,
+                                 float* scales, tim_stream_t stream) {
+  if (x == nullptr || codes == nullptr || scales == nullptr) return TIM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 8) || !aligned(scales, 4)) return TIM_ERR_INVALID_ARG;
+  if (rows < 1 || rows > INT32_MAX || K < 16 || (K % 16) != 0) return TIM_ERR_SHAPE;
+  tim_status s = check_device(nullptr);
+  if (s != TIM_OK) return s;
+  return from_cuda(launch_quantize_rows_e4m3(x, rows, K, codes, scales,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t tim_logprob_fp8_workspace_size(int64_t T, int32_t d, int32_t V) {
+  if (check_shape(T, d, V) != TIM_OK || (d % 128) != 0) return 0;
+  return fp8_layout(T, d, V).total;
+}
+
+tim_status tim_logprob_fp8(const void* hidden, const void* gamma, const void* W_codes,
+                           const float* W_scales, const int32_t* token_ids, int64_t T, int32_t d,
+                           int32_t V, float temperature, float eps, float* out_logprob,
+                           float* out_lse, int32_t* out_top1, void* workspace,
+                           size_t workspace_bytes, tim_stream_t stream) {
+  if (hidden == nullptr || gamma == nullptr || W_codes == nullptr || W_scales == nullptr ||
+      token_ids == nullptr || out_logprob == nullptr || out_lse == nullptr ||
+      out_top1 == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(gamma, 16) || !aligned(W_codes, 16) ||
+      !aligned(W_scales, 4) || !aligned(token_ids, 4) || !aligned(out_logprob, 4) ||
+      !aligned(out_lse, 4) || !aligned(out_top1, 4))
+    return TIM_ERR_INVALID_ARG;
+  tim_status s = check_shape(T, d, V);
+  if (s != TIM_OK) return s;
+  if ((d % 128) != 0) return TIM_ERR_SHAPE;
+  if ((s = check_scalars(temperature, eps)) != TIM_OK) return s;
+  const Fp8Layout F = fp8_layout(T, d, V);
+  if ((s = check_workspace(workspace, workspace_bytes, F.total)) != TIM_OK) return s;
+  int sms = 0;
+  if ((s = check_device(&sms)) != TIM_OK) return s;
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(b + F.base.status_off);
+  void* y = b + F.base.y_off;
+  void* part = b + F.base.part_off;
+  float* tgt = reinterpret_cast<float*>(b + F.base.tgt_off);
+  void* y8 = b + F.y8_off;
+  float* sy = reinterpret_cast<float*>(b + F.sy_off);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_rmsnorm_rows(hidden, gamma, T, d, eps, y, status, st) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  if (launch_quantize_rows_e4m3(y, rows_padded(T), d, y8, sy, st) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  if (launch_lmhead_lse_fp8(y8, sy, W_codes, W_scales, token_ids, T, d, V, temperature, part, tgt,
+                            status, st, sms) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  return from_cuda(launch_lse_finalize(part, tgt, token_ids, T, V, out_logprob, out_lse, out_top1,
+                                       status, st));
 }
 
 size_t tim_processed_logprob_workspace_size(int64_t T, int32_t d, int32_t V) {

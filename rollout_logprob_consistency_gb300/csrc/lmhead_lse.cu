@@ -70,6 +70,9 @@ struct GemmArgs {
   int* cnt;
   uint2* cand;
   int cap;
+  // e4m3 operands only: per-row scales of y and per-vocabulary-row scales of W
+  const float* sy;
+  const float* sw;
 };
 
 constexpr size_t kGemmSmemBytes =
@@ -142,7 +145,10 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], int nval
 // kMode 1: candidate collection -- every logit >= the row's threshold is appended
 //          (in no particular order) to the row's candidate slots; used by the
 //          processed (top-k / top-p) score, which sorts the candidates afterwards.
-template <int kMode>
+// kFp8: operands are e4m3 codes (kind::f8f6f4, 128 K-elements per 128-byte
+// stage row) and the epilogue multiplies each logit by s_y[row] * s_W[col]
+// (powers of two, so the scaling is exact).
+template <int kMode, bool kFp8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     lmhead_lse_kernel(const __grid_constant__ CUtensorMap tmap_y,
                       const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
@@ -163,6 +169,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  constexpr int kKElems = kFp8 ? 2 * kBK : kBK;  // K elements per 128-byte stage row
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -206,11 +213,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int pre = min(kStages, a.num_kb);
           for (int s = 0; s < pre; ++s) {
             mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
-            tma_load_2d(sB + s * kBBytes, &tmap_w, s * kBK, n * kBN, &full[s]);
+            tma_load_2d(sB + s * kBBytes, &tmap_w, s * kKElems, n * kBN, &full[s]);
           }
           pdl_wait();
           for (int s = 0; s < pre; ++s) {
-            tma_load_2d(sA + s * kABytes, &tmap_y, s * kBK, m * kBM, &full[s]);
+            tma_load_2d(sA + s * kABytes, &tmap_y, s * kKElems, m * kBM, &full[s]);
             last_parity[s] = 0;
           }
           stage = pre % kStages;
@@ -224,8 +231,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
-          tma_load_2d(sA + stage * kABytes, &tmap_y, kb * kBK, m * kBM, &full[stage]);
-          tma_load_2d(sB + stage * kBBytes, &tmap_w, kb * kBK, n * kBN, &full[stage]);
+          tma_load_2d(sA + stage * kABytes, &tmap_y, kb * kKElems, m * kBM, &full[stage]);
+          tma_load_2d(sB + stage * kBBytes, &tmap_w, kb * kKElems, n * kBN, &full[stage]);
           last_parity[stage] = ph;
           if (++stage == kStages) {
             stage = 0;
@@ -239,7 +246,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16_f32(kBM, kBN);
+      const uint32_t idesc =
+          kFp8 ? umma_idesc_e4m3_f32(kBM, kBN) : umma_idesc_bf16_f32(kBM, kBN);
       int stage = 0;
       uint32_t ph = 0;
       uint32_t acc = 0, acc_ph = 0;
@@ -260,9 +268,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a0 = smem_u32(sA + stage * kABytes);
           const uint32_t b0 = smem_u32(sB + stage * kBBytes);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
-            umma_bf16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
-                      idesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of K per 128-byte row
+            if constexpr (kFp8)
+              umma_e4m3(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
+                        idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              umma_bf16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
+                        idesc, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == kStages) {
@@ -304,6 +316,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int bi = col_base;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
       if constexpr (kMode == 0) {
+        const float srow = kFp8 ? __ldg(a.sy + row) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           const int col0 = col_base + c * 32;
@@ -311,6 +324,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint32_t r[32];
           tmem_ld32(tbase + c * 32, r);
           const int nvalid = min(32, a.v_end - col0);
+          if constexpr (kFp8) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float sc = srow * __ldg(a.sw + min(col0 + j, a.v_end - 1));
+              r[j] = __float_as_uint(__uint_as_float(r[j]) * sc);
+            }
+          }
           if (nvalid == 32)
             epilogue_chunk<false>(r, 32, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
           else
@@ -386,28 +406,31 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// bf16 [rows, d] row-major, box = [box_rows x 64] with 128-byte swizzle,
-// out-of-range rows read as zeros.
+// [rows, d] row-major operand (bf16, or e4m3 codes when fp8), box = one
+// 128-byte row of K x box_rows rows with 128-byte swizzle; rows past the end
+// read as zeros.
 static bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t d,
-                            uint32_t box_rows) {
+                            uint32_t box_rows, bool fp8 = false) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
+  const uint64_t esize = fp8 ? 1 : 2;
   const cuuint64_t dims[2] = {d, rows};
-  const cuuint64_t strides[1] = {d * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  const cuuint64_t strides[1] = {d * esize};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r =
-      enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int kMode>
+template <int kMode, bool kFp8>
 static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_w,
                                const GemmArgs& a, cudaStream_t stream, int num_sms,
                                bool programmatic) {
-  cudaError_t e = cudaFuncSetAttribute(lmhead_lse_kernel<kMode>,
+  cudaError_t e = cudaFuncSetAttribute(lmhead_lse_kernel<kMode, kFp8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kGemmSmemBytes));
   if (e != cudaSuccess) return e;
@@ -425,15 +448,15 @@ static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = programmatic ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, lmhead_lse_kernel<kMode>, map_y, map_w, a);
+  return cudaLaunchKernelEx(&cfg, lmhead_lse_kernel<kMode, kFp8>, map_y, map_w, a);
 }
 
 static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w, const void* y,
                              const void* W, const int32_t* ids, int64_t T, int d, int V, int v0,
-                             float temperature, int* status) {
+                             float temperature, int* status, bool fp8 = false) {
   if (!make_kmajor_map(&map_y, y, static_cast<uint64_t>(rows_padded(T)),
-                       static_cast<uint64_t>(d), kBM) ||
-      !make_kmajor_map(&map_w, W, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN))
+                       static_cast<uint64_t>(d), kBM, fp8) ||
+      !make_kmajor_map(&map_w, W, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN, fp8))
     return cudaErrorInvalidValue;
   a.T = T;
   a.v0 = v0;
@@ -441,7 +464,7 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   a.d = d;
   a.num_m = static_cast<int>((T + kBM - 1) / kBM);
   a.num_n = (V + kBN - 1) / kBN;
-  a.num_kb = d / kBK;
+  a.num_kb = fp8 ? d / (2 * kBK) : d / kBK;
   a.group_m = 48;
   a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
   a.k2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
@@ -454,6 +477,8 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   a.cnt = nullptr;
   a.cand = nullptr;
   a.cap = 0;
+  a.sy = nullptr;
+  a.sw = nullptr;
   return cudaSuccess;
 }
 
@@ -474,7 +499,24 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
   // (3 ms at 32768 rows), so larger batches are launched in stream order.  The
   // arithmetic is identical either way.
   const bool programmatic = a.num_m <= a.group_m;
-  return launch_gemm<0>(map_y, map_w, a, stream, num_sms, programmatic);
+  return launch_gemm<0, false>(map_y, map_w, a, stream, num_sms, programmatic);
+}
+
+// FP8 head: y8 e4m3 [rows_padded(T), d] with per-row scales sy, W8 e4m3 [V, d]
+// with per-row scales sw (d a multiple of 128).
+cudaError_t launch_lmhead_lse_fp8(const void* y8, const float* sy, const void* W8,
+                                  const float* sw, const int32_t* ids, int64_t T, int d, int V,
+                                  float temperature, void* part, float* tgt, int* status,
+                                  cudaStream_t stream, int num_sms) {
+  CUtensorMap map_y, map_w;
+  GemmArgs a;
+  cudaError_t e = make_args(a, map_y, map_w, y8, W8, ids, T, d, V, 0, temperature, status, true);
+  if (e != cudaSuccess) return e;
+  a.part = static_cast<float4*>(part);
+  a.tgt = tgt;
+  a.sy = sy;
+  a.sw = sw;
+  return launch_gemm<0, true>(map_y, map_w, a, stream, num_sms, false);
 }
 
 // Candidate collection pass of the processed score: logits >= thr[row] are
@@ -493,7 +535,7 @@ cudaError_t launch_lmhead_collect(const void* y, const void* W, const int32_t* i
   a.cnt = cnt;
   a.cand = static_cast<uint2*>(cand);
   a.cap = cap;
-  return launch_gemm<1>(map_y, map_w, a, stream, num_sms, false);
+  return launch_gemm<1, false>(map_y, map_w, a, stream, num_sms, false);
 }
 
 cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T,

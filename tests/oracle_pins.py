@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import json
 import math
+import struct
 import os
 from fractions import Fraction
 
@@ -823,7 +824,8 @@ def pin_fp8_quantized_dot_product():
     """Random rows: z_fp8 = (Q(y) s_y) . (Q(W) s_W) written out term by term in exact rational
     arithmetic matches the oracle's logits to 1e-12."""
     b = synth.make_custom(T=2, d=64, V=12, tag="fp8dot")
-    y = oracle.rmsnorm(oracle.widen_bf16(b.hidden_gen), oracle.widen_bf16(b.head.gamma), b.eps)
+    y = oracle.rmsnorm_fp32(oracle.widen_bf16(b.hidden_gen), oracle.widen_bf16(b.head.gamma),
+                            b.eps)
     Wf = oracle.widen_bf16(b.head.W)
     out = oracle.oracle_logprob_fp8(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 1.0, b.eps)
     for t in range(2):
@@ -838,6 +840,70 @@ def pin_fp8_quantized_dot_product():
         lse = m + math.log(sum(math.exp(v - m) for v in zs))
         assert abs(out["lse"][t] - lse) < 1e-12
         assert abs(out["logprob"][t] - (zs[b.token_ids[t]] - lse)) < 1e-12
+
+
+def _f32(x: float) -> float:
+    """Round a Python float (fp64) to the nearest fp32 value, ties to even."""
+    return struct.unpack("<f", struct.pack("<f", x))[0]
+
+
+def _rmsnorm_fp32_scalar(h_row, g_row, eps):
+    """The fixed-order fp32 RMSNorm of one row written as plain scalar steps: 32 partial
+    sums over interleaved 8-element chunks, a butterfly over the partials, then
+    rstd and y.  Rounding fp64 results of +, /, sqrt to fp32 equals the fp32 operation
+    itself (fp64 carries more than 2 x 24 + 2 bits, so the double rounding is harmless)."""
+    d = len(h_row)
+    part = [0.0] * 32
+    for c in range(0, -(-d // 8)):
+        lane = c % 32
+        for i in range(8):
+            k = 8 * c + i
+            if k < d:
+                sq = h_row[k] * h_row[k]
+                assert Fraction(part[lane]) + Fraction(sq) == Fraction(part[lane] + sq)
+                part[lane] = _f32(part[lane] + sq)
+    for o in (16, 8, 4, 2, 1):
+        part = [_f32(part[l] + part[l ^ o]) for l in range(32)]
+    assert len(set(part)) == 1
+    rstd = _f32(1.0 / _f32(math.sqrt(_f32(_f32(part[0] / d) + _f32(eps)))))
+    y = [_f32(_f32(h_row[k] * rstd) * g_row[k]) for k in range(d)]
+    return y, rstd
+
+
+def pin_rmsnorm_fp32_scalar():
+    """The vectorised fixed-order fp32 RMSNorm equals the same steps written as scalar
+    Python arithmetic rounded to fp32 after every operation (rstd bit-exact, y bit-exact),
+    for d with a partial last round of chunks (320) and with fewer chunks than partials
+    (96)."""
+    for d, tag in ((320, "r320"), (96, "r96")):
+        b = synth.make_custom(T=12, d=d, V=4, tag=tag)
+        h = oracle.widen_bf16(b.hidden_gen)
+        g = oracle.widen_bf16(b.head.gamma)
+        y, rstd = oracle.rmsnorm_fp32(h, g, b.eps, return_rstd=True)
+        for t in range(h.shape[0]):
+            ys, rs = _rmsnorm_fp32_scalar([float(v) for v in h[t]], [float(v) for v in g], b.eps)
+            assert float(rstd[t]) == rs, (d, t)
+            assert np.array_equal(y[t], oracle.round_to_bf16(np.array(ys))), (d, t)
+
+
+def pin_rmsnorm_fp32_against_fp64():
+    """The fp32 RMSNorm agrees with the fp64 one: rstd to 2^-18 relative, y within one bf16
+    step everywhere and equal in all but a few elements per 10^4; with |h| = 2 everywhere
+    and eps = 0 every step is exact and both equal (h / 2) * gamma rounded to bf16."""
+    b = synth.make_custom(T=64, d=2048, V=4, tag="r2048")
+    h = oracle.widen_bf16(b.hidden_gen)
+    g = oracle.widen_bf16(b.head.gamma)
+    y32, rstd = oracle.rmsnorm_fp32(h, g, b.eps, return_rstd=True)
+    rstd64 = 1.0 / np.sqrt(np.mean(h * h, axis=1) + b.eps)
+    assert np.max(np.abs(rstd / rstd64 - 1.0)) < 2.0 ** -18
+    y64 = oracle.rmsnorm(h, g, b.eps)
+    step = np.ldexp(1.0, np.frexp(np.maximum(np.abs(y32), np.abs(y64)))[1] - 8)
+    assert np.all(np.abs(y32 - y64) <= step)
+    assert np.mean(y32 != y64) < 1e-3
+    hh = np.where(np.arange(256) % 3 == 0, -2.0, 2.0)[None, :].repeat(3, axis=0)
+    gg = oracle.widen_bf16(b.head.gamma[:256])
+    assert np.array_equal(oracle.rmsnorm_fp32(hh, gg, 0.0), oracle.round_to_bf16(hh / 2 * gg))
+    assert np.array_equal(oracle.rmsnorm(hh, gg, 0.0), oracle.rmsnorm_fp32(hh, gg, 0.0))
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

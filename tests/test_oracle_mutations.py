@@ -195,6 +195,28 @@ def _scale_max_over_448(amax):
     return amax / 448.0 if amax else 1.0
 
 
+_orig_rmsnorm_fp32 = of8.rmsnorm_fp32
+
+
+def _rms32_in_fp64(h, gamma, eps, return_rstd=False):
+    h = np.asarray(h, dtype=np.float64)
+    rstd = 1.0 / np.sqrt(np.mean(h * h, axis=1) + eps)
+    y = ol.round_to_bf16(h * rstd[:, None] * np.asarray(gamma)[None, :])
+    return (y, rstd) if return_rstd else y
+
+
+def _rms32_sequential_partials(h, gamma, eps, return_rstd=False):
+    f32 = np.float32
+    h = np.asarray(h, dtype=np.float64)
+    ss = np.zeros(h.shape[0], dtype=f32)
+    for k in range(h.shape[1]):                      # one running sum, element order
+        ss = (ss.astype(np.float64) + h[:, k] ** 2).astype(f32)
+    rstd = f32(1.0) / np.sqrt(ss / f32(h.shape[1]) + f32(eps))
+    y = ol.round_to_bf16(((h.astype(f32) * rstd[:, None]) *
+                          np.asarray(gamma).astype(f32)[None, :]).astype(np.float64))
+    return (y, rstd) if return_rstd else y
+
+
 MUTATIONS = [
     ("temperature after softmax", ol, "lse_stats", _lse_after_softmax, ["pin_v8_temperature"]),
     ("no max shift", ol, "lse_stats", _lse_no_shift, ["pin_large_logits"]),
@@ -234,6 +256,10 @@ MUTATIONS = [
     ("e4m3 with two mantissa bits", of8, "e4m3_round", _e4m3_two_mantissa_bits,
      ["pin_e4m3_rounding_exhaustive"]),
     ("non-power-of-two scale", of8, "fp8_scale", _scale_max_over_448, ["pin_fp8_scale_rule"]),
+    ("fp32 RMSNorm computed in fp64", of8, "rmsnorm_fp32", _rms32_in_fp64,
+     ["pin_rmsnorm_fp32_scalar"]),
+    ("fp32 RMSNorm with one running sum", of8, "rmsnorm_fp32", _rms32_sequential_partials,
+     ["pin_rmsnorm_fp32_scalar"]),
 ]
 
 
