@@ -276,6 +276,37 @@ tim_status tim_logprob_fp8(const void *hidden, const void *gamma, const void *W_
                            size_t workspace_bytes, tim_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * FP32 variant of the linear logprob.
+ *
+ * "Rollout-Training Mismatch in LLM RL", section 4.3 (an FP32 rollout LM head)
+ * and section 5.2 (wider arithmetic beside the aligned forward): the head in
+ * fp32.  y = (h * rstd) * gamma stays fp32 (no bf16 rounding; RMSNorm as in
+ * tim_logprob otherwise) and W is fp32 [V, d] (fp32 master weights, or bf16
+ * weights widened).  The GEMM runs on the tcgen05 tensor cores as three tf32
+ * products per K step: each fp32 operand x is given as big = x with its low 13
+ * mantissa bits cleared (a tf32 value) and small = x - big (exact), and
+ * z = big_y.big_W + big_y.small_W + small_y.big_W with fp32 accumulation
+ * (the dropped small.small term is below 2^-20 of each product).  Everything
+ * after the logits is the tim_logprob path.  Batch-invariant like tim_logprob.
+ *
+ * tim_split_tf32: x fp32 [n] -> big, small fp32 [n] (all 16-byte aligned, n a
+ *   multiple of 4).  Asynchronous on `stream`.  Run once per weight version on
+ *   W (the caller keeps W_big and W_small, 8 V d bytes).
+ * tim_logprob_fp32: as tim_logprob, with W_big / W_small fp32 [V, d] from
+ *   tim_split_tf32 and a workspace of tim_logprob_fp32_workspace_size bytes.
+ * ------------------------------------------------------------------------ */
+tim_status tim_split_tf32(const float *x, int64_t n, float *big, float *small,
+                          tim_stream_t stream);
+
+size_t tim_logprob_fp32_workspace_size(int64_t T, int32_t d, int32_t V);
+
+tim_status tim_logprob_fp32(const void *hidden, const void *gamma, const float *W_big,
+                            const float *W_small, const int32_t *token_ids, int64_t T, int32_t d,
+                            int32_t V, float temperature, float eps, float *out_logprob,
+                            float *out_lse, int32_t *out_top1, void *workspace,
+                            size_t workspace_bytes, tim_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * Processed (top-k, then top-p) selected-token logprob.
  *
  * "Debugging Logprob Mismatches in LLM Reinforcement Learning", Make Sure

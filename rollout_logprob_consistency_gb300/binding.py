@@ -76,6 +76,10 @@ _SIGNATURES = {
     "tim_logprob_fp8_workspace_size": (_sz, [_i64, _i32, _i32]),
     "tim_logprob_fp8": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _vp, _vp,
                                    _vp, _vp, _sz, _vp]),
+    "tim_split_tf32": (_c.c_int, [_vp, _i64, _vp, _vp, _vp]),
+    "tim_logprob_fp32_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "tim_logprob_fp32": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _vp, _vp,
+                                    _vp, _vp, _sz, _vp]),
     "tim_processed_logprob_workspace_size": (_sz, [_i64, _i32, _i32]),
     "tim_processed_logprob": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _i32,
                                          _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -389,6 +393,48 @@ def logprob_fp8(hidden, gamma, W_codes, W_scales, token_ids, temperature: float,
     _check(code, "tim_logprob_fp8")
     if check:
         workspace.check("tim_logprob_fp8", stream)
+    return out
+
+
+def split_tf32(x, *, stream=None):
+    """tf32 split of an fp32 CUDA tensor (tim_split_tf32): returns (big, small), same shape."""
+    torch = _torch()
+    _need(x, torch.float32, "x")
+    big = torch.empty_like(x)
+    small = torch.empty_like(x)
+    _check(lib().tim_split_tf32(_ptr(x), x.numel(), _ptr(big), _ptr(small), _stream_ptr(stream)),
+           "tim_split_tf32")
+    return big, small
+
+
+def logprob_fp32(hidden, gamma, W_big, W_small, token_ids, temperature: float, eps: float, *,
+                 out=None, workspace: Optional[Workspace] = None, stream=None, check: bool = True):
+    """FP32-head score (tim_logprob_fp32) with W split by split_tf32.  Returns (logprob, lse,
+    top1) like ``logprob``."""
+    torch = _torch()
+    hidden = _as_bf16(hidden, "hidden")
+    gamma = _as_bf16(gamma, "gamma")
+    _need(W_big, torch.float32, "W_big", 2)
+    _need(W_small, torch.float32, "W_small", 2)
+    _need(token_ids, torch.int32, "token_ids", 1)
+    if W_big.shape != W_small.shape:
+        raise ValueError("W_big and W_small must have the same shape")
+    T, d = hidden.shape
+    V = W_big.shape[0]
+    dev = hidden.device
+    if out is None:
+        out = (torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = Workspace(int(lib().tim_logprob_fp32_workspace_size(T, d, V)), dev, stream)
+    code = lib().tim_logprob_fp32(_ptr(hidden), _ptr(gamma), _ptr(W_big), _ptr(W_small),
+                                  _ptr(token_ids), T, d, V, float(temperature), float(eps),
+                                  _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), workspace.ptr,
+                                  workspace.nbytes, _stream_ptr(stream))
+    _check(code, "tim_logprob_fp32")
+    if check:
+        workspace.check("tim_logprob_fp32", stream)
     return out
 
 

@@ -26,6 +26,15 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
 void vocab_shard_range(int V, int G, int g, int* v0, int* v_len);
 cudaError_t launch_quantize_rows_e4m3(const void* x, int64_t rows, int K, void* codes,
                                       float* scales, cudaStream_t stream);
+cudaError_t launch_rmsnorm_rows_split(const void* hidden, const void* gamma, int64_t T, int d,
+                                      float eps, float* ybig, float* ysmall, int* status,
+                                      cudaStream_t stream);
+cudaError_t launch_split_tf32(const float* x, int64_t n, float* big, float* small,
+                              cudaStream_t stream, int num_sms);
+cudaError_t launch_lmhead_lse_tf32x3(const float* y_big, const float* y_small, const float* W_big,
+                                     const float* W_small, const int32_t* ids, int64_t T, int d,
+                                     int V, float temperature, void* part, float* tgt,
+                                     int* status, cudaStream_t stream, int num_sms);
 cudaError_t launch_lmhead_lse_fp8(const void* y8, const float* sy, const void* W8,
                                   const float* sw, const int32_t* ids, int64_t T, int d, int V,
                                   float temperature, void* part, float* tgt, int* status,
@@ -146,6 +155,22 @@ Fp8Layout fp8_layout(int64_t T, int32_t d, int32_t V) {
   F.y8_off = align_up(F.base.total, 1024);
   F.sy_off = align_up(F.y8_off + rows * static_cast<size_t>(d), 1024);
   F.total = align_up(F.sy_off + rows * 4, 1024);
+  return F;
+}
+
+// FP32 workspace: the scoring workspace, then the tf32 part and the remainder of
+// y, fp32 [rows_padded(T), d] each.
+struct Fp32Layout {
+  WsLayout base;
+  size_t ybig_off, ysmall_off, total;
+};
+Fp32Layout fp32_layout(int64_t T, int32_t d, int32_t V) {
+  Fp32Layout F;
+  F.base = logprob_layout(T, d, V);
+  const size_t n = static_cast<size_t>(rows_padded(T)) * static_cast<size_t>(d) * 4;
+  F.ybig_off = align_up(F.base.total, 1024);
+  F.ysmall_off = align_up(F.ybig_off + n, 1024);
+  F.total = align_up(F.ysmall_off + n, 1024);
   return F;
 }
 
@@ -352,6 +377,59 @@ tim_status tim_logprob_fp8(const void* hidden, const void* gamma, const void* W_
     return TIM_ERR_CUDA;
   if (launch_lmhead_lse_fp8(y8, sy, W_codes, W_scales, token_ids, T, d, V, temperature, part, tgt,
                             status, st, sms) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  return from_cuda(launch_lse_finalize(part, tgt, token_ids, T, V, out_logprob, out_lse, out_top1,
+                                       status, st));
+}
+
+tim_status tim_split_tf32(const float* x, int64_t n, float* big, float* small,
+                          tim_stream_t stream) {
+  if (x == nullptr || big == nullptr || small == nullptr) return TIM_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(big, 16) || !aligned(small, 16)) return TIM_ERR_INVALID_ARG;
+  if (n < 4 || (n % 4) != 0) return TIM_ERR_SHAPE;
+  int sms = 0;
+  tim_status s = check_device(&sms);
+  if (s != TIM_OK) return s;
+  return from_cuda(launch_split_tf32(x, n, big, small, reinterpret_cast<cudaStream_t>(stream), sms));
+}
+
+size_t tim_logprob_fp32_workspace_size(int64_t T, int32_t d, int32_t V) {
+  if (check_shape(T, d, V) != TIM_OK) return 0;
+  return fp32_layout(T, d, V).total;
+}
+
+tim_status tim_logprob_fp32(const void* hidden, const void* gamma, const float* W_big,
+                            const float* W_small, const int32_t* token_ids, int64_t T, int32_t d,
+                            int32_t V, float temperature, float eps, float* out_logprob,
+                            float* out_lse, int32_t* out_top1, void* workspace,
+                            size_t workspace_bytes, tim_stream_t stream) {
+  if (hidden == nullptr || gamma == nullptr || W_big == nullptr || W_small == nullptr ||
+      token_ids == nullptr || out_logprob == nullptr || out_lse == nullptr ||
+      out_top1 == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(gamma, 16) || !aligned(W_big, 16) ||
+      !aligned(W_small, 16) || !aligned(token_ids, 4) || !aligned(out_logprob, 4) ||
+      !aligned(out_lse, 4) || !aligned(out_top1, 4))
+    return TIM_ERR_INVALID_ARG;
+  tim_status s = check_shape(T, d, V);
+  if (s != TIM_OK) return s;
+  if ((s = check_scalars(temperature, eps)) != TIM_OK) return s;
+  const Fp32Layout F = fp32_layout(T, d, V);
+  if ((s = check_workspace(workspace, workspace_bytes, F.total)) != TIM_OK) return s;
+  int sms = 0;
+  if ((s = check_device(&sms)) != TIM_OK) return s;
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(b + F.base.status_off);
+  void* part = b + F.base.part_off;
+  float* tgt = reinterpret_cast<float*>(b + F.base.tgt_off);
+  float* ybig = reinterpret_cast<float*>(b + F.ybig_off);
+  float* ysmall = reinterpret_cast<float*>(b + F.ysmall_off);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_rmsnorm_rows_split(hidden, gamma, T, d, eps, ybig, ysmall, status, st) !=
+      cudaSuccess)
+    return TIM_ERR_CUDA;
+  if (launch_lmhead_lse_tf32x3(ybig, ysmall, W_big, W_small, token_ids, T, d, V, temperature,
+                               part, tgt, status, st, sms) != cudaSuccess)
     return TIM_ERR_CUDA;
   return from_cuda(launch_lse_finalize(part, tgt, token_ids, T, V, out_logprob, out_lse, out_top1,
                                        status, st));

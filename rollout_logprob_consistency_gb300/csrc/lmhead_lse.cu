@@ -75,6 +75,27 @@ struct GemmArgs {
   const float* sw;
 };
 
+// Operand precision of the GEMM.
+//   kPrecBf16   bf16 y and W, kind::f16, 64 K-elements per 128-byte stage row.
+//   kPrecE4m3   e4m3 codes, kind::f8f6f4, 128 K-elements per stage row; the
+//               epilogue multiplies each logit by s_y[row] * s_W[col] (powers of
+//               two, so the scaling is exact).
+//   kPrecTf32x3 fp32 y and W, each given as a tf32 part (low 13 mantissa bits
+//               cleared) and the exact fp32 remainder; kind::tf32 computes
+//               big*big + big*small + small*big per K step, 32 K-elements per
+//               stage row; a stage holds both parts of both operands, so the
+//               ring has half as many stages in the same shared memory.
+enum Prec : int { kPrecBf16 = 0, kPrecE4m3 = 1, kPrecTf32x3 = 2 };
+
+template <int kPrec>
+struct StageGeom {
+  static constexpr int kParts = kPrec == kPrecTf32x3 ? 2 : 1;
+  static constexpr int kS = kStages / kParts;
+  static constexpr int kStageA = kParts * kABytes;
+  static constexpr int kStageB = kParts * kBBytes;
+  static constexpr int kKElems = kPrec == kPrecE4m3 ? 2 * kBK : kPrec == kPrecTf32x3 ? kBK / 2 : kBK;
+};
+
 constexpr size_t kGemmSmemBytes =
     1024 /* alignment slack */ + kStages * (kABytes + kBBytes) + 256 /* barriers, flags */;
 
@@ -145,19 +166,23 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], int nval
 // kMode 1: candidate collection -- every logit >= the row's threshold is appended
 //          (in no particular order) to the row's candidate slots; used by the
 //          processed (top-k / top-p) score, which sorts the candidates afterwards.
-// kFp8: operands are e4m3 codes (kind::f8f6f4, 128 K-elements per 128-byte
-// stage row) and the epilogue multiplies each logit by s_y[row] * s_W[col]
-// (powers of two, so the scaling is exact).
-template <int kMode, bool kFp8>
+// kPrec: operand precision (see Prec).  tmap_y2 / tmap_w2 are the remainder
+// parts for kPrecTf32x3 and unused otherwise.
+template <int kMode, int kPrec>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     lmhead_lse_kernel(const __grid_constant__ CUtensorMap tmap_y,
-                      const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a) {
+                      const __grid_constant__ CUtensorMap tmap_w,
+                      const __grid_constant__ CUtensorMap tmap_y2,
+                      const __grid_constant__ CUtensorMap tmap_w2, const GemmArgs a) {
+  using G = StageGeom<kPrec>;
+  constexpr bool kFp8 = kPrec == kPrecE4m3;
+  constexpr bool kX3 = kPrec == kPrecTf32x3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint8_t* sB = smem + G::kS * G::kStageA;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + G::kS * G::kStageB);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* acc_full = bars + 2 * kStages;
@@ -169,10 +194,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr int kKElems = kFp8 ? 2 * kBK : kBK;  // K elements per 128-byte stage row
+  constexpr int kKElems = G::kKElems;  // K elements per 128-byte stage row
+  constexpr uint32_t kTx = G::kStageA + G::kStageB;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < G::kS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       last_parity[s] = 0xFFFFFFFFu;  // no load issued into this stage yet
@@ -186,6 +212,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_mbarrier_init();
     prefetch_tmap(&tmap_y);
     prefetch_tmap(&tmap_w);
+    if (kX3) {
+      prefetch_tmap(&tmap_y2);
+      prefetch_tmap(&tmap_w2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, kTmemCols);
@@ -210,18 +240,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (first) {
           // W does not depend on the RMSNorm kernel that precedes this one in the
           // stream: stream the first stages of W before waiting for y to be ready.
-          const int pre = min(kStages, a.num_kb);
+          const int pre = min(G::kS, a.num_kb);
           for (int s = 0; s < pre; ++s) {
-            mbar_arrive_expect_tx(&full[s], kABytes + kBBytes);
-            tma_load_2d(sB + s * kBBytes, &tmap_w, s * kKElems, n * kBN, &full[s]);
+            mbar_arrive_expect_tx(&full[s], kTx);
+            tma_load_2d(sB + s * G::kStageB, &tmap_w, s * kKElems, n * kBN, &full[s]);
+            if (kX3)
+              tma_load_2d(sB + s * G::kStageB + kBBytes, &tmap_w2, s * kKElems, n * kBN, &full[s]);
           }
           pdl_wait();
           for (int s = 0; s < pre; ++s) {
-            tma_load_2d(sA + s * kABytes, &tmap_y, s * kKElems, m * kBM, &full[s]);
+            tma_load_2d(sA + s * G::kStageA, &tmap_y, s * kKElems, m * kBM, &full[s]);
+            if (kX3)
+              tma_load_2d(sA + s * G::kStageA + kABytes, &tmap_y2, s * kKElems, m * kBM, &full[s]);
             last_parity[s] = 0;
           }
-          stage = pre % kStages;
-          ph = (pre == kStages) ? 1u : 0u;
+          stage = pre % G::kS;
+          ph = (pre == G::kS) ? 1u : 0u;
           kb0 = pre;
           first = false;
         }
@@ -230,11 +264,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
-          tma_load_2d(sA + stage * kABytes, &tmap_y, kb * kKElems, m * kBM, &full[stage]);
-          tma_load_2d(sB + stage * kBBytes, &tmap_w, kb * kKElems, n * kBN, &full[stage]);
+          mbar_arrive_expect_tx(&full[stage], kTx);
+          tma_load_2d(sA + stage * G::kStageA, &tmap_y, kb * kKElems, m * kBM, &full[stage]);
+          tma_load_2d(sB + stage * G::kStageB, &tmap_w, kb * kKElems, n * kBN, &full[stage]);
+          if (kX3) {
+            tma_load_2d(sA + stage * G::kStageA + kABytes, &tmap_y2, kb * kKElems, m * kBM,
+                        &full[stage]);
+            tma_load_2d(sB + stage * G::kStageB + kBBytes, &tmap_w2, kb * kKElems, n * kBN,
+                        &full[stage]);
+          }
           last_parity[stage] = ph;
-          if (++stage == kStages) {
+          if (++stage == G::kS) {
             stage = 0;
             ph ^= 1u;
           }
@@ -246,8 +286,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc =
-          kFp8 ? umma_idesc_e4m3_f32(kBM, kBN) : umma_idesc_bf16_f32(kBM, kBN);
+      const uint32_t idesc = kFp8  ? umma_idesc_e4m3_f32(kBM, kBN)
+                             : kX3 ? umma_idesc_tf32_f32(kBM, kBN)
+                                   : umma_idesc_bf16_f32(kBM, kBN);
       int stage = 0;
       uint32_t ph = 0;
       uint32_t acc = 0, acc_ph = 0;
@@ -265,19 +306,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + stage * kABytes);
-          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+          const uint32_t a0 = smem_u32(sA + stage * G::kStageA);
+          const uint32_t b0 = smem_u32(sB + stage * G::kStageB);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // 4 x 32 bytes of K per 128-byte row
-            if constexpr (kFp8)
+            const uint32_t acc_k = (kb | k) != 0 ? 1u : 0u;
+            if constexpr (kFp8) {
               umma_e4m3(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
-                        idesc, (kb | k) != 0 ? 1u : 0u);
-            else
+                        idesc, acc_k);
+            } else if constexpr (kX3) {
+              const uint64_t ab = sw128_kmajor_desc(a0 + k * 32);
+              const uint64_t as = sw128_kmajor_desc(a0 + kABytes + k * 32);
+              const uint64_t bb = sw128_kmajor_desc(b0 + k * 32);
+              const uint64_t bs = sw128_kmajor_desc(b0 + kBBytes + k * 32);
+              umma_tf32(d_tmem, ab, bb, idesc, acc_k);
+              umma_tf32(d_tmem, ab, bs, idesc, 1u);
+              umma_tf32(d_tmem, as, bb, idesc, 1u);
+            } else {
               umma_bf16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
-                        idesc, (kb | k) != 0 ? 1u : 0u);
+                        idesc, acc_k);
+            }
           }
           umma_commit(&empty[stage]);
-          if (++stage == kStages) {
+          if (++stage == G::kS) {
             stage = 0;
             ph ^= 1u;
           }
@@ -374,7 +425,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (*abort_flag) {
     if (warp == 0 && lane == 0) {
       // wait for TMA copies still landing in shared memory
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < G::kS; ++s)
         if (last_parity[s] != 0xFFFFFFFFu) mbar_wait_drain(&full[s], last_parity[s]);
     }
     if (warp == 1 && lane == 0) {
@@ -406,31 +457,33 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// [rows, d] row-major operand (bf16, or e4m3 codes when fp8), box = one
-// 128-byte row of K x box_rows rows with 128-byte swizzle; rows past the end
+// [rows, d] row-major operand (bf16; e4m3 codes; fp32 for the tf32 parts), box =
+// one 128-byte row of K x box_rows rows with 128-byte swizzle; rows past the end
 // read as zeros.
 static bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t d,
-                            uint32_t box_rows, bool fp8 = false) {
+                            uint32_t box_rows, int prec) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
-  const uint64_t esize = fp8 ? 1 : 2;
+  const uint64_t esize = prec == kPrecE4m3 ? 1 : prec == kPrecTf32x3 ? 4 : 2;
+  const CUtensorMapDataType dt = prec == kPrecE4m3     ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : prec == kPrecTf32x3 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const cuuint64_t dims[2] = {d, rows};
   const cuuint64_t strides[1] = {d * esize};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r =
-      enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int kMode, bool kFp8>
+template <int kMode, int kPrec>
 static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_w,
+                               const CUtensorMap& map_y2, const CUtensorMap& map_w2,
                                const GemmArgs& a, cudaStream_t stream, int num_sms,
                                bool programmatic) {
-  cudaError_t e = cudaFuncSetAttribute(lmhead_lse_kernel<kMode, kFp8>,
+  cudaError_t e = cudaFuncSetAttribute(lmhead_lse_kernel<kMode, kPrec>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kGemmSmemBytes));
   if (e != cudaSuccess) return e;
@@ -448,15 +501,16 @@ static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = programmatic ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, lmhead_lse_kernel<kMode, kFp8>, map_y, map_w, a);
+  return cudaLaunchKernelEx(&cfg, lmhead_lse_kernel<kMode, kPrec>, map_y, map_w, map_y2, map_w2,
+                            a);
 }
 
 static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w, const void* y,
                              const void* W, const int32_t* ids, int64_t T, int d, int V, int v0,
-                             float temperature, int* status, bool fp8 = false) {
+                             float temperature, int* status, int prec = kPrecBf16) {
   if (!make_kmajor_map(&map_y, y, static_cast<uint64_t>(rows_padded(T)),
-                       static_cast<uint64_t>(d), kBM, fp8) ||
-      !make_kmajor_map(&map_w, W, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN, fp8))
+                       static_cast<uint64_t>(d), kBM, prec) ||
+      !make_kmajor_map(&map_w, W, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN, prec))
     return cudaErrorInvalidValue;
   a.T = T;
   a.v0 = v0;
@@ -464,7 +518,9 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   a.d = d;
   a.num_m = static_cast<int>((T + kBM - 1) / kBM);
   a.num_n = (V + kBN - 1) / kBN;
-  a.num_kb = fp8 ? d / (2 * kBK) : d / kBK;
+  a.num_kb = prec == kPrecE4m3     ? d / StageGeom<kPrecE4m3>::kKElems
+             : prec == kPrecTf32x3 ? d / StageGeom<kPrecTf32x3>::kKElems
+                                   : d / StageGeom<kPrecBf16>::kKElems;
   a.group_m = 48;
   a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
   a.k2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
@@ -499,7 +555,7 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
   // (3 ms at 32768 rows), so larger batches are launched in stream order.  The
   // arithmetic is identical either way.
   const bool programmatic = a.num_m <= a.group_m;
-  return launch_gemm<0, false>(map_y, map_w, a, stream, num_sms, programmatic);
+  return launch_gemm<0, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, programmatic);
 }
 
 // FP8 head: y8 e4m3 [rows_padded(T), d] with per-row scales sy, W8 e4m3 [V, d]
@@ -510,13 +566,35 @@ cudaError_t launch_lmhead_lse_fp8(const void* y8, const float* sy, const void* W
                                   cudaStream_t stream, int num_sms) {
   CUtensorMap map_y, map_w;
   GemmArgs a;
-  cudaError_t e = make_args(a, map_y, map_w, y8, W8, ids, T, d, V, 0, temperature, status, true);
+  cudaError_t e =
+      make_args(a, map_y, map_w, y8, W8, ids, T, d, V, 0, temperature, status, kPrecE4m3);
   if (e != cudaSuccess) return e;
   a.part = static_cast<float4*>(part);
   a.tgt = tgt;
   a.sy = sy;
   a.sw = sw;
-  return launch_gemm<0, true>(map_y, map_w, a, stream, num_sms, false);
+  return launch_gemm<0, kPrecE4m3>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
+}
+
+// FP32 head: y and W in fp32, each split into a tf32 part and its fp32 remainder:
+// y_big / y_small [rows_padded(T), d], W_big / W_small [V, d] (d a multiple of 32).
+cudaError_t launch_lmhead_lse_tf32x3(const float* y_big, const float* y_small, const float* W_big,
+                                     const float* W_small, const int32_t* ids, int64_t T, int d,
+                                     int V, float temperature, void* part, float* tgt,
+                                     int* status, cudaStream_t stream, int num_sms) {
+  CUtensorMap map_y, map_w, map_y2, map_w2;
+  GemmArgs a;
+  cudaError_t e = make_args(a, map_y, map_w, y_big, W_big, ids, T, d, V, 0, temperature, status,
+                            kPrecTf32x3);
+  if (e != cudaSuccess) return e;
+  if (!make_kmajor_map(&map_y2, y_small, static_cast<uint64_t>(rows_padded(T)),
+                       static_cast<uint64_t>(d), kBM, kPrecTf32x3) ||
+      !make_kmajor_map(&map_w2, W_small, static_cast<uint64_t>(V), static_cast<uint64_t>(d), kBN,
+                       kPrecTf32x3))
+    return cudaErrorInvalidValue;
+  a.part = static_cast<float4*>(part);
+  a.tgt = tgt;
+  return launch_gemm<0, kPrecTf32x3>(map_y, map_w, map_y2, map_w2, a, stream, num_sms, false);
 }
 
 // Candidate collection pass of the processed score: logits >= thr[row] are
@@ -535,7 +613,7 @@ cudaError_t launch_lmhead_collect(const void* y, const void* W, const int32_t* i
   a.cnt = cnt;
   a.cand = static_cast<uint2*>(cand);
   a.cap = cap;
-  return launch_gemm<1, false>(map_y, map_w, a, stream, num_sms, false);
+  return launch_gemm<1, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }
 
 cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T,

@@ -29,6 +29,21 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
   }
 }
 
+// Sum of squares of one row in the fixed order above; every lane returns the same
+// value.
+__device__ __forceinline__ float row_sum_squares(const uint4* h, int nvec, int lane) {
+  float ss = 0.f;
+  for (int c = lane; c < nvec; c += 32) {
+    float f[8];
+    unpack_bf16x8(__ldg(h + c), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  return ss;
+}
+
 __global__ void __launch_bounds__(32 * kNormRowsPerBlock)
     rmsnorm_rows_kernel(const uint4* __restrict__ hidden, const uint4* __restrict__ gamma,
                         int64_t T, int64_t T_pad, int d, float eps, uint4* __restrict__ y,
@@ -46,16 +61,7 @@ __global__ void __launch_bounds__(32 * kNormRowsPerBlock)
   }
   const uint4* h = hidden + row * nvec;
 
-  float ss = 0.f;
-  for (int c = lane; c < nvec; c += 32) {
-    float f[8];
-    unpack_bf16x8(__ldg(h + c), f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-
+  const float ss = row_sum_squares(h, nvec, lane);
   if (!isfinite(ss)) {
     if (lane == 0) set_status(status, TIM_ERR_NONFINITE);
   }
@@ -75,6 +81,94 @@ __global__ void __launch_bounds__(32 * kNormRowsPerBlock)
     }
     out[c] = make_uint4(w[0], w[1], w[2], w[3]);
   }
+}
+
+// FP32 head: the same RMSNorm with y kept in fp32 (no bf16 rounding), written as
+// a tf32 part (the low 13 mantissa bits cleared) and the remainder y - big,
+// which fp32 holds exactly.  Rows T .. T_pad-1 are written as zeros.
+__global__ void __launch_bounds__(32 * kNormRowsPerBlock)
+    rmsnorm_rows_split_kernel(const uint4* __restrict__ hidden, const uint4* __restrict__ gamma,
+                              int64_t T, int64_t T_pad, int d, float eps,
+                              float4* __restrict__ ybig, float4* __restrict__ ysmall,
+                              int* status) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kNormRowsPerBlock + warp;
+  if (row >= T_pad) return;
+  const int nvec = d >> 3;
+  float4* ob = ybig + row * (2 * nvec);
+  float4* os = ysmall + row * (2 * nvec);
+  if (row >= T) {
+    for (int c = lane; c < 2 * nvec; c += 32) {
+      ob[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      os[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+  const uint4* h = hidden + row * nvec;
+  const float ss = row_sum_squares(h, nvec, lane);
+  if (!isfinite(ss)) {
+    if (lane == 0) set_status(status, TIM_ERR_NONFINITE);
+  }
+  const float rstd = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+  for (int c = lane; c < nvec; c += 32) {
+    float f[8], g[8], b[8], r[8];
+    unpack_bf16x8(__ldg(h + c), f);
+    unpack_bf16x8(__ldg(gamma + c), g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // __fmul_rn: the product must be rounded before the subtraction below
+      // (no contraction into a fused multiply-add).
+      const float y = __fmul_rn(__fmul_rn(f[i], rstd), g[i]);
+      b[i] = __uint_as_float(__float_as_uint(y) & 0xFFFFE000u);
+      r[i] = y - b[i];
+    }
+    ob[2 * c] = make_float4(b[0], b[1], b[2], b[3]);
+    ob[2 * c + 1] = make_float4(b[4], b[5], b[6], b[7]);
+    os[2 * c] = make_float4(r[0], r[1], r[2], r[3]);
+    os[2 * c + 1] = make_float4(r[4], r[5], r[6], r[7]);
+  }
+}
+
+// Elementwise tf32 split of fp32 values: big = x with the low 13 mantissa bits
+// cleared, small = x - big (exact).  n4 = number of float4 groups.
+__global__ void split_tf32_kernel(const float4* __restrict__ x, int64_t n4,
+                                  float4* __restrict__ big, float4* __restrict__ small) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = __ldg(x + i);
+    float4 b;
+    b.x = __uint_as_float(__float_as_uint(v.x) & 0xFFFFE000u);
+    b.y = __uint_as_float(__float_as_uint(v.y) & 0xFFFFE000u);
+    b.z = __uint_as_float(__float_as_uint(v.z) & 0xFFFFE000u);
+    b.w = __uint_as_float(__float_as_uint(v.w) & 0xFFFFE000u);
+    big[i] = b;
+    small[i] = make_float4(v.x - b.x, v.y - b.y, v.z - b.z, v.w - b.w);
+  }
+}
+
+cudaError_t launch_rmsnorm_rows_split(const void* hidden, const void* gamma, int64_t T, int d,
+                                      float eps, float* ybig, float* ysmall, int* status,
+                                      cudaStream_t stream) {
+  const int64_t T_pad = rows_padded(T);
+  const int64_t blocks = (T_pad + kNormRowsPerBlock - 1) / kNormRowsPerBlock;
+  rmsnorm_rows_split_kernel<<<static_cast<unsigned>(blocks), 32 * kNormRowsPerBlock, 0, stream>>>(
+      static_cast<const uint4*>(hidden), static_cast<const uint4*>(gamma), T, T_pad, d, eps,
+      reinterpret_cast<float4*>(ybig), reinterpret_cast<float4*>(ysmall), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_tf32(const float* x, int64_t n, float* big, float* small,
+                              cudaStream_t stream, int num_sms) {
+  const int64_t n4 = n / 4;
+  int64_t blocks = (n4 + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  split_tf32_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(x), n4, reinterpret_cast<float4*>(big),
+      reinterpret_cast<float4*>(small));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rmsnorm_rows(const void* hidden, const void* gamma, int64_t T, int d,

@@ -126,6 +126,15 @@ def make_head(workload: str, d: int, V: int, seed: int = SEED) -> Head:
     return Head(d=d, V=V, W=W, gamma=gamma, vocab_perm=perm)
 
 
+def fp32_weights(head: Head, seed: int = SEED, rel_sigma: float = 1e-3) -> np.ndarray:
+    """fp32 [V, d] weights near the head's bf16 W: W * (1 + N(0, rel_sigma^2)) rounded to
+    fp32, so that almost no element is a bf16 (or tf32) value (fp32 master weights)."""
+    g = stream("fp32w", f"W{head.V}x{head.d}", seed)
+    base = bf16_bits_to_f32(head.W).astype(np.float64)
+    noise = g.standard_normal(base.shape, dtype=np.float32).astype(np.float64)
+    return (base * (1.0 + rel_sigma * noise)).astype(np.float32)
+
+
 @dataclasses.dataclass
 class ScoreBatch:
     """One workload's rows plus the three score-set inputs and the compare layout.

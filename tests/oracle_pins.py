@@ -906,4 +906,65 @@ def pin_rmsnorm_fp32_against_fp64():
     assert np.array_equal(oracle.rmsnorm(hh, gg, 0.0), oracle.rmsnorm_fp32(hh, gg, 0.0))
 
 
+# ---------------------------------------------------------------------------
+# FP32 head pins
+
+def pin_fp32_head_mpmath():
+    """FP32 head rows evaluated end to end at 50 digits (mpmath) with fp32 weights that are
+    not bf16 values and y never rounded; the oracle must agree to 1e-12."""
+    import mpmath
+    mpmath.mp.dps = 50
+    b = synth.make_custom(T=3, d=16, V=40, temperature=0.7, eps=1e-6, tag="mp32")
+    W32 = synth.fp32_weights(b.head)
+    assert np.mean(oracle.round_to_bf16(W32.astype(np.float64)) != W32) > 0.9
+    out = oracle.oracle_logprob_fp32(b.hidden_gen, b.head.gamma, W32, b.token_ids, 0.7, 1e-6)
+    hb = oracle.widen_bf16(b.hidden_gen)
+    gb = oracle.widen_bf16(b.head.gamma)
+    for t in range(b.T):
+        h = [mpmath.mpf(float(v)) for v in hb[t]]
+        rstd = 1 / mpmath.sqrt(mpmath.fsum(v * v for v in h) / len(h) + mpmath.mpf(1e-6))
+        y = [v * rstd * mpmath.mpf(float(gb[i])) for i, v in enumerate(h)]
+        z = [mpmath.fsum(y[i] * mpmath.mpf(float(W32[v, i])) for i in range(len(y)))
+             for v in range(b.V)]
+        s = [zz / mpmath.mpf(0.7) for zz in z]
+        lse = mpmath.log(mpmath.fsum(mpmath.exp(v) for v in s))
+        x = int(b.token_ids[t])
+        assert abs(float(s[x] - lse) - out["logprob"][t]) < 1e-12
+        assert abs(float(lse) - out["lse"][t]) < 1e-12
+        assert out["top1"][t] == int(np.argmax([float(v) for v in z]))
+
+
+def pin_fp32_head_reduces_to_bf16():
+    """With |h| = 2 everywhere and eps = 0, y = (h / 2) gamma is a bf16 value, so rounding y
+    changes nothing; with bf16-valued W the FP32 oracle equals the bf16 oracle exactly.
+    With fp32 weights the two differ (the head is not silently rounded)."""
+    b = synth.make_custom(T=5, d=64, V=300, tag="r32")
+    h = np.where((np.arange(5 * 64).reshape(5, 64) % 5) == 0, 0xC000, 0x4000).astype(np.uint16)
+    Wf = oracle.widen_bf16(b.head.W).astype(np.float32)
+    a = oracle.oracle_logprob(h, b.head.gamma, b.head.W, b.token_ids, 0.8, 0.0)
+    c = oracle.oracle_logprob_fp32(h, b.head.gamma, Wf, b.token_ids, 0.8, 0.0)
+    for k in ("logprob", "lse", "top1"):
+        assert np.array_equal(a[k], c[k]), k
+    c2 = oracle.oracle_logprob_fp32(h, b.head.gamma, synth.fp32_weights(b.head), b.token_ids,
+                                    0.8, 0.0)
+    assert np.max(np.abs(c2["lse"] - a["lse"])) > 1e-6
+
+
+def pin_fp32_head_torch():
+    """fp64 torch: rms_norm (library routine), matmul, log_softmax and argmax agree with the
+    FP32 oracle to 1e-12 on a ragged shape."""
+    import torch
+    b = synth.make_custom(T=7, d=192, V=777, temperature=1.3, eps=1e-5, tag="t32")
+    W32 = synth.fp32_weights(b.head)
+    out = oracle.oracle_logprob_fp32(b.hidden_gen, b.head.gamma, W32, b.token_ids, 1.3, 1e-5)
+    h = torch.from_numpy(oracle.widen_bf16(b.hidden_gen))
+    g = torch.from_numpy(oracle.widen_bf16(b.head.gamma))
+    y = torch.nn.functional.rms_norm(h, (192,), weight=g, eps=1e-5)
+    z = y @ torch.from_numpy(W32.astype(np.float64)).T
+    ls = torch.log_softmax(z / 1.3, dim=1)
+    ids = torch.from_numpy(b.token_ids.astype(np.int64))
+    assert np.max(np.abs(ls.gather(1, ids[:, None])[:, 0].numpy() - out["logprob"])) < 1e-12
+    assert np.array_equal(torch.argmax(z, dim=1).numpy(), out["top1"])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

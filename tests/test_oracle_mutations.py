@@ -217,6 +217,18 @@ def _rms32_sequential_partials(h, gamma, eps, return_rstd=False):
     return (y, rstd) if return_rstd else y
 
 
+import oracle.fp32head as of32
+
+
+def _rms_unrounded_but_rounded(h, gamma, eps):
+    return ol.round_to_bf16(h * (1.0 / np.sqrt(np.mean(h * h, axis=1) + eps))[:, None] *
+                            gamma[None, :])
+
+
+def _rms_unrounded_eps_outside(h, gamma, eps):
+    return h * (1.0 / (np.sqrt(np.mean(h * h, axis=1)) + eps))[:, None] * gamma[None, :]
+
+
 MUTATIONS = [
     ("temperature after softmax", ol, "lse_stats", _lse_after_softmax, ["pin_v8_temperature"]),
     ("no max shift", ol, "lse_stats", _lse_no_shift, ["pin_large_logits"]),
@@ -260,6 +272,10 @@ MUTATIONS = [
      ["pin_rmsnorm_fp32_scalar"]),
     ("fp32 RMSNorm with one running sum", of8, "rmsnorm_fp32", _rms32_sequential_partials,
      ["pin_rmsnorm_fp32_scalar"]),
+    ("FP32 head rounds y to bf16", of32, "rmsnorm_unrounded", _rms_unrounded_but_rounded,
+     ["pin_fp32_head_mpmath", "pin_fp32_head_torch"]),
+    ("FP32 head eps outside the sqrt", of32, "rmsnorm_unrounded", _rms_unrounded_eps_outside,
+     ["pin_fp32_head_mpmath", "pin_fp32_head_torch"]),
 ]
 
 
