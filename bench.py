@@ -503,6 +503,28 @@ def main():
             call_TFLOPs=round(2.0 * T * d * V / (fms / 1e3) / 1e12, 1),
             peak_TFLOPs=fp8_peak, peak_note="2 x measured sustained bf16 (nominal fp8:bf16 ratio)")
         del fws, W8, sW8
+        # FP32 head: W (fp32 here: the bf16 W widened) split once per weight version (untimed)
+        Wb32, Ws32 = tim.split_tf32(W.view(torch.bfloat16).float().contiguous())
+        f32ws = tim.Workspace(int(tim.lib().tim_logprob_fp32_workspace_size(T, d, V)), dev)
+        tim.logprob_fp32(hid_train, gam, Wb32, Ws32, ids, tau, eps, out=pout, workspace=f32ws,
+                         check=False)
+        e_a.record(stream)
+        for _ in range(2):
+            tim.logprob_fp32(hid_train, gam, Wb32, Ws32, ids, tau, eps, out=pout, workspace=f32ws,
+                             check=False)
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        f32ws.check("fp32 head")
+        f32ms = e_a.elapsed_time(e_b) / 2
+        tf32_peak = 0.5 * peaks["bf16_sustained"] if peaks.get("bf16_sustained") else None
+        extras["fp32_tf32x3_head"] = dict(
+            ms=round(f32ms, 3), tokens_per_s=round(T / (f32ms / 1e3), 1),
+            fp32_equiv_TFLOPs=round(2.0 * T * d * V / (f32ms / 1e3) / 1e12, 1),
+            tensor_TFLOPs=round(3 * 2.0 * T * d * V / (f32ms / 1e3) / 1e12, 1),
+            tensor_peak_TFLOPs=tf32_peak,
+            peak_note="tf32 = 0.5 x measured sustained bf16 (nominal ratio); three tf32 products "
+                      "per multiply-add")
+        del f32ws, Wb32, Ws32
         G = 8
         e_a.record(stream)
         for _ in range(2):

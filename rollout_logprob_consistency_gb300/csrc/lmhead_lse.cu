@@ -94,6 +94,14 @@ struct StageGeom {
   static constexpr int kStageA = kParts * kABytes;
   static constexpr int kStageB = kParts * kBBytes;
   static constexpr int kKElems = kPrec == kPrecE4m3 ? 2 * kBK : kPrec == kPrecTf32x3 ? kBK / 2 : kBK;
+  // TMEM per tile: one 256-column fp32 accumulator, double-buffered; the tf32x3
+  // path adds a second 256-column accumulator for the two correction products
+  // (big*small + small*big), so its tile takes all 512 columns, single-buffered.
+  // Keeping the corrections apart leaves the main sum with d/8 accumulation
+  // steps instead of 3d/8 (each step of the tensor-core accumulation costs up to
+  // one rounding of the running sum).
+  static constexpr int kAccCols = kPrec == kPrecTf32x3 ? 2 * kBN : kBN;
+  static constexpr int kNumAcc = kTmemCols / kAccCols;
 };
 
 constexpr size_t kGemmSmemBytes =
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kBN;
+        const uint32_t d_tmem = tmem_base + acc * G::kAccCols;
         for (int kb = 0; kb < a.num_kb; ++kb) {
           if (!mbar_wait(&full[stage], ph, abort_flag)) {
             ok = false;
@@ -320,8 +328,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const uint64_t bb = sw128_kmajor_desc(b0 + k * 32);
               const uint64_t bs = sw128_kmajor_desc(b0 + kBBytes + k * 32);
               umma_tf32(d_tmem, ab, bb, idesc, acc_k);
-              umma_tf32(d_tmem, ab, bs, idesc, 1u);
-              umma_tf32(d_tmem, as, bb, idesc, 1u);
+              umma_tf32(d_tmem + kBN, ab, bs, idesc, acc_k);
+              umma_tf32(d_tmem + kBN, as, bb, idesc, 1u);
             } else {
               umma_bf16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
                         idesc, acc_k);
@@ -335,8 +343,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (!ok) break;
         umma_commit(&acc_full[acc]);
-        acc ^= 1u;
-        if (acc == 0) acc_ph ^= 1u;
+        if (++acc == static_cast<uint32_t>(G::kNumAcc)) {
+          acc = 0;
+          acc_ph ^= 1u;
+        }
       }
       if (!ok) raise_abort(abort_flag, a.status);
     }
@@ -365,7 +375,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
       float m2 = -INFINITY, sum = 0.f, bz = -INFINITY, zt = 0.f;
       int bi = col_base;
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * G::kAccCols;
       if constexpr (kMode == 0) {
         const float srow = kFp8 ? __ldg(a.sy + row) : 1.f;
 #pragma unroll 1
@@ -381,6 +392,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const float sc = srow * __ldg(a.sw + min(col0 + j, a.v_end - 1));
               r[j] = __float_as_uint(__uint_as_float(r[j]) * sc);
             }
+          }
+          if constexpr (kX3) {
+            uint32_t rc[32];
+            tmem_ld32(tbase + kBN + c * 32, rc);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(rc[j]));
           }
           if (nvalid == 32)
             epilogue_chunk<false>(r, 32, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
@@ -414,8 +432,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             make_float4(m2, sum, bz, __int_as_float(bi));
         if (static_cast<unsigned>(rel) < static_cast<unsigned>(kBN)) a.tgt[row] = zt * a.inv_temp;
       }
-      acc ^= 1u;
-      if (acc == 0) acc_ph ^= 1u;
+      if (++acc == static_cast<uint32_t>(G::kNumAcc)) {
+        acc = 0;
+        acc_ph ^= 1u;
+      }
     }
   }
 
