@@ -17,6 +17,7 @@ Modules
 ``oracle.processed`` the processed (top-k, then top-p) selected-token logprob.
 ``oracle.fp8``      the FP8 (e4m3, per-row power-of-two scales) head variant.
 ``oracle.fp32head`` the FP32 head variant (fp32 y, fp32 W).
+``oracle.backward`` the backward of the linear logprob (dL/dy, dL/dW).
 ``oracle.diag``     extended per-sequence diagnostics: |delta| quantiles,
                     probability MAE, top-1 flips, sequence TIS, K1/K3 sums,
                     ratio error, MIS weights, mean w^2.
@@ -39,6 +40,7 @@ from .processed import oracle_processed_logprob, process_row  # noqa: F401
 from .fp8 import (e4m3_round, fp8_scale, oracle_logprob_fp8, quantize_rows,  # noqa: F401
                   rmsnorm_fp32)
 from .fp32head import oracle_logprob_fp32, rmsnorm_unrounded  # noqa: F401
+from .backward import logit_grad, oracle_logprob_backward  # noqa: F401
 from .diag import (  # noqa: F401
     FLAG_QUANTILE_SKIPPED, QUANTILE_MAX_TOKENS, QUANTILES, oracle_diag, oracle_diag_lenient,
     quantile_linear,

@@ -1,0 +1,68 @@
+"""fp64 oracle for the backward of the linear logprob.  TEST INFRASTRUCTURE ONLY.
+
+"Rollout-Training Mismatch in LLM RL", section 5.2: the inference kernels
+define the forward values and the trainer supplies the backward, through a
+custom autograd wrapper around each forward operation, with gradients checked
+against an independent reference; the recipe recomputes the forward instead of
+saving its intermediates.  For the selected-token logprob of the "linear
+logprob" path (logprob_t = s_t[x_t] - lse_t, s = z / tau, z = y . W^T; see
+``oracle.logprob``) and an upstream gradient g_t = dL/dlogprob_t:
+
+    dL/dz_tv = (g_t / tau) * (1[v = x_t] - p_tv),   p_tv = exp(s_tv - lse_t)
+    dL/dy    = G . W          [T, d]
+    dL/dW    = G^T . y        [V, d]
+
+with y the bf16-rounded RMSNorm output of the forward (the GEMM operand).
+Readings: a row whose token id is outside [0, V) contributes nothing (its G row
+is zero; the forward reports such rows as errors); the gradient is taken with
+respect to y as the GEMM consumes it (the RMSNorm backward is not part of it).
+The result dict also carries, for the parity tests, the magnitudes
+|G| . |W| and |G|^T . |y| that bound how far bf16 rounding of G can move each
+output element.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .logprob import logits, lse_stats, rmsnorm, widen_bf16
+
+
+def logit_grad(z: np.ndarray, token_ids, grad, temperature: float) -> np.ndarray:
+    """G = dL/dz for L = sum_t grad_t * logprob_t (rows with invalid ids give zero rows)."""
+    T, V = z.shape
+    s, lse = lse_stats(z, temperature)
+    p = np.exp(s - lse[:, None])
+    ids = np.asarray(token_ids, dtype=np.int64)
+    ok = (ids >= 0) & (ids < V)
+    onehot = np.zeros((T, V))
+    onehot[np.flatnonzero(ok), ids[ok]] = 1.0
+    G = (np.asarray(grad, dtype=np.float64) / temperature)[:, None] * (onehot - p)
+    G[~ok] = 0.0
+    return G
+
+
+def oracle_logprob_backward(hidden_bits, gamma_bits, W_bits, token_ids, temperature: float,
+                            eps: float, grad_logprob, vocab_block: int = 8192):
+    """Returns dict: dy [T, d], dW [V, d], bound_dy [T, d], bound_dW [V, d], y [T, d]."""
+    hidden_bits = np.asarray(hidden_bits, dtype=np.uint16)
+    W_bits = np.asarray(W_bits, dtype=np.uint16)
+    V, d = W_bits.shape
+    y = rmsnorm(widen_bf16(hidden_bits), widen_bf16(gamma_bits), eps)
+    z = logits(y, W_bits, vocab_block)
+    G = logit_grad(z, token_ids, grad_logprob, temperature)
+    del z
+    T = y.shape[0]
+    dy = np.zeros((T, d))
+    bdy = np.zeros((T, d))
+    dW = np.empty((V, d))
+    bdW = np.empty((V, d))
+    ay = np.abs(y)
+    for v0 in range(0, V, vocab_block):
+        v1 = min(V, v0 + vocab_block)
+        Wb = widen_bf16(W_bits[v0:v1])
+        Gb = G[:, v0:v1]
+        dy += Gb @ Wb
+        bdy += np.abs(Gb) @ np.abs(Wb)
+        dW[v0:v1] = Gb.T @ y
+        bdW[v0:v1] = np.abs(Gb).T @ ay
+    return dict(dy=dy, dW=dW, bound_dy=bdy, bound_dW=bdW, y=y)

@@ -967,4 +967,93 @@ def pin_fp32_head_torch():
     assert np.array_equal(torch.argmax(z, dim=1).numpy(), out["top1"])
 
 
+# ---------------------------------------------------------------------------
+# Backward pins
+
+def _bwd_case(tag, T=4, d=16, V=40, tau=0.7):
+    b = synth.make_custom(T=T, d=d, V=V, temperature=tau, tag=tag)
+    g = np.random.default_rng(sum(tag.encode())).standard_normal(T)
+    return b, g
+
+
+def pin_backward_finite_differences():
+    """dL/dy and dL/dW against central differences of L = sum_t g_t logprob_t, the forward
+    taken through the oracle's lse_stats on z = y W^T (fp64, step 1e-6)."""
+    b, g = _bwd_case("bwdfd")
+    tau = b.temperature
+    out = oracle.oracle_logprob_backward(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, tau,
+                                         b.eps, g)
+    y = out["y"]
+    W = oracle.widen_bf16(b.head.W)
+    ids = b.token_ids.astype(np.int64)
+
+    def loss(yy, WW):
+        s, lse = oracle.lse_stats(yy @ WW.T, tau)
+        return float(np.sum(g * (s[np.arange(len(ids)), ids] - lse)))
+
+    h = 1e-6
+    for t, i in ((0, 0), (1, 5), (3, 15), (2, 7)):
+        e = np.zeros_like(y)
+        e[t, i] = h
+        fd = (loss(y + e, W) - loss(y - e, W)) / (2 * h)
+        assert abs(fd - out["dy"][t, i]) < 1e-7 * max(1.0, abs(fd)), (t, i)
+    for v, i in ((0, 0), (int(ids[0]), 3), (39, 15), (17, 8)):
+        e = np.zeros_like(W)
+        e[v, i] = h
+        fd = (loss(y, W + e) - loss(y, W - e)) / (2 * h)
+        assert abs(fd - out["dW"][v, i]) < 1e-7 * max(1.0, abs(fd)), (v, i)
+
+
+def pin_backward_torch_autograd():
+    """torch fp64 autograd of sum_t g_t log_softmax(y W^T / tau)[t, x_t] (a library routine)
+    matches dL/dy and dL/dW to 1e-12 on a ragged shape."""
+    import torch
+    b, g = _bwd_case("bwdtorch", T=9, d=48, V=333, tau=1.3)
+    out = oracle.oracle_logprob_backward(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 1.3,
+                                         b.eps, g, vocab_block=100)
+    y = torch.tensor(out["y"], requires_grad=True)
+    W = torch.tensor(oracle.widen_bf16(b.head.W), requires_grad=True)
+    lp = torch.log_softmax(y @ W.T / 1.3, dim=1)
+    ids = torch.from_numpy(b.token_ids.astype(np.int64))
+    (torch.from_numpy(g) * lp.gather(1, ids[:, None])[:, 0]).sum().backward()
+    assert np.max(np.abs(y.grad.numpy() - out["dy"])) < 1e-12
+    assert np.max(np.abs(W.grad.numpy() - out["dW"])) < 1e-12
+
+
+def pin_backward_invariants():
+    """Each G row sums to zero (the probabilities sum to one), so every column of dW sums to
+    zero; g = 0 gives zero gradients; a one-word vocabulary has logprob 0 and no gradient;
+    an invalid token id row contributes nothing; the bounds dominate the results."""
+    b, g = _bwd_case("bwdinv", T=6, d=32, V=50, tau=0.9)
+    ids = b.token_ids.copy()
+    ids[2] = 50
+    out = oracle.oracle_logprob_backward(b.hidden_gen, b.head.gamma, b.head.W, ids, 0.9, b.eps, g)
+    assert np.max(np.abs(out["dW"].sum(axis=0))) < 1e-12
+    assert np.all(out["dy"][2] == 0.0)
+    assert np.all(np.abs(out["dy"]) <= out["bound_dy"] + 1e-15)
+    assert np.all(np.abs(out["dW"]) <= out["bound_dW"] + 1e-15)
+    z = oracle.backward.logit_grad(np.random.default_rng(1).standard_normal((3, 7)),
+                                   np.array([0, 6, 3]), np.ones(3), 0.5)
+    assert np.max(np.abs(z.sum(axis=1))) < 1e-15
+    zero = oracle.oracle_logprob_backward(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids,
+                                          0.9, b.eps, np.zeros(6))
+    assert not np.any(zero["dy"]) and not np.any(zero["dW"])
+    one = oracle.oracle_logprob_backward(b.hidden_gen, b.head.gamma, b.head.W[:1],
+                                         np.zeros(6, np.int32), 0.9, b.eps, g)
+    assert np.max(np.abs(one["dy"])) < 1e-15 and np.max(np.abs(one["dW"])) < 1e-15
+
+
+def pin_backward_temperature_closed_form():
+    """Two-word vocabulary, one row, y = (1), W = (a, b): logprob of word 0 is
+    -log(1 + e^((b - a) / tau)), so dL/dy = (a - b) q / tau with q = sigmoid((b - a) / tau)."""
+    a, bb, tau = 1.5, -0.25, 0.6
+    h = np.array([[0x3F80]], dtype=np.uint16)            # h = 1
+    gam = np.array([0x3F80], dtype=np.uint16)            # gamma = 1 -> y = 1 (eps = 0)
+    W = np.array([[trunc_bf16_bits(a)], [trunc_bf16_bits(bb)]], dtype=np.uint16)
+    out = oracle.oracle_logprob_backward(h, gam, W, np.array([0]), tau, 0.0, np.array([1.0]))
+    q = 1.0 / (1.0 + math.exp(-(bb - a) / tau))
+    assert abs(out["dy"][0, 0] - (a - bb) * q / tau) < 1e-14
+    assert abs(out["dW"][0, 0] - q / tau) < 1e-14 and abs(out["dW"][1, 0] + q / tau) < 1e-14
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

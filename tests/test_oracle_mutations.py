@@ -229,6 +229,27 @@ def _rms_unrounded_eps_outside(h, gamma, eps):
     return h * (1.0 / (np.sqrt(np.mean(h * h, axis=1)) + eps))[:, None] * gamma[None, :]
 
 
+import oracle.backward as obw
+
+_orig_logit_grad = obw.logit_grad
+
+
+def _grad_no_temperature(z, token_ids, grad, temperature):
+    return _orig_logit_grad(z, token_ids, grad, temperature) * temperature
+
+
+def _grad_softmax_of_raw_logits(z, token_ids, grad, temperature):
+    return _orig_logit_grad(z * temperature, token_ids, grad, temperature)
+
+
+def _grad_sign_flipped(z, token_ids, grad, temperature):
+    return -_orig_logit_grad(z, token_ids, grad, temperature)
+
+
+def _grad_next_token(z, token_ids, grad, temperature):
+    return _orig_logit_grad(z, (np.asarray(token_ids) + 1) % z.shape[1], grad, temperature)
+
+
 MUTATIONS = [
     ("temperature after softmax", ol, "lse_stats", _lse_after_softmax, ["pin_v8_temperature"]),
     ("no max shift", ol, "lse_stats", _lse_no_shift, ["pin_large_logits"]),
@@ -276,6 +297,14 @@ MUTATIONS = [
      ["pin_fp32_head_mpmath", "pin_fp32_head_torch"]),
     ("FP32 head eps outside the sqrt", of32, "rmsnorm_unrounded", _rms_unrounded_eps_outside,
      ["pin_fp32_head_mpmath", "pin_fp32_head_torch"]),
+    ("backward without 1/tau", obw, "logit_grad", _grad_no_temperature,
+     ["pin_backward_finite_differences", "pin_backward_torch_autograd"]),
+    ("backward softmax of raw logits", obw, "logit_grad", _grad_softmax_of_raw_logits,
+     ["pin_backward_torch_autograd", "pin_backward_temperature_closed_form"]),
+    ("backward sign flipped", obw, "logit_grad", _grad_sign_flipped,
+     ["pin_backward_finite_differences"]),
+    ("backward one-hot on the next id", obw, "logit_grad", _grad_next_token,
+     ["pin_backward_torch_autograd"]),
 ]
 
 
