@@ -525,6 +525,28 @@ def main():
             peak_note="tf32 = 0.5 x measured sustained bf16 (nominal ratio); three tf32 products "
                       "per multiply-add")
         del f32ws, Wb32, Ws32
+        # backward of the linear logprob (recompute + G + dL/dy + dL/dW), upstream gradient 1
+        gup = torch.ones(T, dtype=torch.float32, device=dev)
+        lse_c = C[1]                      # the trainer-set lse of the timed steps
+        bws = tim.Workspace(int(tim.lib().tim_logprob_backward_workspace_size(T, d, V)), dev)
+        dy_b = torch.empty(T, d, dtype=torch.float32, device=dev)
+        dW_b = torch.empty(V, d, dtype=torch.float32, device=dev)
+        tim.logprob_backward(hid_train, gam, W, ids, lse_c, gup, tau, eps, out_dy=dy_b,
+                             out_dW=dW_b, workspace=bws, check=False)
+        e_a.record(stream)
+        for _ in range(2):
+            tim.logprob_backward(hid_train, gam, W, ids, lse_c, gup, tau, eps, out_dy=dy_b,
+                                 out_dW=dW_b, workspace=bws, check=False)
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        bws.check("backward")
+        bms = e_a.elapsed_time(e_b) / 2
+        extras["backward_dy_dW"] = dict(
+            ms=round(bms, 3), tokens_per_s=round(T / (bms / 1e3), 1),
+            TFLOPs=round(3 * 2.0 * T * d * V / (bms / 1e3) / 1e12, 1),
+            note="three GEMMs (logit recompute, G.W, G^T.y) + transposes; workspace "
+                 f"{bws.nbytes / 1e9:.1f} GB")
+        del bws, dy_b, dW_b
         G = 8
         e_a.record(stream)
         for _ in range(2):

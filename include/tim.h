@@ -307,6 +307,39 @@ tim_status tim_logprob_fp32(const void *hidden, const void *gamma, const float *
                             size_t workspace_bytes, tim_stream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * Backward of the linear logprob.
+ *
+ * "Rollout-Training Mismatch in LLM RL", section 5.2: the inference kernels
+ * define the forward values, the trainer supplies the backward through a
+ * custom autograd wrapper, and the recipe recomputes the forward rather than
+ * saving its intermediates.  For L = sum_t g_t * logprob_t (g = grad_logprob,
+ * the upstream gradient) this computes, with y the bf16 RMSNorm output exactly
+ * as tim_logprob computes it:
+ *   G_tv  = (g_t / temperature) * (1[v = x_t] - p_tv),
+ *           p_tv = exp(z_tv / temperature - lse_t),  z = y . W^T recomputed;
+ *   out_dy = dL/dy = G . W     fp32 [T, d]  (row-major, 16-byte aligned);
+ *   out_dW = dL/dW = G^T . y   fp32 [V, d]  (row-major, 16-byte aligned);
+ *           accumulate_dW = 1 adds to out_dW instead (for callers that split a
+ *           batch into row chunks), 0 overwrites it.
+ * lse: fp32 [T], the out_lse of the tim_logprob call on the same inputs.  G is
+ * rounded to bf16 for the two tensor-core products (fp32 accumulation).  A row
+ * whose token id is outside [0, V) contributes nothing and records
+ * TIM_ERR_TOKEN_RANGE.  Each out_dy row depends only on its own row (batch-
+ * invariant); out_dW sums over the rows in a fixed order.
+ * Workspace: tim_logprob_backward_workspace_size(T, d, V) bytes (it holds G in
+ * both layouts: about 4 T V bytes), 256-byte aligned, zero-initialised once;
+ * T up to 4.19 M rows and V up to 4.19 M.  Errors as tim_logprob.
+ * ------------------------------------------------------------------------ */
+size_t tim_logprob_backward_workspace_size(int64_t T, int32_t d, int32_t V);
+
+tim_status tim_logprob_backward(const void *hidden, const void *gamma, const void *W,
+                                const int32_t *token_ids, const float *lse,
+                                const float *grad_logprob, int64_t T, int32_t d, int32_t V,
+                                float temperature, float eps, float *out_dy, float *out_dW,
+                                int32_t accumulate_dW, void *workspace, size_t workspace_bytes,
+                                tim_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * Processed (top-k, then top-p) selected-token logprob.
  *
  * "Debugging Logprob Mismatches in LLM Reinforcement Learning", Make Sure

@@ -42,8 +42,9 @@ def logit_grad(z: np.ndarray, token_ids, grad, temperature: float) -> np.ndarray
 
 
 def oracle_logprob_backward(hidden_bits, gamma_bits, W_bits, token_ids, temperature: float,
-                            eps: float, grad_logprob, vocab_block: int = 8192):
-    """Returns dict: dy [T, d], dW [V, d], bound_dy [T, d], bound_dW [V, d], y [T, d]."""
+                            eps: float, grad_logprob, vocab_block: int = 8192, dW_rows=None):
+    """Returns dict: dy [T, d], dW [V, d], bound_dy [T, d], bound_dW [V, d], y [T, d].
+    With ``dW_rows`` (vocabulary ids) dW and bound_dW hold only those rows, in that order."""
     hidden_bits = np.asarray(hidden_bits, dtype=np.uint16)
     W_bits = np.asarray(W_bits, dtype=np.uint16)
     V, d = W_bits.shape
@@ -54,8 +55,6 @@ def oracle_logprob_backward(hidden_bits, gamma_bits, W_bits, token_ids, temperat
     T = y.shape[0]
     dy = np.zeros((T, d))
     bdy = np.zeros((T, d))
-    dW = np.empty((V, d))
-    bdW = np.empty((V, d))
     ay = np.abs(y)
     for v0 in range(0, V, vocab_block):
         v1 = min(V, v0 + vocab_block)
@@ -63,6 +62,8 @@ def oracle_logprob_backward(hidden_bits, gamma_bits, W_bits, token_ids, temperat
         Gb = G[:, v0:v1]
         dy += Gb @ Wb
         bdy += np.abs(Gb) @ np.abs(Wb)
-        dW[v0:v1] = Gb.T @ y
-        bdW[v0:v1] = np.abs(Gb).T @ ay
+    rows = np.arange(V) if dW_rows is None else np.asarray(dW_rows, dtype=np.int64)
+    Gr = G[:, rows]
+    dW = Gr.T @ y
+    bdW = np.abs(Gr).T @ ay
     return dict(dy=dy, dW=dW, bound_dy=bdy, bound_dW=bdW, y=y)

@@ -80,6 +80,9 @@ _SIGNATURES = {
     "tim_logprob_fp32_workspace_size": (_sz, [_i64, _i32, _i32]),
     "tim_logprob_fp32": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _vp, _vp,
                                     _vp, _vp, _sz, _vp]),
+    "tim_logprob_backward_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "tim_logprob_backward": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32,
+                                        _f32, _vp, _vp, _i32, _vp, _sz, _vp]),
     "tim_processed_logprob_workspace_size": (_sz, [_i64, _i32, _i32]),
     "tim_processed_logprob": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _i32,
                                          _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -436,6 +439,44 @@ def logprob_fp32(hidden, gamma, W_big, W_small, token_ids, temperature: float, e
     if check:
         workspace.check("tim_logprob_fp32", stream)
     return out
+
+
+def logprob_backward(hidden, gamma, W, token_ids, lse, grad_logprob, temperature: float,
+                     eps: float, *, chunk_rows: Optional[int] = None, out_dy=None, out_dW=None,
+                     workspace: Optional[Workspace] = None, stream=None, check: bool = True):
+    """Backward of the linear logprob (tim_logprob_backward): returns (dy fp32 [T, d],
+    dW fp32 [V, d]) for L = sum_t grad_logprob[t] * logprob[t].  ``lse`` is the forward's
+    out_lse.  With ``chunk_rows`` the rows are processed in chunks (dW accumulated across
+    them in chunk order), bounding the workspace to that many rows."""
+    torch = _torch()
+    hidden = _as_bf16(hidden, "hidden")
+    gamma = _as_bf16(gamma, "gamma")
+    W = _as_bf16(W, "W")
+    _need(token_ids, torch.int32, "token_ids", 1)
+    _need(lse, torch.float32, "lse", 1)
+    _need(grad_logprob, torch.float32, "grad_logprob", 1)
+    T, d = hidden.shape
+    V = W.shape[0]
+    dev = hidden.device
+    if out_dy is None:
+        out_dy = torch.empty(T, d, dtype=torch.float32, device=dev)
+    if out_dW is None:
+        out_dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+    step = T if not chunk_rows else max(1, min(int(chunk_rows), T))
+    if workspace is None:
+        workspace = Workspace(int(lib().tim_logprob_backward_workspace_size(step, d, V)), dev,
+                              stream)
+    for r0 in range(0, T, step):
+        r1 = min(T, r0 + step)
+        code = lib().tim_logprob_backward(
+            _ptr(hidden) + r0 * d * 2, _ptr(gamma), _ptr(W), _ptr(token_ids) + r0 * 4,
+            _ptr(lse) + r0 * 4, _ptr(grad_logprob) + r0 * 4, r1 - r0, d, V, float(temperature),
+            float(eps), _ptr(out_dy) + r0 * d * 4, _ptr(out_dW), 0 if r0 == 0 else 1,
+            workspace.ptr, workspace.nbytes, _stream_ptr(stream))
+        _check(code, "tim_logprob_backward")
+    if check:
+        workspace.check("tim_logprob_backward", stream)
+    return out_dy, out_dW
 
 
 def processed_logprob(hidden, gamma, W, token_ids, temperature: float, eps: float, top_k: int,

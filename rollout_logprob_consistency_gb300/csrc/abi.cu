@@ -35,6 +35,15 @@ cudaError_t launch_lmhead_lse_tf32x3(const float* y_big, const float* y_small, c
                                      const float* W_small, const int32_t* ids, int64_t T, int d,
                                      int V, float temperature, void* part, float* tgt,
                                      int* status, cudaStream_t stream, int num_sms);
+cudaError_t launch_logit_grad(const void* y, const void* W, const int32_t* ids, const float* lse,
+                              const float* gup, int64_t T, int d, int V, float temperature,
+                              uint16_t* gz, int64_t ldg, uint16_t* gzt, int64_t ldgt, int* status,
+                              cudaStream_t stream, int num_sms);
+cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, const void* B, int N,
+                              int64_t ldb, int64_t K, int64_t M, float* C, int64_t ldc,
+                              int accumulate, int* status, cudaStream_t stream, int num_sms);
+cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in,
+                                  void* out, int64_t ld_out, cudaStream_t stream);
 cudaError_t launch_lmhead_lse_fp8(const void* y8, const float* sy, const void* W8,
                                   const float* sw, const int32_t* ids, int64_t T, int d, int V,
                                   float temperature, void* part, float* tgt, int* status,
@@ -172,6 +181,27 @@ Fp32Layout fp32_layout(int64_t T, int32_t d, int32_t V) {
   F.ysmall_off = align_up(F.ybig_off + n, 1024);
   F.total = align_up(F.ysmall_off + n, 1024);
   return F;
+}
+
+// Backward workspace: status | y bf16 [Tp, d] | y^T [d, Tp] | W^T [d, Vp] |
+// G [Tp, Vp] | G^T [Vp, Tp], with Tp = rows_padded(T) and Vp = V rounded up to 64.
+struct BwdLayout {
+  int64_t Tp, Vp;
+  size_t status_off, y_off, yt_off, wt_off, g_off, gt_off, total;
+};
+BwdLayout backward_layout(int64_t T, int32_t d, int32_t V) {
+  BwdLayout B;
+  B.Tp = rows_padded(T);
+  B.Vp = (static_cast<int64_t>(V) + 63) / 64 * 64;
+  const size_t dd = static_cast<size_t>(d);
+  B.status_off = 0;
+  B.y_off = 1024;
+  B.yt_off = align_up(B.y_off + static_cast<size_t>(B.Tp) * dd * 2, 1024);
+  B.wt_off = align_up(B.yt_off + dd * static_cast<size_t>(B.Tp) * 2, 1024);
+  B.g_off = align_up(B.wt_off + dd * static_cast<size_t>(B.Vp) * 2, 1024);
+  B.gt_off = align_up(B.g_off + static_cast<size_t>(B.Tp) * static_cast<size_t>(B.Vp) * 2, 1024);
+  B.total = align_up(B.gt_off + static_cast<size_t>(B.Vp) * static_cast<size_t>(B.Tp) * 2, 1024);
+  return B;
 }
 
 bool valid_shard(int32_t G, int32_t g) {
@@ -433,6 +463,61 @@ tim_status tim_logprob_fp32(const void* hidden, const void* gamma, const float* 
     return TIM_ERR_CUDA;
   return from_cuda(launch_lse_finalize(part, tgt, token_ids, T, V, out_logprob, out_lse, out_top1,
                                        status, st));
+}
+
+size_t tim_logprob_backward_workspace_size(int64_t T, int32_t d, int32_t V) {
+  if (check_shape(T, d, V) != TIM_OK) return 0;
+  if (rows_padded(T) / 64 > 65535 || (static_cast<int64_t>(V) + 63) / 64 > 65535) return 0;
+  return backward_layout(T, d, V).total;
+}
+
+tim_status tim_logprob_backward(const void* hidden, const void* gamma, const void* W,
+                                const int32_t* token_ids, const float* lse,
+                                const float* grad_logprob, int64_t T, int32_t d, int32_t V,
+                                float temperature, float eps, float* out_dy, float* out_dW,
+                                int32_t accumulate_dW, void* workspace, size_t workspace_bytes,
+                                tim_stream_t stream) {
+  if (hidden == nullptr || gamma == nullptr || W == nullptr || token_ids == nullptr ||
+      lse == nullptr || grad_logprob == nullptr || out_dy == nullptr || out_dW == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(gamma, 16) || !aligned(W, 16) || !aligned(token_ids, 4) ||
+      !aligned(lse, 4) || !aligned(grad_logprob, 4) || !aligned(out_dy, 16) ||
+      !aligned(out_dW, 16))
+    return TIM_ERR_INVALID_ARG;
+  if (accumulate_dW != 0 && accumulate_dW != 1) return TIM_ERR_INVALID_ARG;
+  tim_status s = check_shape(T, d, V);
+  if (s != TIM_OK) return s;
+  if ((s = check_scalars(temperature, eps)) != TIM_OK) return s;
+  if (rows_padded(T) / 64 > 65535 || (static_cast<int64_t>(V) + 63) / 64 > 65535)
+    return TIM_ERR_SHAPE;
+  const BwdLayout B = backward_layout(T, d, V);
+  if ((s = check_workspace(workspace, workspace_bytes, B.total)) != TIM_OK) return s;
+  int sms = 0;
+  if ((s = check_device(&sms)) != TIM_OK) return s;
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(b + B.status_off);
+  uint16_t* y = reinterpret_cast<uint16_t*>(b + B.y_off);
+  uint16_t* yt = reinterpret_cast<uint16_t*>(b + B.yt_off);
+  uint16_t* wt = reinterpret_cast<uint16_t*>(b + B.wt_off);
+  uint16_t* gz = reinterpret_cast<uint16_t*>(b + B.g_off);
+  uint16_t* gzt = reinterpret_cast<uint16_t*>(b + B.gt_off);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // y exactly as the forward computes it (same kernel), then the operand layouts
+  if (launch_rmsnorm_rows(hidden, gamma, T, d, eps, y, status, st) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  if (launch_transpose_bf16(y, B.Tp, d, d, yt, B.Tp, st) != cudaSuccess) return TIM_ERR_CUDA;
+  if (launch_transpose_bf16(W, V, d, d, wt, B.Vp, st) != cudaSuccess) return TIM_ERR_CUDA;
+  // G = dL/dz from the recomputed logits
+  if (launch_logit_grad(y, W, token_ids, lse, grad_logprob, T, d, V, temperature, gz, B.Vp, gzt,
+                        B.Tp, status, st, sms) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  // dL/dy = G . W  (A = G [Tp, V], B = W^T [d, V])
+  if (launch_gemm_store(gz, B.Tp, B.Vp, wt, d, B.Vp, V, T, out_dy, d, 0, status, st, sms) !=
+      cudaSuccess)
+    return TIM_ERR_CUDA;
+  // dL/dW = G^T . y  (A = G^T [V, Tp], B = y^T [d, Tp])
+  return from_cuda(launch_gemm_store(gzt, V, B.Tp, yt, d, B.Tp, B.Tp, V, out_dW, d, accumulate_dW,
+                                     status, st, sms));
 }
 
 size_t tim_processed_logprob_workspace_size(int64_t T, int32_t d, int32_t V) {

@@ -40,6 +40,7 @@
 // TIM_ERR_TIMEOUT, raises a CTA-wide abort flag, waits (bounded) for its own
 // TMA copies and MMAs still in flight, frees its TMEM and returns.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -73,6 +74,19 @@ struct GemmArgs {
   // e4m3 operands only: per-row scales of y and per-vocabulary-row scales of W
   const float* sy;
   const float* sw;
+  // logit-gradient mode only: forward lse [T] and upstream gradient [T]; outputs
+  // G = dL/dz in bf16, row-major [rows_padded(T)][ldg] and transposed [V][ldgt]
+  const float* lse;
+  const float* gup;
+  uint16_t* gz;
+  int64_t ldg;
+  uint16_t* gzt;
+  int64_t ldgt;
+  // store mode only: C fp32 [T][ldc] (T = rows of A, v_end = columns), C = A.B^T
+  // or C += A.B^T
+  float* c;
+  int64_t ldc;
+  int accumulate;
 };
 
 // Operand precision of the GEMM.
@@ -174,6 +188,10 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], int nval
 // kMode 1: candidate collection -- every logit >= the row's threshold is appended
 //          (in no particular order) to the row's candidate slots; used by the
 //          processed (top-k / top-p) score, which sorts the candidates afterwards.
+// kMode 2: logit gradient of the backward -- G = (g_t / tau)(1[v = x_t] - p_tv)
+//          with p = exp(z / tau - lse_t), written in bf16 both row-major and
+//          transposed (rows T .. rows_padded(T)-1 get zeros).
+// kMode 3: plain GEMM C (+)= A . B^T stored in fp32 (the two backward products).
 // kPrec: operand precision (see Prec).  tmap_y2 / tmap_w2 are the remainder
 // parts for kPrecTf32x3 and unused otherwise.
 template <int kMode, int kPrec>
@@ -359,7 +377,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int m, n;
       tile_coords(tile, a, m, n);
       const int64_t row = static_cast<int64_t>(m) * kBM + q * 32 + lane;
-      const int x = (row < a.T) ? __ldg(a.ids + row) : -1;
+      const int x = (kMode != 3 && row < a.T) ? __ldg(a.ids + row) : -1;
       const int col_base = a.v0 + n * kBN;  // global vocabulary id of the tile's column 0
       const int rel = x - col_base;
 
@@ -404,6 +422,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             epilogue_chunk<false>(r, 32, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
           else
             epilogue_chunk<true>(r, nvalid, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
+        }
+      } else if constexpr (kMode == 2) {
+        const bool live = row < a.T;
+        const bool bad = live && (x < 0 || x >= a.v_end);
+        if (bad) set_status(a.status, TIM_ERR_TOKEN_RANGE);
+        const float gs = (live && !bad) ? __ldg(a.gup + row) * a.inv_temp : 0.f;
+        const float l2 = live ? __ldg(a.lse + row) * 1.4426950408889634f : 0.f;
+        uint16_t* grow = a.gz + row * a.ldg;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          const int col0 = col_base + c * 32;
+          if (col0 >= a.v_end) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          const int nvalid = min(32, a.v_end - col0);
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float gv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const float p = ex2_approx(fmaf(__uint_as_float(r[j + u]), a.k2, -l2));
+              const float oh = (col0 + j + u == x) ? 1.f : 0.f;
+              gv[u] = (j + u < nvalid) ? gs * (oh - p) : 0.f;
+            }
+            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(gv[0]));
+            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(gv[1]));
+            packed[j >> 1] = lo | (hi << 16);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              if (j + u < nvalid)
+                a.gzt[static_cast<int64_t>(col0 + j + u) * a.ldgt + row] =
+                    static_cast<uint16_t>(u ? hi : lo);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(grow + col0);
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            dst[w] = make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2],
+                                packed[4 * w + 3]);
+        }
+      } else if constexpr (kMode == 3) {
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          const int col0 = col_base + c * 32;
+          if (col0 >= a.v_end) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          if (row < a.T) {
+            float4* dst = reinterpret_cast<float4*>(a.c + row * a.ldc + col0);
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+              float4 v = make_float4(__uint_as_float(r[4 * w]), __uint_as_float(r[4 * w + 1]),
+                                     __uint_as_float(r[4 * w + 2]), __uint_as_float(r[4 * w + 3]));
+              if (a.accumulate) {
+                const float4 o = dst[w];
+                v.x += o.x;
+                v.y += o.y;
+                v.z += o.z;
+                v.w += o.w;
+              }
+              dst[w] = v;
+            }
+          }
         }
       } else {
         const float thr = (row < a.T) ? __ldcg(a.thr + row) : INFINITY;
@@ -498,6 +579,23 @@ static bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t rows, u
   return r == CUDA_SUCCESS;
 }
 
+// bf16 [rows, K] operand with row stride ld elements (ld * 2 a multiple of 16);
+// columns K .. and rows past `rows` read as zeros.
+static bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t K,
+                          uint64_t ld, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int kMode, int kPrec>
 static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_w,
                                const CUtensorMap& map_y2, const CUtensorMap& map_w2,
@@ -555,6 +653,15 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   a.cap = 0;
   a.sy = nullptr;
   a.sw = nullptr;
+  a.lse = nullptr;
+  a.gup = nullptr;
+  a.gz = nullptr;
+  a.ldg = 0;
+  a.gzt = nullptr;
+  a.ldgt = 0;
+  a.c = nullptr;
+  a.ldc = 0;
+  a.accumulate = 0;
   return cudaSuccess;
 }
 
@@ -634,6 +741,57 @@ cudaError_t launch_lmhead_collect(const void* y, const void* W, const int32_t* i
   a.cand = static_cast<uint2*>(cand);
   a.cap = cap;
   return launch_gemm<1, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
+}
+
+// Backward, step 1: recompute z = y . W^T and write G = dL/dz (bf16) as
+// gz [rows_padded(T)][ldg] and gzt [V][ldgt] (ldgt >= rows_padded(T)).
+cudaError_t launch_logit_grad(const void* y, const void* W, const int32_t* ids, const float* lse,
+                              const float* gup, int64_t T, int d, int V, float temperature,
+                              uint16_t* gz, int64_t ldg, uint16_t* gzt, int64_t ldgt, int* status,
+                              cudaStream_t stream, int num_sms) {
+  CUtensorMap map_y, map_w;
+  GemmArgs a;
+  cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, 0, temperature, status);
+  if (e != cudaSuccess) return e;
+  a.lse = lse;
+  a.gup = gup;
+  a.gz = gz;
+  a.ldg = ldg;
+  a.gzt = gzt;
+  a.ldgt = ldgt;
+  return launch_gemm<2, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
+}
+
+// Backward, steps 2 and 3: C [M][N] (+)= A . B^T with A bf16 [M][K] (row stride
+// lda, rows_a >= M rows readable) and B bf16 [N][K] (row stride ldb); fp32 C
+// with row stride ldc.  N a multiple of 32.
+cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, const void* B, int N,
+                              int64_t ldb, int64_t K, int64_t M, float* C, int64_t ldc,
+                              int accumulate, int* status, cudaStream_t stream, int num_sms) {
+  CUtensorMap map_a, map_b;
+  if (!make_bf16_map(&map_a, A, static_cast<uint64_t>(rows_a), static_cast<uint64_t>(K),
+                     static_cast<uint64_t>(lda), kBM) ||
+      !make_bf16_map(&map_b, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K),
+                     static_cast<uint64_t>(ldb), kBN))
+    return cudaErrorInvalidValue;
+  GemmArgs a = {};
+  a.T = M;
+  a.v0 = 0;
+  a.v_end = N;
+  a.d = static_cast<int>(K < INT32_MAX ? K : INT32_MAX);
+  a.num_m = static_cast<int>((M + kBM - 1) / kBM);
+  a.num_n = (N + kBN - 1) / kBN;
+  a.num_kb = static_cast<int>((K + kBK - 1) / kBK);
+  a.group_m = 48;
+  a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
+  a.k2 = 0.f;
+  a.inv_temp = 0.f;
+  a.ids = nullptr;
+  a.status = status;
+  a.c = C;
+  a.ldc = ldc;
+  a.accumulate = accumulate;
+  return launch_gemm<3, kPrecBf16>(map_a, map_b, map_a, map_b, a, stream, num_sms, false);
 }
 
 cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T,
