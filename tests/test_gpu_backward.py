@@ -41,7 +41,7 @@ def f32_cuda(a):
 
 def upstream(T, seed):
     g = np.random.default_rng(seed).standard_normal(T).astype(np.float32)
-    g[::7] = 0.0                      # masked tokens
+    g[3::7] = 0.0                     # masked tokens
     return g
 
 
@@ -73,7 +73,7 @@ def check(b, g, dy, dW, orc, dW_rows=None, what=""):
     errw = np.abs(dW[rows] - orc["dW"])
     badw = np.argwhere(errw > tol_dW)
     assert badw.size == 0, f"{what}: dW off at {badw[:3].tolist()}, err {errw.max():.3e}"
-    rel = np.linalg.norm(dy - orc["dy"]) / np.linalg.norm(orc["dy"])
+    rel = np.linalg.norm(dy - orc["dy"]) / max(np.linalg.norm(orc["dy"]), 1e-300)
     assert rel < 5e-3, f"{what}: dy relative error {rel:.2e}"
 
 
