@@ -63,6 +63,9 @@ def parse():
                    help="T,d,V: only run --profile-iters tim_logprob calls of this shape "
                         "(small case for ncu captures), print nothing")
     p.add_argument("--profile-iters", type=int, default=3)
+    p.add_argument("--profile-variant", default="bf16",
+                   choices=["bf16", "fp8", "fp32", "backward"],
+                   help="with --profile-shape: which head variant to run")
     p.add_argument("--cpu-rows", type=int, default=1024,
                    help="rows of the workload the oracle scores for the CPU baseline")
     return p.parse_args()
@@ -252,6 +255,36 @@ def reference_arm(args):
 
 # ------------------------------------------------------------------------------ GPU arm
 
+def profile_variant(args, tim, b, hid, gam, W, ids, out):
+    """--profile-iters calls of the FP8 head, the FP32 head or the backward (weights
+    prepared once beforehand, as a caller would)."""
+    import torch
+    T, d, V = b.T, b.head.d, b.head.V
+    if args.profile_variant == "fp8":
+        W8, sW = tim.quantize_fp8_rows(W)
+        ws = tim.Workspace(int(tim.lib().tim_logprob_fp8_workspace_size(T, d, V)))
+        for _ in range(args.profile_iters):
+            tim.logprob_fp8(hid, gam, W8, sW, ids, 0.7, b.eps, out=out, workspace=ws, check=False)
+    elif args.profile_variant == "fp32":
+        Wb, Wsm = tim.split_tf32(W.float().contiguous())
+        ws = tim.Workspace(int(tim.lib().tim_logprob_fp32_workspace_size(T, d, V)))
+        for _ in range(args.profile_iters):
+            tim.logprob_fp32(hid, gam, Wb, Wsm, ids, 0.7, b.eps, out=out, workspace=ws,
+                             check=False)
+    else:
+        tim.logprob(hid, gam, W, ids, 0.7, b.eps, out=out)
+        ws = tim.Workspace(int(tim.lib().tim_logprob_backward_workspace_size(T, d, V)))
+        g = torch.ones(T, dtype=torch.float32, device="cuda")
+        dy = torch.empty(T, d, dtype=torch.float32, device="cuda")
+        dW = torch.empty(V, d, dtype=torch.float32, device="cuda")
+        for _ in range(args.profile_iters):
+            tim.logprob_backward(hid, gam, W, ids, out[1], g, 0.7, b.eps, out_dy=dy, out_dW=dW,
+                                 workspace=ws, check=False)
+    ws.check(f"profile {args.profile_variant}")
+    torch.cuda.synchronize()
+    return 0
+
+
 def profile_case(args):
     """A few tim_logprob calls of one shape, for ncu captures of the kernels."""
     import numpy as np
@@ -268,9 +301,11 @@ def profile_case(args):
 
     hid, gam, W = bf16(b.hidden_gen), bf16(b.head.gamma), bf16(b.head.W)
     ids = torch.from_numpy(b.token_ids).cuda()
-    ws = tim.Workspace(tim.logprob_workspace_size(T, d, V))
     out = (torch.empty(T, device="cuda"), torch.empty(T, device="cuda"),
            torch.empty(T, dtype=torch.int32, device="cuda"))
+    if args.profile_variant != "bf16":
+        return profile_variant(args, tim, b, hid, gam, W, ids, out)
+    ws = tim.Workspace(tim.logprob_workspace_size(T, d, V))
     for _ in range(args.profile_iters):
         tim.logprob(hid, gam, W, ids, 0.7, b.eps, out=out, workspace=ws, check=False)
     ws.check("profile case")
