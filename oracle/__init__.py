@@ -36,7 +36,7 @@ from .compare import (  # noqa: F401
     FLAG_K3_OVERFLOW, PAIRS, oracle_compare, oracle_compare_lenient, compare_summary,
     compare_bitwise,
 )
-from .processed import oracle_processed_logprob, process_row  # noqa: F401
+from .processed import oracle_processed_logprob, process_head, process_row  # noqa: F401
 from .fp8 import (e4m3_round, fp8_scale, oracle_logprob_fp8, quantize_rows,  # noqa: F401
                   rmsnorm_fp32)
 from .fp32head import oracle_logprob_fp32, rmsnorm_unrounded  # noqa: F401

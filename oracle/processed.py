@@ -20,6 +20,11 @@ Readings (the pages give the top-k example only):
 * processed logprob = s_x - log sum_{v kept} exp(s_v) for a kept target,
   -inf for a filtered-out target (probability 0), with s = z / tau.
 
+``process_head`` gives the sampler's top-k head of a row (ids and processed
+logprobs), the support a sampler-expected score is taken over ("Rollout-Training
+Mismatch in LLM RL", section 4.3: the reference implementation of score
+centering stores a top-k head).
+
 Per row the oracle also reports the decision margins used by the parity
 tests: ``gap_k`` = z_(k) - z_(k+1) (the logit gap at the top-k boundary) and
 ``margin_p`` = the distance of the top-p cumulative sums next to the cut from p.
@@ -31,6 +36,25 @@ import math
 import numpy as np
 
 from .logprob import logits, rmsnorm, widen_bf16
+
+
+def process_head(z: np.ndarray, temperature: float, top_k: int, top_p: float):
+    """The sampler's top-k head of one row of fp64 logits: the min(top_k, V) token ids in
+    top-k order (logit descending, lower id first on ties) and their processed logprobs
+    (log of the renormalised top-k / top-p distribution; -inf where top-p removed the
+    token).  The support that a sampler-expected score is taken over."""
+    V = z.shape[0]
+    order = np.lexsort((np.arange(V), -z))
+    top = order[:min(top_k, V)]
+    s = z[top] / temperature
+    m = s[0]
+    e = np.exp(s - m)
+    q = e / np.sum(e)
+    before = np.concatenate(([0.0], np.cumsum(q)[:-1]))
+    keep = before < top_p
+    keep[0] = True
+    lse = m + math.log(float(np.sum(np.exp(s[keep] - m))))
+    return top.astype(np.int64), np.where(keep, s - lse, -math.inf)
 
 
 def process_row(z: np.ndarray, x: int, temperature: float, top_k: int, top_p: float):
@@ -65,8 +89,11 @@ def oracle_processed_logprob(hidden_bits, gamma_bits, W_bits, token_ids, tempera
     hidden_bits = np.asarray(hidden_bits, dtype=np.uint16)
     T = hidden_bits.shape[0]
     gamma = widen_bf16(gamma_bits)
+    V = np.asarray(W_bits).shape[0]
+    kk = min(top_k, V)
     out = dict(logprob=np.empty(T), lse_kept=np.empty(T), kept=np.empty(T, dtype=np.int64),
-               gap_k=np.empty(T), margin_p=np.empty(T))
+               gap_k=np.empty(T), margin_p=np.empty(T),
+               topk_ids=np.empty((T, kk), dtype=np.int64), topk_logprob=np.empty((T, kk)))
     ids = np.asarray(token_ids, dtype=np.int64)
     for r0 in range(0, T, row_block):
         r1 = min(T, r0 + row_block)
@@ -76,4 +103,6 @@ def oracle_processed_logprob(hidden_bits, gamma_bits, W_bits, token_ids, tempera
             res = process_row(z[i], int(ids[r0 + i]), temperature, top_k, top_p)
             (out["logprob"][r0 + i], out["lse_kept"][r0 + i], out["kept"][r0 + i],
              out["gap_k"][r0 + i], out["margin_p"][r0 + i]) = res
+            out["topk_ids"][r0 + i], out["topk_logprob"][r0 + i] = process_head(
+                z[i], temperature, top_k, top_p)
     return out

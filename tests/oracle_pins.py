@@ -745,6 +745,31 @@ def pin_processed_library_topk():
     assert np.max(np.abs(pr["logprob"] - ls[:, 3].numpy())) < 1e-12
 
 
+def pin_processed_head():
+    """The top-k head: k = 2 on (0.5, 0.3, 0.2) gives ids (0, 1) with ln 0.625, ln 0.375;
+    k = 3, p = 0.7 keeps two and reports -inf for the third; torch.topk (a library routine)
+    gives the same ids on distinct logits and log_softmax of the top-k values the same
+    logprobs when p = 1."""
+    import torch
+    z = np.log(np.array([0.5, 0.3, 0.2]))
+    ids, lp = oracle.process_head(z, 1.0, 2, 1.0)
+    assert list(ids) == [0, 1]
+    assert np.max(np.abs(lp - np.log([0.625, 0.375]))) < 1e-12
+    ids, lp = oracle.process_head(z, 1.0, 3, 0.7)
+    assert list(ids) == [0, 1, 2] and lp[2] == -math.inf
+    assert np.max(np.abs(lp[:2] - np.log([0.625, 0.375]))) < 1e-12
+    ids, lp = oracle.process_head(np.array([1.0, 1.0, 1.0, 0.0]), 1.0, 2, 1.0)
+    assert list(ids) == [0, 1]                     # ties keep the lower ids
+    b = synth.make_custom(T=6, d=128, V=300, temperature=0.7, tag="proc_head")
+    pr = oracle.oracle_processed_logprob(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 0.7,
+                                         b.eps, 9, 1.0)
+    y = oracle.rmsnorm(oracle.widen_bf16(b.hidden_gen), oracle.widen_bf16(b.head.gamma), b.eps)
+    vals, idx = torch.topk(torch.from_numpy(oracle.logits(y, b.head.W)), 9, dim=1)
+    assert np.array_equal(pr["topk_ids"], idx.numpy())
+    ls = torch.log_softmax(vals / 0.7, dim=1).numpy()
+    assert np.max(np.abs(pr["topk_logprob"] - ls)) < 1e-12
+
+
 # ---------------------------------------------------------------------------
 # FP8 (e4m3) head pins
 

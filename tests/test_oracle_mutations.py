@@ -174,6 +174,22 @@ def _proc_ties_high_id(z, x, temperature, top_k, top_p):
     return _orig_process_row(zz[::-1].copy(), V - 1 - x, temperature, top_k, top_p)
 
 
+_orig_process_head = opr.process_head
+
+
+def _head_not_renormalised(z, temperature, top_k, top_p):
+    ids, lp = _orig_process_head(z, temperature, top_k, top_p)
+    s = z / temperature
+    full = float(np.max(s) + np.log(np.sum(np.exp(s - np.max(s)))))
+    return ids, np.where(np.isfinite(lp), s[ids] - full, lp)
+
+
+def _head_id_order(z, temperature, top_k, top_p):
+    ids, lp = _orig_process_head(z, temperature, top_k, top_p)
+    o = np.argsort(ids, kind="stable")
+    return ids[o], lp[o]
+
+
 import oracle.fp8 as of8
 
 
@@ -285,6 +301,9 @@ MUTATIONS = [
      ["pin_processed_page_topk"]),
     ("top-k ties keep the higher ids", opr, "process_row", _proc_ties_high_id,
      ["pin_processed_ties_and_temperature"]),
+    ("top-k head not renormalised", opr, "process_head", _head_not_renormalised,
+     ["pin_processed_head"]),
+    ("top-k head in id order", opr, "process_head", _head_id_order, ["pin_processed_head"]),
     ("e4m3 truncation", of8, "e4m3_round", _e4m3_truncate, ["pin_e4m3_rounding_exhaustive"]),
     ("e4m3 with two mantissa bits", of8, "e4m3_round", _e4m3_two_mantissa_bits,
      ["pin_e4m3_rounding_exhaustive"]),
