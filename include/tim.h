@@ -376,6 +376,23 @@ tim_status tim_processed_logprob(const void *hidden, const void *gamma, const vo
                                  float *out_logprob, float *out_lse_kept, int32_t *out_kept,
                                  void *workspace, size_t workspace_bytes, tim_stream_t stream);
 
+/* The same score, also returning the sampler's top-k head of every row: the
+ * K = min(top_k, V) token ids in top-k order (logit descending, lower id first
+ * on equal logits) and their processed logprobs, s_v - out_lse_kept[t] for a
+ * kept token and -inf for one past the top-p cut.  "Rollout-Training Mismatch
+ * in LLM RL", section 4.3: score centering needs the sampler-expected trainer
+ * score, and its reference implementation stores a top-k head.
+ *   out_head_ids      int32 [T, K] row-major; out_head_logprob fp32 [T, K].
+ * Both NULL is tim_processed_logprob; one NULL is TIM_ERR_INVALID_ARG.  A row
+ * that reports TIM_ERR_CAPACITY gets ids -1 and NaN logprobs. */
+tim_status tim_processed_logprob_head(const void *hidden, const void *gamma, const void *W,
+                                      const int32_t *token_ids, int64_t T, int32_t d, int32_t V,
+                                      float temperature, float eps, int32_t top_k, float top_p,
+                                      float *out_logprob, float *out_lse_kept, int32_t *out_kept,
+                                      int32_t *out_head_ids, float *out_head_logprob,
+                                      void *workspace, size_t workspace_bytes,
+                                      tim_stream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * Vocabulary-parallel linear logprob.
  *

@@ -27,7 +27,8 @@ centering stores a top-k head).
 
 Per row the oracle also reports the decision margins used by the parity
 tests: ``gap_k`` = z_(k) - z_(k+1) (the logit gap at the top-k boundary) and
-``margin_p`` = the distance of the top-p cumulative sums next to the cut from p.
+``margin_p`` = the distance of the top-p cumulative sums next to the cut from p,
+``rank_gap`` = the smallest logit gap between neighbours inside the top-k head.
 """
 from __future__ import annotations
 
@@ -93,7 +94,8 @@ def oracle_processed_logprob(hidden_bits, gamma_bits, W_bits, token_ids, tempera
     kk = min(top_k, V)
     out = dict(logprob=np.empty(T), lse_kept=np.empty(T), kept=np.empty(T, dtype=np.int64),
                gap_k=np.empty(T), margin_p=np.empty(T),
-               topk_ids=np.empty((T, kk), dtype=np.int64), topk_logprob=np.empty((T, kk)))
+               topk_ids=np.empty((T, kk), dtype=np.int64), topk_logprob=np.empty((T, kk)),
+               rank_gap=np.empty(T))
     ids = np.asarray(token_ids, dtype=np.int64)
     for r0 in range(0, T, row_block):
         r1 = min(T, r0 + row_block)
@@ -105,4 +107,6 @@ def oracle_processed_logprob(hidden_bits, gamma_bits, W_bits, token_ids, tempera
              out["gap_k"][r0 + i], out["margin_p"][r0 + i]) = res
             out["topk_ids"][r0 + i], out["topk_logprob"][r0 + i] = process_head(
                 z[i], temperature, top_k, top_p)
+            zk = z[i][out["topk_ids"][r0 + i]]
+            out["rank_gap"][r0 + i] = float(np.min(zk[:-1] - zk[1:])) if kk > 1 else math.inf
     return out

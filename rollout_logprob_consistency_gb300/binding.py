@@ -84,6 +84,9 @@ _SIGNATURES = {
     "tim_logprob_backward": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32,
                                         _f32, _vp, _vp, _i32, _vp, _sz, _vp]),
     "tim_processed_logprob_workspace_size": (_sz, [_i64, _i32, _i32]),
+    "tim_processed_logprob_head": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32,
+                                              _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                              _vp]),
     "tim_processed_logprob": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _i32,
                                          _f32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "tim_vocab_shard": (_c.c_int, [_i32, _i32, _i32, _c.POINTER(_i32), _c.POINTER(_i32)]),
@@ -481,9 +484,11 @@ def logprob_backward(hidden, gamma, W, token_ids, lse, grad_logprob, temperature
 
 def processed_logprob(hidden, gamma, W, token_ids, temperature: float, eps: float, top_k: int,
                       top_p: float = 1.0, *, out=None, workspace: Optional[Workspace] = None,
-                      stream=None, check: bool = True):
+                      stream=None, check: bool = True, head: bool = False):
     """Top-k / top-p processed score with tim_processed_logprob.
-    Returns (logprob f32 [T] (-inf if filtered out), lse_kept f32 [T], kept i32 [T])."""
+    Returns (logprob f32 [T] (-inf if filtered out), lse_kept f32 [T], kept i32 [T]); with
+    ``head`` also the top-k head (ids i32 [T, K], processed logprobs f32 [T, K],
+    K = min(top_k, V)) from tim_processed_logprob_head."""
     torch = _torch()
     hidden = _as_bf16(hidden, "hidden")
     gamma = _as_bf16(gamma, "gamma")
@@ -498,14 +503,24 @@ def processed_logprob(hidden, gamma, W, token_ids, temperature: float, eps: floa
                torch.empty(T, dtype=torch.int32, device=dev))
     if workspace is None:
         workspace = Workspace(int(lib().tim_processed_logprob_workspace_size(T, d, V)), dev, stream)
-    code = lib().tim_processed_logprob(_ptr(hidden), _ptr(gamma), _ptr(W), _ptr(token_ids), T, d,
-                                       V, float(temperature), float(eps), int(top_k), float(top_p),
-                                       _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), workspace.ptr,
-                                       workspace.nbytes, _stream_ptr(stream))
+    if head:
+        K = min(int(top_k), V)
+        hid_ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+        hid_lp = torch.empty(T, K, dtype=torch.float32, device=dev)
+        code = lib().tim_processed_logprob_head(
+            _ptr(hidden), _ptr(gamma), _ptr(W), _ptr(token_ids), T, d, V, float(temperature),
+            float(eps), int(top_k), float(top_p), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+            _ptr(hid_ids), _ptr(hid_lp), workspace.ptr, workspace.nbytes, _stream_ptr(stream))
+    else:
+        code = lib().tim_processed_logprob(_ptr(hidden), _ptr(gamma), _ptr(W), _ptr(token_ids), T,
+                                           d, V, float(temperature), float(eps), int(top_k),
+                                           float(top_p), _ptr(out[0]), _ptr(out[1]),
+                                           _ptr(out[2]), workspace.ptr, workspace.nbytes,
+                                           _stream_ptr(stream))
     _check(code, "tim_processed_logprob")
     if check:
         workspace.check("tim_processed_logprob", stream)
-    return out
+    return (*out, hid_ids, hid_lp) if head else out
 
 
 # ----------------------------------------------------------------------------- vocab-parallel

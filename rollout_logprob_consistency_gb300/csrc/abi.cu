@@ -56,7 +56,8 @@ cudaError_t launch_topk_threshold(const void* part, int64_t T, int V, int k, flo
                                   cudaStream_t stream);
 cudaError_t launch_topk_finalize(const void* cand, const int* cnt, const int32_t* ids, int64_t T,
                                  int V, int k, float top_p, float temperature, int cap,
-                                 float* out_lp, float* out_lse, int32_t* out_kept, int* status,
+                                 float* out_lp, float* out_lse, int32_t* out_kept,
+                                 int32_t* head_ids, float* head_lp, int* status,
                                  cudaStream_t stream);
 cudaError_t launch_shard_reduce(const void* part, const float* tgt, int64_t T, int V, int G, int g,
                                 int v_len, void* out_rec, float* out_tgt, cudaStream_t stream);
@@ -530,8 +531,23 @@ tim_status tim_processed_logprob(const void* hidden, const void* gamma, const vo
                                  float temperature, float eps, int32_t top_k, float top_p,
                                  float* out_logprob, float* out_lse_kept, int32_t* out_kept,
                                  void* workspace, size_t workspace_bytes, tim_stream_t stream) {
+  return tim_processed_logprob_head(hidden, gamma, W, token_ids, T, d, V, temperature, eps, top_k,
+                                    top_p, out_logprob, out_lse_kept, out_kept, nullptr, nullptr,
+                                    workspace, workspace_bytes, stream);
+}
+
+tim_status tim_processed_logprob_head(const void* hidden, const void* gamma, const void* W,
+                                      const int32_t* token_ids, int64_t T, int32_t d, int32_t V,
+                                      float temperature, float eps, int32_t top_k, float top_p,
+                                      float* out_logprob, float* out_lse_kept, int32_t* out_kept,
+                                      int32_t* out_head_ids, float* out_head_logprob,
+                                      void* workspace, size_t workspace_bytes,
+                                      tim_stream_t stream) {
   if (hidden == nullptr || gamma == nullptr || W == nullptr || token_ids == nullptr ||
       out_logprob == nullptr || out_lse_kept == nullptr || out_kept == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if ((out_head_ids == nullptr) != (out_head_logprob == nullptr)) return TIM_ERR_INVALID_ARG;
+  if (out_head_ids != nullptr && (!aligned(out_head_ids, 4) || !aligned(out_head_logprob, 4)))
     return TIM_ERR_INVALID_ARG;
   if (!aligned(hidden, 16) || !aligned(gamma, 16) || !aligned(W, 16) || !aligned(token_ids, 4) ||
       !aligned(out_logprob, 4) || !aligned(out_lse_kept, 4) || !aligned(out_kept, 4))
@@ -568,7 +584,7 @@ tim_status tim_processed_logprob(const void* hidden, const void* gamma, const vo
     return TIM_ERR_CUDA;
   return from_cuda(launch_topk_finalize(cand, cnt, token_ids, T, V, top_k, top_p, temperature,
                                         TIM_PROCESSED_CAPACITY, out_logprob, out_lse_kept,
-                                        out_kept, status, st));
+                                        out_kept, out_head_ids, out_head_logprob, status, st));
 }
 
 tim_status tim_vocab_shard(int32_t V, int32_t G, int32_t g, int32_t* v0, int32_t* v_len) {

@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(32 * kProcWarps)
                          const int32_t* __restrict__ ids, int64_t T, int V, int k, double top_p,
                          double temperature, int cap, float* __restrict__ out_lp,
                          float* __restrict__ out_lse, int32_t* __restrict__ out_kept,
+                         int32_t* __restrict__ head_ids, float* __restrict__ head_lp,
                          int* status) {
   extern __shared__ unsigned long long sbuf[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(32 * kProcWarps)
   if (row >= T) return;
   const int n = __ldcg(cnt + row);
   const int x = __ldg(ids + row);
+  const int kh = k < V ? k : V;  // head entries per row
   if (n > cap || n < 1) {
     if (lane == 0) {
       set_status(status, n > cap ? TIM_ERR_CAPACITY : TIM_ERR_NONFINITE);
@@ -105,6 +107,11 @@ __global__ void __launch_bounds__(32 * kProcWarps)
       out_lse[row] = __int_as_float(0x7FC00000);
       out_kept[row] = 0;
     }
+    if (head_ids != nullptr)
+      for (int i = lane; i < kh; i += 32) {
+        head_ids[row * kh + i] = -1;
+        head_lp[row * kh + i] = __int_as_float(0x7FC00000);
+      }
     return;
   }
   unsigned long long* b = sbuf + warp * kProcSortMax;
@@ -159,6 +166,13 @@ __global__ void __launch_bounds__(32 * kProcWarps)
   out_lp[row] = static_cast<float>(lp);
   out_lse[row] = static_cast<float>(lse);
   out_kept[row] = kept;
+  if (head_ids != nullptr) {
+    // the top-k head: ids in top-k order, processed logprobs (-inf past the top-p cut)
+    for (int i = 0; i < kh; ++i) {
+      head_ids[row * kh + i] = i < kk ? idv[i] : -1;
+      head_lp[row * kh + i] = i < kept ? static_cast<float>(s[i] - lse) : -INFINITY;
+    }
+  }
 }
 
 cudaError_t launch_topk_threshold(const void* part, int64_t T, int V, int k, float* thr, int* cnt,
@@ -177,7 +191,8 @@ cudaError_t launch_topk_threshold(const void* part, int64_t T, int V, int k, flo
 
 cudaError_t launch_topk_finalize(const void* cand, const int* cnt, const int32_t* ids, int64_t T,
                                  int V, int k, float top_p, float temperature, int cap,
-                                 float* out_lp, float* out_lse, int32_t* out_kept, int* status,
+                                 float* out_lp, float* out_lse, int32_t* out_kept,
+                                 int32_t* head_ids, float* head_lp, int* status,
                                  cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(kProcWarps) * kProcSortMax * 8;
   cudaError_t e = cudaFuncSetAttribute(topk_finalize_kernel,
@@ -187,7 +202,7 @@ cudaError_t launch_topk_finalize(const void* cand, const int* cnt, const int32_t
   const int64_t blocks = (T + kProcWarps - 1) / kProcWarps;
   topk_finalize_kernel<<<static_cast<unsigned>(blocks), 32 * kProcWarps, smem, stream>>>(
       static_cast<const uint2*>(cand), cnt, ids, T, V, k, static_cast<double>(top_p),
-      static_cast<double>(temperature), cap, out_lp, out_lse, out_kept, status);
+      static_cast<double>(temperature), cap, out_lp, out_lse, out_kept, head_ids, head_lp, status);
   return cudaGetLastError();
 }
 

@@ -43,6 +43,25 @@ def check(got, orc, what):
         assert abs(float(lse[i]) - orc["lse_kept"][i]) <= LP_TOL, (what, i)
 
 
+def check_head(got_ids, got_lp, orc, what):
+    """Rows whose top-k boundary and top-p cut are decided (as in ``check``): the head holds
+    the same ids; where the ranks inside the head are decided too (neighbour gaps > 1e-3)
+    the order matches; the logprob of every id matches within 2e-3 (or both -inf)."""
+    ok = (orc["gap_k"] > 1e-3) & (orc["margin_p"] > 1e-4)
+    for i in np.flatnonzero(ok):
+        gi, oi = got_ids[i].astype(np.int64), orc["topk_ids"][i]
+        assert set(gi.tolist()) == set(oi.tolist()), (what, i)
+        if orc["rank_gap"][i] > 1e-3:
+            assert np.array_equal(gi, oi), (what, i)
+        want = dict(zip(oi.tolist(), orc["topk_logprob"][i].tolist()))
+        for v, a in zip(gi.tolist(), got_lp[i].tolist()):
+            b = want[v]
+            if b == -math.inf:
+                assert a == -math.inf, (what, i, v, a)
+            else:
+                assert abs(a - b) <= LP_TOL, (what, i, v, a, b)
+
+
 def targets(b, tau):
     """Half the rows target the oracle's top-1 token (kept), half a Zipf draw."""
     raw = oracle.oracle_logprob(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, tau, b.eps)
@@ -64,6 +83,10 @@ def test_processed_parity(tim, T, d, V, tau, k, p):
     orc = oracle.oracle_processed_logprob(b.hidden_gen, b.head.gamma, b.head.W, ids,
                                           float(np.float32(tau)), b.eps, k, float(np.float32(p)))
     check(got, orc, f"T={T} V={V} k={k} p={p}")
+    r = tim.processed_logprob(bf16_cuda(b.hidden_gen), bf16_cuda(b.head.gamma),
+                              bf16_cuda(b.head.W), cuda_tensor(ids), tau, b.eps, k, p, head=True)
+    assert r[3].shape == (T, min(k, V))
+    check_head(r[3].cpu().numpy(), r[4].cpu().numpy(), orc, f"T={T} V={V} k={k} p={p} head")
 
 
 def test_processed_full_head_and_batch_invariance(tim):
@@ -77,6 +100,9 @@ def test_processed_full_head_and_batch_invariance(tim):
                                               float(np.float32(0.7)), b.eps, k,
                                               float(np.float32(p)))
         check(full, orc, f"full head k={k} p={p}")
+        r = tim.processed_logprob(hid, gam, W, cuda_tensor(ids), 0.7, b.eps, k, p, head=True)
+        assert all(np.array_equal(r[j].cpu().numpy(), full[j]) for j in range(3))
+        check_head(r[3].cpu().numpy(), r[4].cpu().numpy(), orc, f"full head k={k} p={p} head")
         # rows scored in another batch split give the same bits
         part = [x.cpu().numpy() for x in tim.processed_logprob(
             hid[7:40].contiguous(), gam, W, cuda_tensor(ids[7:40]), 0.7, b.eps, k, p)]
