@@ -120,6 +120,13 @@ struct StageGeom {
 
 constexpr size_t kGemmSmemBytes =
     1024 /* alignment slack */ + kStages * (kABytes + kBBytes) + 256 /* barriers, flags */;
+// The logit-gradient mode also stages each epilogue warp's 32 x 32 bf16 block of G
+// (2 KB per warp) so that its row-major stores cover whole 32-byte sectors.
+constexpr size_t kGradStageBytes = kEpiWarps * 32 * 64;
+
+__host__ __device__ constexpr size_t gemm_smem_bytes(int mode) {
+  return kGemmSmemBytes + (mode == 2 ? kGradStageBytes : 0);
+}
 
 __device__ __forceinline__ void tile_coords(int64_t tile, const GemmArgs& a, int& m, int& n) {
   const int64_t per_group = static_cast<int64_t>(a.group_m) * a.num_n;
@@ -217,6 +224,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   uint32_t* last_parity = reinterpret_cast<uint32_t*>(tmem_holder + 2);  // [kStages], producer
+  uint8_t* grad_stage = reinterpret_cast<uint8_t*>(bars) + 256;  // mode 2 only
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -429,7 +437,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (bad) set_status(a.status, TIM_ERR_TOKEN_RANGE);
         const float gs = (live && !bad) ? __ldg(a.gup + row) * a.inv_temp : 0.f;
         const float l2 = live ? __ldg(a.lse + row) * 1.4426950408889634f : 0.f;
-        uint16_t* grow = a.gz + row * a.ldg;
+        const uint64_t pol = l2_policy_evict_first();
+        // this warp's staging block: row l (= lane) holds 4 x 16 bytes, stored at
+        // 16-byte slot (w ^ ((l >> 1) & 3)) -- conflict-free writes by row and
+        // reads by (row, quarter)
+        uint8_t* stg = grad_stage + q * (32 * 64);
+        const int64_t row0 = row - lane;  // first row of this warp's 32
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           const int col0 = col_base + c * 32;
@@ -453,14 +466,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int u = 0; u < 2; ++u)
               if (j + u < nvalid)
-                a.gzt[static_cast<int64_t>(col0 + j + u) * a.ldgt + row] =
-                    static_cast<uint16_t>(u ? hi : lo);
+                st_global_u16_hint(a.gzt + static_cast<int64_t>(col0 + j + u) * a.ldgt + row,
+                                   static_cast<uint16_t>(u ? hi : lo), pol);
           }
-          uint4* dst = reinterpret_cast<uint4*>(grow + col0);
 #pragma unroll
           for (int w = 0; w < 4; ++w)
-            dst[w] = make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2],
-                                packed[4 * w + 3]);
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((w ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(packed[4 * w], packed[4 * w + 1], packed[4 * w + 2],
+                           packed[4 * w + 3]);
+          __syncwarp();
+          // 4 stores, each writing 8 rows x 64 bytes (whole sectors)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = 8 * i + (lane >> 2), qq = lane & 3;
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(stg + r * 64 + ((qq ^ ((r >> 1) & 3)) << 4));
+            st_global_v4_hint(a.gz + (row0 + r) * a.ldg + col0 + qq * 8, v, pol);
+          }
+          __syncwarp();
         }
       } else if constexpr (kMode == 3) {
 #pragma unroll 1
@@ -603,7 +626,7 @@ static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_
                                bool programmatic) {
   cudaError_t e = cudaFuncSetAttribute(lmhead_lse_kernel<kMode, kPrec>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kGemmSmemBytes));
+                                       static_cast<int>(gemm_smem_bytes(kMode)));
   if (e != cudaSuccess) return e;
   const int64_t grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
   // Programmatic dependent launch: the kernel's prologue and its first W loads
@@ -612,7 +635,7 @@ static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.dynamicSmemBytes = gemm_smem_bytes(kMode);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
