@@ -537,6 +537,23 @@ tim_status tim_logprob_noalloc(const void *hidden, const void *gamma, const void
                                float temperature, float eps, float *out_logprob, float *out_lse,
                                int32_t *out_top1, int32_t *out_status, tim_stream_t stream);
 
+/* ------------------------------------------------------------------------ *
+ * Self-test of the bounded waits (the pages have no counterpart: it exercises
+ * this library's own failure detection).  Every mbarrier wait in the LM-head
+ * kernel gives up after a time limit, records TIM_ERR_TIMEOUT in the status
+ * word, winds the CTA down (waiting, bounded, for its own copies and MMAs in
+ * flight) and frees its tensor memory, so the CUDA context stays usable.  This
+ * call runs that kernel on a 128 x 64 x 512 problem with its TMA producer
+ * stalled: nothing ever arrives on the pipeline barriers, the waits run out
+ * after limit_ms (1 .. 2000), and tim_status_sync(workspace, stream) then
+ * returns TIM_ERR_TIMEOUT.  No fault, trap or unbounded wait is involved.
+ * workspace: tim_selftest_workspace_size() bytes, zero-initialised once.
+ * ------------------------------------------------------------------------ */
+size_t tim_selftest_workspace_size(void);
+
+tim_status tim_selftest_wait_timeout(int32_t limit_ms, void *workspace, size_t workspace_bytes,
+                                     tim_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

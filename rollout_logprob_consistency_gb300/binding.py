@@ -83,6 +83,8 @@ _SIGNATURES = {
     "tim_logprob_backward_workspace_size": (_sz, [_i64, _i32, _i32]),
     "tim_logprob_backward": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32,
                                         _f32, _vp, _vp, _i32, _vp, _sz, _vp]),
+    "tim_selftest_workspace_size": (_sz, []),
+    "tim_selftest_wait_timeout": (_c.c_int, [_i32, _vp, _sz, _vp]),
     "tim_processed_logprob_workspace_size": (_sz, [_i64, _i32, _i32]),
     "tim_processed_logprob_head": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32,
                                               _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -480,6 +482,17 @@ def logprob_backward(hidden, gamma, W, token_ids, lse, grad_logprob, temperature
     if check:
         workspace.check("tim_logprob_backward", stream)
     return out_dy, out_dW
+
+
+def selftest_wait_timeout(limit_ms: int = 50, *, stream=None) -> str:
+    """Run the bounded-wait self-test (tim_selftest_wait_timeout) and return the status name
+    that tim_status_sync reports afterwards (``TIM_ERR_TIMEOUT`` when the waits gave up as
+    designed)."""
+    ws = Workspace(int(lib().tim_selftest_workspace_size()), stream=stream)
+    _check(lib().tim_selftest_wait_timeout(int(limit_ms), ws.ptr, ws.nbytes, _stream_ptr(stream)),
+           "tim_selftest_wait_timeout")
+    code = lib().tim_status_sync(ws.ptr, _stream_ptr(stream))
+    return STATUS_NAMES.get(int(code), f"code {code}")
 
 
 def processed_logprob(hidden, gamma, W, token_ids, temperature: float, eps: float, top_k: int,

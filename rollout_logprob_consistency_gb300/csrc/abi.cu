@@ -44,6 +44,9 @@ cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, const 
                               int accumulate, int* status, cudaStream_t stream, int num_sms);
 cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in,
                                   void* out, int64_t ld_out, cudaStream_t stream);
+cudaError_t launch_wait_selftest(const void* y, const void* W, const int32_t* ids, int64_t T,
+                                 int d, int V, void* part, float* tgt, int* status,
+                                 uint64_t limit_ns, cudaStream_t stream, int num_sms);
 cudaError_t launch_lmhead_lse_fp8(const void* y8, const float* sy, const void* W8,
                                   const float* sw, const int32_t* ids, int64_t T, int d, int V,
                                   float temperature, void* part, float* tgt, int* status,
@@ -519,6 +522,36 @@ tim_status tim_logprob_backward(const void* hidden, const void* gamma, const voi
   // dL/dW = G^T . y  (A = G^T [V, Tp], B = y^T [d, Tp])
   return from_cuda(launch_gemm_store(gzt, V, B.Tp, yt, d, B.Tp, B.Tp, V, out_dW, d, accumulate_dW,
                                      status, st, sms));
+}
+
+// Self-test shapes: one 128-row tile group against two vocabulary tiles.
+constexpr int64_t kSelftestT = 128;
+constexpr int32_t kSelftestD = 64;
+constexpr int32_t kSelftestV = 512;
+
+size_t tim_selftest_workspace_size(void) {
+  const size_t base = logprob_layout(kSelftestT, kSelftestD, kSelftestV).total;
+  return align_up(base + static_cast<size_t>(kSelftestV) * kSelftestD * 2, 1024) +
+         align_up(static_cast<size_t>(kSelftestT) * 4, 1024);
+}
+
+tim_status tim_selftest_wait_timeout(int32_t limit_ms, void* workspace, size_t workspace_bytes,
+                                     tim_stream_t stream) {
+  if (limit_ms < 1 || limit_ms > 2000) return TIM_ERR_INVALID_ARG;
+  tim_status s = check_workspace(workspace, workspace_bytes, tim_selftest_workspace_size());
+  if (s != TIM_OK) return s;
+  int sms = 0;
+  if ((s = check_device(&sms)) != TIM_OK) return s;
+  const WsLayout L = logprob_layout(kSelftestT, kSelftestD, kSelftestV);
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  const size_t w_off = align_up(L.total, 1024);
+  const size_t ids_off = align_up(w_off + static_cast<size_t>(kSelftestV) * kSelftestD * 2, 1024);
+  return from_cuda(launch_wait_selftest(
+      b + L.y_off, b + w_off, reinterpret_cast<const int32_t*>(b + ids_off), kSelftestT,
+      kSelftestD, kSelftestV, b + L.part_off, reinterpret_cast<float*>(b + L.tgt_off),
+      reinterpret_cast<int*>(b + L.status_off),
+      static_cast<uint64_t>(limit_ms) * 1000ull * 1000ull, reinterpret_cast<cudaStream_t>(stream),
+      sms));
 }
 
 size_t tim_processed_logprob_workspace_size(int64_t T, int32_t d, int32_t V) {

@@ -87,6 +87,10 @@ struct GemmArgs {
   float* c;
   int64_t ldc;
   int accumulate;
+  // bounded-wait limit of every mbarrier wait; the wait self-test shortens it and
+  // sets stall_producer so that no load is ever issued
+  uint64_t wait_limit_ns;
+  int stall_producer;
 };
 
 // Operand precision of the GEMM.
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && !a.stall_producer) {
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -294,7 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           first = false;
         }
         for (int kb = kb0; kb < a.num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag)) {
+          if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, a.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -328,14 +332,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc = 0, acc_ph = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
-        if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1u, abort_flag)) {
+        if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1u, abort_flag, a.wait_limit_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * G::kAccCols;
         for (int kb = 0; kb < a.num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], ph, abort_flag)) {
+          if (!mbar_wait(&full[stage], ph, abort_flag, a.wait_limit_ns)) {
             ok = false;
             break;
           }
@@ -390,7 +394,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int rel = x - col_base;
 
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_ph, abort_flag) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_ph, abort_flag, a.wait_limit_ns) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) {
         if (lane == 0) raise_abort(abort_flag, a.status);
@@ -685,6 +689,8 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   a.c = nullptr;
   a.ldc = 0;
   a.accumulate = 0;
+  a.wait_limit_ns = kWaitLimitNs;
+  a.stall_producer = 0;
   return cudaSuccess;
 }
 
@@ -818,7 +824,28 @@ cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, const 
   a.c = C;
   a.ldc = ldc;
   a.accumulate = accumulate;
+  a.wait_limit_ns = kWaitLimitNs;
+  a.stall_producer = 0;
   return launch_gemm<3, kPrecBf16>(map_a, map_b, map_a, map_b, a, stream, num_sms, false);
+}
+
+// Self-test of the bounded waits: the scoring kernel with its producer stalled (no
+// load is ever issued), so the MMA warp's first wait on a full stage and the
+// epilogue's wait on the accumulator run out after limit_ns; every CTA records
+// TIM_ERR_TIMEOUT, winds down and frees its TMEM.  y, W and ids must be valid
+// device memory of the stated shapes (never read by the tensor cores).
+cudaError_t launch_wait_selftest(const void* y, const void* W, const int32_t* ids, int64_t T,
+                                 int d, int V, void* part, float* tgt, int* status,
+                                 uint64_t limit_ns, cudaStream_t stream, int num_sms) {
+  CUtensorMap map_y, map_w;
+  GemmArgs a;
+  cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, 0, 1.0f, status);
+  if (e != cudaSuccess) return e;
+  a.part = static_cast<float4*>(part);
+  a.tgt = tgt;
+  a.wait_limit_ns = limit_ns;
+  a.stall_producer = 1;
+  return launch_gemm<0, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }
 
 cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T,
