@@ -33,11 +33,11 @@ L2_NOTE = "inputs larger than L2 (W 1.245 GB + hidden 268 MB per step vs 129 MB 
 
 # DRAM bytes per lmhead_lse launch of this workload (T=32768, d=4096, V=151936),
 # measured by a one-pass ncu capture of the full-size launch
-# (profiles/lmhead_lse_T32768_dram.md): 8.902 GB read + 0.315 GB written.  Valid
+# (profiles/lmhead_lse_T32768_dram.md): 8.879 GB read + 0.315 GB written.  Valid
 # only for the kernel sources hashed here and for T = 32768.
-TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "613e100cd688b966",
-                                "tim_common.cuh": "af09b7b183d5a347"},
-                       T=32768, bytes=8.902e9 + 314.78e6)
+TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "06cf4ab314822298",
+                                "tim_common.cuh": "7d45de47242fa9ed"},
+                       T=32768, bytes=8.879e9 + 314.94e6)
 
 
 def traffic_per_launch(T):
