@@ -168,15 +168,18 @@ def gpu_uuid(torch):
 
 # ------------------------------------------------------------------------------ distributed
 
-def dist_setup(n):
+def dist_setup(n, timeout_s: float = 600.0):
+    """Join the process group (one rank per GPU).  A rank that dies or never joins makes
+    the others' next collective fail after ``timeout_s`` instead of waiting forever."""
     if n <= 1 and "WORLD_SIZE" not in os.environ:
         return 0, 1, 0, None
+    import datetime
     import torch.distributed as dist
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local = int(os.environ.get("LOCAL_RANK", 0))
     backend = "nccl" if os.environ.get("TIM_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
-    dist.init_process_group(backend=backend)
+    dist.init_process_group(backend=backend, timeout=datetime.timedelta(seconds=timeout_s))
     return rank, world, local, dist
 
 
