@@ -78,7 +78,8 @@ def check(b, g, dy, dW, orc, dW_rows=None, what=""):
 
 
 @pytest.mark.parametrize("T,d,V,tau", [(1, 64, 300, 1.0), (64, 128, 1000, 1.0),
-                                       (129, 256, 2049, 0.7), (300, 320, 5000, 1.3)])
+                                       (129, 256, 2049, 0.7), (300, 320, 5000, 1.3),
+                                       (77, 5120, 3001, 0.7)])
 def test_backward_parity(tim, T, d, V, tau):
     b = synth.make_custom(T=T, d=d, V=V, temperature=tau, tag=f"bw{T}_{d}_{V}")
     g = upstream(T, T + d)

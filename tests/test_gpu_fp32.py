@@ -71,7 +71,8 @@ def test_split_tf32_definition(tim):
 
 
 @pytest.mark.parametrize("T,d,V,tau", [(1, 64, 300, 1.0), (64, 128, 1000, 1.0),
-                                       (129, 256, 2049, 0.7), (300, 320, 5000, 1.3)])
+                                       (129, 256, 2049, 0.7), (300, 320, 5000, 1.3),
+                                       (77, 5120, 3001, 0.7)])
 def test_fp32_parity(tim, T, d, V, tau):
     b = synth.make_custom(T=T, d=d, V=V, temperature=tau, tag=f"f32{T}_{d}_{V}")
     W32 = synth.fp32_weights(b.head)

@@ -38,7 +38,8 @@ def test_quantizer_bit_exact(tim):
 
 
 @pytest.mark.parametrize("T,d,V,tau", [(1, 128, 300, 1.0), (64, 128, 1000, 1.0),
-                                       (129, 256, 2049, 0.7), (300, 384, 5000, 1.3)])
+                                       (129, 256, 2049, 0.7), (300, 384, 5000, 1.3),
+                                       (77, 5120, 3001, 0.7)])
 def test_fp8_parity(tim, T, d, V, tau):
     b = synth.make_custom(T=T, d=d, V=V, temperature=tau, tag=f"f8{T}_{d}_{V}")
     W8, sW = tim.quantize_fp8_rows(bf16_cuda(b.head.W))
