@@ -64,7 +64,7 @@ def parse():
                         "(small case for ncu captures), print nothing")
     p.add_argument("--profile-iters", type=int, default=3)
     p.add_argument("--profile-variant", default="bf16",
-                   choices=["bf16", "fp8", "fp32", "backward"],
+                   choices=["bf16", "fp8", "fp32", "backward", "processed", "diag"],
                    help="with --profile-shape: which head variant to run")
     p.add_argument("--cpu-rows", type=int, default=1024,
                    help="rows of the workload the oracle scores for the CPU baseline")
@@ -274,6 +274,23 @@ def profile_variant(args, tim, b, hid, gam, W, ids, out):
         for _ in range(args.profile_iters):
             tim.logprob_fp32(hid, gam, Wb, Wsm, ids, 0.7, b.eps, out=out, workspace=ws,
                              check=False)
+    elif args.profile_variant == "processed":
+        ws = tim.Workspace(int(tim.lib().tim_processed_logprob_workspace_size(T, d, V)))
+        for _ in range(args.profile_iters):
+            tim.processed_logprob(hid, gam, W, ids, 0.7, b.eps, 50, 0.95, out=out, workspace=ws,
+                                  check=False)
+    elif args.profile_variant == "diag":
+        import numpy as np
+        tim.logprob(hid, gam, W, ids, 0.7, b.eps, out=out)
+        S = 8 if T >= 8 else 1
+        offs = torch.from_numpy(np.linspace(0, T, S + 1).astype(np.int64)).cuda()
+        mask = torch.ones(T, dtype=torch.uint8, device="cuda")
+        ws = tim.Workspace(int(tim.lib().tim_compare_diag_workspace_size(T, S)))
+        noisy = out[0] + 1e-3 * torch.randn(T, device="cuda")
+        for _ in range(args.profile_iters):
+            tim.compare_diag(out[0], out[0], noisy, offs, mask, 2.0, 0.5, 2.0,
+                             top1=(out[2], out[2], out[2]), workspace=ws, check=False,
+                             to_host=False)
     else:
         tim.logprob(hid, gam, W, ids, 0.7, b.eps, out=out)
         ws = tim.Workspace(int(tim.lib().tim_logprob_backward_workspace_size(T, d, V)))
