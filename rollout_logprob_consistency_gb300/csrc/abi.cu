@@ -70,7 +70,9 @@ cudaError_t launch_merge_shards(const void* recs, const float* tgts, const int32
 cudaError_t launch_seg_diag(const float* A, const float* B, const float* C, const int32_t* tA,
                             const int32_t* tB, const int32_t* tC, const int64_t* offs, int n_seq,
                             const uint8_t* mask, int64_t T, float tis_cap, float mis_lo,
-                            float mis_hi, tim_seq_diag* out, int* status, cudaStream_t stream);
+                            float mis_hi, tim_seq_diag* out, void* workspace,
+                            cudaStream_t stream);
+size_t diag_workspace_bytes(int64_t T, int n_seq);
 
 namespace {
 
@@ -695,7 +697,7 @@ tim_status tim_logprob_merge_shards(const void* recs, const float* tgts, const i
 
 size_t tim_compare_diag_workspace_size(int64_t T, int32_t n_seq) {
   if (T < 1 || n_seq < 1) return 0;
-  return 1024;
+  return diag_workspace_bytes(T, n_seq);
 }
 
 tim_status tim_compare_diag(const float* lp_gen, const float* lp_replay, const float* lp_train,
@@ -723,8 +725,7 @@ tim_status tim_compare_diag(const float* lp_gen, const float* lp_replay, const f
   if ((s = check_device(nullptr)) != TIM_OK) return s;
   return from_cuda(launch_seg_diag(lp_gen, lp_replay, lp_train, top1_gen, top1_replay, top1_train,
                                    seq_offsets, n_seq, mask, T, tis_cap, mis_lo, mis_hi, out_diag,
-                                   static_cast<int*>(workspace),
-                                   reinterpret_cast<cudaStream_t>(stream)));
+                                   workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

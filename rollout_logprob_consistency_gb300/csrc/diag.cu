@@ -1,4 +1,4 @@
-// Extended per-sequence mismatch diagnostics, one CTA per sequence.
+// Extended per-sequence mismatch diagnostics.
 //
 // Same roles and masking as the three-way compare (A generation, B replay,
 // C trainer; pairs A-B, B-C, A-C; active tokens only; d = C - A).  Per sequence:
@@ -17,12 +17,18 @@
 //  - MIS: w 1[lo <= w <= hi], w = exp(d) ("Rollout-Training Mismatch in LLM RL",
 //    section 2.1); mean w^2 = mean exp(2d) (same page, section 5.3).
 //
-// Sums: each thread accumulates its strided tokens in order, then a fixed
-// xor-butterfly and warp-order reduction (deterministic).  Quantiles: the
-// sequence's |left - right| values of active tokens are gathered into shared
-// memory (any order), padded with +inf to a power of two and bitonic-sorted;
-// the order statistics are exact, the interpolation is the formula above.
-// Sequences with more than kQuantMax active tokens skip the quantiles (flag).
+// Work split: the per-token sums run over many CTAs per sequence (a fixed
+// partition of each sequence into P contiguous parts, P from the batch shape as
+// in the compare kernel); each CTA accumulates its tokens per thread in order,
+// then a fixed xor-butterfly and warp-order fold, and writes one partial record.
+// A second kernel runs four CTAs per sequence: one folds the P partials in part
+// order (deterministic) and writes every field but the quantiles; three gather
+// one pair's |left - right| values of the active tokens into shared memory (any
+// order), pad them with +inf to a power of two and bitonic-sort them as 64-bit
+// keys (the bit patterns of non-negative doubles order like the values, so the
+// sort is integer work); the order statistics are exact and the interpolation
+// is the formula above.  Sequences with more than kQuantMax active tokens skip
+// the quantiles (flag, NaN).
 #include <cmath>
 #include <cstring>
 
@@ -30,47 +36,58 @@
 
 namespace tim {
 
-constexpr int kDiagThreads = 512;
-constexpr int kDiagWarps = kDiagThreads / 32;
+constexpr int kDiagThreads = 512;      // quantile / fold CTAs
+constexpr int kDiagPartThreads = 256;  // per-token partial CTAs
+constexpr int kDiagPartWarps = kDiagPartThreads / 32;
+constexpr int kDiagTokensPerPart = 256;
+constexpr int kDiagMaxParts = 256;
 constexpr int kQuantMax = TIM_DIAG_QUANTILE_MAX_TOKENS;
-constexpr size_t kDiagSmemBytes = static_cast<size_t>(kQuantMax) * sizeof(double);
+constexpr size_t kDiagSmemBytes = static_cast<size_t>(kQuantMax) * sizeof(unsigned long long);
 
-// per-thread sums: prob[3], dsum, k3, rerr, mis, w2
+// per-part sums: prob[3], dsum, k3, rerr, mis, w2
 constexpr int kDiagSums = 8;
-// per-thread counts: n, kept, flips[3]
+// per-part counts: n, kept, flips[3]
 constexpr int kDiagCounts = 5;
+
+struct DiagPart {
+  double sum[kDiagSums];
+  long long cnt[kDiagCounts];
+  int flags;
+  int pad;
+};
+
+__host__ __device__ inline int diag_parts(int64_t T, int n_seq) {
+  const int64_t avg = (T + n_seq - 1) / n_seq;
+  int64_t P = (avg + kDiagTokensPerPart - 1) / kDiagTokensPerPart;
+  if (P < 1) P = 1;
+  if (P > kDiagMaxParts) P = kDiagMaxParts;
+  return static_cast<int>(P);
+}
 
 __device__ __forceinline__ double pair_abs(int p, double a, double b, double c) {
   return p == 0 ? fabs(a - b) : (p == 1 ? fabs(b - c) : fabs(a - c));
 }
 
-__global__ void __launch_bounds__(kDiagThreads)
-    seg_diag_kernel(const float* __restrict__ A, const float* __restrict__ B,
-                    const float* __restrict__ C, const int32_t* __restrict__ tA,
-                    const int32_t* __restrict__ tB, const int32_t* __restrict__ tC,
-                    const int64_t* __restrict__ offs, const uint8_t* __restrict__ mask,
-                    int64_t T, double cap, double ln_cap, double ln_lo, double ln_hi,
-                    tim_seq_diag* __restrict__ out, int* status) {
-  extern __shared__ double buf[];
-  __shared__ double s_sum[kDiagWarps][kDiagSums];
-  __shared__ long long s_cnt[kDiagWarps][kDiagCounts];
-  __shared__ int s_flags[kDiagWarps];
-  __shared__ int s_fill;
+__device__ __forceinline__ bool offsets_ok(int64_t s, int64_t e, int64_t T) {
+  return s >= 0 && s <= e && e <= T;
+}
 
+__global__ void __launch_bounds__(kDiagPartThreads)
+    seg_diag_part_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                         const float* __restrict__ C, const int32_t* __restrict__ tA,
+                         const int32_t* __restrict__ tB, const int32_t* __restrict__ tC,
+                         const int64_t* __restrict__ offs, const uint8_t* __restrict__ mask,
+                         int64_t T, double ln_lo, double ln_hi, DiagPart* __restrict__ parts) {
+  __shared__ double s_sum[kDiagPartWarps][kDiagSums];
+  __shared__ long long s_cnt[kDiagPartWarps][kDiagCounts];
+  __shared__ int s_flags[kDiagPartWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j = blockIdx.x;
+  const int j = blockIdx.x, part = blockIdx.y, P = gridDim.y;
   const int64_t s = offs[j], e = offs[j + 1];
-  tim_seq_diag st;
-  if (!(s >= 0 && s <= e && e <= T)) {
-    if (tid == 0) {
-      memset(&st, 0, sizeof(st));
-      for (int p = 0; p < 3; ++p) st.top1_flips[p] = -1;
-      st.flags = TIM_SEQ_BAD_OFFSETS;
-      out[j] = st;
-      set_status(status, TIM_ERR_INVALID_ARG);
-    }
-    return;
-  }
+  if (!offsets_ok(s, e, T)) return;  // the fold CTA reports the sequence
+  const int64_t chunk = (e - s + P - 1) / P;
+  const int64_t t0 = s + static_cast<int64_t>(part) * chunk;
+  const int64_t t1 = t0 + chunk < e ? t0 + chunk : e;
 
   double sum[kDiagSums];
   long long cnt[kDiagCounts];
@@ -79,8 +96,7 @@ __global__ void __launch_bounds__(kDiagThreads)
 #pragma unroll
   for (int i = 0; i < kDiagCounts; ++i) cnt[i] = 0;
   int flags = 0;
-
-  for (int64_t t = s + tid; t < e; t += kDiagThreads) {
+  for (int64_t t = t0 + tid; t < t1; t += kDiagPartThreads) {
     const uint8_t m = __ldg(mask + t);
     if (m > 1) flags |= TIM_SEQ_BAD_MASK;
     if (m != 1) continue;
@@ -122,124 +138,200 @@ __global__ void __launch_bounds__(kDiagThreads)
     s_flags[warp] = flags;
   }
   __syncthreads();
-  // every thread folds the warp partials in warp order (same bits everywhere)
-  double S[kDiagSums];
-  long long N[kDiagCounts];
-  int F = 0;
-#pragma unroll
-  for (int i = 0; i < kDiagSums; ++i) S[i] = 0.0;
-#pragma unroll
-  for (int i = 0; i < kDiagCounts; ++i) N[i] = 0;
-  for (int w = 0; w < kDiagWarps; ++w) {
-#pragma unroll
-    for (int i = 0; i < kDiagSums; ++i) S[i] += s_sum[w][i];
-#pragma unroll
-    for (int i = 0; i < kDiagCounts; ++i) N[i] += s_cnt[w][i];
-    F |= s_flags[w];
-  }
-  const long long n = N[0];
-  const bool valid = !(F & TIM_SEQ_BAD_MASK) && n > 0;
-
-  double q50[3] = {0, 0, 0}, q95[3] = {0, 0, 0}, q99[3] = {0, 0, 0};
-  const bool do_q = valid && n <= kQuantMax;
-  if (do_q) {
-    int n2 = 1;
-    while (n2 < n) n2 <<= 1;
-    for (int p = 0; p < 3; ++p) {
-      if (tid == 0) s_fill = 0;
-      __syncthreads();
-      for (int64_t t = s + tid; t < e; t += kDiagThreads) {
-        if (__ldg(mask + t) != 1) continue;
-        const double a = __ldg(A + t), b = __ldg(B + t), c = __ldg(C + t);
-        const int slot = atomicAdd(&s_fill, 1);
-        if (slot < kQuantMax) buf[slot] = pair_abs(p, a, b, c);
-      }
-      __syncthreads();
-      for (int i = static_cast<int>(n) + tid; i < n2; i += kDiagThreads) buf[i] = INFINITY;
-      __syncthreads();
-      for (int k = 2; k <= n2; k <<= 1) {
-        for (int jj = k >> 1; jj > 0; jj >>= 1) {
-          for (int i = tid; i < n2; i += kDiagThreads) {
-            const int ixj = i ^ jj;
-            if (ixj > i) {
-              const double x = buf[i], y = buf[ixj];
-              const bool up = (i & k) == 0;
-              if ((x > y) == up) {
-                buf[i] = y;
-                buf[ixj] = x;
-              }
-            }
-          }
-          __syncthreads();
-        }
-      }
-      if (tid == 0) {
-        const double qs[3] = {0.5, 0.95, 0.99};
-        double r[3];
-        for (int qi = 0; qi < 3; ++qi) {
-          const double h = static_cast<double>(n - 1) * qs[qi];
-          const double fl = floor(h);
-          const long long lo = static_cast<long long>(fl);
-          const long long hi = lo + 1 < n ? lo + 1 : n - 1;
-          r[qi] = buf[lo] + (h - fl) * (buf[hi] - buf[lo]);
-        }
-        q50[p] = r[0];
-        q95[p] = r[1];
-        q99[p] = r[2];
-      }
-      __syncthreads();
-    }
-  }
   if (tid != 0) return;
-
-  memset(&st, 0, sizeof(st));
-  for (int p = 0; p < 3; ++p) st.top1_flips[p] = -1;
-  if (F & TIM_SEQ_BAD_MASK) {
-    st.flags = TIM_SEQ_BAD_MASK;
-    set_status(status, TIM_ERR_BAD_MASK);
-  } else if (n == 0) {
-    st.flags = TIM_SEQ_EMPTY;
-    set_status(status, TIM_ERR_EMPTY_SEQUENCE);
-  } else {
-    const double dn = static_cast<double>(n);
-    st.n_valid = n;
-    for (int p = 0; p < 3; ++p) {
-      st.abs_q50[p] = do_q ? q50[p] : NAN;
-      st.abs_q95[p] = do_q ? q95[p] : NAN;
-      st.abs_q99[p] = do_q ? q99[p] : NAN;
-      st.prob_mae[p] = S[p] / dn;
-    }
-    if (tA != nullptr && tB != nullptr) st.top1_flips[0] = N[2];
-    if (tB != nullptr && tC != nullptr) st.top1_flips[1] = N[3];
-    if (tA != nullptr && tC != nullptr) st.top1_flips[2] = N[4];
-    st.log_ratio_sum = S[3];
-    st.k1_sum = -S[3];
-    st.k3_sum = S[4];
-    st.seq_tis = S[3] > ln_cap ? cap : exp(S[3]);
-    st.ratio_err_mean = S[5] / dn;
-    st.mis_mean = S[6] / dn;
-    st.mis_kept = N[1];
-    st.w2_mean = S[7] / dn;
-    st.flags = F;
-    if (!do_q) st.flags |= TIM_SEQ_QUANTILE_SKIPPED;
-    if (!isfinite(st.k3_sum)) st.flags |= TIM_SEQ_K3_OVERFLOW;
-    if (F & TIM_SEQ_NONFINITE) set_status(status, TIM_ERR_NONFINITE);
+  DiagPart r;
+#pragma unroll
+  for (int i = 0; i < kDiagSums; ++i) r.sum[i] = 0.0;
+#pragma unroll
+  for (int i = 0; i < kDiagCounts; ++i) r.cnt[i] = 0;
+  r.flags = 0;
+  r.pad = 0;
+  for (int w = 0; w < kDiagPartWarps; ++w) {  // warp order
+#pragma unroll
+    for (int i = 0; i < kDiagSums; ++i) r.sum[i] += s_sum[w][i];
+#pragma unroll
+    for (int i = 0; i < kDiagCounts; ++i) r.cnt[i] += s_cnt[w][i];
+    r.flags |= s_flags[w];
   }
-  out[j] = st;
+  parts[static_cast<int64_t>(j) * P + part] = r;
+}
+
+// blockIdx.y = 0, 1, 2: quantiles of pair p; blockIdx.y = 3: fold and the other fields.
+__global__ void __launch_bounds__(kDiagThreads)
+    seg_diag_final_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                          const float* __restrict__ C, const int32_t* __restrict__ tA,
+                          const int32_t* __restrict__ tB, const int32_t* __restrict__ tC,
+                          const int64_t* __restrict__ offs, const uint8_t* __restrict__ mask,
+                          int64_t T, double cap, double ln_cap, const DiagPart* __restrict__ parts,
+                          int P, tim_seq_diag* __restrict__ out, int* status) {
+  extern __shared__ unsigned long long keys[];
+  __shared__ int s_fill, s_bad;
+  const int tid = threadIdx.x;
+  const int j = blockIdx.x, role = blockIdx.y;
+  const int64_t s = offs[j], e = offs[j + 1];
+  tim_seq_diag* o = out + j;
+  const bool ok_offs = offsets_ok(s, e, T);
+
+  if (role == 3) {
+    if (tid != 0) return;
+    if (!ok_offs) {
+      tim_seq_diag st;
+      memset(&st, 0, sizeof(st));
+      for (int p = 0; p < 3; ++p) st.top1_flips[p] = -1;
+      st.flags = TIM_SEQ_BAD_OFFSETS;
+      *o = st;
+      set_status(status, TIM_ERR_INVALID_ARG);
+      return;
+    }
+    double S[kDiagSums];
+    long long N[kDiagCounts];
+    int F = 0;
+#pragma unroll
+    for (int i = 0; i < kDiagSums; ++i) S[i] = 0.0;
+#pragma unroll
+    for (int i = 0; i < kDiagCounts; ++i) N[i] = 0;
+    for (int q = 0; q < P; ++q) {  // part order
+      const DiagPart& r = parts[static_cast<int64_t>(j) * P + q];
+#pragma unroll
+      for (int i = 0; i < kDiagSums; ++i) S[i] += r.sum[i];
+#pragma unroll
+      for (int i = 0; i < kDiagCounts; ++i) N[i] += r.cnt[i];
+      F |= r.flags;
+    }
+    const long long n = N[0];
+    // every field except the quantiles (written by the other three CTAs)
+    o->reserved = 0;
+    for (int p = 0; p < 3; ++p) {
+      o->prob_mae[p] = 0.0;
+      o->top1_flips[p] = -1;
+    }
+    o->n_valid = 0;
+    o->log_ratio_sum = o->k1_sum = o->k3_sum = o->seq_tis = 0.0;
+    o->ratio_err_mean = o->mis_mean = o->w2_mean = 0.0;
+    o->mis_kept = 0;
+    if (F & TIM_SEQ_BAD_MASK) {
+      o->flags = TIM_SEQ_BAD_MASK;
+      set_status(status, TIM_ERR_BAD_MASK);
+    } else if (n == 0) {
+      o->flags = TIM_SEQ_EMPTY;
+      set_status(status, TIM_ERR_EMPTY_SEQUENCE);
+    } else {
+      const double dn = static_cast<double>(n);
+      o->n_valid = n;
+      for (int p = 0; p < 3; ++p) o->prob_mae[p] = S[p] / dn;
+      if (tA != nullptr && tB != nullptr) o->top1_flips[0] = N[2];
+      if (tB != nullptr && tC != nullptr) o->top1_flips[1] = N[3];
+      if (tA != nullptr && tC != nullptr) o->top1_flips[2] = N[4];
+      o->log_ratio_sum = S[3];
+      o->k1_sum = -S[3];
+      o->k3_sum = S[4];
+      o->seq_tis = S[3] > ln_cap ? cap : exp(S[3]);
+      o->ratio_err_mean = S[5] / dn;
+      o->mis_mean = S[6] / dn;
+      o->mis_kept = N[1];
+      o->w2_mean = S[7] / dn;
+      int flags = F;
+      if (n > kQuantMax) flags |= TIM_SEQ_QUANTILE_SKIPPED;
+      if (!isfinite(S[4])) flags |= TIM_SEQ_K3_OVERFLOW;
+      o->flags = flags;
+      if (F & TIM_SEQ_NONFINITE) set_status(status, TIM_ERR_NONFINITE);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ quantiles of pair p
+  const int p = role;
+  if (!ok_offs) return;  // the fold CTA writes the whole record
+  if (tid == 0) {
+    s_fill = 0;
+    s_bad = 0;
+  }
+  __syncthreads();
+  for (int64_t t = s + tid; t < e; t += kDiagThreads) {
+    const uint8_t m = __ldg(mask + t);
+    if (m > 1) s_bad = 1;
+    if (m != 1) continue;
+    const double a = __ldg(A + t), b = __ldg(B + t), c = __ldg(C + t);
+    const int slot = atomicAdd(&s_fill, 1);
+    if (slot < kQuantMax)
+      keys[slot] = static_cast<unsigned long long>(__double_as_longlong(pair_abs(p, a, b, c)));
+  }
+  __syncthreads();
+  const int n = s_fill;
+  if (s_bad || n == 0 || n > kQuantMax) {
+    if (tid == 0) {
+      const double v = (s_bad || n == 0) ? 0.0 : NAN;
+      o->abs_q50[p] = v;
+      o->abs_q95[p] = v;
+      o->abs_q99[p] = v;
+    }
+    return;
+  }
+  int n2 = 1;
+  while (n2 < n) n2 <<= 1;
+  const unsigned long long kInf = static_cast<unsigned long long>(__double_as_longlong(INFINITY));
+  for (int i = n + tid; i < n2; i += kDiagThreads) keys[i] = kInf;
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int i = tid; i < n2; i += kDiagThreads) {
+        const int ixj = i ^ jj;
+        if (ixj > i) {
+          const unsigned long long x = keys[i], y = keys[ixj];
+          const bool up = (i & k) == 0;
+          if ((x > y) == up) {
+            keys[i] = y;
+            keys[ixj] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (tid == 0) {
+    const double qs[3] = {0.5, 0.95, 0.99};
+    double r[3];
+    for (int qi = 0; qi < 3; ++qi) {
+      const double h = static_cast<double>(n - 1) * qs[qi];
+      const double fl = floor(h);
+      const int lo = static_cast<int>(fl);
+      const int hi = lo + 1 < n ? lo + 1 : n - 1;
+      const double xlo = __longlong_as_double(static_cast<long long>(keys[lo]));
+      const double xhi = __longlong_as_double(static_cast<long long>(keys[hi]));
+      r[qi] = xlo + (h - fl) * (xhi - xlo);
+    }
+    o->abs_q50[p] = r[0];
+    o->abs_q95[p] = r[1];
+    o->abs_q99[p] = r[2];
+  }
+}
+
+size_t diag_workspace_bytes(int64_t T, int n_seq) {
+  return align_up(1024 + static_cast<size_t>(n_seq) * diag_parts(T, n_seq) * sizeof(DiagPart),
+                  1024);
 }
 
 cudaError_t launch_seg_diag(const float* A, const float* B, const float* C, const int32_t* tA,
                             const int32_t* tB, const int32_t* tC, const int64_t* offs, int n_seq,
                             const uint8_t* mask, int64_t T, float tis_cap, float mis_lo,
-                            float mis_hi, tim_seq_diag* out, int* status, cudaStream_t stream) {
+                            float mis_hi, tim_seq_diag* out, void* workspace,
+                            cudaStream_t stream) {
   const double cap = static_cast<double>(tis_cap);
-  cudaError_t err = cudaFuncSetAttribute(seg_diag_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kDiagSmemBytes));
+  int* status = static_cast<int*>(workspace);
+  DiagPart* parts = reinterpret_cast<DiagPart*>(static_cast<uint8_t*>(workspace) + 1024);
+  const int P = diag_parts(T, n_seq);
+  seg_diag_part_kernel<<<dim3(static_cast<unsigned>(n_seq), static_cast<unsigned>(P)),
+                         kDiagPartThreads, 0, stream>>>(
+      A, B, C, tA, tB, tC, offs, mask, T, std::log(static_cast<double>(mis_lo)),
+      std::log(static_cast<double>(mis_hi)), parts);
+  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  seg_diag_kernel<<<n_seq, kDiagThreads, kDiagSmemBytes, stream>>>(
-      A, B, C, tA, tB, tC, offs, mask, T, cap, std::log(cap),
-      std::log(static_cast<double>(mis_lo)), std::log(static_cast<double>(mis_hi)), out, status);
+  err = cudaFuncSetAttribute(seg_diag_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kDiagSmemBytes));
+  if (err != cudaSuccess) return err;
+  seg_diag_final_kernel<<<dim3(static_cast<unsigned>(n_seq), 4), kDiagThreads, kDiagSmemBytes,
+                          stream>>>(A, B, C, tA, tB, tC, offs, mask, T, cap, std::log(cap), parts,
+                                    P, out, status);
   return cudaGetLastError();
 }
 
