@@ -13,12 +13,15 @@
 //  1. topk_threshold_kernel: per row, thr = the k-th largest tile maximum.  The
 //     k largest tile maxima are k distinct logits, so the k-th largest logit of
 //     the row is >= thr: every top-k logit is >= thr.  (Rows of a vocabulary
-//     with fewer than k tiles use thr = -inf.)
+//     with fewer than k tiles use thr = -inf.)  One warp per row selects it
+//     bit by bit on order-preserving 32-bit keys (32 counting rounds, no sort).
 //  2. the LM-head kernel again, in candidate mode: logits >= thr are appended
 //     to the row's candidate slots.
 //  3. topk_finalize_kernel: per row, the candidates are sorted by (logit
 //     descending, id ascending) with a warp bitonic sort; the first k form the
-//     top-k set; top-p and the score are evaluated in fp64.
+//     top-k set; the fp64 exponentials of the top-k are taken in parallel (one
+//     or two per lane), then one lane walks them in order for top-p and the
+//     score.
 #include <cmath>
 
 #include "tim_common.cuh"
@@ -53,10 +56,11 @@ __device__ __forceinline__ uint32_t ordered_bits(uint32_t f) {
   return (f & 0x80000000u) ? ~f : (f | 0x80000000u);
 }
 
+constexpr int kThrPerLane = (TIM_PROCESSED_CAPACITY + 31) / 32;  // tile maxima per lane
+
 __global__ void __launch_bounds__(32 * kProcWarps)
     topk_threshold_kernel(const float4* __restrict__ part, int64_t T, int n_tiles, int k,
                           float* __restrict__ thr, int* __restrict__ cnt) {
-  extern __shared__ unsigned long long sbuf[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kProcWarps + warp;
   if (row >= T) return;
@@ -67,20 +71,31 @@ __global__ void __launch_bounds__(32 * kProcWarps)
     }
     return;
   }
-  unsigned long long* b = sbuf + warp * kProcSortMax;
-  int n2 = 1;
-  while (n2 < n_tiles) n2 <<= 1;
+  // this lane's tile maxima as order-preserving keys (0 = below every real key)
+  uint32_t key[kThrPerLane];
   const float4* p = part + (row >> 5) * static_cast<int64_t>(n_tiles) * 32 + (row & 31);
-  for (int i = lane; i < n2; i += 32) {
-    const uint32_t zb = (i < n_tiles) ? __float_as_uint(__ldg(p + static_cast<int64_t>(i) * 32).z)
-                                      : __float_as_uint(-INFINITY);
-    b[i] = static_cast<unsigned long long>(ordered_bits(zb)) << 32;
+  const int nr = (n_tiles + 31) / 32;  // rounds of 32 tile maxima actually present
+#pragma unroll
+  for (int r = 0; r < kThrPerLane; ++r) {
+    const int i = lane + 32 * r;
+    key[r] = (r < nr && i < n_tiles)
+                 ? ordered_bits(__float_as_uint(__ldg(p + static_cast<int64_t>(i) * 32).z))
+                 : 0u;
   }
-  __syncwarp();
-  warp_sort_desc_u64(b, n2, lane);
+  // the k-th largest key, one bit at a time from the top: keep the bit if at
+  // least k keys are >= the prefix with it set
+  uint32_t prefix = 0;
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t cand = prefix | (1u << b);
+    int c = 0;
+#pragma unroll
+    for (int r = 0; r < kThrPerLane; ++r)
+      if (r < nr) c += key[r] >= cand ? 1 : 0;
+    c = __reduce_add_sync(0xFFFFFFFFu, c);
+    if (c >= k) prefix = cand;
+  }
   if (lane == 0) {
-    const uint32_t key = static_cast<uint32_t>(b[k - 1] >> 32);
-    const uint32_t fb = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+    const uint32_t fb = (prefix & 0x80000000u) ? (prefix & 0x7FFFFFFFu) : ~prefix;
     thr[row] = __uint_as_float(fb);
     cnt[row] = 0;
   }
@@ -129,25 +144,51 @@ __global__ void __launch_bounds__(32 * kProcWarps)
   }
   __syncwarp();
   warp_sort_desc_u64(b, n2, lane);
-  if (lane != 0) return;
+  __syncwarp();
 
   const int kk = k < n ? k : n;
-  double s[TIM_PROCESSED_MAX_K];
-  int idv[TIM_PROCESSED_MAX_K];
-  for (int i = 0; i < kk; ++i) {
-    const uint32_t key = static_cast<uint32_t>(b[i] >> 32);
-    const uint32_t fb = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
-    s[i] = static_cast<double>(__uint_as_float(fb)) / temperature;
-    idv[i] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(b[i] & 0xFFFFFFFFull));
+  // scaled logits and exp(s_i - s_0) of the top-k, two entries per lane at most
+  // (k <= 64), written back over the sorted keys as doubles
+  double* ev = reinterpret_cast<double*>(b);
+  int* idv_s = reinterpret_cast<int*>(b + TIM_PROCESSED_MAX_K * 2);
+  const uint32_t key0 = static_cast<uint32_t>(b[0] >> 32);
+  const double m =
+      static_cast<double>(__uint_as_float((key0 & 0x80000000u) ? (key0 & 0x7FFFFFFFu) : ~key0)) /
+      temperature;
+  double sv[2], evv[2];
+  int idl[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = lane + 32 * h;
+    if (i < kk) {
+      const uint32_t key = static_cast<uint32_t>(b[i] >> 32);
+      const uint32_t fb = (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
+      sv[h] = static_cast<double>(__uint_as_float(fb)) / temperature;
+      idl[h] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(b[i] & 0xFFFFFFFFull));
+      evv[h] = exp(sv[h] - m);
+    }
   }
-  const double m = s[0];
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = lane + 32 * h;
+    if (i < kk) {
+      ev[i] = evv[h];
+      ev[TIM_PROCESSED_MAX_K + i] = sv[h];
+      idv_s[i] = idl[h];
+    }
+  }
+  __syncwarp();
+  if (lane != 0) return;
+  const double* s = ev + TIM_PROCESSED_MAX_K;  // scaled logits of the top-k, in order
+  const int* idv = idv_s;                      // their token ids
   double total = 0.0;
-  for (int i = 0; i < kk; ++i) total += exp(s[i] - m);
+  for (int i = 0; i < kk; ++i) total += ev[i];
   // top-p on the renormalised top-k distribution
   int kept = 0;
   double before = 0.0, kept_sum = 0.0;
   for (int i = 0; i < kk; ++i) {
-    const double e = exp(s[i] - m);
+    const double e = ev[i];
     if (i > 0 && !(before < top_p * total)) break;
     kept_sum += e;
     before += e;
@@ -178,13 +219,8 @@ __global__ void __launch_bounds__(32 * kProcWarps)
 cudaError_t launch_topk_threshold(const void* part, int64_t T, int V, int k, float* thr, int* cnt,
                                   cudaStream_t stream) {
   const int n_tiles = (V + kBN - 1) / kBN;
-  const size_t smem = static_cast<size_t>(kProcWarps) * kProcSortMax * 8;
-  cudaError_t e = cudaFuncSetAttribute(topk_threshold_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
   const int64_t blocks = (T + kProcWarps - 1) / kProcWarps;
-  topk_threshold_kernel<<<static_cast<unsigned>(blocks), 32 * kProcWarps, smem, stream>>>(
+  topk_threshold_kernel<<<static_cast<unsigned>(blocks), 32 * kProcWarps, 0, stream>>>(
       static_cast<const float4*>(part), T, n_tiles, k, thr, cnt);
   return cudaGetLastError();
 }
