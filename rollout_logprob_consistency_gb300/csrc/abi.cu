@@ -53,10 +53,15 @@ cudaError_t launch_lmhead_lse_fp8(const void* y8, const float* sy, const void* W
                                   cudaStream_t stream, int num_sms);
 cudaError_t launch_lmhead_collect(const void* y, const void* W, const int32_t* ids, int64_t T,
                                   int d, int V, float temperature, const float* thr, int* cnt,
-                                  void* cand, int cap, int* status, cudaStream_t stream,
-                                  int num_sms);
-cudaError_t launch_topk_threshold(const void* part, int64_t T, int V, int k, float* thr, int* cnt,
-                                  cudaStream_t stream);
+                                  void* cand, int cap, const int* dyn_T, const int* row_map,
+                                  int* status, cudaStream_t stream, int num_sms);
+cudaError_t launch_lmhead_top4(const void* y, const void* W, const int32_t* ids, int64_t T, int d,
+                               int V, void* top4, int* status, cudaStream_t stream, int num_sms);
+cudaError_t launch_topk_candidates(const void* top4, int64_t T, int V, int k, float* thr,
+                                   int* cnt, void* cand, int cap, int* fb_count, int* fb_rows,
+                                   cudaStream_t stream);
+cudaError_t launch_gather_rows(const void* y, const int* fb_rows, const int* fb_count, int64_t T,
+                               int d, void* y_fb, cudaStream_t stream, int num_sms);
 cudaError_t launch_topk_finalize(const void* cand, const int* cnt, const int32_t* ids, int64_t T,
                                  int V, int k, float top_p, float temperature, int cap,
                                  float* out_lp, float* out_lse, int32_t* out_kept,
@@ -142,18 +147,26 @@ tim_status validate_logprob_common(int64_t T, int32_t d, int32_t V, float temper
 }
 
 // Processed-score workspace: the scoring workspace, then thresholds [T],
-// candidate counters [T] and candidate slots [T][TIM_PROCESSED_CAPACITY].
+// candidate counters [T], candidate slots [T][TIM_PROCESSED_CAPACITY], top-4
+// records [ceil(T/32) * 32][n_tiles], the fallback row count and list [T], and
+// the gathered fallback rows of y [rows_padded(T), d].
 struct ProcLayout {
   WsLayout base;
-  size_t thr_off, cnt_off, cand_off, total;
+  size_t thr_off, cnt_off, cand_off, top4_off, fbn_off, fbrows_off, yfb_off, total;
 };
 ProcLayout processed_layout(int64_t T, int32_t d, int32_t V) {
   ProcLayout P;
   P.base = logprob_layout(T, d, V);
+  const size_t n_tiles = (static_cast<size_t>(V) + kBN - 1) / kBN;
+  const size_t t32 = (static_cast<size_t>(T) + 31) / 32 * 32;
   P.thr_off = align_up(P.base.total, 1024);
   P.cnt_off = align_up(P.thr_off + static_cast<size_t>(T) * 4, 1024);
   P.cand_off = align_up(P.cnt_off + static_cast<size_t>(T) * 4, 1024);
-  P.total = align_up(P.cand_off + static_cast<size_t>(T) * TIM_PROCESSED_CAPACITY * 8, 1024);
+  P.top4_off = align_up(P.cand_off + static_cast<size_t>(T) * TIM_PROCESSED_CAPACITY * 8, 1024);
+  P.fbn_off = align_up(P.top4_off + t32 * n_tiles * sizeof(Top4Rec), 1024);
+  P.fbrows_off = P.fbn_off + 256;
+  P.yfb_off = align_up(P.fbrows_off + static_cast<size_t>(T) * 4, 1024);
+  P.total = align_up(P.yfb_off + static_cast<size_t>(rows_padded(T)) * d * 2, 1024);
   return P;
 }
 
@@ -610,12 +623,24 @@ tim_status tim_processed_logprob_head(const void* hidden, const void* gamma, con
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (launch_rmsnorm_rows(hidden, gamma, T, d, eps, y, status, st) != cudaSuccess)
     return TIM_ERR_CUDA;
-  if (launch_lmhead_lse(y, W, token_ids, T, d, V, temperature, part, tgt, status, st, sms) !=
-      cudaSuccess)
+  void* top4 = b + P.top4_off;
+  int* fb_n = reinterpret_cast<int*>(b + P.fbn_off);
+  int* fb_rows = reinterpret_cast<int*>(b + P.fbrows_off);
+  void* y_fb = b + P.yfb_off;
+  (void)part;
+  (void)tgt;
+  if (launch_lmhead_top4(y, W, token_ids, T, d, V, top4, status, st, sms) != cudaSuccess)
     return TIM_ERR_CUDA;
-  if (launch_topk_threshold(part, T, V, top_k, thr, cnt, st) != cudaSuccess) return TIM_ERR_CUDA;
-  if (launch_lmhead_collect(y, W, token_ids, T, d, V, temperature, thr, cnt, cand,
-                            TIM_PROCESSED_CAPACITY, status, st, sms) != cudaSuccess)
+  if (cudaMemsetAsync(fb_n, 0, sizeof(int), st) != cudaSuccess) return TIM_ERR_CUDA;
+  if (launch_topk_candidates(top4, T, V, top_k, thr, cnt, cand, TIM_PROCESSED_CAPACITY, fb_n,
+                             fb_rows, st) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  // rows whose candidates the top-4 lists cannot vouch for: gathered and rescored
+  if (launch_gather_rows(y, fb_rows, fb_n, T, d, y_fb, st, sms) != cudaSuccess)
+    return TIM_ERR_CUDA;
+  if (launch_lmhead_collect(y_fb, W, token_ids, T, d, V, temperature, thr, cnt, cand,
+                            TIM_PROCESSED_CAPACITY, fb_n, fb_rows, status, st, sms) !=
+      cudaSuccess)
     return TIM_ERR_CUDA;
   return from_cuda(launch_topk_finalize(cand, cnt, token_ids, T, V, top_k, top_p, temperature,
                                         TIM_PROCESSED_CAPACITY, out_logprob, out_lse_kept,

@@ -91,7 +91,15 @@ struct GemmArgs {
   // sets stall_producer so that no load is ever issued
   uint64_t wait_limit_ns;
   int stall_producer;
+  // top-4 mode only: per-(row, tile) records of the four largest logits
+  void* top4;
+  // collect mode only: when dyn_T is set, only row tiles below *dyn_T (a row
+  // count written by an earlier kernel) are computed, and local row r stands for
+  // row row_map[r] of the candidate slots and thresholds
+  const int* dyn_T;
+  const int* row_map;
 };
+
 
 // Operand precision of the GEMM.
 //   kPrecBf16   bf16 y and W, kind::f16, 64 K-elements per 128-byte stage row.
@@ -203,6 +211,8 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], int nval
 //          with p = exp(z / tau - lse_t), written in bf16 both row-major and
 //          transposed (rows T .. rows_padded(T)-1 get zeros).
 // kMode 3: plain GEMM C (+)= A . B^T stored in fp32 (the two backward products).
+// kMode 4: top-4 records -- the four largest logits of every (row, tile) and
+//          their ids (the first pass of the processed score).
 // kPrec: operand precision (see Prec).  tmap_y2 / tmap_w2 are the remainder
 // parts for kPrecTf32x3 and unused otherwise.
 template <int kMode, int kPrec>
@@ -263,6 +273,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // rows actually present (collect mode with a device-side row count)
+  const int64_t t_rows = (kMode == 1 && a.dyn_T != nullptr) ? static_cast<int64_t>(*a.dyn_T) : a.T;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -274,6 +286,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int64_t tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
         int m, n;
         tile_coords(tile, a, m, n);
+        if (static_cast<int64_t>(m) * kBM >= t_rows) continue;  // no rows in this tile
         int kb0 = 0;
         if (first) {
           // W does not depend on the RMSNorm kernel that precedes this one in the
@@ -332,6 +345,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc = 0, acc_ph = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+        if (kMode == 1 && a.dyn_T != nullptr) {
+          int m, n;
+          tile_coords(tile, a, m, n);
+          if (static_cast<int64_t>(m) * kBM >= t_rows) continue;
+        }
         if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1u, abort_flag, a.wait_limit_ns)) {
           ok = false;
           break;
@@ -388,6 +406,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int64_t tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
       int m, n;
       tile_coords(tile, a, m, n);
+      if (static_cast<int64_t>(m) * kBM >= t_rows) continue;
       const int64_t row = static_cast<int64_t>(m) * kBM + q * 32 + lane;
       const int x = (kMode != 3 && row < a.T) ? __ldg(a.ids + row) : -1;
       const int col_base = a.v0 + n * kBN;  // global vocabulary id of the tile's column 0
@@ -513,8 +532,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
-      } else {
-        const float thr = (row < a.T) ? __ldcg(a.thr + row) : INFINITY;
+      } else if constexpr (kMode == 4) {
+        float tv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        int ti[4] = {-1, -1, -1, -1};
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           const int col0 = col_base + c * 32;
@@ -524,9 +544,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int nvalid = min(32, a.v_end - col0);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (j < nvalid && row < a.T && __uint_as_float(r[j]) >= thr) {
-              const int slot = atomicAdd(a.cnt + row, 1);
-              if (slot < a.cap) a.cand[row * a.cap + slot] = make_uint2(r[j], col0 + j);
+            float cv = j < nvalid ? __uint_as_float(r[j]) : -INFINITY;
+            if (cv > tv[3]) {  // insert; strict > keeps the earlier (lower) id first on ties
+              int ci = col0 + j;
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                if (cv > tv[p]) {
+                  const float fv = tv[p];
+                  const int fi = ti[p];
+                  tv[p] = cv;
+                  ti[p] = ci;
+                  cv = fv;
+                  ci = fi;
+                }
+              }
+            }
+          }
+        }
+        if (row < a.T) {
+          Top4Rec* rec = static_cast<Top4Rec*>(a.top4) + ((row >> 5) * a.num_n + n) * 32 + (row & 31);
+          *reinterpret_cast<float4*>(rec->v) = make_float4(tv[0], tv[1], tv[2], tv[3]);
+          *reinterpret_cast<int4*>(rec->id) = make_int4(ti[0], ti[1], ti[2], ti[3]);
+        }
+      } else {
+        const bool live = row < t_rows;
+        const int64_t orow = (live && a.row_map != nullptr) ? __ldg(a.row_map + row) : row;
+        const float thr = live ? __ldcg(a.thr + orow) : INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          const int col0 = col_base + c * 32;
+          if (col0 >= a.v_end) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          const int nvalid = min(32, a.v_end - col0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < nvalid && live && __uint_as_float(r[j]) >= thr) {
+              const int slot = atomicAdd(a.cnt + orow, 1);
+              if (slot < a.cap) a.cand[orow * a.cap + slot] = make_uint2(r[j], col0 + j);
             }
           }
         }
@@ -691,6 +746,9 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   a.accumulate = 0;
   a.wait_limit_ns = kWaitLimitNs;
   a.stall_producer = 0;
+  a.top4 = nullptr;
+  a.dyn_T = nullptr;
+  a.row_map = nullptr;
   return cudaSuccess;
 }
 
@@ -757,10 +815,14 @@ cudaError_t launch_lmhead_lse_tf32x3(const float* y_big, const float* y_small, c
 // appended to cand[row][0 .. cap) with cnt[row] counting them (counts above cap
 // mean the row overflowed).  Launched without programmatic overlap: the
 // thresholds and zeroed counters come from the kernel just before it.
+// With dyn_T set, y holds up to T gathered rows of which only the first *dyn_T
+// are live; row r's candidates and threshold belong to row row_map[r].  Row tiles
+// are then scheduled one after another (raster groups of one row tile), so the
+// few live ones spread over all CTAs.
 cudaError_t launch_lmhead_collect(const void* y, const void* W, const int32_t* ids, int64_t T,
                                   int d, int V, float temperature, const float* thr, int* cnt,
-                                  void* cand, int cap, int* status, cudaStream_t stream,
-                                  int num_sms) {
+                                  void* cand, int cap, const int* dyn_T, const int* row_map,
+                                  int* status, cudaStream_t stream, int num_sms) {
   CUtensorMap map_y, map_w;
   GemmArgs a;
   cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, 0, temperature, status);
@@ -769,11 +831,26 @@ cudaError_t launch_lmhead_collect(const void* y, const void* W, const int32_t* i
   a.cnt = cnt;
   a.cand = static_cast<uint2*>(cand);
   a.cap = cap;
+  a.dyn_T = dyn_T;
+  a.row_map = row_map;
+  if (dyn_T != nullptr) a.group_m = 1;
   return launch_gemm<1, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }
 
 // Backward, step 1: recompute z = y . W^T and write G = dL/dz (bf16) as
 // gz [rows_padded(T)][ldg] and gzt [V][ldgt] (ldgt >= rows_padded(T)).
+// Processed score, pass 1: the four largest logits of every (row, 256-column
+// tile) with their ids, as Top4 records [ceil(T/32)][num_n][32].
+cudaError_t launch_lmhead_top4(const void* y, const void* W, const int32_t* ids, int64_t T, int d,
+                               int V, void* top4, int* status, cudaStream_t stream, int num_sms) {
+  CUtensorMap map_y, map_w;
+  GemmArgs a;
+  cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, 0, 1.0f, status);
+  if (e != cudaSuccess) return e;
+  a.top4 = top4;
+  return launch_gemm<4, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
+}
+
 cudaError_t launch_logit_grad(const void* y, const void* W, const int32_t* ids, const float* lse,
                               const float* gup, int64_t T, int d, int V, float temperature,
                               uint16_t* gz, int64_t ldg, uint16_t* gzt, int64_t ldgt, int* status,

@@ -8,20 +8,28 @@
 // (keep tokens whose preceding cumulative probability is < p).  A filtered-out
 // target scores -inf.
 //
-// Three steps after the scoring kernels have produced per-(row, 256-column
-// tile) records:
-//  1. topk_threshold_kernel: per row, thr = the k-th largest tile maximum.  The
-//     k largest tile maxima are k distinct logits, so the k-th largest logit of
-//     the row is >= thr: every top-k logit is >= thr.  (Rows of a vocabulary
-//     with fewer than k tiles use thr = -inf.)  One warp per row selects it
-//     bit by bit on order-preserving 32-bit keys (32 counting rounds, no sort).
-//  2. the LM-head kernel again, in candidate mode: logits >= thr are appended
-//     to the row's candidate slots.
-//  3. topk_finalize_kernel: per row, the candidates are sorted by (logit
+// Steps:
+//  1. the LM-head kernel in top-4 mode: for every (row, 256-column tile) the four
+//     largest logits and their ids;
+//  2. topk_candidates_kernel, one warp per row: thr = the k-th largest tile
+//     maximum (bitwise radix select on order-preserving keys).  The k largest
+//     tile maxima are k distinct logits, so every top-k logit is >= thr, and a
+//     logit >= thr can only sit in a tile whose maximum is >= thr.  If in each
+//     such tile the 4th largest logit is < thr, the stored top-4 lists hold every
+//     logit >= thr: they become the row's candidates.  Otherwise (a tile with
+//     four or more logits >= thr, or a vocabulary with fewer than k tiles) the
+//     row goes on a fallback list;
+//  3. the fallback rows are gathered and the LM-head kernel runs again over them
+//     in candidate mode (every logit >= thr appended), scheduling only the row
+//     tiles that hold them;
+//  4. topk_finalize_kernel: per row, the candidates are sorted by (logit
 //     descending, id ascending) with a warp bitonic sort; the first k form the
 //     top-k set; the fp64 exponentials of the top-k are taken in parallel (one
 //     or two per lane), then one lane walks them in order for top-p and the
 //     score.
+// Both routes produce the same candidate set (all logits >= thr, the same fp32
+// values from the same MMA sequence), so a row's result does not depend on
+// which route it took or on the batch.
 #include <cmath>
 
 #include "tim_common.cuh"
@@ -59,45 +67,102 @@ __device__ __forceinline__ uint32_t ordered_bits(uint32_t f) {
 constexpr int kThrPerLane = (TIM_PROCESSED_CAPACITY + 31) / 32;  // tile maxima per lane
 
 __global__ void __launch_bounds__(32 * kProcWarps)
-    topk_threshold_kernel(const float4* __restrict__ part, int64_t T, int n_tiles, int k,
-                          float* __restrict__ thr, int* __restrict__ cnt) {
+    topk_candidates_kernel(const Top4Rec* __restrict__ top4, int64_t T, int n_tiles, int k,
+                           float* __restrict__ thr, int* __restrict__ cnt,
+                           uint2* __restrict__ cand, int cap, int* __restrict__ fb_count,
+                           int* __restrict__ fb_rows) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kProcWarps + warp;
   if (row >= T) return;
-  if (n_tiles < k) {
+  if (n_tiles < k) {  // every logit is a candidate: the collect pass takes the row
     if (lane == 0) {
       thr[row] = -INFINITY;
       cnt[row] = 0;
+      fb_rows[atomicAdd(fb_count, 1)] = static_cast<int>(row);
     }
     return;
   }
-  // this lane's tile maxima as order-preserving keys (0 = below every real key)
+  const Top4Rec* rec = top4 + (row >> 5) * static_cast<int64_t>(n_tiles) * 32 + (row & 31);
+  const int nr = (n_tiles + 31) / 32;  // rounds of 32 tiles actually present
   uint32_t key[kThrPerLane];
-  const float4* p = part + (row >> 5) * static_cast<int64_t>(n_tiles) * 32 + (row & 31);
-  const int nr = (n_tiles + 31) / 32;  // rounds of 32 tile maxima actually present
 #pragma unroll
   for (int r = 0; r < kThrPerLane; ++r) {
     const int i = lane + 32 * r;
     key[r] = (r < nr && i < n_tiles)
-                 ? ordered_bits(__float_as_uint(__ldg(p + static_cast<int64_t>(i) * 32).z))
+                 ? ordered_bits(__float_as_uint(__ldg(&rec[static_cast<int64_t>(i) * 32].v[0])))
                  : 0u;
   }
-  // the k-th largest key, one bit at a time from the top: keep the bit if at
-  // least k keys are >= the prefix with it set
+  // the k-th largest tile maximum, one bit at a time from the top
   uint32_t prefix = 0;
   for (int b = 31; b >= 0; --b) {
-    const uint32_t cand = prefix | (1u << b);
+    const uint32_t candk = prefix | (1u << b);
     int c = 0;
 #pragma unroll
     for (int r = 0; r < kThrPerLane; ++r)
-      if (r < nr) c += key[r] >= cand ? 1 : 0;
+      if (r < nr) c += key[r] >= candk ? 1 : 0;
     c = __reduce_add_sync(0xFFFFFFFFu, c);
-    if (c >= k) prefix = cand;
+    if (c >= k) prefix = candk;
+  }
+  const float t = __uint_as_float((prefix & 0x80000000u) ? (prefix & 0x7FFFFFFFu) : ~prefix);
+  // count this lane's candidates; a tile with four logits >= t may hold more
+  int mine = 0, ovf = 0;
+#pragma unroll
+  for (int r = 0; r < kThrPerLane; ++r) {
+    const int i = lane + 32 * r;
+    if (r < nr && i < n_tiles) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(rec[static_cast<int64_t>(i) * 32].v));
+      if (v.x >= t) {
+        mine += 1 + (v.y >= t ? 1 : 0) + (v.z >= t ? 1 : 0) + (v.w >= t ? 1 : 0);
+        ovf |= v.w >= t ? 1 : 0;
+      }
+    }
+  }
+  const int total = __reduce_add_sync(0xFFFFFFFFu, mine);
+  if (__any_sync(0xFFFFFFFFu, ovf) || total > cap) {
+    if (lane == 0) {
+      thr[row] = t;
+      cnt[row] = 0;
+      fb_rows[atomicAdd(fb_count, 1)] = static_cast<int>(row);
+    }
+    return;
+  }
+  int off = mine;  // exclusive prefix over lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xFFFFFFFFu, off, o);
+    if (lane >= o) off += u;
+  }
+  off -= mine;
+  uint2* dst = cand + row * cap;
+#pragma unroll
+  for (int r = 0; r < kThrPerLane; ++r) {
+    const int i = lane + 32 * r;
+    if (r < nr && i < n_tiles) {
+      const Top4Rec& q = rec[static_cast<int64_t>(i) * 32];
+      const float4 v = __ldg(reinterpret_cast<const float4*>(q.v));
+      if (v.x >= t) {
+        const int4 id = __ldg(reinterpret_cast<const int4*>(q.id));
+        dst[off++] = make_uint2(__float_as_uint(v.x), static_cast<uint32_t>(id.x));
+        if (v.y >= t) dst[off++] = make_uint2(__float_as_uint(v.y), static_cast<uint32_t>(id.y));
+        if (v.z >= t) dst[off++] = make_uint2(__float_as_uint(v.z), static_cast<uint32_t>(id.z));
+      }
+    }
   }
   if (lane == 0) {
-    const uint32_t fb = (prefix & 0x80000000u) ? (prefix & 0x7FFFFFFFu) : ~prefix;
-    thr[row] = __uint_as_float(fb);
-    cnt[row] = 0;
+    thr[row] = t;
+    cnt[row] = total;
+  }
+}
+
+// Copies the fallback rows of y (bf16 [*, d]) into consecutive rows of y_fb.
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint4* __restrict__ y, const int* __restrict__ fb_rows,
+                       const int* __restrict__ fb_count, int nvec, uint4* __restrict__ y_fb) {
+  const int n = __ldcg(fb_count);
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < n;
+       w += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+    const int64_t src = __ldcg(fb_rows + w);
+    for (int c = threadIdx.x & 31; c < nvec; c += 32) y_fb[w * nvec + c] = __ldg(y + src * nvec + c);
   }
 }
 
@@ -216,12 +281,24 @@ __global__ void __launch_bounds__(32 * kProcWarps)
   }
 }
 
-cudaError_t launch_topk_threshold(const void* part, int64_t T, int V, int k, float* thr, int* cnt,
-                                  cudaStream_t stream) {
+cudaError_t launch_topk_candidates(const void* top4, int64_t T, int V, int k, float* thr,
+                                   int* cnt, void* cand, int cap, int* fb_count, int* fb_rows,
+                                   cudaStream_t stream) {
   const int n_tiles = (V + kBN - 1) / kBN;
   const int64_t blocks = (T + kProcWarps - 1) / kProcWarps;
-  topk_threshold_kernel<<<static_cast<unsigned>(blocks), 32 * kProcWarps, 0, stream>>>(
-      static_cast<const float4*>(part), T, n_tiles, k, thr, cnt);
+  topk_candidates_kernel<<<static_cast<unsigned>(blocks), 32 * kProcWarps, 0, stream>>>(
+      static_cast<const Top4Rec*>(top4), T, n_tiles, k, thr, cnt, static_cast<uint2*>(cand), cap,
+      fb_count, fb_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* y, const int* fb_rows, const int* fb_count, int64_t T,
+                               int d, void* y_fb, cudaStream_t stream, int num_sms) {
+  int64_t blocks = (T * 32 + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint4*>(y), fb_rows, fb_count, d / 8, static_cast<uint4*>(y_fb));
   return cudaGetLastError();
 }
 

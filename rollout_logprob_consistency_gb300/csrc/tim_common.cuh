@@ -249,6 +249,15 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
+// The four largest logits of one (row, 256-column tile): values descending and
+// their vocabulary ids (equal values: the lower id first); -inf / -1 past the
+// tile.  Written by the LM-head kernel in top-4 mode, read by the processed
+// score's candidate kernel.  Layout [ceil(T/32)][n_tiles][32].
+struct Top4Rec {
+  float v[4];
+  int32_t id[4];
+};
+
 // L2 policy for data written once and read back only much later (streams that
 // would otherwise evict the operands the tensor cores are re-reading).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

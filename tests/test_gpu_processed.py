@@ -123,6 +123,36 @@ def test_processed_k1_is_top1(tim):
     assert np.all(lp[0::3] == 0.0) and np.all(lp[1::3] == -np.inf)
 
 
+def test_processed_fallback_rows(tim):
+    """Rows whose top logits crowd one 256-column tile (five copies of the row's arg-max
+    W row placed in one tile) cannot be vouched for by the per-tile top-4 lists and are
+    rescored over the gathered fallback rows; the result must still match the oracle and
+    be identical when the row is scored alone."""
+    b = synth.make_custom(T=64, d=256, V=20000, temperature=0.9, tag="pr_fb")
+    raw = oracle.oracle_logprob(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 0.9, b.eps)
+    W = b.head.W.copy()
+    t_fb = [0, 5, 33]
+    for r in t_fb:                                  # five ties at the top inside tile 40 + r
+        base = (40 + r) * 256
+        for c in range(5):
+            W[base + 17 * c] = b.head.W[raw["top1"][r]]
+    ids = targets(b, 0.9)
+    ids[t_fb] = [(40 + r) * 256 + 34 for r in t_fb]  # the third copy of the tie
+    hid, gam, Wd = bf16_cuda(b.hidden_gen), bf16_cuda(b.head.gamma), bf16_cuda(W)
+    for k, p in ((8, 1.0), (20, 0.9)):
+        got = [x.cpu().numpy() for x in tim.processed_logprob(hid, gam, Wd, cuda_tensor(ids), 0.9,
+                                                              b.eps, k, p)]
+        orc = oracle.oracle_processed_logprob(b.hidden_gen, b.head.gamma, W, ids,
+                                              float(np.float32(0.9)), b.eps, k,
+                                              float(np.float32(p)))
+        check(got, orc, f"fallback k={k} p={p}")
+        for r in t_fb:
+            assert got[2][r] >= min(5, k) or p < 1.0
+            one = [x.cpu().numpy() for x in tim.processed_logprob(
+                hid[r:r + 1].contiguous(), gam, Wd, cuda_tensor(ids[r:r + 1]), 0.9, b.eps, k, p)]
+            assert all(one[j].tobytes() == got[j][r:r + 1].tobytes() for j in range(3))
+
+
 def test_processed_capacity_error(tim):
     """Every logit tied: more candidates than the per-row capacity -> TIM_ERR_CAPACITY."""
     b = synth.make_custom(T=8, d=64, V=4096, tag="pr_cap")
