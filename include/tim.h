@@ -354,9 +354,12 @@ tim_status tim_logprob_backward(const void *hidden, const void *gamma, const voi
  *   out_lse_kept[t] = ln sum_{v kept} exp(s_v);
  *   out_logprob[t]  = s_x - out_lse_kept[t] if the target x is kept, else -inf;
  *   out_kept[t]     = number of kept tokens.
- * Cost: the LM-head GEMM runs twice (the second pass collects, per row, the
- * logits at or above the k-th largest 256-column-tile maximum, a bound that
- * every top-k logit meets).  Results are batch-invariant like tim_logprob's.
+ * Cost: one LM-head GEMM pass that keeps the four largest logits of every
+ * (row, 256-column tile).  The k-th largest tile maximum is a bound every
+ * top-k logit meets; a row with a tile holding four or more logits at or above
+ * it (or a vocabulary of fewer than top_k tiles) is gathered and rescored,
+ * collecting every logit at or above the bound.  Results are batch-invariant
+ * like tim_logprob's and do not depend on which route a row took.
  *
  * Limits: 1 <= top_k <= TIM_PROCESSED_MAX_K, 0 < top_p <= 1, at most 2048
  * vocabulary tiles (V <= 524288), and either V >= 256 * top_k or
