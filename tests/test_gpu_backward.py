@@ -10,7 +10,11 @@ forward's logit and lse errors), inside the bound for every entry except the
 target's, where G = (g / tau)(1 - p_x) can be small while its absolute error
 is (g / tau) p_x 1e-4; that term is allowed as DELTA * (|g_t| / tau) * |W| (dy)
 and DELTA * sum over rows with x_t = v of (|g_t| / tau) |y_t| (dW), DELTA = 1e-3.
-fp32 accumulation adds 1e-6 of the largest bound."""
+fp32 accumulation adds 1e-6 of the largest bound.  dW = G^T.y is also linear in
+y, and the GPU's bf16 y and the oracle's differ by one bf16 step (at most 2^-7
+relative) on a few elements per hundred thousand (the fp32 and fp64 RMSNorms
+round them to different neighbours); a column of dW holding such an element
+moves by up to 2^-7 of its bound, so dW is allowed 3 * 2^-8 of the bound."""
 import numpy as np
 import pytest
 
@@ -69,7 +73,7 @@ def check(b, g, dy, dW, orc, dW_rows=None, what=""):
     for t, x in enumerate(ids):
         if int(x) in pos:
             tgt_dW[pos[int(x)]] += ag[t] * np.abs(orc["y"][t])
-    tol_dW = 2.0 ** -8 * orc["bound_dW"] + DELTA * tgt_dW + 1e-6 * orc["bound_dW"].max()
+    tol_dW = 3 * 2.0 ** -8 * orc["bound_dW"] + DELTA * tgt_dW + 1e-6 * orc["bound_dW"].max()
     errw = np.abs(dW[rows] - orc["dW"])
     badw = np.argwhere(errw > tol_dW)
     assert badw.size == 0, f"{what}: dW off at {badw[:3].tolist()}, err {errw.max():.3e}"
