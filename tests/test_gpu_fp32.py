@@ -11,9 +11,11 @@ the error grows linearly with the number of steps (d/8 for the main sum; the
 correction products go to their own accumulator).  Measured on GB300 over 128
 rows, V = 8192: mean lse error -3.7e-5, max 4.5e-5 at d = 4096 (-7e-5 / 9.7e-5
 at d = 8192), the bf16 head showing the same trend at half the size (d/16
-steps).  Logprob and lse are checked to FP32_TOL = 2e-4 (4x the measured
-maximum at d = 4096, ten times tighter than the bf16 head); top-1 where the
-oracle's logit gap exceeds 1e-4."""
+steps).  The bias grows with d (steps) and a logprob divides logit errors by
+tau, so logprob and lse are checked to 6e-5 * (d / 1024) / tau: 2.4e-4 at
+d = 4096, tau = 1 (3x the measured maximum there; ten times tighter than the bf16
+head), 4.3e-4 at d = 5120, tau = 0.7 (measured 2.5e-4); top-1 where the oracle's
+logit gap exceeds 1e-4."""
 import numpy as np
 import pytest
 
@@ -23,8 +25,11 @@ from parity import bf16_cuda, cuda_tensor, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-FP32_TOL = 2e-4
 FP32_TOP1_GAP = 1e-4
+
+
+def fp32_tol(d, tau):
+    return 6e-5 * (d / 1024.0) / tau
 
 
 @pytest.fixture(scope="module")
@@ -43,15 +48,16 @@ def f32_cuda(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
 
 
-def assert_fp32_parity(got, orc, rows=None, what=""):
+def assert_fp32_parity(got, orc, d, tau, rows=None, what=""):
+    tol = fp32_tol(d, tau)
     lp, lse, top1 = got
     if rows is not None:
         lp, lse, top1 = lp[rows], lse[rows], top1[rows]
     ok = ~orc["bad_token"]
     dlp = np.abs(lp[ok].astype(np.float64) - orc["logprob"][ok])
     dlse = np.abs(lse.astype(np.float64) - orc["lse"])
-    assert dlp.max(initial=0) <= FP32_TOL, f"{what}: logprob max err {dlp.max():.3e}"
-    assert dlse.max(initial=0) <= FP32_TOL, f"{what}: lse max err {dlse.max():.3e}"
+    assert dlp.max(initial=0) <= tol, f"{what}: logprob max err {dlp.max():.3e}"
+    assert dlse.max(initial=0) <= tol, f"{what}: lse max err {dlse.max():.3e}"
     sel = orc["gap"] > FP32_TOP1_GAP
     bad = np.flatnonzero(sel & (top1.astype(np.int64) != orc["top1"]))
     assert bad.size == 0, f"{what}: top1 differs on {bad.size} rows"
@@ -81,7 +87,7 @@ def test_fp32_parity(tim, T, d, V, tau):
                                                      bf16_cuda(b.head.gamma), Wb, Ws,
                                                      cuda_tensor(b.token_ids), tau, b.eps)]
     orc = oracle.oracle_logprob_fp32(b.hidden_gen, b.head.gamma, W32, b.token_ids, tau, b.eps)
-    assert_fp32_parity(got, orc, what=f"fp32 T={T} d={d} V={V}")
+    assert_fp32_parity(got, orc, d, tau, what=f"fp32 T={T} d={d} V={V}")
 
 
 def test_fp32_full_head_batch_invariance_and_precision_gain(tim):
@@ -93,7 +99,7 @@ def test_fp32_full_head_batch_invariance_and_precision_gain(tim):
     rows = sample_rows(200, 40)
     orc = oracle.oracle_logprob_fp32(b.hidden_gen[rows], b.head.gamma, W32, b.token_ids[rows],
                                      0.7, b.eps)
-    err32 = assert_fp32_parity(full, orc, rows=rows, what="fp32 full head")
+    err32 = assert_fp32_parity(full, orc, 4096, 0.7, rows=rows, what="fp32 full head")
     part = [x.cpu().numpy() for x in tim.logprob_fp32(hid[13:77].contiguous(), gam, Wb, Ws,
                                                       cuda_tensor(b.token_ids[13:77]), 0.7, b.eps)]
     for x, y in zip(part, full):
