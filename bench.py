@@ -233,7 +233,9 @@ def reference_arm(args):
     if rank != 0:
         return 0
     b = synth.make_qwen3_8b()
-    rows_per_step = 16
+    # one oracle row block per step: its fixed cost (widening W to fp64) is then
+    # shared by 128 rows, about 2 s per step on 16 cores
+    rows_per_step = 128
     g = np.random.default_rng(77)
     for _ in range(args.warmup):
         time_oracle(b, np.sort(g.choice(b.T, rows_per_step, replace=False)))
