@@ -40,7 +40,7 @@ from .processed import oracle_processed_logprob, process_head, process_row  # no
 from .fp8 import (e4m3_round, fp8_scale, oracle_logprob_fp8, quantize_rows,  # noqa: F401
                   rmsnorm_fp32)
 from .fp32head import oracle_logprob_fp32, rmsnorm_unrounded  # noqa: F401
-from .backward import logit_grad, oracle_logprob_backward  # noqa: F401
+from .backward import logit_grad, oracle_logprob_backward, rmsnorm_backward  # noqa: F401
 from .diag import (  # noqa: F401
     FLAG_QUANTILE_SKIPPED, QUANTILE_MAX_TOKENS, QUANTILES, oracle_diag, oracle_diag_lenient,
     quantile_linear,

@@ -15,7 +15,10 @@ logprob" path (logprob_t = s_t[x_t] - lse_t, s = z / tau, z = y . W^T; see
 with y the bf16-rounded RMSNorm output of the forward (the GEMM operand).
 Readings: a row whose token id is outside [0, V) contributes nothing (its G row
 is zero; the forward reports such rows as errors); the gradient is taken with
-respect to y as the GEMM consumes it (the RMSNorm backward is not part of it).
+respect to y as the GEMM consumes it.  ``rmsnorm_backward`` continues it to the
+hidden states and gamma, passing the bf16 rounding of y straight through (the
+usual reading for a rounding inside a differentiated forward), so a custom
+autograd wrapper can return dL/dh, dL/dgamma and dL/dW.
 The result dict also carries, for the parity tests, the magnitudes
 |G| . |W| and |G|^T . |y| that bound how far bf16 rounding of G can move each
 output element.
@@ -67,3 +70,22 @@ def oracle_logprob_backward(hidden_bits, gamma_bits, W_bits, token_ids, temperat
     dW = Gr.T @ y
     bdW = np.abs(Gr).T @ ay
     return dict(dy=dy, dW=dW, bound_dy=bdy, bound_dW=bdW, y=y)
+
+
+def rmsnorm_backward(h: np.ndarray, gamma: np.ndarray, eps: float, dy: np.ndarray):
+    """Backward of y = h * rstd * gamma (rstd = 1/sqrt(mean(h^2) + eps)) in fp64, taking
+    the bf16 rounding of y as the identity (straight through).  Returns (dh [T, d],
+    dgamma [d]):
+
+        dh_ti    = rstd_t gamma_i dy_ti - (rstd_t^3 / d) h_ti sum_j gamma_j dy_tj h_tj
+        dgamma_i = sum_t dy_ti h_ti rstd_t
+    """
+    h = np.asarray(h, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    d = h.shape[1]
+    rstd = 1.0 / np.sqrt(np.mean(h * h, axis=1) + eps)
+    s = np.sum(gamma[None, :] * dy * h, axis=1)
+    dh = rstd[:, None] * gamma[None, :] * dy - (rstd ** 3 / d)[:, None] * h * s[:, None]
+    dgamma = np.sum(dy * h * rstd[:, None], axis=0)
+    return dh, dgamma

@@ -1081,4 +1081,37 @@ def pin_backward_temperature_closed_form():
     assert abs(out["dW"][0, 0] - q / tau) < 1e-14 and abs(out["dW"][1, 0] + q / tau) < 1e-14
 
 
+def pin_rmsnorm_backward_finite_differences():
+    """dL/dh and dL/dgamma of L = sum dy * y(h, gamma) (y unrounded) against central
+    differences, and torch fp64 autograd of rms_norm (a library routine)."""
+    import torch
+    b = synth.make_custom(T=5, d=24, V=4, tag="rmsbwd")
+    h = oracle.widen_bf16(b.hidden_gen)
+    g = oracle.widen_bf16(b.head.gamma)
+    dy = np.random.default_rng(9).standard_normal(h.shape)
+    eps = 1e-5
+    dh, dgam = oracle.rmsnorm_backward(h, g, eps, dy)
+
+    def loss(hh, gg):
+        return float(np.sum(dy * oracle.rmsnorm_unrounded(hh, gg, eps)))
+
+    step = 1e-6
+    for t, i in ((0, 0), (2, 7), (4, 23)):
+        e = np.zeros_like(h)
+        e[t, i] = step
+        fd = (loss(h + e, g) - loss(h - e, g)) / (2 * step)
+        assert abs(fd - dh[t, i]) < 1e-7 * max(1.0, abs(fd)), (t, i)
+    for i in (0, 11, 23):
+        e = np.zeros_like(g)
+        e[i] = step
+        fd = (loss(h, g + e) - loss(h, g - e)) / (2 * step)
+        assert abs(fd - dgam[i]) < 1e-7 * max(1.0, abs(fd)), i
+    ht = torch.tensor(h, requires_grad=True)
+    gt = torch.tensor(g, requires_grad=True)
+    y = torch.nn.functional.rms_norm(ht, (24,), weight=gt, eps=eps)
+    (y * torch.from_numpy(dy)).sum().backward()
+    assert np.max(np.abs(ht.grad.numpy() - dh)) < 1e-12
+    assert np.max(np.abs(gt.grad.numpy() - dgam)) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

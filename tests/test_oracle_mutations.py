@@ -266,6 +266,21 @@ def _grad_next_token(z, token_ids, grad, temperature):
     return _orig_logit_grad(z, (np.asarray(token_ids) + 1) % z.shape[1], grad, temperature)
 
 
+_orig_rms_bwd = obw.rmsnorm_backward
+
+
+def _rms_bwd_no_projection(h, gamma, eps, dy):
+    h = np.asarray(h, dtype=np.float64)
+    rstd = 1.0 / np.sqrt(np.mean(h * h, axis=1) + eps)
+    dh = rstd[:, None] * np.asarray(gamma)[None, :] * dy          # drops the rstd' term
+    return dh, np.sum(dy * h * rstd[:, None], axis=0)
+
+
+def _rms_bwd_dgamma_without_rstd(h, gamma, eps, dy):
+    dh, _ = _orig_rms_bwd(h, gamma, eps, dy)
+    return dh, np.sum(np.asarray(dy) * np.asarray(h), axis=0)
+
+
 MUTATIONS = [
     ("temperature after softmax", ol, "lse_stats", _lse_after_softmax, ["pin_v8_temperature"]),
     ("no max shift", ol, "lse_stats", _lse_no_shift, ["pin_large_logits"]),
@@ -324,6 +339,10 @@ MUTATIONS = [
      ["pin_backward_finite_differences"]),
     ("backward one-hot on the next id", obw, "logit_grad", _grad_next_token,
      ["pin_backward_torch_autograd"]),
+    ("RMSNorm backward without the rstd derivative", obw, "rmsnorm_backward",
+     _rms_bwd_no_projection, ["pin_rmsnorm_backward_finite_differences"]),
+    ("RMSNorm backward dgamma without rstd", obw, "rmsnorm_backward",
+     _rms_bwd_dgamma_without_rstd, ["pin_rmsnorm_backward_finite_differences"]),
 ]
 
 
