@@ -339,6 +339,26 @@ tim_status tim_logprob_backward(const void *hidden, const void *gamma, const voi
                                 int32_t accumulate_dW, void *workspace, size_t workspace_bytes,
                                 tim_stream_t stream);
 
+/* RMSNorm backward, to carry out_dy of tim_logprob_backward on to the hidden
+ * states and gamma (same section: a custom autograd wrapper around the forward
+ * needs the gradients of its inputs).  The bf16 rounding of y is passed straight
+ * through; with r_t = 1 / sqrt(mean_i h_ti^2 + eps) computed exactly as the
+ * forward computes it:
+ *   out_dh[t, i]    = r_t gamma_i dy_ti - (r_t^3 / d) h_ti sum_j gamma_j dy_tj h_tj
+ *   out_dgamma[i]   = sum_t dy_ti h_ti r_t   (+= when accumulate_dgamma = 1)
+ * hidden bf16 [T, d], gamma bf16 [d], dy fp32 [T, d] (16-byte aligned), out_dh
+ * fp32 [T, d] (16-byte aligned), out_dgamma fp32 [d].  Rows are independent;
+ * out_dgamma sums rows in a fixed order.  Workspace:
+ * tim_rmsnorm_backward_workspace_size(T, d) bytes; T up to 16.7 M rows.  Errors
+ * as tim_logprob (non-finite hidden values: TIM_ERR_NONFINITE via
+ * tim_status_sync). */
+size_t tim_rmsnorm_backward_workspace_size(int64_t T, int32_t d);
+
+tim_status tim_rmsnorm_backward(const void *hidden, const void *gamma, const float *dy, int64_t T,
+                                int32_t d, float eps, float *out_dh, float *out_dgamma,
+                                int32_t accumulate_dgamma, void *workspace,
+                                size_t workspace_bytes, tim_stream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * Processed (top-k, then top-p) selected-token logprob.
  *

@@ -85,6 +85,9 @@ _SIGNATURES = {
                                         _f32, _vp, _vp, _i32, _vp, _sz, _vp]),
     "tim_selftest_workspace_size": (_sz, []),
     "tim_selftest_wait_timeout": (_c.c_int, [_i32, _vp, _sz, _vp]),
+    "tim_rmsnorm_backward_workspace_size": (_sz, [_i64, _i32]),
+    "tim_rmsnorm_backward": (_c.c_int, [_vp, _vp, _vp, _i64, _i32, _f32, _vp, _vp, _i32, _vp, _sz,
+                                        _vp]),
     "tim_processed_logprob_workspace_size": (_sz, [_i64, _i32, _i32]),
     "tim_processed_logprob_head": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32,
                                               _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -493,6 +496,75 @@ def selftest_wait_timeout(limit_ms: int = 50, *, stream=None) -> str:
            "tim_selftest_wait_timeout")
     code = lib().tim_status_sync(ws.ptr, _stream_ptr(stream))
     return STATUS_NAMES.get(int(code), f"code {code}")
+
+
+def rmsnorm_backward(hidden, gamma, dy, eps: float, *, out_dh=None, out_dgamma=None,
+                     accumulate_dgamma: bool = False, workspace: Optional[Workspace] = None,
+                     stream=None, check: bool = True):
+    """RMSNorm backward (tim_rmsnorm_backward): returns (dh fp32 [T, d], dgamma fp32 [d])
+    for the upstream gradient dy fp32 [T, d] of y = RMSNorm(hidden) * gamma."""
+    torch = _torch()
+    hidden = _as_bf16(hidden, "hidden")
+    gamma = _as_bf16(gamma, "gamma")
+    _need(dy, torch.float32, "dy", 2)
+    T, d = hidden.shape
+    dev = hidden.device
+    if out_dh is None:
+        out_dh = torch.empty(T, d, dtype=torch.float32, device=dev)
+    if out_dgamma is None:
+        out_dgamma = torch.empty(d, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = Workspace(int(lib().tim_rmsnorm_backward_workspace_size(T, d)), dev, stream)
+    _check(lib().tim_rmsnorm_backward(_ptr(hidden), _ptr(gamma), _ptr(dy), T, d, float(eps),
+                                      _ptr(out_dh), _ptr(out_dgamma), int(bool(accumulate_dgamma)),
+                                      workspace.ptr, workspace.nbytes, _stream_ptr(stream)),
+           "tim_rmsnorm_backward")
+    if check:
+        workspace.check("tim_rmsnorm_backward", stream)
+    return out_dh, out_dgamma
+
+
+def _linear_logprob_function():
+    torch = _torch()
+
+    class LinearLogprob(torch.autograd.Function):
+        """Custom autograd around the scoring kernels: the forward values are exactly
+        tim_logprob's (batch-invariant), the backward recomputes the logits
+        (tim_logprob_backward) and carries the gradient through the RMSNorm
+        (tim_rmsnorm_backward).  Gradients of hidden, gamma and W are returned in their
+        dtypes."""
+
+        @staticmethod
+        def forward(ctx, hidden, gamma, W, token_ids, temperature, eps):
+            lp, lse, _ = logprob(hidden, gamma, W, token_ids, temperature, eps)
+            ctx.save_for_backward(hidden, gamma, W, token_ids, lse)
+            ctx.temperature, ctx.eps = float(temperature), float(eps)
+            return lp
+
+        @staticmethod
+        def backward(ctx, grad_logprob):
+            hidden, gamma, W, token_ids, lse = ctx.saved_tensors
+            g = grad_logprob.contiguous().float()
+            dy, dW = logprob_backward(hidden, gamma, W, token_ids, lse, g, ctx.temperature,
+                                      ctx.eps)
+            dh, dgamma = rmsnorm_backward(hidden, gamma, dy, ctx.eps)
+            return (dh.to(hidden.dtype), dgamma.to(gamma.dtype), dW.to(W.dtype), None, None,
+                    None)
+
+    return LinearLogprob
+
+
+def linear_logprob(hidden, gamma, W, token_ids, temperature: float, eps: float):
+    """Differentiable selected-token logprob (bf16 hidden, gamma, W as torch bfloat16
+    tensors): forward = tim_logprob, backward = tim_logprob_backward +
+    tim_rmsnorm_backward (the bf16 rounding of y passed straight through)."""
+    global _LINEAR_LOGPROB
+    if _LINEAR_LOGPROB is None:
+        _LINEAR_LOGPROB = _linear_logprob_function()
+    return _LINEAR_LOGPROB.apply(hidden, gamma, W, token_ids, temperature, eps)
+
+
+_LINEAR_LOGPROB = None
 
 
 def processed_logprob(hidden, gamma, W, token_ids, temperature: float, eps: float, top_k: int,

@@ -47,6 +47,11 @@ cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, in
 cudaError_t launch_wait_selftest(const void* y, const void* W, const int32_t* ids, int64_t T,
                                  int d, int V, void* part, float* tgt, int* status,
                                  uint64_t limit_ns, cudaStream_t stream, int num_sms);
+int rmsnorm_backward_chunks(int64_t T);
+cudaError_t launch_rmsnorm_backward(const void* hidden, const void* gamma, const float* dy,
+                                    int64_t T, int d, float eps, float* dh, float* dgamma,
+                                    int accumulate, float* rstd, float* partial, int* status,
+                                    cudaStream_t stream);
 cudaError_t launch_lmhead_lse_fp8(const void* y8, const float* sy, const void* W8,
                                   const float* sw, const int32_t* ids, int64_t T, int d, int V,
                                   float temperature, void* part, float* tgt, int* status,
@@ -567,6 +572,43 @@ tim_status tim_selftest_wait_timeout(int32_t limit_ms, void* workspace, size_t w
       reinterpret_cast<int*>(b + L.status_off),
       static_cast<uint64_t>(limit_ms) * 1000ull * 1000ull, reinterpret_cast<cudaStream_t>(stream),
       sms));
+}
+
+// RMSNorm-backward workspace: status | rstd [T] | dgamma partials [chunks][d].
+size_t tim_rmsnorm_backward_workspace_size(int64_t T, int32_t d) {
+  if (T < 1 || T > INT32_MAX || d < 64 || d > 65536 || (d % 64) != 0 ||
+      rmsnorm_backward_chunks(T) > 65535)
+    return 0;
+  return align_up(1024 + static_cast<size_t>(T) * 4, 1024) +
+         align_up(static_cast<size_t>(rmsnorm_backward_chunks(T)) * d * 4, 1024);
+}
+
+tim_status tim_rmsnorm_backward(const void* hidden, const void* gamma, const float* dy, int64_t T,
+                                int32_t d, float eps, float* out_dh, float* out_dgamma,
+                                int32_t accumulate_dgamma, void* workspace,
+                                size_t workspace_bytes, tim_stream_t stream) {
+  if (hidden == nullptr || gamma == nullptr || dy == nullptr || out_dh == nullptr ||
+      out_dgamma == nullptr)
+    return TIM_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(gamma, 16) || !aligned(dy, 16) || !aligned(out_dh, 16) ||
+      !aligned(out_dgamma, 4))
+    return TIM_ERR_INVALID_ARG;
+  if (accumulate_dgamma != 0 && accumulate_dgamma != 1) return TIM_ERR_INVALID_ARG;
+  if (T < 1 || T > INT32_MAX || d < 64 || d > 65536 || (d % 64) != 0 ||
+      rmsnorm_backward_chunks(T) > 65535)
+    return TIM_ERR_SHAPE;
+  if (!(std::isfinite(eps) && eps >= 0.f)) return TIM_ERR_INVALID_ARG;
+  tim_status s =
+      check_workspace(workspace, workspace_bytes, tim_rmsnorm_backward_workspace_size(T, d));
+  if (s != TIM_OK) return s;
+  if ((s = check_device(nullptr)) != TIM_OK) return s;
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  float* rstd = reinterpret_cast<float*>(b + 1024);
+  float* partial = reinterpret_cast<float*>(b + align_up(1024 + static_cast<size_t>(T) * 4, 1024));
+  return from_cuda(launch_rmsnorm_backward(hidden, gamma, dy, T, d, eps, out_dh, out_dgamma,
+                                           accumulate_dgamma, rstd, partial,
+                                           reinterpret_cast<int*>(b),
+                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t tim_processed_logprob_workspace_size(int64_t T, int32_t d, int32_t V) {

@@ -147,6 +147,113 @@ __global__ void split_tf32_kernel(const float4* __restrict__ x, int64_t n4,
   }
 }
 
+// ---------------------------------------------------------------------------
+// RMSNorm backward (the bf16 rounding of y passed straight through).  With
+// r = rstd (recomputed exactly as the forward computes it):
+//   dh_ti    = r_t gamma_i dy_ti - (r_t^3 / d) h_ti s_t,  s_t = sum_j gamma_j dy_tj h_tj
+//   dgamma_i = sum_t dy_ti h_ti r_t
+// Rows: one warp per row, s_t in the forward's lane / butterfly order.  dgamma:
+// per-column sums over chunks of kDgRows rows (rows in order), then the chunk
+// partials folded in chunk order -- deterministic for a given batch.
+constexpr int kDgRows = 256;
+
+__global__ void __launch_bounds__(32 * kNormRowsPerBlock)
+    rmsnorm_backward_rows_kernel(const uint4* __restrict__ hidden, const uint4* __restrict__ gamma,
+                                 const float4* __restrict__ dy, int64_t T, int d, float eps,
+                                 float4* __restrict__ dh, float* __restrict__ rstd_out,
+                                 int* status) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kNormRowsPerBlock + warp;
+  if (row >= T) return;
+  const int nvec = d >> 3;
+  const uint4* h = hidden + row * nvec;
+  const float4* g = dy + row * (2 * nvec);
+  const float ss = row_sum_squares(h, nvec, lane);
+  if (!isfinite(ss)) {
+    if (lane == 0) set_status(status, TIM_ERR_NONFINITE);
+  }
+  const float rstd = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+  float sgd = 0.f;
+  for (int c = lane; c < nvec; c += 32) {
+    float f[8], w[8];
+    unpack_bf16x8(__ldg(h + c), f);
+    unpack_bf16x8(__ldg(gamma + c), w);
+    const float4 a = __ldg(g + 2 * c), b = __ldg(g + 2 * c + 1);
+    const float gv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sgd = fmaf(w[i] * gv[i], f[i], sgd);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sgd += __shfl_xor_sync(0xFFFFFFFFu, sgd, o);
+  const float coef = rstd * rstd * rstd / static_cast<float>(d) * sgd;
+  float4* out = dh + row * (2 * nvec);
+  for (int c = lane; c < nvec; c += 32) {
+    float f[8], w[8];
+    unpack_bf16x8(__ldg(h + c), f);
+    unpack_bf16x8(__ldg(gamma + c), w);
+    const float4 a = __ldg(g + 2 * c), b = __ldg(g + 2 * c + 1);
+    const float gv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = rstd * w[i] * gv[i] - coef * f[i];
+    out[2 * c] = make_float4(o[0], o[1], o[2], o[3]);
+    out[2 * c + 1] = make_float4(o[4], o[5], o[6], o[7]);
+  }
+  if (lane == 0) rstd_out[row] = rstd;
+}
+
+// partial[chunk][i] = sum over the chunk's rows (in order) of dy_ti h_ti r_t
+__global__ void __launch_bounds__(256)
+    dgamma_partial_kernel(const uint16_t* __restrict__ hidden, const float* __restrict__ dy,
+                          const float* __restrict__ rstd, int64_t T, int d,
+                          float* __restrict__ partial) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i >= d) return;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * kDgRows;
+  const int64_t t1 = t0 + kDgRows < T ? t0 + kDgRows : T;
+  float acc = 0.f;
+  for (int64_t t = t0; t < t1; ++t) {
+    const float hv = __uint_as_float(static_cast<uint32_t>(__ldg(hidden + t * d + i)) << 16);
+    acc = fmaf(__ldg(dy + t * d + i) * hv, __ldg(rstd + t), acc);
+  }
+  partial[static_cast<int64_t>(blockIdx.y) * d + i] = acc;
+}
+
+__global__ void __launch_bounds__(256)
+    dgamma_fold_kernel(const float* __restrict__ partial, int n_chunks, int d, float* dgamma,
+                       int accumulate) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i >= d) return;
+  float acc = 0.f;
+  for (int c = 0; c < n_chunks; ++c) acc += partial[static_cast<int64_t>(c) * d + i];
+  dgamma[i] = accumulate ? dgamma[i] + acc : acc;
+}
+
+int rmsnorm_backward_chunks(int64_t T) { return static_cast<int>((T + kDgRows - 1) / kDgRows); }
+
+cudaError_t launch_rmsnorm_backward(const void* hidden, const void* gamma, const float* dy,
+                                    int64_t T, int d, float eps, float* dh, float* dgamma,
+                                    int accumulate, float* rstd, float* partial, int* status,
+                                    cudaStream_t stream) {
+  const int64_t blocks = (T + kNormRowsPerBlock - 1) / kNormRowsPerBlock;
+  rmsnorm_backward_rows_kernel<<<static_cast<unsigned>(blocks), 32 * kNormRowsPerBlock, 0,
+                                 stream>>>(static_cast<const uint4*>(hidden),
+                                           static_cast<const uint4*>(gamma),
+                                           reinterpret_cast<const float4*>(dy), T, d, eps,
+                                           reinterpret_cast<float4*>(dh), rstd, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int nc = rmsnorm_backward_chunks(T);
+  const dim3 grid(static_cast<unsigned>((d + 255) / 256), static_cast<unsigned>(nc));
+  dgamma_partial_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(hidden), dy, rstd,
+                                                  T, d, partial);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  dgamma_fold_kernel<<<static_cast<unsigned>((d + 255) / 256), 256, 0, stream>>>(partial, nc, d,
+                                                                                 dgamma, accumulate);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rmsnorm_rows_split(const void* hidden, const void* gamma, int64_t T, int d,
                                       float eps, float* ybig, float* ysmall, int* status,
                                       cudaStream_t stream) {
