@@ -598,12 +598,29 @@ def main():
         torch.cuda.synchronize()
         bws.check("backward")
         bms = e_a.elapsed_time(e_b) / 2
+        # the RMSNorm backward that carries dy on to the hidden states and gamma
+        rws = tim.Workspace(int(tim.lib().tim_rmsnorm_backward_workspace_size(T, d)), dev)
+        dh_b = torch.empty(T, d, dtype=torch.float32, device=dev)
+        dg_b = torch.empty(d, dtype=torch.float32, device=dev)
+        tim.rmsnorm_backward(hid_train, gam, dy_b, eps, out_dh=dh_b, out_dgamma=dg_b,
+                             workspace=rws, check=False)
+        e_a.record(stream)
+        for _ in range(5):
+            tim.rmsnorm_backward(hid_train, gam, dy_b, eps, out_dh=dh_b, out_dgamma=dg_b,
+                                 workspace=rws, check=False)
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        rws.check("rmsnorm backward")
+        rms_ms = e_a.elapsed_time(e_b) / 5
+        rms_bytes = T * d * (2 + 4 + 4) + T * d * (2 + 4)   # rows pass + dgamma pass
         extras["backward_dy_dW"] = dict(
             ms=round(bms, 3), tokens_per_s=round(T / (bms / 1e3), 1),
             TFLOPs=round(3 * 2.0 * T * d * V / (bms / 1e3) / 1e12, 1),
             note="three GEMMs (logit recompute, G.W, G^T.y) + transposes; workspace "
-                 f"{bws.nbytes / 1e9:.1f} GB")
-        del bws, dy_b, dW_b
+                 f"{bws.nbytes / 1e9:.1f} GB",
+            rmsnorm_backward_ms=round(rms_ms, 3),
+            rmsnorm_backward_GBps=round(rms_bytes / (rms_ms / 1e3) / 1e9, 1))
+        del bws, dy_b, dW_b, rws, dh_b, dg_b
         G = 8
         e_a.record(stream)
         for _ in range(2):
