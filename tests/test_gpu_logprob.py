@@ -38,6 +38,8 @@ SHAPES = [
     (300, 256, 513, 1.3),
     (257, 192, 2048, 1.0),
     (513, 320, 4099, 0.9),
+    (64, 128, 1000, 0.05),      # sharp: scaled logits up to ~200
+    (64, 128, 1000, 10.0),      # flat
 ]
 
 
@@ -47,6 +49,22 @@ def test_parity_small(tim, T, d, V, tau):
     gpu = run(tim, b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, tau, b.eps)
     orc = oracle.oracle_logprob(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, tau, b.eps)
     assert_logprob_parity(gpu, orc, what=f"T={T} d={d} V={V}")
+
+
+def test_large_logits(tim):
+    """W scaled by 16 (exact in bf16): logits of +-100 and more, logprobs near -200 for
+    the tail; the max-shifted merge keeps every row finite and within tolerance."""
+    b = synth.make_custom(T=100, d=256, V=3000, temperature=0.8, tag="biglogit")
+    W16 = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(b.head.W) * 16.0)
+    # hidden = +-2 with eps = 0: y = +-gamma exactly, so no bf16 rounding of y can differ
+    # between the fp32 kernel and the fp64 oracle (a one-step difference of y would move
+    # these large logits by ~1e-3)
+    sign = np.random.default_rng(4).random((100, 256)) < 0.5
+    hid = np.where(sign, 0xC000, 0x4000).astype(np.uint16)
+    gpu = run(tim, hid, b.head.gamma, W16, b.token_ids, 0.8, 0.0)
+    orc = oracle.oracle_logprob(hid, b.head.gamma, W16, b.token_ids, 0.8, 0.0)
+    assert orc["zmax"].max() > 50
+    assert_logprob_parity(gpu, orc, what="W x 16")
 
 
 def test_tiny_workload_parity_and_replay_split(tim):
