@@ -95,6 +95,53 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.tim_workspace_init(None, 0, None) == STATUS["TIM_ERR_WORKSPACE"]
 
 
+def test_variant_sizes_and_argument_errors_need_no_gpu(lib):
+    """The next-row entry points validate before touching the device."""
+    from rollout_logprob_consistency_gb300.binding import STATUS
+    fake, ws = 1 << 20, 1 << 24
+    inv, shape = STATUS["TIM_ERR_INVALID_ARG"], STATUS["TIM_ERR_SHAPE"]
+    # workspace sizes: zero for invalid shapes, covering the parts for valid ones
+    assert lib.tim_logprob_fp8_workspace_size(4, 192, 10) == 0          # d % 128
+    assert lib.tim_logprob_fp8_workspace_size(4, 256, 10) > lib.tim_logprob_workspace_size(4, 256, 10)
+    assert lib.tim_logprob_fp32_workspace_size(4, 96, 10) == 0
+    assert lib.tim_logprob_fp32_workspace_size(128, 64, 10) >= 2 * 128 * 64 * 4
+    T, d, V = 1000, 256, 3000
+    Tp, Vp = 1024, 3008
+    assert lib.tim_logprob_backward_workspace_size(T, d, V) >= 4 * Tp * Vp + 4 * Tp * d + 2 * d * Vp
+    assert lib.tim_rmsnorm_backward_workspace_size(T, d) >= 4 * T + 4 * d * 4
+    assert lib.tim_rmsnorm_backward_workspace_size(T, 100) == 0
+    assert lib.tim_selftest_workspace_size() > 0
+    assert lib.tim_compare_diag_workspace_size(0, 1) == 0
+    # FP8: d not a multiple of 128; null scales
+    assert lib.tim_logprob_fp8(fake, fake, fake, fake, fake, 4, 192, 300, 1.0, 0.0, fake, fake,
+                               fake, ws, 1 << 30, None) == shape
+    assert lib.tim_logprob_fp8(fake, fake, fake, None, fake, 4, 256, 300, 1.0, 0.0, fake, fake,
+                               fake, ws, 1 << 30, None) == inv
+    assert lib.tim_quantize_fp8_rows(fake, 4, 24, fake, fake, None) == shape   # K % 16
+    # FP32 / split: misaligned W part, n not a multiple of 4
+    assert lib.tim_logprob_fp32(fake, fake, fake + 4, fake, fake, 4, 64, 300, 1.0, 0.0, fake,
+                                fake, fake, ws, 1 << 30, None) == inv
+    assert lib.tim_split_tf32(fake, 6, fake, fake, None) == shape
+    # backward: accumulate flag, temperature, misaligned outputs
+    assert lib.tim_logprob_backward(fake, fake, fake, fake, fake, fake, 4, 64, 300, 1.0, 0.0,
+                                    fake, fake, 2, ws, 1 << 30, None) == inv
+    assert lib.tim_logprob_backward(fake, fake, fake, fake, fake, fake, 4, 64, 300, -1.0, 0.0,
+                                    fake, fake, 0, ws, 1 << 30, None) == inv
+    assert lib.tim_logprob_backward(fake, fake, fake, fake, fake, fake, 4, 64, 300, 1.0, 0.0,
+                                    fake + 4, fake, 0, ws, 1 << 30, None) == inv
+    assert lib.tim_rmsnorm_backward(fake, fake, fake, 4, 96, 0.0, fake, fake, 0, ws, 1 << 30,
+                                    None) == shape
+    assert lib.tim_rmsnorm_backward(fake, fake, fake, 4, 64, -1.0, fake, fake, 0, ws, 1 << 30,
+                                    None) == inv
+    # processed head: exactly one head output given
+    assert lib.tim_processed_logprob_head(fake, fake, fake, fake, 4, 64, 5000, 1.0, 0.0, 4, 1.0,
+                                          fake, fake, fake, fake, None, ws, 1 << 30,
+                                          None) == inv
+    # self-test limit out of range
+    assert lib.tim_selftest_wait_timeout(0, ws, 1 << 30, None) == inv
+    assert lib.tim_selftest_wait_timeout(2001, ws, 1 << 30, None) == inv
+
+
 def test_product_path_does_not_import_oracle():
     """The package and its binding never import the oracle (test infrastructure only)."""
     pkg = os.path.join(ROOT, "rollout_logprob_consistency_gb300")
