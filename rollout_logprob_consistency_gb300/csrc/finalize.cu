@@ -75,6 +75,9 @@ __global__ void __launch_bounds__(32 * kFinWarps)
                         float* __restrict__ out_lp, float* __restrict__ out_lse,
                         int32_t* __restrict__ out_top1, int* status) {
   __shared__ Rec red[kFinWarps][32];
+  // launched with programmatic stream serialisation: the launch overlaps the
+  // LM-head kernel's tail, and the records are read only after it has completed
+  pdl_wait();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t group = blockIdx.x;
@@ -116,10 +119,18 @@ cudaError_t launch_lse_finalize(const void* part, const float* tgt, const int32_
                                 int* status, cudaStream_t stream) {
   const int n_tiles = (V + kBN - 1) / kBN;
   const int64_t groups = (T + kRowGroup - 1) / kRowGroup;
-  lse_finalize_kernel<<<static_cast<unsigned>(groups), 32 * kFinWarps, 0, stream>>>(
-      static_cast<const float4*>(part), tgt, ids, T, V, n_tiles, out_lp, out_lse, out_top1,
-      status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(groups));
+  cfg.blockDim = dim3(32 * kFinWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lse_finalize_kernel, static_cast<const float4*>(part), tgt, ids,
+                            T, V, n_tiles, out_lp, out_lse, out_top1, status);
 }
 
 // ---------------------------------------------------------------------------
