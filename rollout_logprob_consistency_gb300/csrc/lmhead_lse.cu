@@ -28,17 +28,27 @@
 //
 // Batch invariance: every logit is the same sequence of MMAs (k-blocks in
 // order, 4 K=16 steps each) whatever T is; rows past T (zeros written by the
-// RMSNorm kernel up to the next 128-row boundary) never touch other rows; the epilogue arithmetic of a (row, tile) pair
-// is fixed.  Which CTA computes a tile does not matter.
+// RMSNorm kernel up to the next 128-row boundary) never touch other rows; the
+// epilogue arithmetic of a (row, tile) pair is fixed.  Which CTA computes a
+// tile does not matter.
+//
+// The same kernel serves the other paths through two template parameters:
+//   kMode  0 scoring records (above); 1 candidate collection and 4 top-4
+//          records (processed score); 2 logit gradient and 3 plain fp32-output
+//          GEMM (backward);
+//   kPrec  bf16 (above), e4m3 codes with power-of-two row scales (FP8 head),
+//          or fp32 operands as three tf32 products (FP32 head).
+// Only the operand staging, the MMA kind and the epilogue differ; the tile
+// shape, the ring, the accumulator hand-off and the raster are shared.
 //
 // Launched with programmatic stream serialisation when the batch fits one
 // raster group: the producer streams its first W stages, then waits
 // (griddepcontrol.wait, a no-op for an ordinary launch) for the RMSNorm kernel
 // before the first load of y.
 //
-// Every mbarrier wait is bounded (2 s); on timeout the kernel records
-// TIM_ERR_TIMEOUT, raises a CTA-wide abort flag, waits (bounded) for its own
-// TMA copies and MMAs still in flight, frees its TMEM and returns.
+// Every mbarrier wait is bounded (2 s by default); on timeout the kernel
+// records TIM_ERR_TIMEOUT, raises a CTA-wide abort flag, waits (bounded) for
+// its own TMA copies and MMAs still in flight, frees its TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
