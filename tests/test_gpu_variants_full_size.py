@@ -77,9 +77,10 @@ def test_fp32_head_full_size(tim, work):
 def test_backward_full_size(tim, work):
     """dy on sampled rows against the oracle (rows are independent); dW by an exact
     property of the gradient: every row of G sums to zero, so every column of dW sums to
-    zero up to the bf16 rounding of G, which moves a row's sum by at most
-    2^-9 sum_v |G_tv| <= 2^-8 |g_t| / tau; the bound per column is therefore
-    2^-8 sum_t (|g_t| / tau) |y_ti| (the fp32 accumulation adds far less)."""
+    zero up to the bf16 rounding of G (relative error at most 2^-8 per element), which
+    moves a row's sum by at most 2^-8 sum_v |G_tv| <= 2^-7 |g_t| / tau; the bound per
+    column is therefore 2^-7 sum_t (|g_t| / tau) |y_ti| (the fp32 accumulation adds far
+    less)."""
     import torch
     from test_gpu_backward import DELTA
     b, dv = work
@@ -102,6 +103,6 @@ def test_backward_full_size(tim, work):
     for r0 in range(0, b.T, 4096):
         y = oracle.rmsnorm(oracle.widen_bf16(b.hidden_train[r0:r0 + 4096]), gam, b.eps)
         bound += (np.abs(g[r0:r0 + 4096].astype(np.float64)) / 0.7) @ np.abs(y)
-    assert np.all(np.abs(colsum) <= 2.0 ** -8 * bound * 1.05), float(
+    assert np.all(np.abs(colsum) <= 2.0 ** -7 * bound), float(
         np.max(np.abs(colsum) / bound))
     assert math.isfinite(float(dW.abs().max()))
