@@ -294,9 +294,13 @@ __global__ void __launch_bounds__(kCmpThreads)
     s_last = (ticket == P - 1) ? 1 : 0;
   }
   __syncthreads();
-  if (!s_last || tid != 0) return;
+  if (!s_last || warp != 0) return;
 
-  // last CTA of sequence j: merge the P partials in part order
+  // last CTA of sequence j: warp 0 merges the P partials in part order.  Lane l
+  // folds the contiguous block of parts [l*per, (l+1)*per) in order (its loads
+  // all in flight together), then an ordered tree across lanes combines lane l
+  // (left) with lane l + off (right), so the run statistics keep the sequence
+  // order.
   __threadfence();
   const CmpPart* pj = parts + static_cast<int64_t>(j) * P;
   Runs<long long> R[3] = {runs_identity<long long>(), runs_identity<long long>(),
@@ -305,7 +309,10 @@ __global__ void __launch_bounds__(kCmpThreads)
   for (int i = 0; i < 11; ++i) tot[i] = 0.0;
   long long clipped = 0;
   int fl = 0;
-  for (int q = 0; q < P; ++q) {
+  const int per = (P + 31) / 32;
+  const int q0 = lane * per;
+  const int q1 = q0 + per < P ? q0 + per : P;
+  for (int q = q0; q < q1; ++q) {
     const CmpPart* pp = pj + q;
     for (int r = 0; r < 3; ++r) {
       Runs<long long> x;
@@ -324,6 +331,33 @@ __global__ void __launch_bounds__(kCmpThreads)
     clipped += __ldcg(&pp->clipped);
     fl |= __ldcg(&pp->flags);
   }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    Runs<long long> o[3];
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      o[r].n = __shfl_down_sync(0xFFFFFFFFu, R[r].n, off);
+      o[r].ndiff = __shfl_down_sync(0xFFFFFFFFu, R[r].ndiff, off);
+      o[r].first = __shfl_down_sync(0xFFFFFFFFu, R[r].first, off);
+      o[r].pre = __shfl_down_sync(0xFFFFFFFFu, R[r].pre, off);
+      o[r].suf = __shfl_down_sync(0xFFFFFFFFu, R[r].suf, off);
+      o[r].best = __shfl_down_sync(0xFFFFFFFFu, R[r].best, off);
+    }
+    double ot[11];
+#pragma unroll
+    for (int i = 0; i < 11; ++i) ot[i] = __shfl_down_sync(0xFFFFFFFFu, tot[i], off);
+    const long long oc = __shfl_down_sync(0xFFFFFFFFu, clipped, off);
+    const int of = __shfl_down_sync(0xFFFFFFFFu, fl, off);
+    if ((lane & (2 * off - 1)) == 0 && lane + off < 32) {
+#pragma unroll
+      for (int r = 0; r < 3; ++r) R[r] = runs_combine(R[r], o[r]);
+#pragma unroll
+      for (int i = 0; i < 11; ++i) tot[i] = is_max_slot(i) ? fmax(tot[i], ot[i]) : tot[i] + ot[i];
+      clipped += oc;
+      fl |= of;
+    }
+  }
+  if (lane != 0) return;
   cnt[j] = 0;  // ready for the next call on this workspace
 
   tim_seq_stats st;
