@@ -247,14 +247,23 @@ __global__ void __launch_bounds__(kDiagThreads)
     s_bad = 0;
   }
   __syncthreads();
-  for (int64_t t = s + tid; t < e; t += kDiagThreads) {
-    const uint8_t m = __ldg(mask + t);
+  const int lane = tid & 31;
+  for (int64_t base = s; base < e; base += kDiagThreads) {  // uniform trip count
+    const int64_t t = base + tid;
+    const uint8_t m = t < e ? __ldg(mask + t) : 0;
     if (m > 1) s_bad = 1;
-    if (m != 1) continue;
-    const double a = __ldg(A + t), b = __ldg(B + t), c = __ldg(C + t);
-    const int slot = atomicAdd(&s_fill, 1);
-    if (slot < kQuantMax)
-      keys[slot] = static_cast<unsigned long long>(__double_as_longlong(pair_abs(p, a, b, c)));
+    const bool act = (m == 1);
+    // one shared-memory atomic per warp: the warp's active lanes take consecutive slots
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, act);
+    int slot0 = 0;
+    if (lane == 0 && bal != 0u) slot0 = atomicAdd(&s_fill, __popc(bal));
+    slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
+    if (act) {
+      const double a = __ldg(A + t), b = __ldg(B + t), c = __ldg(C + t);
+      const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
+      if (slot < kQuantMax)
+        keys[slot] = static_cast<unsigned long long>(__double_as_longlong(pair_abs(p, a, b, c)));
+    }
   }
   __syncthreads();
   const int n = s_fill;
