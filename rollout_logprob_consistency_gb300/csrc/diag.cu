@@ -281,17 +281,18 @@ __global__ void __launch_bounds__(kDiagThreads)
   const unsigned long long kInf = static_cast<unsigned long long>(__double_as_longlong(INFINITY));
   for (int i = n + tid; i < n2; i += kDiagThreads) keys[i] = kInf;
   __syncthreads();
+  // bitonic sort, ascending; each phase visits its n2 / 2 compare-exchange pairs
+  // directly (pair idx -> lower index i: a zero bit inserted at the stride's bit)
   for (int k = 2; k <= n2; k <<= 1) {
     for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int i = tid; i < n2; i += kDiagThreads) {
-        const int ixj = i ^ jj;
-        if (ixj > i) {
-          const unsigned long long x = keys[i], y = keys[ixj];
-          const bool up = (i & k) == 0;
-          if ((x > y) == up) {
-            keys[i] = y;
-            keys[ixj] = x;
-          }
+      for (int idx = tid; idx < (n2 >> 1); idx += kDiagThreads) {
+        const int i = ((idx & ~(jj - 1)) << 1) | (idx & (jj - 1));
+        const int ixj = i + jj;
+        const unsigned long long x = keys[i], y = keys[ixj];
+        const bool up = (i & k) == 0;
+        if ((x > y) == up) {
+          keys[i] = y;
+          keys[ixj] = x;
         }
       }
       __syncthreads();

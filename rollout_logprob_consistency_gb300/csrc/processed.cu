@@ -40,18 +40,19 @@ constexpr int kProcWarps = 4;
 constexpr int kProcSortMax = TIM_PROCESSED_CAPACITY;  // elements per warp sort
 
 // Bitonic sort of n2 (power of two) 64-bit keys, descending, by one warp.
+// Each phase visits its n2 / 2 compare-exchange pairs directly (pair idx -> lower
+// index i: a zero bit inserted at the stride's bit).
 __device__ __forceinline__ void warp_sort_desc_u64(unsigned long long* b, int n2, int lane) {
   for (int k = 2; k <= n2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = lane; i < n2; i += 32) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long x = b[i], y = b[ixj];
-          const bool down = (i & k) == 0;
-          if ((x < y) == down) {
-            b[i] = y;
-            b[ixj] = x;
-          }
+      for (int idx = lane; idx < (n2 >> 1); idx += 32) {
+        const int i = ((idx & ~(j - 1)) << 1) | (idx & (j - 1));
+        const int ixj = i + j;
+        const unsigned long long x = b[i], y = b[ixj];
+        const bool down = (i & k) == 0;
+        if ((x < y) == down) {
+          b[i] = y;
+          b[ixj] = x;
         }
       }
       __syncwarp();
