@@ -49,6 +49,33 @@ def test_parity_small(tim, T, d, V, tau):
     assert_logprob_parity(gpu, orc, what=f"T={T} d={d} V={V}")
 
 
+def test_concurrent_streams_same_bits(tim):
+    """Scoring the same rows on two streams at once, each in its own batch composition
+    (the GEMMs then share the SMs and run with fewer resident CTAs each), gives exactly
+    the bits of a lone call: no result depends on which CTA or SM computes a tile."""
+    import torch
+    b = synth.make_custom(T=700, d=512, V=20000, temperature=0.9, tag="streams")
+    hid, gam, W = bf16_cuda(b.hidden_gen), bf16_cuda(b.head.gamma), bf16_cuda(b.head.W)
+    ids = cuda_tensor(b.token_ids)
+    ref = [x.cpu().numpy() for x in tim.logprob(hid, gam, W, ids, 0.9, b.eps)]
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(3):
+        with torch.cuda.stream(s1):
+            a = tim.logprob(hid, gam, W, ids, 0.9, b.eps, stream=s1, check=False)
+        with torch.cuda.stream(s2):
+            c = tim.logprob(hid[100:600].contiguous(), gam, W, ids[100:600].contiguous(), 0.9,
+                            b.eps, stream=s2, check=False)
+        outs.append((a, c))
+    torch.cuda.synchronize()
+    for a, c in outs:
+        for x, r in zip(a, ref):
+            assert x.cpu().numpy().tobytes() == r.tobytes()
+        for x, r in zip(c, ref):
+            assert x.cpu().numpy().tobytes() == r[100:600].tobytes()
+
+
 def test_large_logits(tim):
     """W scaled by 16 (exact in bf16): logits of +-100 and more, logprobs near -200 for
     the tail; the max-shifted merge keeps every row finite and within tolerance."""
