@@ -66,6 +66,11 @@ def parse():
     p.add_argument("--profile-variant", default="bf16",
                    choices=["bf16", "fp8", "fp32", "backward", "processed", "diag"],
                    help="with --profile-shape: which head variant to run")
+    p.add_argument("--score-workload", default=None,
+                   choices=["tiny", "qwen3_1p7b", "qwen3_8b", "long_5120"],
+                   help="instead of the benchmark step: time tim_logprob on the trainer rows "
+                        "of this parity workload and the oracle on a bounded row sample, print "
+                        "one JSON line (not the benchmark contract line)")
     p.add_argument("--cpu-rows", type=int, default=1024,
                    help="rows of the workload the oracle scores for the CPU baseline")
     return p.parse_args()
@@ -344,10 +349,66 @@ def profile_case(args):
     return 0
 
 
+def score_workload(args):
+    """--score-workload: tokens/s of one scoring call over a whole parity workload (CUDA
+    events, back-to-back calls after warm-up) and of the oracle on a bounded seeded sample."""
+    import numpy as np
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import synth
+    import rollout_logprob_consistency_gb300 as tim
+    make = dict(tiny=synth.make_tiny, qwen3_1p7b=synth.make_qwen3_1p7b,
+                qwen3_8b=synth.make_qwen3_8b, long_5120=synth.make_long_5120)[args.score_workload]
+    b = make()
+    T, d, V = b.T, b.head.d, b.head.V
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    hid, gam = bf16(b.hidden_train), bf16(b.head.gamma)
+    W = bf16(b.W_train if b.W_train is not None else b.head.W)
+    ids = torch.from_numpy(b.token_ids).cuda()
+    ws = tim.Workspace(tim.logprob_workspace_size(T, d, V))
+    out = (torch.empty(T, device="cuda"), torch.empty(T, device="cuda"),
+           torch.empty(T, dtype=torch.int32, device="cuda"))
+    for _ in range(max(args.warmup, 3)):
+        tim.logprob(hid, gam, W, ids, b.temperature, b.eps, out=out, workspace=ws, check=False)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        tim.logprob(hid, gam, W, ids, b.temperature, b.eps, out=out, workspace=ws, check=False)
+    e1.record()
+    torch.cuda.synchronize()
+    ws.check("score workload")
+    ms = e0.elapsed_time(e1) / args.steps
+    peaks = load_peaks()
+    tflops = 2.0 * T * d * V / (ms / 1e3) / 1e12
+    gbps = (2.0 * V * d + 2.0 * T * d) / (ms / 1e3) / 1e9
+    frac = max(tflops / peaks["bf16_sustained"], gbps / peaks["hbm_gbs"])
+    n_or = min(T, args.cpu_rows)
+    rows = np.sort(np.random.default_rng(99).choice(T, n_or, replace=False))
+    import oracle
+    t0 = time.perf_counter()
+    oracle.oracle_logprob(b.hidden_train[rows], b.head.gamma,
+                          b.W_train if b.W_train is not None else b.head.W, b.token_ids[rows],
+                          b.temperature, b.eps)
+    dt = time.perf_counter() - t0
+    print(json.dumps(dict(workload=b.name, T=T, d=d, V=V, ms_per_call=round(ms, 4),
+                          tokens_per_s=round(T / (ms / 1e3), 1), TFLOPs=round(tflops, 1),
+                          GBps=round(gbps, 1), roofline_frac=round(frac, 3),
+                          peak_source=peaks["source"], oracle_rows=int(n_or),
+                          oracle_s=round(dt, 2), oracle_tokens_per_s=round(n_or / dt, 1),
+                          host_cores=cpu_cores())), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return reference_arm(args)
+    if args.score_workload:
+        return score_workload(args)
     if args.profile_shape:
         return profile_case(args)
     import numpy as np
