@@ -734,8 +734,12 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   // Raster groups of row tiles that sweep the vocabulary together (each group
   // streams W once and keeps its y tiles in L2).  Measured on GB300: 48 row tiles
   // at d <= 4096 (d = 4096: 36-48 equal, 64 10% slower); 36 at larger d (d = 5120:
-  // 116-118 ms per 131072 rows with 28-36, 130 ms with 48).
+  // 116-118 ms per 131072 rows with 28-36, 130 ms with 48).  The fp32 operands of
+  // the tf32x3 path are four times the bytes of bf16 ones, so their group is a
+  // quarter (d = 4096: 136 ms with 12 row tiles, 145 ms with 48, 168 ms with 96);
+  // e4m3 operands do as well with 48 as with 96.
   a.group_m = d <= 4096 ? 48 : 36;
+  if (prec == kPrecTf32x3) a.group_m /= 4;
   a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
   a.k2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   a.inv_temp = static_cast<float>(1.0 / static_cast<double>(temperature));
