@@ -282,22 +282,52 @@ __global__ void __launch_bounds__(kDiagThreads)
   for (int i = n + tid; i < n2; i += kDiagThreads) keys[i] = kInf;
   __syncthreads();
   // bitonic sort, ascending; each phase visits its n2 / 2 compare-exchange pairs
-  // directly (pair idx -> lower index i: a zero bit inserted at the stride's bit)
+  // directly (pair idx -> lower index i: a zero bit inserted at the stride's bit).
+  // Phases with a stride below kSeg keep every pair inside one kSeg-element
+  // segment; a warp owns whole segments there, so those phases need only a warp
+  // barrier, and the block synchronises only around the longer strides.
+  constexpr int kSeg = 256;
+  const int warp = tid >> 5;
+  const int seg = n2 < kSeg ? n2 : kSeg;
+  const int n_seg = n2 / seg;
+  bool warp_phase = false;  // the previous phase ended with a warp barrier only
   for (int k = 2; k <= n2; k <<= 1) {
     for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int idx = tid; idx < (n2 >> 1); idx += kDiagThreads) {
-        const int i = ((idx & ~(jj - 1)) << 1) | (idx & (jj - 1));
-        const int ixj = i + jj;
-        const unsigned long long x = keys[i], y = keys[ixj];
-        const bool up = (i & k) == 0;
-        if ((x > y) == up) {
-          keys[i] = y;
-          keys[ixj] = x;
+      const bool local = jj < seg;
+      if (!local && warp_phase) __syncthreads();
+      if (local) {
+        for (int sg = warp; sg < n_seg; sg += kDiagThreads / 32) {
+          unsigned long long* kb = keys + sg * seg;
+          const int base = sg * seg;
+          for (int idx = lane; idx < (seg >> 1); idx += 32) {
+            const int i = ((idx & ~(jj - 1)) << 1) | (idx & (jj - 1));
+            const unsigned long long x = kb[i], y = kb[i + jj];
+            const bool up = ((base + i) & k) == 0;
+            if ((x > y) == up) {
+              kb[i] = y;
+              kb[i + jj] = x;
+            }
+          }
         }
+        __syncwarp();
+        warp_phase = true;
+      } else {
+        for (int idx = tid; idx < (n2 >> 1); idx += kDiagThreads) {
+          const int i = ((idx & ~(jj - 1)) << 1) | (idx & (jj - 1));
+          const int ixj = i + jj;
+          const unsigned long long x = keys[i], y = keys[ixj];
+          const bool up = (i & k) == 0;
+          if ((x > y) == up) {
+            keys[i] = y;
+            keys[ixj] = x;
+          }
+        }
+        __syncthreads();
+        warp_phase = false;
       }
-      __syncthreads();
     }
   }
+  if (warp_phase) __syncthreads();
   if (tid == 0) {
     const double qs[3] = {0.5, 0.95, 0.99};
     double r[3];
