@@ -11,4 +11,5 @@ from .binding import (  # noqa: F401
     gather_shard_records, logprob_vocab_parallel, logprob_vocab_parallel_emulated,
     processed_logprob, quantize_fp8_rows, logprob_fp8, split_tf32, logprob_fp32,
     logprob_backward, selftest_wait_timeout, rmsnorm_backward, linear_logprob,
+    logprob_noalloc,
 )

@@ -83,6 +83,8 @@ _SIGNATURES = {
     "tim_logprob_backward_workspace_size": (_sz, [_i64, _i32, _i32]),
     "tim_logprob_backward": (_c.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32,
                                         _f32, _vp, _vp, _i32, _vp, _sz, _vp]),
+    "tim_logprob_noalloc": (_c.c_int, [_vp, _vp, _vp, _vp, _i64, _i32, _i32, _f32, _f32, _vp, _vp,
+                                       _vp, _vp, _vp]),
     "tim_selftest_workspace_size": (_sz, []),
     "tim_selftest_wait_timeout": (_c.c_int, [_i32, _vp, _sz, _vp]),
     "tim_rmsnorm_backward_workspace_size": (_sz, [_i64, _i32]),
@@ -485,6 +487,28 @@ def logprob_backward(hidden, gamma, W, token_ids, lse, grad_logprob, temperature
     if check:
         workspace.check("tim_logprob_backward", stream)
     return out_dy, out_dW
+
+
+def logprob_noalloc(hidden, gamma, W, token_ids, temperature: float, eps: float, out,
+                    out_status=None, *, stream=None):
+    """tim_logprob_noalloc: the scoring path with the library's static scratch instead of
+    a workspace, for callers that must not allocate device memory.  ``out`` = (logprob f32
+    [T], lse f32 [T], top1 i32 [T]) preallocated; ``out_status`` an optional device int32
+    [1] receiving the call's first data-dependent error code.  Nothing is allocated."""
+    torch = _torch()
+    hidden = _as_bf16(hidden, "hidden")
+    gamma = _as_bf16(gamma, "gamma")
+    W = _as_bf16(W, "W")
+    _need(token_ids, torch.int32, "token_ids", 1)
+    T, d = hidden.shape
+    V = W.shape[0]
+    code = lib().tim_logprob_noalloc(_ptr(hidden), _ptr(gamma), _ptr(W), _ptr(token_ids), T, d, V,
+                                     float(temperature), float(eps), _ptr(out[0]), _ptr(out[1]),
+                                     _ptr(out[2]),
+                                     _ptr(out_status) if out_status is not None else None,
+                                     _stream_ptr(stream))
+    _check(code, "tim_logprob_noalloc")
+    return out
 
 
 def selftest_wait_timeout(limit_ms: int = 50, *, stream=None) -> str:

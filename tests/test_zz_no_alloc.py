@@ -92,3 +92,13 @@ def test_noalloc_status_and_limit(env):
     big_ids = torch.zeros(big_T, dtype=torch.int32, device="cuda")
     code, _, _ = call_noalloc(torch, f, big, gam, W, big_ids, 1.0, b.eps)
     assert code == tim.STATUS["TIM_ERR_WORKSPACE"]
+    # the binding's thin wrapper gives the same bits as the direct call
+    ids = cuda_tensor(b.token_ids)
+    _, got, _ = call_noalloc(torch, f, hid, gam, W, ids, 1.0, b.eps)
+    out = (torch.empty(40, device="cuda"), torch.empty(40, device="cuda"),
+           torch.empty(40, dtype=torch.int32, device="cuda"))
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    tim.logprob_noalloc(hid, gam, W, ids, 1.0, b.eps, out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert all(x.cpu().numpy().tobytes() == y.tobytes() for x, y in zip(out, got))
