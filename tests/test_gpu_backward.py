@@ -77,11 +77,12 @@ def check(b, g, dy, dW, orc, dW_rows=None, what=""):
     errw = np.abs(dW[rows] - orc["dW"])
     badw = np.argwhere(errw > tol_dW)
     assert badw.size == 0, f"{what}: dW off at {badw[:3].tolist()}, err {errw.max():.3e}"
-    rel = np.linalg.norm(dy - orc["dy"]) / max(np.linalg.norm(orc["dy"]), 1e-300)
-    assert rel < 5e-3, f"{what}: dy relative error {rel:.2e}"
+    if np.linalg.norm(orc["dy"]) > 0:      # (a one-word vocabulary has no gradient at all)
+        rel = np.linalg.norm(dy - orc["dy"]) / np.linalg.norm(orc["dy"])
+        assert rel < 5e-3, f"{what}: dy relative error {rel:.2e}"
 
 
-@pytest.mark.parametrize("T,d,V,tau", [(1, 64, 300, 1.0), (64, 128, 1000, 1.0),
+@pytest.mark.parametrize("T,d,V,tau", [(1, 64, 300, 1.0), (5, 64, 1, 1.0), (64, 128, 1000, 1.0),
                                        (129, 256, 2049, 0.7), (300, 320, 5000, 1.3),
                                        (77, 5120, 3001, 0.7)])
 def test_backward_parity(tim, T, d, V, tau):

@@ -76,7 +76,7 @@ def test_split_tf32_definition(tim):
     assert np.array_equal((big.astype(np.float64) + small), x.astype(np.float64))   # exact split
 
 
-@pytest.mark.parametrize("T,d,V,tau", [(1, 64, 300, 1.0), (64, 128, 1000, 1.0),
+@pytest.mark.parametrize("T,d,V,tau", [(1, 64, 300, 1.0), (5, 64, 1, 1.0), (64, 128, 1000, 1.0),
                                        (129, 256, 2049, 0.7), (300, 320, 5000, 1.3),
                                        (77, 5120, 3001, 0.7)])
 def test_fp32_parity(tim, T, d, V, tau):

@@ -37,7 +37,7 @@ def test_quantizer_bit_exact(tim):
     assert np.array_equal(e4m3_bits_to_f64(codes), want_c)
 
 
-@pytest.mark.parametrize("T,d,V,tau", [(1, 128, 300, 1.0), (64, 128, 1000, 1.0),
+@pytest.mark.parametrize("T,d,V,tau", [(1, 128, 300, 1.0), (5, 128, 1, 1.0), (64, 128, 1000, 1.0),
                                        (129, 256, 2049, 0.7), (300, 384, 5000, 1.3),
                                        (77, 5120, 3001, 0.7)])
 def test_fp8_parity(tim, T, d, V, tau):
