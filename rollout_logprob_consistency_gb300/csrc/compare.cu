@@ -38,8 +38,6 @@ namespace tim {
 
 constexpr int kCmpThreads = 64;
 constexpr int kCmpWarps = kCmpThreads / 32;
-constexpr int kCmpTokensPerPart = 256;
-constexpr int kCmpMaxParts = 256;
 
 template <typename I>
 struct Runs {
@@ -97,26 +95,66 @@ struct alignas(16) CmpPart {
 };
 static_assert(sizeof(CmpPart) == 256, "compare partial is 256 bytes");
 
-__host__ __device__ inline int compare_parts(int64_t T, int n_seq) {
-  const int64_t avg = (T + n_seq - 1) / n_seq;
-  int64_t P = (avg + kCmpTokensPerPart - 1) / kCmpTokensPerPart;
-  if (P < 1) P = 1;
-  if (P > kCmpMaxParts) P = kCmpMaxParts;
-  return static_cast<int>(P);
-}
-
-// Compare workspace: status word | per-sequence tickets int32 [S] | parts [S][P].
+// Compare workspace: status word | per-sequence tickets int32 [S] | part bases
+// int32 [S + 1] | parts [sum of P_j] (at most seq_parts_bound(T, S)).
 struct CmpLayout {
-  size_t cnt_off, part_off, total;
+  size_t cnt_off, base_off, part_off, total;
 };
 __host__ inline CmpLayout compare_layout(int64_t T, int n_seq) {
   CmpLayout L;
   L.cnt_off = 256;
-  L.part_off = align_up(L.cnt_off + static_cast<size_t>(n_seq) * 4, 256);
-  L.total = align_up(L.part_off + static_cast<size_t>(n_seq) * compare_parts(T, n_seq) *
+  L.base_off = align_up(L.cnt_off + static_cast<size_t>(n_seq) * 4, 256);
+  L.part_off = align_up(L.base_off + static_cast<size_t>(n_seq + 1) * 4, 256);
+  L.total = align_up(L.part_off + static_cast<size_t>(seq_parts_bound(T, n_seq)) *
                                       sizeof(CmpPart),
                      1024);
   return L;
+}
+
+// base[j] = sum of P_i for i < j, base[n_seq] = total; one block, each thread a
+// contiguous run of sequences, then a block-wide exclusive scan of the run sums.
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
+    seq_partition_kernel(const int64_t* __restrict__ offs, int n_seq, int64_t T,
+                         int* __restrict__ base) {
+  __shared__ int s_warp[kScanThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (n_seq + kScanThreads - 1) / kScanThreads;
+  const int j0 = tid * per;
+  const int j1 = j0 + per < n_seq ? j0 + per : n_seq;
+  int sum = 0;
+  for (int j = j0; j < j1; ++j) sum += seq_parts(offs[j], offs[j + 1], T);
+  int incl = sum;  // inclusive scan within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += u;
+    }
+    s_warp[lane] = w;  // inclusive prefix of the warp sums
+  }
+  __syncthreads();
+  int run = incl - sum + (warp > 0 ? s_warp[warp - 1] : 0);  // exclusive prefix
+  for (int j = j0; j < j1; ++j) {
+    base[j] = run;
+    run += seq_parts(offs[j], offs[j + 1], T);
+  }
+  if (tid == kScanThreads - 1) base[n_seq] = s_warp[31];
+}
+
+cudaError_t launch_seq_partition(const int64_t* offs, int n_seq, int64_t T, int* base,
+                                 cudaStream_t stream) {
+  seq_partition_kernel<<<1, kScanThreads, 0, stream>>>(offs, n_seq, T, base);
+  return cudaGetLastError();
 }
 
 struct Acc {
@@ -159,9 +197,10 @@ template <bool kVec>
 __global__ void __launch_bounds__(kCmpThreads)
     seg_compare_kernel(const float* __restrict__ A, const float* __restrict__ B,
                        const float* __restrict__ C, const int64_t* __restrict__ offs,
-                       const uint8_t* __restrict__ mask, int64_t T, int P, double cap,
-                       double ln_cap, tim_seq_stats* __restrict__ out, float* __restrict__ tis_w,
-                       int* status, int* cnt, CmpPart* parts) {
+                       const uint8_t* __restrict__ mask, int64_t T, int n_seq,
+                       const int* __restrict__ base, double cap, double ln_cap,
+                       tim_seq_stats* __restrict__ out, float* __restrict__ tis_w, int* status,
+                       int* cnt, CmpPart* parts) {
   __shared__ Runs<int> s_runs[kCmpWarps][3];
   __shared__ double s_red[kCmpWarps][11];
   __shared__ long long s_clip[kCmpWarps];
@@ -169,8 +208,11 @@ __global__ void __launch_bounds__(kCmpThreads)
   __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j = blockIdx.x;
-  const int p = blockIdx.y;
+  const int b = blockIdx.x;  // global part index
+  if (b >= __ldcg(base + n_seq)) return;
+  const int j = part_sequence(base, n_seq, b);
+  const int p = b - __ldcg(base + j);
+  const int P = __ldcg(base + j + 1) - __ldcg(base + j);
   const int64_t s = offs[j], e = offs[j + 1];
   if (!(s >= 0 && s <= e && e <= T)) {
     if (tid == 0 && p == 0) {
@@ -288,7 +330,7 @@ __global__ void __launch_bounds__(kCmpThreads)
       part.flags |= s_flags[w];
     }
     for (int q = 0; q < 3; ++q) part.runs[q] = total[q];
-    parts[static_cast<int64_t>(j) * P + p] = part;
+    parts[b] = part;
     __threadfence();
     const int ticket = atomicAdd(&cnt[j], 1);
     s_last = (ticket == P - 1) ? 1 : 0;
@@ -302,7 +344,7 @@ __global__ void __launch_bounds__(kCmpThreads)
   // (left) with lane l + off (right), so the run statistics keep the sequence
   // order.
   __threadfence();
-  const CmpPart* pj = parts + static_cast<int64_t>(j) * P;
+  const CmpPart* pj = parts + __ldcg(base + j);
   Runs<long long> R[3] = {runs_identity<long long>(), runs_identity<long long>(),
                           runs_identity<long long>()};
   double tot[11];
@@ -403,21 +445,23 @@ cudaError_t launch_seg_compare(const float* A, const float* B, const float* C,
   const double cap = static_cast<double>(tis_cap);
   const double ln_cap = std::log(cap);
   const CmpLayout L = compare_layout(T, n_seq);
-  const int P = compare_parts(T, n_seq);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(ws);
   int* cnt = reinterpret_cast<int*>(ws + L.cnt_off);
+  int* base = reinterpret_cast<int*>(ws + L.base_off);
   CmpPart* parts = reinterpret_cast<CmpPart*>(ws + L.part_off);
+  cudaError_t e = launch_seq_partition(offs, n_seq, T, base, stream);
+  if (e != cudaSuccess) return e;
   const bool vec = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
                      reinterpret_cast<uintptr_t>(C)) & 15u) == 0 &&
                    (reinterpret_cast<uintptr_t>(mask) & 3u) == 0;
-  const dim3 grid(static_cast<unsigned>(n_seq), static_cast<unsigned>(P));
+  const dim3 grid(static_cast<unsigned>(seq_parts_bound(T, n_seq)));
   if (vec)
     seg_compare_kernel<true><<<grid, kCmpThreads, 0, stream>>>(
-        A, B, C, offs, mask, T, P, cap, ln_cap, out, tis_w, status, cnt, parts);
+        A, B, C, offs, mask, T, n_seq, base, cap, ln_cap, out, tis_w, status, cnt, parts);
   else
     seg_compare_kernel<false><<<grid, kCmpThreads, 0, stream>>>(
-        A, B, C, offs, mask, T, P, cap, ln_cap, out, tis_w, status, cnt, parts);
+        A, B, C, offs, mask, T, n_seq, base, cap, ln_cap, out, tis_w, status, cnt, parts);
   return cudaGetLastError();
 }
 

@@ -17,10 +17,11 @@
 //  - MIS: w 1[lo <= w <= hi], w = exp(d) ("Rollout-Training Mismatch in LLM RL",
 //    section 2.1); mean w^2 = mean exp(2d) (same page, section 5.3).
 //
-// Work split: the per-token sums run over many CTAs per sequence (a fixed
-// partition of each sequence into P contiguous parts, P from the batch shape as
-// in the compare kernel); each CTA accumulates its tokens per thread in order,
-// then a fixed xor-butterfly and warp-order fold, and writes one partial record.
+// Work split: the per-token sums run over many CTAs per sequence (each sequence
+// cut into P_j contiguous parts with P_j from its own length, as in the compare
+// kernel, so a sequence's results do not depend on the batch); each CTA
+// accumulates its tokens per thread in order, then a fixed xor-butterfly and
+// warp-order fold, and writes one partial record.
 // A second kernel runs four CTAs per sequence: one folds the P partials in part
 // order (deterministic) and writes every field but the quantiles; three gather
 // one pair's |left - right| values of the active tokens into shared memory (any
@@ -39,8 +40,6 @@ namespace tim {
 constexpr int kDiagThreads = 512;      // quantile / fold CTAs
 constexpr int kDiagPartThreads = 256;  // per-token partial CTAs
 constexpr int kDiagPartWarps = kDiagPartThreads / 32;
-constexpr int kDiagTokensPerPart = 256;
-constexpr int kDiagMaxParts = 256;
 constexpr int kQuantMax = TIM_DIAG_QUANTILE_MAX_TOKENS;
 constexpr size_t kDiagSmemBytes = static_cast<size_t>(kQuantMax) * sizeof(unsigned long long);
 
@@ -56,13 +55,8 @@ struct DiagPart {
   int pad;
 };
 
-__host__ __device__ inline int diag_parts(int64_t T, int n_seq) {
-  const int64_t avg = (T + n_seq - 1) / n_seq;
-  int64_t P = (avg + kDiagTokensPerPart - 1) / kDiagTokensPerPart;
-  if (P < 1) P = 1;
-  if (P > kDiagMaxParts) P = kDiagMaxParts;
-  return static_cast<int>(P);
-}
+cudaError_t launch_seq_partition(const int64_t* offs, int n_seq, int64_t T, int* base,
+                                 cudaStream_t stream);
 
 __device__ __forceinline__ double pair_abs(int p, double a, double b, double c) {
   return p == 0 ? fabs(a - b) : (p == 1 ? fabs(b - c) : fabs(a - c));
@@ -77,12 +71,17 @@ __global__ void __launch_bounds__(kDiagPartThreads)
                          const float* __restrict__ C, const int32_t* __restrict__ tA,
                          const int32_t* __restrict__ tB, const int32_t* __restrict__ tC,
                          const int64_t* __restrict__ offs, const uint8_t* __restrict__ mask,
-                         int64_t T, double ln_lo, double ln_hi, DiagPart* __restrict__ parts) {
+                         int64_t T, int n_seq, const int* __restrict__ base, double ln_lo,
+                         double ln_hi, DiagPart* __restrict__ parts) {
   __shared__ double s_sum[kDiagPartWarps][kDiagSums];
   __shared__ long long s_cnt[kDiagPartWarps][kDiagCounts];
   __shared__ int s_flags[kDiagPartWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j = blockIdx.x, part = blockIdx.y, P = gridDim.y;
+  const int b = blockIdx.x;  // global part index
+  if (b >= __ldcg(base + n_seq)) return;
+  const int j = part_sequence(base, n_seq, b);
+  const int part = b - __ldcg(base + j);
+  const int P = __ldcg(base + j + 1) - __ldcg(base + j);
   const int64_t s = offs[j], e = offs[j + 1];
   if (!offsets_ok(s, e, T)) return;  // the fold CTA reports the sequence
   const int64_t chunk = (e - s + P - 1) / P;
@@ -153,7 +152,7 @@ __global__ void __launch_bounds__(kDiagPartThreads)
     for (int i = 0; i < kDiagCounts; ++i) r.cnt[i] += s_cnt[w][i];
     r.flags |= s_flags[w];
   }
-  parts[static_cast<int64_t>(j) * P + part] = r;
+  parts[b] = r;
 }
 
 // blockIdx.y = 0, 1, 2: quantiles of pair p; blockIdx.y = 3: fold and the other fields.
@@ -163,7 +162,8 @@ __global__ void __launch_bounds__(kDiagThreads)
                           const int32_t* __restrict__ tB, const int32_t* __restrict__ tC,
                           const int64_t* __restrict__ offs, const uint8_t* __restrict__ mask,
                           int64_t T, double cap, double ln_cap, const DiagPart* __restrict__ parts,
-                          int P, tim_seq_diag* __restrict__ out, int* status) {
+                          const int* __restrict__ base, tim_seq_diag* __restrict__ out,
+                          int* status) {
   extern __shared__ unsigned long long keys[];
   __shared__ int s_fill, s_bad;
   const int tid = threadIdx.x;
@@ -190,8 +190,9 @@ __global__ void __launch_bounds__(kDiagThreads)
     for (int i = 0; i < kDiagSums; ++i) S[i] = 0.0;
 #pragma unroll
     for (int i = 0; i < kDiagCounts; ++i) N[i] = 0;
-    for (int q = 0; q < P; ++q) {  // part order
-      const DiagPart& r = parts[static_cast<int64_t>(j) * P + q];
+    const int q0 = __ldcg(base + j), q1 = __ldcg(base + j + 1);
+    for (int q = q0; q < q1; ++q) {  // part order
+      const DiagPart& r = parts[q];
 #pragma unroll
       for (int i = 0; i < kDiagSums; ++i) S[i] += r.sum[i];
 #pragma unroll
@@ -346,8 +347,14 @@ __global__ void __launch_bounds__(kDiagThreads)
   }
 }
 
+// Diagnostics workspace: status | part bases int32 [S + 1] | parts.
+size_t diag_base_offset() { return 1024; }
+size_t diag_parts_offset(int n_seq) {
+  return align_up(1024 + static_cast<size_t>(n_seq + 1) * 4, 1024);
+}
 size_t diag_workspace_bytes(int64_t T, int n_seq) {
-  return align_up(1024 + static_cast<size_t>(n_seq) * diag_parts(T, n_seq) * sizeof(DiagPart),
+  return align_up(diag_parts_offset(n_seq) +
+                      static_cast<size_t>(seq_parts_bound(T, n_seq)) * sizeof(DiagPart),
                   1024);
 }
 
@@ -358,20 +365,23 @@ cudaError_t launch_seg_diag(const float* A, const float* B, const float* C, cons
                             cudaStream_t stream) {
   const double cap = static_cast<double>(tis_cap);
   int* status = static_cast<int*>(workspace);
-  DiagPart* parts = reinterpret_cast<DiagPart*>(static_cast<uint8_t*>(workspace) + 1024);
-  const int P = diag_parts(T, n_seq);
-  seg_diag_part_kernel<<<dim3(static_cast<unsigned>(n_seq), static_cast<unsigned>(P)),
-                         kDiagPartThreads, 0, stream>>>(
-      A, B, C, tA, tB, tC, offs, mask, T, std::log(static_cast<double>(mis_lo)),
-      std::log(static_cast<double>(mis_hi)), parts);
-  cudaError_t err = cudaGetLastError();
+  int* base = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + diag_base_offset());
+  DiagPart* parts =
+      reinterpret_cast<DiagPart*>(static_cast<uint8_t*>(workspace) + diag_parts_offset(n_seq));
+  cudaError_t err = launch_seq_partition(offs, n_seq, T, base, stream);
+  if (err != cudaSuccess) return err;
+  seg_diag_part_kernel<<<static_cast<unsigned>(seq_parts_bound(T, n_seq)), kDiagPartThreads, 0,
+                         stream>>>(A, B, C, tA, tB, tC, offs, mask, T, n_seq, base,
+                                   std::log(static_cast<double>(mis_lo)),
+                                   std::log(static_cast<double>(mis_hi)), parts);
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   err = cudaFuncSetAttribute(seg_diag_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kDiagSmemBytes));
   if (err != cudaSuccess) return err;
   seg_diag_final_kernel<<<dim3(static_cast<unsigned>(n_seq), 4), kDiagThreads, kDiagSmemBytes,
                           stream>>>(A, B, C, tA, tB, tC, offs, mask, T, cap, std::log(cap), parts,
-                                    P, out, status);
+                                    base, out, status);
   return cudaGetLastError();
 }
 

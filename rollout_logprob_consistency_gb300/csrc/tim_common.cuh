@@ -249,6 +249,38 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
+// Per-sequence work partition shared by the compare and diagnostics kernels:
+// sequence j is cut into P_j = clamp(ceil(len_j / 256), 1, 256) contiguous parts
+// (1 for invalid offsets), numbered globally from base[j]; base[n_seq] = total.
+// P_j depends only on the sequence's own length, so its partial sums -- and the
+// fp64 statistics folded from them -- do not depend on the batch.
+constexpr int kSeqTokensPerPart = 256;
+constexpr int kSeqMaxParts = 256;
+
+__host__ __device__ inline int seq_parts(int64_t s, int64_t e, int64_t T) {
+  if (!(s >= 0 && s <= e && e <= T)) return 1;
+  int64_t P = (e - s + kSeqTokensPerPart - 1) / kSeqTokensPerPart;
+  if (P < 1) P = 1;
+  if (P > kSeqMaxParts) P = kSeqMaxParts;
+  return static_cast<int>(P);
+}
+
+// Upper bound of the total part count (sum_j ceil(len_j / 256) <= T / 256 + n_seq).
+__host__ inline int64_t seq_parts_bound(int64_t T, int n_seq) {
+  return (T + kSeqTokensPerPart - 1) / kSeqTokensPerPart + n_seq;
+}
+
+// The sequence whose parts include global part index b: the largest j with
+// base[j] <= b (base ascending, n_seq + 1 entries, base[0] = 0).
+__device__ __forceinline__ int part_sequence(const int* base, int n_seq, int b) {
+  int lo = 0, hi = n_seq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldcg(base + mid) <= b) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // The four largest logits of one (row, 256-column tile): values descending and
 // their vocabulary ids (equal values: the lower id first); -inf / -1 past the
 // tile.  Written by the LM-head kernel in top-4 mode, read by the processed

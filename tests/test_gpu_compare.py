@@ -137,3 +137,26 @@ def test_k3_overflow_and_tis_clip(tim):
     assert_compare_parity(g, r)
     assert_tis_parity(w, rw, np.ones(4, bool))
     assert g[1]["tis_clipped"] == 1
+
+
+def test_sequence_stats_do_not_depend_on_the_batch(tim):
+    """A sequence's statistics (integers and fp64 sums alike) are the same bits whatever
+    batch it is compared in: each sequence is cut into parts by its own length."""
+    A, B, C = scores(30000, 11)
+    offs = np.array([0, 700, 9000, 9001, 23000, 30000], np.int64)
+    mask = np.ones(30000, np.uint8)
+    full, wf = gpu_compare(tim, A, B, C, offs, mask, 2.0)
+    for j in range(len(offs) - 1):
+        a, b = offs[j], offs[j + 1]
+        one, w1 = gpu_compare(tim, A[a:b], B[a:b], C[a:b], np.array([0, b - a], np.int64),
+                              mask[a:b], 2.0)
+        assert one[0] == full[j], j
+        assert w1.tobytes() == wf[a:b].tobytes()
+    # and inside a differently shaped batch (another sequence in front)
+    pre = 5000
+    A2 = np.concatenate([A[:pre], A[700:9000]])
+    B2 = np.concatenate([B[:pre], B[700:9000]])
+    C2 = np.concatenate([C[:pre], C[700:9000]])
+    two, _ = gpu_compare(tim, A2, B2, C2, np.array([0, pre, pre + 8300], np.int64),
+                         np.ones(pre + 8300, np.uint8), 2.0)
+    assert two[1] == full[1]

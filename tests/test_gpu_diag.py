@@ -161,3 +161,24 @@ def test_diag_errors(tim, case):
     r, errs = oracle.oracle_diag_lenient(A, B, C, offs, mask, 2.0, 0.5, 1.5, tops)
     assert errs
     assert_diag_parity(g, r, d_abs(A, C, offs, mask), what=case)
+
+
+def _same(x, y):
+    if isinstance(x, dict):
+        return x.keys() == y.keys() and all(_same(x[k], y[k]) for k in x)
+    if isinstance(x, (list, tuple)):
+        return len(x) == len(y) and all(_same(a, b) for a, b in zip(x, y))
+    if isinstance(x, float) and math.isnan(x):
+        return isinstance(y, float) and math.isnan(y)
+    return x == y
+
+
+def test_diag_sequence_results_do_not_depend_on_the_batch(tim):
+    """Each sequence's diagnostics are the same bits alone or inside any batch."""
+    A, B, C, offs, mask, tops = make_case(20000, 21, n_seq=5)
+    full = run(tim, A, B, C, offs, mask, tops)
+    for j in range(len(offs) - 1):
+        a, b = int(offs[j]), int(offs[j + 1])
+        one = run(tim, A[a:b], B[a:b], C[a:b], np.array([0, b - a], np.int64), mask[a:b],
+                  [t[a:b] for t in tops])
+        assert _same(one[0], full[j]), j
