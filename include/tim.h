@@ -235,6 +235,9 @@ typedef struct tim_seq_stats {
 #define TIM_SEQ_BAD_OFFSETS 8
 #define TIM_SEQ_K3_OVERFLOW 16
 
+/* Each sequence is reduced in parts cut from its own length (256 tokens a part,
+ * at most 256 parts) and the parts are folded in order, so a sequence's
+ * statistics, fp64 sums included, are the same bits in any batch. */
 size_t tim_compare_workspace_size(int64_t T, int32_t n_seq);
 
 tim_status tim_compare(const float *lp_gen, const float *lp_replay, const float *lp_train,
