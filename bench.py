@@ -756,7 +756,8 @@ def main():
             e2e=dict(value=e2e_value, unit="tokens/s", h2d_bytes_per_step=h2d,
                      d2h_bytes_per_step=d2h, steps=e2e_steps,
                      note="pinned host buffers; the copies of step k+1 overlap step k"),
-            gpu_launches=4 * args.steps,
+            # per step: RMSNorm, LM head, finalize, the compare's part numbering, compare
+            gpu_launches=5 * args.steps,
             clocks=clk,
             compare=compare_info,
             decode_shapes=decode,
