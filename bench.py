@@ -570,7 +570,7 @@ def main():
 
     # ---------------------------------------------------------------- next-row paths on this workload
     extras = None
-    if rank == 0 and not args.no_extras:
+    if rank == 0 and world == 1 and not args.no_extras:   # N = 1 runs report these
         extras = {}
         pout = (torch.empty(T, device=dev), torch.empty(T, device=dev),
                 torch.empty(T, dtype=torch.int32, device=dev))
@@ -695,7 +695,7 @@ def main():
 
     # ---------------------------------------------------------------- decode-shaped rows (HBM bound)
     decode = None
-    if not args.no_decode and rank == 0:
+    if not args.no_decode and rank == 0 and world == 1:
         decode = {}
         for M in (1, 7, 64):
             wsm = tim.Workspace(tim.logprob_workspace_size(M, d, V), dev)
@@ -728,7 +728,7 @@ def main():
 
     # ---------------------------------------------------------------- CPU baseline (oracle)
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows = np.sort(np.random.default_rng(99).choice(T, args.cpu_rows, replace=False))
         dt = time_oracle(b, rows)
         cpu = dict(value=args.cpu_rows / dt, unit="tokens/s", cores=cpu_cores(), kind="oracle",
