@@ -33,8 +33,8 @@ valid sequence:
   -- "Rollout-Training Mismatch in LLM RL", section 5.3 (eq. 10 context).
 
 Flags follow ``oracle.compare``; sequences with more than QUANTILE_MAX_TOKENS
-active tokens get FLAG_QUANTILE_SKIPPED and NaN quantiles (the GPU kernel sorts
-a sequence in shared memory).
+active tokens get FLAG_QUANTILE_SKIPPED and NaN quantiles (the GPU kernel holds
+a sequence's keys in shared memory).
 """
 from __future__ import annotations
 

@@ -25,9 +25,9 @@
 // A second kernel runs four CTAs per sequence: one folds the P partials in part
 // order (deterministic) and writes every field but the quantiles; three gather
 // one pair's |left - right| values of the active tokens into shared memory (any
-// order), pad them with +inf to a power of two and bitonic-sort them as 64-bit
-// keys (the bit patterns of non-negative doubles order like the values, so the
-// sort is integer work); the order statistics are exact and the interpolation
+// order) as 64-bit keys (the bit patterns of non-negative doubles order like
+// the values, so selection is integer work) and find the order statistics the
+// interpolation needs by a radix select; they are exact, and the interpolation
 // is the formula above.  Sequences with more than kQuantMax active tokens skip
 // the quantiles (flag, NaN).
 #include <cmath>
@@ -58,8 +58,48 @@ struct DiagPart {
 cudaError_t launch_seq_partition(const int64_t* offs, int n_seq, int64_t T, int* base,
                                  cudaStream_t stream);
 
-__device__ __forceinline__ double pair_abs(int p, double a, double b, double c) {
-  return p == 0 ? fabs(a - b) : (p == 1 ? fabs(b - c) : fabs(a - c));
+// |a - b| of two floats, as the bit pattern of the double (double)a - (double)b
+// rounded to nearest.  When the fp32 difference is exact (TwoSum's error term is
+// zero, which Sterbenz's lemma guarantees for operands within a factor of two)
+// and normal or zero, the double is that float widened, built with integer
+// operations; otherwise the fp64 subtraction runs.  GB300's fp64 pipe is narrow,
+// and every active token of a sequence passes through here.
+__device__ __forceinline__ unsigned long long abs_diff_key(float a, float b) {
+  const float s = __fsub_rn(a, b);
+  const float bv = __fsub_rn(s, a);
+  const float av = __fsub_rn(s, bv);
+  const float err = __fadd_rn(__fsub_rn(a, av), __fsub_rn(-b, bv));  // s + err = a - b
+  const uint32_t u = __float_as_uint(s) & 0x7FFFFFFFu;
+  const uint32_t ex = u >> 23;
+  if (err == 0.f) {
+    if (u == 0u) return 0ull;
+    if (ex != 0u && ex != 255u)  // rebias the exponent, widen the fraction
+      return (static_cast<unsigned long long>(ex + (1023u - 127u)) << 52) |
+             (static_cast<unsigned long long>(u & 0x7FFFFFu) << 29);
+  }
+  return static_cast<unsigned long long>(
+      __double_as_longlong(fabs(static_cast<double>(a) - static_cast<double>(b))));
+}
+
+__device__ __forceinline__ unsigned long long warp_or_u64(unsigned long long v) {
+  const unsigned lo = __reduce_or_sync(0xFFFFFFFFu, static_cast<unsigned>(v));
+  const unsigned hi = __reduce_or_sync(0xFFFFFFFFu, static_cast<unsigned>(v >> 32));
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
+__device__ __forceinline__ unsigned long long warp_and_u64(unsigned long long v) {
+  const unsigned lo = __reduce_and_sync(0xFFFFFFFFu, static_cast<unsigned>(v));
+  const unsigned hi = __reduce_and_sync(0xFFFFFFFFu, static_cast<unsigned>(v >> 32));
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = w < v ? w : v;
+  }
+  return v;
 }
 
 __device__ __forceinline__ bool offsets_ok(int64_t s, int64_t e, int64_t T) {
@@ -166,6 +206,11 @@ __global__ void __launch_bounds__(kDiagThreads)
                           int* status) {
   extern __shared__ unsigned long long keys[];
   __shared__ int s_fill, s_bad;
+  __shared__ unsigned s_hist[3 * 256];  // radix-select digit counts per target
+  __shared__ unsigned long long s_prefix[3], s_mask[3];
+  __shared__ unsigned long long s_or[4], s_and[4];  // [q]: target q's candidates; [3]: all keys
+  __shared__ unsigned long long s_wmin[kDiagThreads / 32][6];
+  __shared__ int s_rem[3], s_cnt[3], s_open[3];
   const int tid = threadIdx.x;
   const int j = blockIdx.x, role = blockIdx.y;
   const int64_t s = offs[j], e = offs[j + 1];
@@ -247,8 +292,16 @@ __global__ void __launch_bounds__(kDiagThreads)
     s_fill = 0;
     s_bad = 0;
   }
+  if (tid < 4) {
+    s_or[tid] = 0ull;
+    s_and[tid] = ~0ull;
+  }
+  for (int i = tid; i < 3 * 256; i += kDiagThreads) s_hist[i] = 0u;
   __syncthreads();
-  const int lane = tid & 31;
+  const int lane = tid & 31, warp = tid >> 5;
+  const float* L = p == 1 ? B : A;
+  const float* R = p == 0 ? B : C;
+  unsigned long long k_or = 0ull, k_and = ~0ull;
   for (int64_t base = s; base < e; base += kDiagThreads) {  // uniform trip count
     const int64_t t = base + tid;
     const uint8_t m = t < e ? __ldg(mask + t) : 0;
@@ -260,11 +313,18 @@ __global__ void __launch_bounds__(kDiagThreads)
     if (lane == 0 && bal != 0u) slot0 = atomicAdd(&s_fill, __popc(bal));
     slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
     if (act) {
-      const double a = __ldg(A + t), b = __ldg(B + t), c = __ldg(C + t);
+      const unsigned long long k = abs_diff_key(__ldg(L + t), __ldg(R + t));
+      k_or |= k;
+      k_and &= k;
       const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
-      if (slot < kQuantMax)
-        keys[slot] = static_cast<unsigned long long>(__double_as_longlong(pair_abs(p, a, b, c)));
+      if (slot < kQuantMax) keys[slot] = k;
     }
+  }
+  k_or = warp_or_u64(k_or);
+  k_and = warp_and_u64(k_and);
+  if (lane == 0) {
+    atomicOr(&s_or[3], k_or);
+    atomicAnd(&s_and[3], k_and);
   }
   __syncthreads();
   const int n = s_fill;
@@ -277,69 +337,177 @@ __global__ void __launch_bounds__(kDiagThreads)
     }
     return;
   }
-  int n2 = 1;
-  while (n2 < n) n2 <<= 1;
-  const unsigned long long kInf = static_cast<unsigned long long>(__double_as_longlong(INFINITY));
-  for (int i = n + tid; i < n2; i += kDiagThreads) keys[i] = kInf;
+  // The three order statistics by an MSD radix select on the keys' bit
+  // patterns.  Target q keeps the key prefix fixed so far (bits [fixed_from,
+  // 64)), the rank it still seeks among the keys with that prefix (its
+  // candidates) and their count.  Bits every key shares are fixed before the
+  // first pass.  A pass histograms the next 8 bits of every candidate of each
+  // open target (shared-memory atomics) and takes the OR and AND of the
+  // candidates; then warp q either settles target q (the OR equals the AND:
+  // every candidate is the same key) or walks its histogram to the digit that
+  // holds the rank.  A target also settles when one candidate is left or no
+  // bits remain.  Any exact selection on this total order returns the
+  // elements a sort would put at those ranks, whatever the gather order.
+  const double qs[3] = {0.5, 0.95, 0.99};
+  const unsigned long long diff = s_or[3] ^ s_and[3];
+  int fixed_from = diff == 0ull ? 0 : 64 - __clzll(static_cast<long long>(diff));
+  if (tid < 3) {
+    const unsigned long long m0 = fixed_from == 64 ? 0ull : (~0ull << fixed_from);
+    s_prefix[tid] = s_and[3] & m0;
+    s_mask[tid] = m0;
+    s_rem[tid] = static_cast<int>(floor(__dmul_rn(static_cast<double>(n - 1), qs[tid])));
+    s_cnt[tid] = n;
+    s_open[tid] = n > 1 && fixed_from > 0;
+  }
   __syncthreads();
-  // bitonic sort, ascending; each phase visits its n2 / 2 compare-exchange pairs
-  // directly (pair idx -> lower index i: a zero bit inserted at the stride's bit).
-  // Phases with a stride below kSeg keep every pair inside one kSeg-element
-  // segment; a warp owns whole segments there, so those phases need only a warp
-  // barrier, and the block synchronises only around the longer strides.
-  constexpr int kSeg = 256;
-  const int warp = tid >> 5;
-  const int seg = n2 < kSeg ? n2 : kSeg;
-  const int n_seg = n2 / seg;
-  bool warp_phase = false;  // the previous phase ended with a warp barrier only
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      const bool local = jj < seg;
-      if (!local && warp_phase) __syncthreads();
-      if (local) {
-        for (int sg = warp; sg < n_seg; sg += kDiagThreads / 32) {
-          unsigned long long* kb = keys + sg * seg;
-          const int base = sg * seg;
-          for (int idx = lane; idx < (seg >> 1); idx += 32) {
-            const int i = ((idx & ~(jj - 1)) << 1) | (idx & (jj - 1));
-            const unsigned long long x = kb[i], y = kb[i + jj];
-            const bool up = ((base + i) & k) == 0;
-            if ((x > y) == up) {
-              kb[i] = y;
-              kb[i + jj] = x;
-            }
+  const int n_round = (n + kDiagThreads - 1) / kDiagThreads * kDiagThreads;
+  while (fixed_from > 0) {
+    bool open[3];
+    bool any = false;
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      open[q] = s_open[q] != 0;
+      any |= open[q];
+    }
+    if (!any) break;
+    const int sh = fixed_from > 8 ? fixed_from - 8 : 0;
+    const unsigned long long hmask = fixed_from == 64 ? 0ull : (~0ull << fixed_from);
+    unsigned long long pre[3], c_or[3], c_and[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      pre[q] = s_prefix[q];
+      c_or[q] = 0ull;
+      c_and[q] = ~0ull;
+    }
+#pragma unroll 4
+    for (int i = tid; i < n_round; i += kDiagThreads) {  // uniform trip count
+      if (i < n) {
+        const unsigned long long k = keys[i];
+        const unsigned dig = static_cast<unsigned>(k >> sh) & 255u;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          if (open[q] && (k & hmask) == pre[q]) {
+            atomicAdd(&s_hist[q * 256 + dig], 1u);
+            c_or[q] |= k;
+            c_and[q] &= k;
           }
         }
-        __syncwarp();
-        warp_phase = true;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      if (open[q]) {
+        c_or[q] = warp_or_u64(c_or[q]);
+        c_and[q] = warp_and_u64(c_and[q]);
+        if (lane == 0) {
+          atomicOr(&s_or[q], c_or[q]);
+          atomicAnd(&s_and[q], c_and[q]);
+        }
+      }
+    }
+    __syncthreads();
+    if (warp < 3 && open[warp]) {
+      const int q = warp;
+      unsigned* hq = s_hist + q * 256 + lane * 8;  // lane owns digits [8 lane, 8 lane + 8)
+      unsigned c[8];
+      unsigned tot = 0u;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        c[b] = hq[b];
+        hq[b] = 0u;  // ready for the next pass
+        tot += c[b];
+      }
+      const unsigned long long cand_or = s_or[q], cand_and = s_and[q];
+      const unsigned rem = static_cast<unsigned>(s_rem[q]);
+      __syncwarp();
+      if (cand_or == cand_and) {  // one distinct key among the candidates
+        if (lane == 0) {
+          s_prefix[q] = cand_and;
+          s_mask[q] = ~0ull;
+          s_open[q] = 0;
+        }
       } else {
-        for (int idx = tid; idx < (n2 >> 1); idx += kDiagThreads) {
-          const int i = ((idx & ~(jj - 1)) << 1) | (idx & (jj - 1));
-          const int ixj = i + jj;
-          const unsigned long long x = keys[i], y = keys[ixj];
-          const bool up = (i & k) == 0;
-          if ((x > y) == up) {
-            keys[i] = y;
-            keys[ixj] = x;
+        unsigned incl = tot;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+          const unsigned v = __shfl_up_sync(0xFFFFFFFFu, incl, o2);
+          if (lane >= o2) incl += v;
+        }
+        unsigned before = incl - tot;
+        if (rem >= before && rem < incl) {  // exactly one lane
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            if (rem >= before && rem < before + c[b]) {
+              s_prefix[q] |= static_cast<unsigned long long>(lane * 8 + b) << sh;
+              s_mask[q] = ~0ull << sh;
+              s_rem[q] = static_cast<int>(rem - before);
+              s_cnt[q] = static_cast<int>(c[b]);
+              s_open[q] = c[b] > 1u && sh > 0;
+            }
+            before += c[b];
           }
         }
-        __syncthreads();
-        warp_phase = false;
+      }
+      if (lane == 0) {
+        s_or[q] = 0ull;
+        s_and[q] = ~0ull;
+      }
+    }
+    fixed_from = sh;
+    __syncthreads();
+  }
+  // Target q's key is its candidates' common value: the one candidate left,
+  // or the prefix once all 64 bits are fixed.  The next order statistic is
+  // that key again while equal keys remain past the rank, else the smallest
+  // key above the candidates' range.
+  {
+    unsigned long long pre[3], msk[3], lo_min[3], up_min[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      pre[q] = s_prefix[q];
+      msk[q] = s_mask[q];
+      lo_min[q] = up_min[q] = ~0ull;
+    }
+#pragma unroll 4
+    for (int i = tid; i < n; i += kDiagThreads) {
+      const unsigned long long k = keys[i];
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const unsigned long long km = k & msk[q];
+        if (km == pre[q]) lo_min[q] = k < lo_min[q] ? k : lo_min[q];
+        else if (km > pre[q]) up_min[q] = k < up_min[q] ? k : up_min[q];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      lo_min[q] = warp_min_u64(lo_min[q]);
+      up_min[q] = warp_min_u64(up_min[q]);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        s_wmin[warp][q] = lo_min[q];
+        s_wmin[warp][3 + q] = up_min[q];
       }
     }
   }
-  if (warp_phase) __syncthreads();
+  __syncthreads();
   if (tid == 0) {
-    const double qs[3] = {0.5, 0.95, 0.99};
     double r[3];
     for (int qi = 0; qi < 3; ++qi) {
-      const double h = static_cast<double>(n - 1) * qs[qi];
+      unsigned long long klo = ~0ull, kup = ~0ull;
+      for (int w = 0; w < kDiagThreads / 32; ++w) {
+        klo = s_wmin[w][qi] < klo ? s_wmin[w][qi] : klo;
+        kup = s_wmin[w][3 + qi] < kup ? s_wmin[w][3 + qi] : kup;
+      }
+      // each operation rounded on its own, as the formula is written
+      const double h = __dmul_rn(static_cast<double>(n - 1), qs[qi]);
       const double fl = floor(h);
       const int lo = static_cast<int>(fl);
-      const int hi = lo + 1 < n ? lo + 1 : n - 1;
-      const double xlo = __longlong_as_double(static_cast<long long>(keys[lo]));
-      const double xhi = __longlong_as_double(static_cast<long long>(keys[hi]));
-      r[qi] = xlo + (h - fl) * (xhi - xlo);
+      const unsigned long long khi = (lo + 1 < n && s_rem[qi] + 1 >= s_cnt[qi]) ? kup : klo;
+      const double xlo = __longlong_as_double(static_cast<long long>(klo));
+      const double xhi = __longlong_as_double(static_cast<long long>(khi));
+      r[qi] = __dadd_rn(xlo, __dmul_rn(__dsub_rn(h, fl), __dsub_rn(xhi, xlo)));
     }
     o->abs_q50[p] = r[0];
     o->abs_q95[p] = r[1];
