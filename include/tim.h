@@ -41,11 +41,12 @@
  *    first recorded error is kept.  tim_status_sync() returns and clears it.
  *    Once an error is reported, the numbers of that call are not to be trusted.
  *  - A workspace must be zero-initialised once (tim_workspace_init) before its
- *    first use; it may then be reused by any number of calls on one stream.
- *    Calls that share a workspace must not overlap in time.  A workspace
- *    serves one family of calls: either the tim_logprob family or tim_compare
- *    (tim_compare keeps per-sequence counters in its workspace that must be
- *    zero between calls; it leaves them zero itself).
+ *    first use; it may then be reused by any number of calls on one stream,
+ *    of any shape whose workspace size it covers.  Calls that share a
+ *    workspace must not overlap in time.  A workspace serves one family of
+ *    calls: either the tim_logprob family or tim_compare / tim_compare_diag
+ *    (these keep per-sequence counters in the workspace; each call zeroes its
+ *    own before use).
  *
  * Only sm_103 devices (GB300) are supported.
  */

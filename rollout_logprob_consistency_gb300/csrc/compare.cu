@@ -113,12 +113,15 @@ __host__ inline CmpLayout compare_layout(int64_t T, int n_seq) {
 
 // base[j] = sum of P_i for i < j, base[n_seq] = total; one block, each thread a
 // contiguous run of sequences, then a block-wide exclusive scan of the run sums.
+// It also zeroes the call's per-sequence tickets (cnt, when given), so they
+// start at zero whatever an earlier call of another shape left in the workspace.
 constexpr int kScanThreads = 1024;
 
 __global__ void __launch_bounds__(kScanThreads)
     seq_partition_kernel(const int64_t* __restrict__ offs, int n_seq, int64_t T,
-                         int* __restrict__ base) {
+                         int* __restrict__ base, int* __restrict__ cnt) {
   __shared__ int s_warp[kScanThreads / 32];
+  pdl_launch_dependents();  // the compare / diagnostics kernel may launch now
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int per = (n_seq + kScanThreads - 1) / kScanThreads;
   const int j0 = tid * per;
@@ -147,13 +150,14 @@ __global__ void __launch_bounds__(kScanThreads)
   for (int j = j0; j < j1; ++j) {
     base[j] = run;
     run += seq_parts(offs[j], offs[j + 1], T);
+    if (cnt != nullptr) cnt[j] = 0;
   }
   if (tid == kScanThreads - 1) base[n_seq] = s_warp[31];
 }
 
-cudaError_t launch_seq_partition(const int64_t* offs, int n_seq, int64_t T, int* base,
+cudaError_t launch_seq_partition(const int64_t* offs, int n_seq, int64_t T, int* base, int* cnt,
                                  cudaStream_t stream) {
-  seq_partition_kernel<<<1, kScanThreads, 0, stream>>>(offs, n_seq, T, base);
+  seq_partition_kernel<<<1, kScanThreads, 0, stream>>>(offs, n_seq, T, base, cnt);
   return cudaGetLastError();
 }
 
@@ -209,6 +213,7 @@ __global__ void __launch_bounds__(kCmpThreads)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;  // global part index
+  pdl_wait();  // the partition kernel's bases and zeroed tickets
   if (b >= __ldcg(base + n_seq)) return;
   const int j = part_sequence(base, n_seq, b);
   const int p = b - __ldcg(base + j);
@@ -400,7 +405,6 @@ __global__ void __launch_bounds__(kCmpThreads)
     }
   }
   if (lane != 0) return;
-  cnt[j] = 0;  // ready for the next call on this workspace
 
   tim_seq_stats st;
   memset(&st, 0, sizeof(st));
@@ -450,19 +454,30 @@ cudaError_t launch_seg_compare(const float* A, const float* B, const float* C,
   int* cnt = reinterpret_cast<int*>(ws + L.cnt_off);
   int* base = reinterpret_cast<int*>(ws + L.base_off);
   CmpPart* parts = reinterpret_cast<CmpPart*>(ws + L.part_off);
-  cudaError_t e = launch_seq_partition(offs, n_seq, T, base, stream);
+  cudaError_t e = launch_seq_partition(offs, n_seq, T, base, cnt, stream);
   if (e != cudaSuccess) return e;
   const bool vec = ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
                      reinterpret_cast<uintptr_t>(C)) & 15u) == 0 &&
                    (reinterpret_cast<uintptr_t>(mask) & 3u) == 0;
-  const dim3 grid(static_cast<unsigned>(seq_parts_bound(T, n_seq)));
+  // Programmatic dependent launch: the compare kernel launches while the
+  // partition kernel runs and waits for its results (griddepcontrol.wait).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(seq_parts_bound(T, n_seq)));
+  cfg.blockDim = dim3(kCmpThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (vec)
-    seg_compare_kernel<true><<<grid, kCmpThreads, 0, stream>>>(
-        A, B, C, offs, mask, T, n_seq, base, cap, ln_cap, out, tis_w, status, cnt, parts);
-  else
-    seg_compare_kernel<false><<<grid, kCmpThreads, 0, stream>>>(
-        A, B, C, offs, mask, T, n_seq, base, cap, ln_cap, out, tis_w, status, cnt, parts);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, seg_compare_kernel<true>, A, B, C, offs, mask, T, n_seq,
+                              static_cast<const int*>(base), cap, ln_cap, out, tis_w, status, cnt,
+                              parts);
+  return cudaLaunchKernelEx(&cfg, seg_compare_kernel<false>, A, B, C, offs, mask, T, n_seq,
+                            static_cast<const int*>(base), cap, ln_cap, out, tis_w, status, cnt,
+                            parts);
 }
 
 }  // namespace tim

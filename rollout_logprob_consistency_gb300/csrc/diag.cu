@@ -17,13 +17,13 @@
 //  - MIS: w 1[lo <= w <= hi], w = exp(d) ("Rollout-Training Mismatch in LLM RL",
 //    section 2.1); mean w^2 = mean exp(2d) (same page, section 5.3).
 //
-// Work split: the per-token sums run over many CTAs per sequence (each sequence
-// cut into P_j contiguous parts with P_j from its own length, as in the compare
-// kernel, so a sequence's results do not depend on the batch); each CTA
-// accumulates its tokens per thread in order, then a fixed xor-butterfly and
-// warp-order fold, and writes one partial record.
-// A second kernel runs four CTAs per sequence: one folds the P partials in part
-// order (deterministic) and writes every field but the quantiles; three gather
+// Work split, one launch: each sequence is cut into P_j contiguous parts with
+// P_j from its own length (as in the compare kernel, so a sequence's results do
+// not depend on the batch); a part CTA accumulates its tokens per thread in
+// order, then a fixed xor-butterfly and warp-order fold, writes one partial
+// record and draws a ticket on the sequence's counter, and the CTA with the last
+// ticket folds the P partials in part order (deterministic) into every field but
+// the quantiles.  Three more CTAs per sequence, independent of the parts, gather
 // one pair's |left - right| values of the active tokens into shared memory (any
 // order) as 64-bit keys (the bit patterns of non-negative doubles order like
 // the values, so selection is integer work) and find the order statistics the
@@ -37,9 +37,8 @@
 
 namespace tim {
 
-constexpr int kDiagThreads = 512;      // quantile / fold CTAs
-constexpr int kDiagPartThreads = 256;  // per-token partial CTAs
-constexpr int kDiagPartWarps = kDiagPartThreads / 32;
+constexpr int kDiagThreads = 512;  // every CTA: quantile selects and per-token parts
+constexpr int kDiagWarps = kDiagThreads / 32;
 constexpr int kQuantMax = TIM_DIAG_QUANTILE_MAX_TOKENS;
 constexpr size_t kDiagSmemBytes = static_cast<size_t>(kQuantMax) * sizeof(unsigned long long);
 
@@ -54,8 +53,11 @@ struct DiagPart {
   int flags;
   int pad;
 };
+static_assert(sizeof(DiagPart) % sizeof(unsigned long long) == 0, "DiagPart is staged in 8-byte words");
+static_assert(static_cast<size_t>(kSeqMaxParts) * sizeof(DiagPart) <= kDiagSmemBytes,
+              "a sequence's partials fit the shared key buffer");
 
-cudaError_t launch_seq_partition(const int64_t* offs, int n_seq, int64_t T, int* base,
+cudaError_t launch_seq_partition(const int64_t* offs, int n_seq, int64_t T, int* base, int* cnt,
                                  cudaStream_t stream);
 
 // |a - b| of two floats, as the bit pattern of the double (double)a - (double)b
@@ -102,31 +104,152 @@ __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
   return v;
 }
 
+// Warp totals of 8 per-lane doubles by recursive halving: at xor offsets 16, 8
+// and 4 a lane keeps half of its remaining sums (adding the partner's) and
+// hands the other half over, then offsets 2 and 1 finish the one it kept.
+// Each level adds the same two subtrees as a full xor butterfly, so every
+// total has the butterfly's bits, for 9 additions a lane instead of 40.
+// Returns the total of sum kind 4 (lane & 16 ? 1 : 0) + 2 (lane & 8 ? 1 : 0) +
+// (lane & 4 ? 1 : 0).
+__device__ __forceinline__ double warp_sum8_halving(const double (&v)[8], int lane) {
+  double w4[4], w2[2];
+  const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0, h4 = (lane & 4) != 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const double give = h16 ? v[i] : v[4 + i];
+    const double keep = h16 ? v[4 + i] : v[i];
+    w4[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, give, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const double give = h8 ? w4[i] : w4[2 + i];
+    const double keep = h8 ? w4[2 + i] : w4[i];
+    w2[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, give, 8);
+  }
+  double z = (h4 ? w2[1] : w2[0]) + __shfl_xor_sync(0xFFFFFFFFu, h4 ? w2[0] : w2[1], 4);
+  z += __shfl_xor_sync(0xFFFFFFFFu, z, 2);
+  z += __shfl_xor_sync(0xFFFFFFFFu, z, 1);
+  return z;
+}
+
 __device__ __forceinline__ bool offsets_ok(int64_t s, int64_t e, int64_t T) {
   return s >= 0 && s <= e && e <= T;
 }
 
-__global__ void __launch_bounds__(kDiagPartThreads)
-    seg_diag_part_kernel(const float* __restrict__ A, const float* __restrict__ B,
-                         const float* __restrict__ C, const int32_t* __restrict__ tA,
-                         const int32_t* __restrict__ tB, const int32_t* __restrict__ tC,
-                         const int64_t* __restrict__ offs, const uint8_t* __restrict__ mask,
-                         int64_t T, int n_seq, const int* __restrict__ base, double ln_lo,
-                         double ln_hi, DiagPart* __restrict__ parts) {
-  __shared__ double s_sum[kDiagPartWarps][kDiagSums];
-  __shared__ long long s_cnt[kDiagPartWarps][kDiagCounts];
-  __shared__ int s_flags[kDiagPartWarps];
+// Every field of sequence j's record but the quantiles, from its P partials
+// (staged in shared memory) folded in part order by one warp: lane i < 8 sums
+// partial field i, lanes 8-12 the counts, lane 13 ORs the flags; the quotients
+// and the exponential then run on separate lanes.
+__device__ void diag_fold(int j, bool ok_offs, const int32_t* __restrict__ tA,
+                          const int32_t* __restrict__ tB, const int32_t* __restrict__ tC,
+                          double cap, double ln_cap, const DiagPart* __restrict__ pj, int P,
+                          tim_seq_diag* __restrict__ o, int* status) {
+  const int lane = threadIdx.x & 31;
+  if (!ok_offs) {
+    if (lane == 0) {
+      tim_seq_diag st;
+      memset(&st, 0, sizeof(st));
+      for (int p = 0; p < 3; ++p) st.top1_flips[p] = -1;
+      st.flags = TIM_SEQ_BAD_OFFSETS;
+      *o = st;
+      set_status(status, TIM_ERR_INVALID_ARG);
+    }
+    return;
+  }
+  double acc = 0.0;
+  long long cacc = 0;
+  int facc = 0;
+  for (int q = 0; q < P; ++q) {  // part order
+    const DiagPart& r = pj[q];
+    if (lane < kDiagSums) acc += r.sum[lane];
+    else if (lane < kDiagSums + kDiagCounts) cacc += r.cnt[lane - kDiagSums];
+    else if (lane == kDiagSums + kDiagCounts) facc |= r.flags;
+  }
+  double S[kDiagSums];
+  long long N[kDiagCounts];
+#pragma unroll
+  for (int i = 0; i < kDiagSums; ++i) S[i] = __shfl_sync(0xFFFFFFFFu, acc, i);
+#pragma unroll
+  for (int i = 0; i < kDiagCounts; ++i) N[i] = __shfl_sync(0xFFFFFFFFu, cacc, kDiagSums + i);
+  const int F = __shfl_sync(0xFFFFFFFFu, facc, kDiagSums + kDiagCounts);
+  const long long n = N[0];
+  const bool ok = !(F & TIM_SEQ_BAD_MASK) && n > 0;
+  double v = 0.0;  // lane 0-2: probability MAE; 3: ratio error; 4: MIS; 5: w^2; 6: sequence TIS
+  if (ok && lane < 7) {
+    const double dn = static_cast<double>(n);
+    if (lane < 3) v = acc / dn;  // lane i < 8 holds S[i]
+    else if (lane == 3) v = S[5] / dn;
+    else if (lane == 4) v = S[6] / dn;
+    else if (lane == 5) v = S[7] / dn;
+    else v = S[3] > ln_cap ? cap : exp(S[3]);
+  }
+  double q[7];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) q[i] = __shfl_sync(0xFFFFFFFFu, v, i);
+  if (lane != 0) return;
+  // every field except the quantiles (written by the quantile CTAs)
+  o->reserved = 0;
+  for (int p = 0; p < 3; ++p) {
+    o->prob_mae[p] = 0.0;
+    o->top1_flips[p] = -1;
+  }
+  o->n_valid = 0;
+  o->log_ratio_sum = o->k1_sum = o->k3_sum = o->seq_tis = 0.0;
+  o->ratio_err_mean = o->mis_mean = o->w2_mean = 0.0;
+  o->mis_kept = 0;
+  if (F & TIM_SEQ_BAD_MASK) {
+    o->flags = TIM_SEQ_BAD_MASK;
+    set_status(status, TIM_ERR_BAD_MASK);
+  } else if (n == 0) {
+    o->flags = TIM_SEQ_EMPTY;
+    set_status(status, TIM_ERR_EMPTY_SEQUENCE);
+  } else {
+    o->n_valid = n;
+    for (int p = 0; p < 3; ++p) o->prob_mae[p] = q[p];
+    if (tA != nullptr && tB != nullptr) o->top1_flips[0] = N[2];
+    if (tB != nullptr && tC != nullptr) o->top1_flips[1] = N[3];
+    if (tA != nullptr && tC != nullptr) o->top1_flips[2] = N[4];
+    o->log_ratio_sum = S[3];
+    o->k1_sum = -S[3];
+    o->k3_sum = S[4];
+    o->seq_tis = q[6];
+    o->ratio_err_mean = q[3];
+    o->mis_mean = q[4];
+    o->mis_kept = N[1];
+    o->w2_mean = q[5];
+    int flags = F;
+    if (n > kQuantMax) flags |= TIM_SEQ_QUANTILE_SKIPPED;
+    if (!isfinite(S[4])) flags |= TIM_SEQ_K3_OVERFLOW;
+    o->flags = flags;
+    if (F & TIM_SEQ_NONFINITE) set_status(status, TIM_ERR_NONFINITE);
+  }
+}
+
+// One part of a sequence: its tokens' sums, then a ticket on the sequence's
+// counter; the CTA that draws the last ticket folds the sequence's parts.
+__device__ void diag_part(int b, unsigned long long* __restrict__ stage,
+                          const float* __restrict__ A, const float* __restrict__ B,
+                          const float* __restrict__ C, const int32_t* __restrict__ tA,
+                          const int32_t* __restrict__ tB, const int32_t* __restrict__ tC,
+                          const int64_t* __restrict__ offs, const uint8_t* __restrict__ mask,
+                          int64_t T, int n_seq, const int* __restrict__ base, double ln_lo,
+                          double ln_hi, double cap, double ln_cap, DiagPart* __restrict__ parts,
+                          int* __restrict__ cnt_seq, tim_seq_diag* __restrict__ out,
+                          int* status) {
+  __shared__ double s_sum[kDiagWarps][kDiagSums];
+  __shared__ long long s_cnt[kDiagWarps][kDiagCounts];
+  __shared__ int s_flags[kDiagWarps];
+  __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.x;  // global part index
   if (b >= __ldcg(base + n_seq)) return;
   const int j = part_sequence(base, n_seq, b);
   const int part = b - __ldcg(base + j);
   const int P = __ldcg(base + j + 1) - __ldcg(base + j);
   const int64_t s = offs[j], e = offs[j + 1];
-  if (!offsets_ok(s, e, T)) return;  // the fold CTA reports the sequence
-  const int64_t chunk = (e - s + P - 1) / P;
+  const bool ok_offs = offsets_ok(s, e, T);  // bad offsets: one part, no tokens
+  const int64_t chunk = ok_offs ? (e - s + P - 1) / P : 0;
   const int64_t t0 = s + static_cast<int64_t>(part) * chunk;
-  const int64_t t1 = t0 + chunk < e ? t0 + chunk : e;
+  const int64_t t1 = !ok_offs ? t0 : (t0 + chunk < e ? t0 + chunk : e);
 
   double sum[kDiagSums];
   long long cnt[kDiagCounts];
@@ -135,7 +258,7 @@ __global__ void __launch_bounds__(kDiagPartThreads)
 #pragma unroll
   for (int i = 0; i < kDiagCounts; ++i) cnt[i] = 0;
   int flags = 0;
-  for (int64_t t = t0 + tid; t < t1; t += kDiagPartThreads) {
+  for (int64_t t = t0 + tid; t < t1; t += kDiagThreads) {
     const uint8_t m = __ldg(mask + t);
     if (m > 1) flags |= TIM_SEQ_BAD_MASK;
     if (m != 1) continue;
@@ -161,133 +284,78 @@ __global__ void __launch_bounds__(kDiagPartThreads)
     if (tB != nullptr && tC != nullptr) cnt[3] += (__ldg(tB + t) != __ldg(tC + t)) ? 1 : 0;
     if (tA != nullptr && tC != nullptr) cnt[4] += (__ldg(tA + t) != __ldg(tC + t)) ? 1 : 0;
   }
+  // Only warps that held tokens reduce (their butterfly is fp64 work on a
+  // narrow pipe); a warp without tokens would only add exact zeros.
+  const int64_t n_tok = t1 - t0;
+  const int busy_warps =
+      n_tok >= static_cast<int64_t>(kDiagThreads) ? kDiagWarps : static_cast<int>((n_tok + 31) / 32);
+  static_assert(kDiagSums == 8, "the halving reduction is written for 8 sums");
+  if (warp < busy_warps) {
+    const double tot = warp_sum8_halving(sum, lane);
+    if ((lane & 3) == 0) s_sum[warp][((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1)] = tot;
+    // counts: at most a few million per warp, exact in 32-bit integer reductions
+    long long wc[kDiagCounts];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
+    for (int i = 0; i < kDiagCounts; ++i)
+      wc[i] = __reduce_add_sync(0xFFFFFFFFu, static_cast<unsigned>(cnt[i]));
+    const int wf = static_cast<int>(__reduce_or_sync(0xFFFFFFFFu, static_cast<unsigned>(flags)));
+    if (lane == 0) {
 #pragma unroll
-    for (int i = 0; i < kDiagSums; ++i) sum[i] += __shfl_xor_sync(0xFFFFFFFFu, sum[i], o);
-#pragma unroll
-    for (int i = 0; i < kDiagCounts; ++i) cnt[i] += __shfl_xor_sync(0xFFFFFFFFu, cnt[i], o);
-    flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, o);
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < kDiagSums; ++i) s_sum[warp][i] = sum[i];
-#pragma unroll
-    for (int i = 0; i < kDiagCounts; ++i) s_cnt[warp][i] = cnt[i];
-    s_flags[warp] = flags;
+      for (int i = 0; i < kDiagCounts; ++i) s_cnt[warp][i] = wc[i];
+      s_flags[warp] = wf;
+    }
   }
   __syncthreads();
-  if (tid != 0) return;
-  DiagPart r;
+  if (tid == 0) {
+    DiagPart r;
 #pragma unroll
-  for (int i = 0; i < kDiagSums; ++i) r.sum[i] = 0.0;
+    for (int i = 0; i < kDiagSums; ++i) r.sum[i] = 0.0;
 #pragma unroll
-  for (int i = 0; i < kDiagCounts; ++i) r.cnt[i] = 0;
-  r.flags = 0;
-  r.pad = 0;
-  for (int w = 0; w < kDiagPartWarps; ++w) {  // warp order
+    for (int i = 0; i < kDiagCounts; ++i) r.cnt[i] = 0;
+    r.flags = 0;
+    r.pad = 0;
+    for (int w = 0; w < busy_warps; ++w) {  // warp order
 #pragma unroll
-    for (int i = 0; i < kDiagSums; ++i) r.sum[i] += s_sum[w][i];
+      for (int i = 0; i < kDiagSums; ++i) r.sum[i] += s_sum[w][i];
 #pragma unroll
-    for (int i = 0; i < kDiagCounts; ++i) r.cnt[i] += s_cnt[w][i];
-    r.flags |= s_flags[w];
+      for (int i = 0; i < kDiagCounts; ++i) r.cnt[i] += s_cnt[w][i];
+      r.flags |= s_flags[w];
+    }
+    parts[b] = r;
+    __threadfence();
+    s_last = atomicAdd(&cnt_seq[j], 1) == P - 1;
   }
-  parts[b] = r;
+  __syncthreads();
+  if (!s_last) return;
+  // the last part CTA of sequence j: stage its P partials (written by other
+  // CTAs of this launch, so read through L2) and fold them on one warp
+  __threadfence();
+  constexpr int kWords = static_cast<int>(sizeof(DiagPart) / sizeof(unsigned long long));
+  const unsigned long long* src =
+      reinterpret_cast<const unsigned long long*>(parts + __ldcg(base + j));
+  for (int i = tid; i < P * kWords; i += kDiagThreads) stage[i] = __ldcg(src + i);
+  __syncthreads();
+  if (warp != 0) return;
+  diag_fold(j, ok_offs, tA, tB, tC, cap, ln_cap, reinterpret_cast<const DiagPart*>(stage), P,
+            out + j, status);
 }
 
-// blockIdx.y = 0, 1, 2: quantiles of pair p; blockIdx.y = 3: fold and the other fields.
-__global__ void __launch_bounds__(kDiagThreads)
-    seg_diag_final_kernel(const float* __restrict__ A, const float* __restrict__ B,
-                          const float* __restrict__ C, const int32_t* __restrict__ tA,
-                          const int32_t* __restrict__ tB, const int32_t* __restrict__ tC,
-                          const int64_t* __restrict__ offs, const uint8_t* __restrict__ mask,
-                          int64_t T, double cap, double ln_cap, const DiagPart* __restrict__ parts,
-                          const int* __restrict__ base, tim_seq_diag* __restrict__ out,
-                          int* status) {
-  extern __shared__ unsigned long long keys[];
+// Quantiles of pair p of sequence j (one CTA; keys: kQuantMax 64-bit slots).
+__device__ void diag_quantiles(int j, int p, unsigned long long* __restrict__ keys,
+                               const float* __restrict__ A, const float* __restrict__ B,
+                               const float* __restrict__ C, const int64_t* __restrict__ offs,
+                               const uint8_t* __restrict__ mask, int64_t T,
+                               tim_seq_diag* __restrict__ out) {
   __shared__ int s_fill, s_bad;
   __shared__ unsigned s_hist[3 * 256];  // radix-select digit counts per target
   __shared__ unsigned long long s_prefix[3], s_mask[3];
   __shared__ unsigned long long s_or[4], s_and[4];  // [q]: target q's candidates; [3]: all keys
-  __shared__ unsigned long long s_wmin[kDiagThreads / 32][6];
+  __shared__ unsigned long long s_wmin[kDiagWarps][6];
   __shared__ int s_rem[3], s_cnt[3], s_open[3];
   const int tid = threadIdx.x;
-  const int j = blockIdx.x, role = blockIdx.y;
   const int64_t s = offs[j], e = offs[j + 1];
   tim_seq_diag* o = out + j;
-  const bool ok_offs = offsets_ok(s, e, T);
-
-  if (role == 3) {
-    if (tid != 0) return;
-    if (!ok_offs) {
-      tim_seq_diag st;
-      memset(&st, 0, sizeof(st));
-      for (int p = 0; p < 3; ++p) st.top1_flips[p] = -1;
-      st.flags = TIM_SEQ_BAD_OFFSETS;
-      *o = st;
-      set_status(status, TIM_ERR_INVALID_ARG);
-      return;
-    }
-    double S[kDiagSums];
-    long long N[kDiagCounts];
-    int F = 0;
-#pragma unroll
-    for (int i = 0; i < kDiagSums; ++i) S[i] = 0.0;
-#pragma unroll
-    for (int i = 0; i < kDiagCounts; ++i) N[i] = 0;
-    const int q0 = __ldcg(base + j), q1 = __ldcg(base + j + 1);
-    for (int q = q0; q < q1; ++q) {  // part order
-      const DiagPart& r = parts[q];
-#pragma unroll
-      for (int i = 0; i < kDiagSums; ++i) S[i] += r.sum[i];
-#pragma unroll
-      for (int i = 0; i < kDiagCounts; ++i) N[i] += r.cnt[i];
-      F |= r.flags;
-    }
-    const long long n = N[0];
-    // every field except the quantiles (written by the other three CTAs)
-    o->reserved = 0;
-    for (int p = 0; p < 3; ++p) {
-      o->prob_mae[p] = 0.0;
-      o->top1_flips[p] = -1;
-    }
-    o->n_valid = 0;
-    o->log_ratio_sum = o->k1_sum = o->k3_sum = o->seq_tis = 0.0;
-    o->ratio_err_mean = o->mis_mean = o->w2_mean = 0.0;
-    o->mis_kept = 0;
-    if (F & TIM_SEQ_BAD_MASK) {
-      o->flags = TIM_SEQ_BAD_MASK;
-      set_status(status, TIM_ERR_BAD_MASK);
-    } else if (n == 0) {
-      o->flags = TIM_SEQ_EMPTY;
-      set_status(status, TIM_ERR_EMPTY_SEQUENCE);
-    } else {
-      const double dn = static_cast<double>(n);
-      o->n_valid = n;
-      for (int p = 0; p < 3; ++p) o->prob_mae[p] = S[p] / dn;
-      if (tA != nullptr && tB != nullptr) o->top1_flips[0] = N[2];
-      if (tB != nullptr && tC != nullptr) o->top1_flips[1] = N[3];
-      if (tA != nullptr && tC != nullptr) o->top1_flips[2] = N[4];
-      o->log_ratio_sum = S[3];
-      o->k1_sum = -S[3];
-      o->k3_sum = S[4];
-      o->seq_tis = S[3] > ln_cap ? cap : exp(S[3]);
-      o->ratio_err_mean = S[5] / dn;
-      o->mis_mean = S[6] / dn;
-      o->mis_kept = N[1];
-      o->w2_mean = S[7] / dn;
-      int flags = F;
-      if (n > kQuantMax) flags |= TIM_SEQ_QUANTILE_SKIPPED;
-      if (!isfinite(S[4])) flags |= TIM_SEQ_K3_OVERFLOW;
-      o->flags = flags;
-      if (F & TIM_SEQ_NONFINITE) set_status(status, TIM_ERR_NONFINITE);
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------------ quantiles of pair p
-  const int p = role;
-  if (!ok_offs) return;  // the fold CTA writes the whole record
+  if (!offsets_ok(s, e, T)) return;  // the fold writes the whole record
   if (tid == 0) {
     s_fill = 0;
     s_bad = 0;
@@ -496,7 +564,7 @@ __global__ void __launch_bounds__(kDiagThreads)
     double r[3];
     for (int qi = 0; qi < 3; ++qi) {
       unsigned long long klo = ~0ull, kup = ~0ull;
-      for (int w = 0; w < kDiagThreads / 32; ++w) {
+      for (int w = 0; w < kDiagWarps; ++w) {
         klo = s_wmin[w][qi] < klo ? s_wmin[w][qi] : klo;
         kup = s_wmin[w][3 + qi] < kup ? s_wmin[w][3 + qi] : kup;
       }
@@ -515,10 +583,38 @@ __global__ void __launch_bounds__(kDiagThreads)
   }
 }
 
-// Diagnostics workspace: status | part bases int32 [S + 1] | parts.
+// One launch: blocks [0, 3 S) select the quantiles of (sequence b / 3, pair
+// b % 3), the rest compute the per-token sums part by part (the quantile CTAs
+// come first so the longest work starts first; the two kinds share no data).
+// The kernel is launched programmatically behind the partition kernel: only
+// the part CTAs wait for the bases (griddepcontrol.wait).
+__global__ void __launch_bounds__(kDiagThreads)
+    seg_diag_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                    const float* __restrict__ C, const int32_t* __restrict__ tA,
+                    const int32_t* __restrict__ tB, const int32_t* __restrict__ tC,
+                    const int64_t* __restrict__ offs, const uint8_t* __restrict__ mask, int64_t T,
+                    int n_seq, const int* __restrict__ base, double ln_lo, double ln_hi,
+                    double cap, double ln_cap, DiagPart* __restrict__ parts,
+                    int* __restrict__ cnt_seq, tim_seq_diag* __restrict__ out, int* status) {
+  extern __shared__ unsigned long long keys[];
+  const int b = static_cast<int>(blockIdx.x);
+  if (b < 3 * n_seq) {
+    diag_quantiles(b / 3, b % 3, keys, A, B, C, offs, mask, T, out);
+  } else {
+    pdl_wait();  // the partition kernel's bases and zeroed counters
+    diag_part(b - 3 * n_seq, keys, A, B, C, tA, tB, tC, offs, mask, T, n_seq, base, ln_lo, ln_hi, cap,
+              ln_cap, parts, cnt_seq, out, status);
+  }
+}
+
+// Diagnostics workspace: status | part bases int32 [S + 1] | per-sequence part
+// counters int32 [S] (zeroed by the partition kernel of each call) | parts.
 size_t diag_base_offset() { return 1024; }
+size_t diag_counter_offset(int n_seq) {
+  return align_up(diag_base_offset() + static_cast<size_t>(n_seq + 1) * 4, 256);
+}
 size_t diag_parts_offset(int n_seq) {
-  return align_up(1024 + static_cast<size_t>(n_seq + 1) * 4, 1024);
+  return align_up(diag_counter_offset(n_seq) + static_cast<size_t>(n_seq) * 4, 1024);
 }
 size_t diag_workspace_bytes(int64_t T, int n_seq) {
   return align_up(diag_parts_offset(n_seq) +
@@ -536,21 +632,28 @@ cudaError_t launch_seg_diag(const float* A, const float* B, const float* C, cons
   int* base = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + diag_base_offset());
   DiagPart* parts =
       reinterpret_cast<DiagPart*>(static_cast<uint8_t*>(workspace) + diag_parts_offset(n_seq));
-  cudaError_t err = launch_seq_partition(offs, n_seq, T, base, stream);
+  int* cnt_seq =
+      reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + diag_counter_offset(n_seq));
+  cudaError_t err = launch_seq_partition(offs, n_seq, T, base, cnt_seq, stream);
   if (err != cudaSuccess) return err;
-  seg_diag_part_kernel<<<static_cast<unsigned>(seq_parts_bound(T, n_seq)), kDiagPartThreads, 0,
-                         stream>>>(A, B, C, tA, tB, tC, offs, mask, T, n_seq, base,
-                                   std::log(static_cast<double>(mis_lo)),
-                                   std::log(static_cast<double>(mis_hi)), parts);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(seg_diag_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  err = cudaFuncSetAttribute(seg_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kDiagSmemBytes));
   if (err != cudaSuccess) return err;
-  seg_diag_final_kernel<<<dim3(static_cast<unsigned>(n_seq), 4), kDiagThreads, kDiagSmemBytes,
-                          stream>>>(A, B, C, tA, tB, tC, offs, mask, T, cap, std::log(cap), parts,
-                                    base, out, status);
-  return cudaGetLastError();
+  const int64_t blocks = 3 * static_cast<int64_t>(n_seq) + seq_parts_bound(T, n_seq);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kDiagThreads);
+  cfg.dynamicSmemBytes = kDiagSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, seg_diag_kernel, A, B, C, tA, tB, tC, offs, mask, T, n_seq,
+                            static_cast<const int*>(base), std::log(static_cast<double>(mis_lo)),
+                            std::log(static_cast<double>(mis_hi)), cap, std::log(cap), parts,
+                            cnt_seq, out, status);
 }
 
 }  // namespace tim
