@@ -229,3 +229,23 @@ def test_diag_quantiles_exact_on_ties_tiny_and_maximal_sequences(tim):
         assert x["flags"] == y["flags"] and x["n_valid"] == y["n_valid"], j
         for k in ("abs_q50", "abs_q95", "abs_q99"):
             assert x[k] == y[k], (j, k, x[k], y[k])
+
+
+def test_diag_and_compare_one_sequence_past_the_part_cap(tim):
+    """A 300000-token sequence: its part count is capped at 256, so every part holds
+    more than 512 tokens (each thread loops, all warps reduce); the quantiles are
+    skipped (more than the maximum active tokens) and flagged."""
+    from parity import assert_compare_parity
+    T = 300000
+    A, B, C, _, _, tops = make_case(T, 41)
+    offs = np.array([0, T], np.int64)
+    mask = (np.random.default_rng(42).random(T) < 0.9).astype(np.uint8)
+    g = run(tim, A, B, C, offs, mask, tops)
+    r, errs = oracle.oracle_diag_lenient(A, B, C, offs, mask, 2.0, 0.5, 1.5, tops)
+    assert not errs and g[0]["flags"] & oracle.FLAG_QUANTILE_SKIPPED
+    assert_diag_parity(g, r, d_abs(A, C, offs, mask), what="past the cap")
+    stats, w = tim.compare(cuda_tensor(A), cuda_tensor(B), cuda_tensor(C), cuda_tensor(offs),
+                           cuda_tensor(mask), 2.0)
+    ro, rw, errs = oracle.oracle_compare_lenient(A, B, C, offs, mask, 2.0)
+    assert not errs
+    assert_compare_parity(tim.stats_to_dicts(stats), ro, what="past the cap")
