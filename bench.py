@@ -35,9 +35,9 @@ L2_NOTE = "inputs larger than L2 (W 1.245 GB + hidden 268 MB per step vs 129 MB 
 # measured by a one-pass ncu capture of the full-size launch
 # (profiles/lmhead_lse_T32768_dram.md): 8.902 GB read + 0.315 GB written.  Valid
 # only for the kernel sources hashed here and for T = 32768.
-TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "e1071b32f80aad00",
+TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "d204a229d3244d06",
                                 "tim_common.cuh": "f67b058262e5bfe0"},
-                       T=32768, bytes=8.902e9 + 315.20e6)
+                       T=32768, bytes=8.91e9 + 315.52e6)
 
 
 def traffic_per_launch(T):
@@ -677,7 +677,7 @@ def main():
         extras["backward_dy_dW"] = dict(
             ms=round(bms, 3), tokens_per_s=round(T / (bms / 1e3), 1),
             TFLOPs=round(3 * 2.0 * T * d * V / (bms / 1e3) / 1e12, 1),
-            note="three GEMMs (logit recompute, G.W, G^T.y) + transposes; workspace "
+            note="three GEMMs (logit recompute writing G once, G.W and G^T.y reading G, W and y in place); workspace "
                  f"{bws.nbytes / 1e9:.1f} GB",
             rmsnorm_backward_ms=round(rms_ms, 3),
             rmsnorm_backward_GBps=round(rms_bytes / (rms_ms / 1e3) / 1e9, 1))

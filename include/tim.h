@@ -330,8 +330,9 @@ tim_status tim_logprob_fp32(const void *hidden, const void *gamma, const float *
  * whose token id is outside [0, V) contributes nothing and records
  * TIM_ERR_TOKEN_RANGE.  Each out_dy row depends only on its own row (batch-
  * invariant); out_dW sums over the rows in a fixed order.
- * Workspace: tim_logprob_backward_workspace_size(T, d, V) bytes (it holds G in
- * both layouts: about 4 T V bytes), 256-byte aligned, zero-initialised once;
+ * Workspace: tim_logprob_backward_workspace_size(T, d, V) bytes (it holds y and
+ * G, about 2 T V bytes: the two products read G, W and y where they lie, G and y
+ * as MN-major operands), 256-byte aligned, zero-initialised once;
  * T up to 4.19 M rows and V up to 4.19 M.  Errors as tim_logprob.
  * ------------------------------------------------------------------------ */
 size_t tim_logprob_backward_workspace_size(int64_t T, int32_t d, int32_t V);

@@ -37,13 +37,12 @@ cudaError_t launch_lmhead_lse_tf32x3(const float* y_big, const float* y_small, c
                                      int* status, cudaStream_t stream, int num_sms);
 cudaError_t launch_logit_grad(const void* y, const void* W, const int32_t* ids, const float* lse,
                               const float* gup, int64_t T, int d, int V, float temperature,
-                              uint16_t* gz, int64_t ldg, uint16_t* gzt, int64_t ldgt, int* status,
-                              cudaStream_t stream, int num_sms);
-cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, const void* B, int N,
-                              int64_t ldb, int64_t K, int64_t M, float* C, int64_t ldc,
-                              int accumulate, int* status, cudaStream_t stream, int num_sms);
-cudaError_t launch_transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in,
-                                  void* out, int64_t ld_out, cudaStream_t stream);
+                              uint16_t* gz, int64_t ldg, int* status, cudaStream_t stream,
+                              int num_sms);
+cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, int a_mn, const void* B,
+                              int N, int64_t ldb, int b_mn, int64_t K, int64_t M, float* C,
+                              int64_t ldc, int accumulate, int* status, cudaStream_t stream,
+                              int num_sms);
 cudaError_t launch_wait_selftest(const void* y, const void* W, const int32_t* ids, int64_t T,
                                  int d, int V, void* part, float* tgt, int* status,
                                  uint64_t limit_ns, cudaStream_t stream, int num_sms);
@@ -209,9 +208,10 @@ Fp32Layout fp32_layout(int64_t T, int32_t d, int32_t V) {
 
 // Backward workspace: status | y bf16 [Tp, d] | y^T [d, Tp] | W^T [d, Vp] |
 // G [Tp, Vp] | G^T [Vp, Tp], with Tp = rows_padded(T) and Vp = V rounded up to 64.
+// Backward workspace: status | y bf16 [Tp][d] | G bf16 [Tp][Vp].
 struct BwdLayout {
   int64_t Tp, Vp;
-  size_t status_off, y_off, yt_off, wt_off, g_off, gt_off, total;
+  size_t status_off, y_off, g_off, total;
 };
 BwdLayout backward_layout(int64_t T, int32_t d, int32_t V) {
   BwdLayout B;
@@ -220,11 +220,8 @@ BwdLayout backward_layout(int64_t T, int32_t d, int32_t V) {
   const size_t dd = static_cast<size_t>(d);
   B.status_off = 0;
   B.y_off = 1024;
-  B.yt_off = align_up(B.y_off + static_cast<size_t>(B.Tp) * dd * 2, 1024);
-  B.wt_off = align_up(B.yt_off + dd * static_cast<size_t>(B.Tp) * 2, 1024);
-  B.g_off = align_up(B.wt_off + dd * static_cast<size_t>(B.Vp) * 2, 1024);
-  B.gt_off = align_up(B.g_off + static_cast<size_t>(B.Tp) * static_cast<size_t>(B.Vp) * 2, 1024);
-  B.total = align_up(B.gt_off + static_cast<size_t>(B.Vp) * static_cast<size_t>(B.Tp) * 2, 1024);
+  B.g_off = align_up(B.y_off + static_cast<size_t>(B.Tp) * dd * 2, 1024);
+  B.total = align_up(B.g_off + static_cast<size_t>(B.Tp) * static_cast<size_t>(B.Vp) * 2, 1024);
   return B;
 }
 
@@ -521,26 +518,22 @@ tim_status tim_logprob_backward(const void* hidden, const void* gamma, const voi
   uint8_t* b = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(b + B.status_off);
   uint16_t* y = reinterpret_cast<uint16_t*>(b + B.y_off);
-  uint16_t* yt = reinterpret_cast<uint16_t*>(b + B.yt_off);
-  uint16_t* wt = reinterpret_cast<uint16_t*>(b + B.wt_off);
   uint16_t* gz = reinterpret_cast<uint16_t*>(b + B.g_off);
-  uint16_t* gzt = reinterpret_cast<uint16_t*>(b + B.gt_off);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // y exactly as the forward computes it (same kernel), then the operand layouts
+  // y exactly as the forward computes it (same kernel)
   if (launch_rmsnorm_rows(hidden, gamma, T, d, eps, y, status, st) != cudaSuccess)
     return TIM_ERR_CUDA;
-  if (launch_transpose_bf16(y, B.Tp, d, d, yt, B.Tp, st) != cudaSuccess) return TIM_ERR_CUDA;
-  if (launch_transpose_bf16(W, V, d, d, wt, B.Vp, st) != cudaSuccess) return TIM_ERR_CUDA;
-  // G = dL/dz from the recomputed logits
-  if (launch_logit_grad(y, W, token_ids, lse, grad_logprob, T, d, V, temperature, gz, B.Vp, gzt,
-                        B.Tp, status, st, sms) != cudaSuccess)
+  // G = dL/dz from the recomputed logits, row-major [Tp][Vp]
+  if (launch_logit_grad(y, W, token_ids, lse, grad_logprob, T, d, V, temperature, gz, B.Vp,
+                        status, st, sms) != cudaSuccess)
     return TIM_ERR_CUDA;
-  // dL/dy = G . W  (A = G [Tp, V], B = W^T [d, V])
-  if (launch_gemm_store(gz, B.Tp, B.Vp, wt, d, B.Vp, V, T, out_dy, d, 0, status, st, sms) !=
+  // dL/dy = G . W: A = G K-major [Tp][Vp] (K = V), B = W read MN-major ([V][d], d contiguous)
+  if (launch_gemm_store(gz, B.Tp, B.Vp, 0, W, d, d, 1, V, T, out_dy, d, 0, status, st, sms) !=
       cudaSuccess)
     return TIM_ERR_CUDA;
-  // dL/dW = G^T . y  (A = G^T [V, Tp], B = y^T [d, Tp])
-  return from_cuda(launch_gemm_store(gzt, V, B.Tp, yt, d, B.Tp, B.Tp, V, out_dW, d, accumulate_dW,
+  // dL/dW = G^T . y: A = G read MN-major ([T][Vp], V contiguous; K = T), B = y read
+  // MN-major ([T][d], d contiguous)
+  return from_cuda(launch_gemm_store(gz, V, B.Vp, 1, y, d, d, 1, T, V, out_dW, d, accumulate_dW,
                                      status, st, sms));
 }
 
@@ -657,8 +650,6 @@ tim_status tim_processed_logprob_head(const void* hidden, const void* gamma, con
   uint8_t* b = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(b + P.base.status_off);
   void* y = b + P.base.y_off;
-  void* part = b + P.base.part_off;
-  float* tgt = reinterpret_cast<float*>(b + P.base.tgt_off);
   float* thr = reinterpret_cast<float*>(b + P.thr_off);
   int* cnt = reinterpret_cast<int*>(b + P.cnt_off);
   void* cand = b + P.cand_off;
@@ -669,8 +660,6 @@ tim_status tim_processed_logprob_head(const void* hidden, const void* gamma, con
   int* fb_n = reinterpret_cast<int*>(b + P.fbn_off);
   int* fb_rows = reinterpret_cast<int*>(b + P.fbrows_off);
   void* y_fb = b + P.yfb_off;
-  (void)part;
-  (void)tgt;
   if (launch_lmhead_top4(y, W, token_ids, T, d, V, top4, status, st, sms) != cudaSuccess)
     return TIM_ERR_CUDA;
   if (cudaMemsetAsync(fb_n, 0, sizeof(int), st) != cudaSuccess) return TIM_ERR_CUDA;

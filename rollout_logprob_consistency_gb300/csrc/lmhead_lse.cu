@@ -84,19 +84,20 @@ struct GemmArgs {
   // e4m3 operands only: per-row scales of y and per-vocabulary-row scales of W
   const float* sy;
   const float* sw;
-  // logit-gradient mode only: forward lse [T] and upstream gradient [T]; outputs
-  // G = dL/dz in bf16, row-major [rows_padded(T)][ldg] and transposed [V][ldgt]
+  // logit-gradient mode only: forward lse [T] and upstream gradient [T]; output
+  // G = dL/dz in bf16, row-major [rows_padded(T)][ldg]
   const float* lse;
   const float* gup;
   uint16_t* gz;
   int64_t ldg;
-  uint16_t* gzt;
-  int64_t ldgt;
   // store mode only: C fp32 [T][ldc] (T = rows of A, v_end = columns), C = A.B^T
-  // or C += A.B^T
+  // or C += A.B^T; a_mn / b_mn: that operand is stored MN-major ([K][rows],
+  // rows contiguous) instead of K-major
   float* c;
   int64_t ldc;
   int accumulate;
+  int a_mn;
+  int b_mn;
   // bounded-wait limit of every mbarrier wait; the wait self-test shortens it and
   // sets stall_producer so that no load is ever issued
   uint64_t wait_limit_ns;
@@ -148,6 +149,26 @@ constexpr size_t kGradStageBytes = kEpiWarps * 32 * 64;
 
 __host__ __device__ constexpr size_t gemm_smem_bytes(int mode) {
   return kGemmSmemBytes + (mode == 2 ? kGradStageBytes : 0);
+}
+
+// MN-major operand tile (store mode): boxes of 64 rows of K x 64 bf16 of M or N
+// (128-byte rows, 128-byte swizzle), one box per 64 elements of M or N.
+constexpr int kMnChunkBytes = 64 * 128;
+
+// Shared-memory descriptor of an MN-major 128-byte-swizzled bf16 tile: within
+// an 8-row atom (1024 bytes) each row holds 64 consecutive elements of M or N
+// for one k; the leading-dimension offset steps to the next 64 elements of M or
+// N (the next box, kMnChunkBytes), the stride-dimension offset to the next 8
+// rows of K (1024 bytes).  Checked bit for bit against a CPU product on
+// small-integer tiles for A, B and both MN-major.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr) {
+  uint64_t desc = 0;
+  desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  desc |= static_cast<uint64_t>(kMnChunkBytes >> 4) << 16;
+  desc |= static_cast<uint64_t>(1024u >> 4) << 32;
+  desc |= static_cast<uint64_t>(1u) << 46;
+  desc |= static_cast<uint64_t>(2u) << 61;
+  return desc;
 }
 
 __device__ __forceinline__ void tile_coords(int64_t tile, const GemmArgs& a, int& m, int& n) {
@@ -289,6 +310,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && !a.stall_producer) {
+      // One stage of each operand: a K-major tile is one box (128-byte rows of K,
+      // 8-row swizzle atoms); an MN-major tile (store mode) is boxes of 64 rows of
+      // K x 64 elements of M or N, placed kMnChunkBytes apart.
+      auto load_a = [&](int st, int kb, int m) {
+        uint8_t* dst = sA + st * G::kStageA;
+        if constexpr (kMode == 3) {
+          if (a.a_mn) {
+#pragma unroll
+            for (int c = 0; c < kBM / 64; ++c)
+              tma_load_2d(dst + c * kMnChunkBytes, &tmap_y, m * kBM + c * 64, kb * kKElems,
+                          &full[st]);
+            return;
+          }
+        }
+        tma_load_2d(dst, &tmap_y, kb * kKElems, m * kBM, &full[st]);
+        if (kX3) tma_load_2d(dst + kABytes, &tmap_y2, kb * kKElems, m * kBM, &full[st]);
+      };
+      auto load_b = [&](int st, int kb, int n) {
+        uint8_t* dst = sB + st * G::kStageB;
+        if constexpr (kMode == 3) {
+          if (a.b_mn) {
+#pragma unroll
+            for (int c = 0; c < kBN / 64; ++c)
+              tma_load_2d(dst + c * kMnChunkBytes, &tmap_w, n * kBN + c * 64, kb * kKElems,
+                          &full[st]);
+            return;
+          }
+        }
+        tma_load_2d(dst, &tmap_w, kb * kKElems, n * kBN, &full[st]);
+        if (kX3) tma_load_2d(dst + kBBytes, &tmap_w2, kb * kKElems, n * kBN, &full[st]);
+      };
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -304,15 +356,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int pre = min(G::kS, a.num_kb);
           for (int s = 0; s < pre; ++s) {
             mbar_arrive_expect_tx(&full[s], kTx);
-            tma_load_2d(sB + s * G::kStageB, &tmap_w, s * kKElems, n * kBN, &full[s]);
-            if (kX3)
-              tma_load_2d(sB + s * G::kStageB + kBBytes, &tmap_w2, s * kKElems, n * kBN, &full[s]);
+            load_b(s, s, n);
           }
           pdl_wait();
           for (int s = 0; s < pre; ++s) {
-            tma_load_2d(sA + s * G::kStageA, &tmap_y, s * kKElems, m * kBM, &full[s]);
-            if (kX3)
-              tma_load_2d(sA + s * G::kStageA + kABytes, &tmap_y2, s * kKElems, m * kBM, &full[s]);
+            load_a(s, s, m);
             last_parity[s] = 0;
           }
           stage = pre % G::kS;
@@ -326,14 +374,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], kTx);
-          tma_load_2d(sA + stage * G::kStageA, &tmap_y, kb * kKElems, m * kBM, &full[stage]);
-          tma_load_2d(sB + stage * G::kStageB, &tmap_w, kb * kKElems, n * kBN, &full[stage]);
-          if (kX3) {
-            tma_load_2d(sA + stage * G::kStageA + kABytes, &tmap_y2, kb * kKElems, m * kBM,
-                        &full[stage]);
-            tma_load_2d(sB + stage * G::kStageB + kBBytes, &tmap_w2, kb * kKElems, n * kBN,
-                        &full[stage]);
-          }
+          load_a(stage, kb, m);
+          load_b(stage, kb, n);
           last_parity[stage] = ph;
           if (++stage == G::kS) {
             stage = 0;
@@ -347,9 +389,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = kFp8  ? umma_idesc_e4m3_f32(kBM, kBN)
-                             : kX3 ? umma_idesc_tf32_f32(kBM, kBN)
-                                   : umma_idesc_bf16_f32(kBM, kBN);
+      uint32_t idesc = kFp8  ? umma_idesc_e4m3_f32(kBM, kBN)
+                       : kX3 ? umma_idesc_tf32_f32(kBM, kBN)
+                             : umma_idesc_bf16_f32(kBM, kBN);
+      if constexpr (kMode == 3)  // bits 15 / 16: A / B major (1 = MN)
+        idesc |= (a.a_mn ? (1u << 15) : 0u) | (a.b_mn ? (1u << 16) : 0u);
       int stage = 0;
       uint32_t ph = 0;
       uint32_t acc = 0, acc_ph = 0;
@@ -389,8 +433,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               umma_tf32(d_tmem + kBN, ab, bs, idesc, acc_k);
               umma_tf32(d_tmem + kBN, as, bb, idesc, 1u);
             } else {
-              umma_bf16(d_tmem, sw128_kmajor_desc(a0 + k * 32), sw128_kmajor_desc(b0 + k * 32),
-                        idesc, acc_k);
+              uint64_t ad = sw128_kmajor_desc(a0 + k * 32);
+              uint64_t bd = sw128_kmajor_desc(b0 + k * 32);
+              if constexpr (kMode == 3) {  // 16 K-rows of an MN-major tile: 2 atoms
+                if (a.a_mn) ad = sw128_mnmajor_desc(a0 + k * 2048);
+                if (a.b_mn) bd = sw128_mnmajor_desc(b0 + k * 2048);
+              }
+              umma_bf16(d_tmem, ad, bd, idesc, acc_k);
             }
           }
           umma_commit(&empty[stage]);
@@ -496,11 +545,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(gv[0]));
             const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(gv[1]));
             packed[j >> 1] = lo | (hi << 16);
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-              if (j + u < nvalid)
-                st_global_u16_hint(a.gzt + static_cast<int64_t>(col0 + j + u) * a.ldgt + row,
-                                   static_cast<uint16_t>(u ? hi : lo), pol);
           }
 #pragma unroll
           for (int w = 0; w < 4; ++w)
@@ -688,6 +732,24 @@ static bool make_bf16_map(CUtensorMap* map, const void* base, uint64_t rows, uin
   return r == CUDA_SUCCESS;
 }
 
+// bf16 operand stored MN-major: [K][ld] with its mn_extent rows of the product
+// (M or N) contiguous; box = 64 elements of M or N x 64 rows of K, 128-byte
+// swizzle; elements past mn_extent or rows past k_extent read as zeros.
+static bool make_bf16_mn_map(CUtensorMap* map, const void* base, uint64_t mn_extent,
+                             uint64_t k_extent, uint64_t ld) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {mn_extent, k_extent};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int kMode, int kPrec>
 static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_w,
                                const CUtensorMap& map_y2, const CUtensorMap& map_w2,
@@ -757,11 +819,11 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   a.gup = nullptr;
   a.gz = nullptr;
   a.ldg = 0;
-  a.gzt = nullptr;
-  a.ldgt = 0;
   a.c = nullptr;
   a.ldc = 0;
   a.accumulate = 0;
+  a.a_mn = 0;
+  a.b_mn = 0;
   a.wait_limit_ns = kWaitLimitNs;
   a.stall_producer = 0;
   a.top4 = nullptr;
@@ -855,8 +917,6 @@ cudaError_t launch_lmhead_collect(const void* y, const void* W, const int32_t* i
   return launch_gemm<1, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }
 
-// Backward, step 1: recompute z = y . W^T and write G = dL/dz (bf16) as
-// gz [rows_padded(T)][ldg] and gzt [V][ldgt] (ldgt >= rows_padded(T)).
 // Processed score, pass 1: the four largest logits of every (row, 256-column
 // tile) with their ids, as Top4 records [ceil(T/32)][num_n][32].
 cudaError_t launch_lmhead_top4(const void* y, const void* W, const int32_t* ids, int64_t T, int d,
@@ -869,10 +929,12 @@ cudaError_t launch_lmhead_top4(const void* y, const void* W, const int32_t* ids,
   return launch_gemm<4, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }
 
+// Backward, step 1: recompute z = y . W^T and write G = dL/dz (bf16) as
+// gz [rows_padded(T)][ldg] (rows past T written as zeros).
 cudaError_t launch_logit_grad(const void* y, const void* W, const int32_t* ids, const float* lse,
                               const float* gup, int64_t T, int d, int V, float temperature,
-                              uint16_t* gz, int64_t ldg, uint16_t* gzt, int64_t ldgt, int* status,
-                              cudaStream_t stream, int num_sms) {
+                              uint16_t* gz, int64_t ldg, int* status, cudaStream_t stream,
+                              int num_sms) {
   CUtensorMap map_y, map_w;
   GemmArgs a;
   cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, 0, temperature, status);
@@ -881,23 +943,28 @@ cudaError_t launch_logit_grad(const void* y, const void* W, const int32_t* ids, 
   a.gup = gup;
   a.gz = gz;
   a.ldg = ldg;
-  a.gzt = gzt;
-  a.ldgt = ldgt;
   return launch_gemm<2, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }
 
-// Backward, steps 2 and 3: C [M][N] (+)= A . B^T with A bf16 [M][K] (row stride
-// lda, rows_a >= M rows readable) and B bf16 [N][K] (row stride ldb); fp32 C
-// with row stride ldc.  N a multiple of 32.
-cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, const void* B, int N,
-                              int64_t ldb, int64_t K, int64_t M, float* C, int64_t ldc,
-                              int accumulate, int* status, cudaStream_t stream, int num_sms) {
+// Backward, steps 2 and 3: C [M][N] (+)= A . B^T, fp32 C with row stride ldc,
+// N a multiple of 32.  A (M x K) is bf16 K-major [M][lda] (a_mn = 0; rows_a >= M
+// rows readable) or MN-major [K][lda] (a_mn = 1; M contiguous); likewise B (N x
+// K) is [N][ldb] (b_mn = 0) or [K][ldb] (b_mn = 1).  The MN-major forms let the
+// products read G, W and y where they lie, with no transposed copies.
+cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, int a_mn, const void* B,
+                              int N, int64_t ldb, int b_mn, int64_t K, int64_t M, float* C,
+                              int64_t ldc, int accumulate, int* status, cudaStream_t stream,
+                              int num_sms) {
   CUtensorMap map_a, map_b;
-  if (!make_bf16_map(&map_a, A, static_cast<uint64_t>(rows_a), static_cast<uint64_t>(K),
-                     static_cast<uint64_t>(lda), kBM) ||
-      !make_bf16_map(&map_b, B, static_cast<uint64_t>(N), static_cast<uint64_t>(K),
-                     static_cast<uint64_t>(ldb), kBN))
-    return cudaErrorInvalidValue;
+  const bool ok_a = a_mn ? make_bf16_mn_map(&map_a, A, static_cast<uint64_t>(M),
+                                            static_cast<uint64_t>(K), static_cast<uint64_t>(lda))
+                         : make_bf16_map(&map_a, A, static_cast<uint64_t>(rows_a),
+                                         static_cast<uint64_t>(K), static_cast<uint64_t>(lda), kBM);
+  const bool ok_b = b_mn ? make_bf16_mn_map(&map_b, B, static_cast<uint64_t>(N),
+                                            static_cast<uint64_t>(K), static_cast<uint64_t>(ldb))
+                         : make_bf16_map(&map_b, B, static_cast<uint64_t>(N),
+                                         static_cast<uint64_t>(K), static_cast<uint64_t>(ldb), kBN);
+  if (!ok_a || !ok_b) return cudaErrorInvalidValue;
   GemmArgs a = {};
   a.T = M;
   a.v0 = 0;
@@ -906,11 +973,12 @@ cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, const 
   a.num_m = static_cast<int>((M + kBM - 1) / kBM);
   a.num_n = (N + kBN - 1) / kBN;
   a.num_kb = static_cast<int>((K + kBK - 1) / kBK);
-  // Raster groups of 16 row tiles: with K = V or K = T the operand panels of a
-  // tile (128 or 256 rows x K) are megabytes long, and a block of 16 row tiles x
-  // ~9 column tiles in flight shares them best (measured 78.6 ms per backward
-  // call at T = 32768 against 82.1 ms with the scoring kernel's 48).
-  a.group_m = 16;
+  // Raster groups of 2 row tiles: with K = V or K = T the operand panels of a
+  // tile (128 or 256 rows x K) are megabytes long; whole backward calls at
+  // T = 32768, d = 4096 (groups for G.W / G^T.y): 2/2 76.6-76.8 ms, 1/2 76.9,
+  // 2/1 77.1, 4/2 77.3, 2/16 77.5, 16/2 78.2, 16/16 79.2 (48: 82.1 before the
+  // products read G and W in place).
+  a.group_m = 2;
   a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
   a.k2 = 0.f;
   a.inv_temp = 0.f;
@@ -919,6 +987,8 @@ cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, const 
   a.c = C;
   a.ldc = ldc;
   a.accumulate = accumulate;
+  a.a_mn = a_mn;
+  a.b_mn = b_mn;
   a.wait_limit_ns = kWaitLimitNs;
   a.stall_producer = 0;
   return launch_gemm<3, kPrecBf16>(map_a, map_b, map_a, map_b, a, stream, num_sms, false);
