@@ -50,17 +50,21 @@ __device__ __forceinline__ Rec merge(const Rec& a, const Rec& b) {
 }
 
 // Fold records t0 .. t1-1 (t0 < t1) of one row left to right; records are
-// fetched 8 at a time so the loads overlap (the merge order is unchanged).
+// fetched kFoldBatch at a time so the loads overlap (the merge order is
+// unchanged).  A 151936-column vocabulary has 594 tiles, 38 per range: two
+// batches, i.e. two round trips to memory per range.
+constexpr int kFoldBatch = 20;
+
 __device__ __forceinline__ Rec fold_range(const float4* p, int t0, int t1) {
-  Rec acc = load_rec(p + static_cast<int64_t>(t0) * 32);
-  for (int t = t0 + 1; t < t1; t += 8) {
-    Rec buf[8];
+  Rec acc = {0.f, 0.f, 0.f, 0};
+  for (int t = t0; t < t1; t += kFoldBatch) {
+    Rec buf[kFoldBatch];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < kFoldBatch; ++i)
       if (t + i < t1) buf[i] = load_rec(p + static_cast<int64_t>(t + i) * 32);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (t + i < t1) acc = merge(acc, buf[i]);
+    for (int i = 0; i < kFoldBatch; ++i)
+      if (t + i < t1) acc = (t + i == t0) ? buf[i] : merge(acc, buf[i]);
   }
   return acc;
 }

@@ -29,15 +29,28 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8]) {
   }
 }
 
+// Loads of a lane's chunks are issued kLoadBatch at a time (chunks c, c + 32,
+// ... of one batch in flight together); the arithmetic that follows keeps the
+// chunk order, so the results do not depend on the batching.
+constexpr int kLoadBatch = 8;
+
 // Sum of squares of one row in the fixed order above; every lane returns the same
 // value.
 __device__ __forceinline__ float row_sum_squares(const uint4* h, int nvec, int lane) {
   float ss = 0.f;
-  for (int c = lane; c < nvec; c += 32) {
-    float f[8];
-    unpack_bf16x8(__ldg(h + c), f);
+  for (int c0 = lane; c0 < nvec; c0 += 32 * kLoadBatch) {
+    uint4 v[kLoadBatch];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+    for (int i = 0; i < kLoadBatch; ++i)
+      if (c0 + 32 * i < nvec) v[i] = __ldg(h + c0 + 32 * i);
+#pragma unroll
+    for (int i = 0; i < kLoadBatch; ++i) {
+      if (c0 + 32 * i >= nvec) break;
+      float f[8];
+      unpack_bf16x8(v[i], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
@@ -67,19 +80,31 @@ __global__ void __launch_bounds__(32 * kNormRowsPerBlock)
   }
   const float rstd = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
 
-  for (int c = lane; c < nvec; c += 32) {
-    float f[8], g[8];
-    unpack_bf16x8(__ldg(h + c), f);
-    unpack_bf16x8(__ldg(gamma + c), g);
-    uint32_t w[4];
+  for (int c0 = lane; c0 < nvec; c0 += 32 * kLoadBatch) {
+    uint4 hv[kLoadBatch], gv[kLoadBatch];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat16 lo = __float2bfloat16_rn((f[2 * i] * rstd) * g[2 * i]);
-      const __nv_bfloat16 hi = __float2bfloat16_rn((f[2 * i + 1] * rstd) * g[2 * i + 1]);
-      w[i] = static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
-             (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+    for (int k = 0; k < kLoadBatch; ++k)
+      if (c0 + 32 * k < nvec) {
+        hv[k] = __ldg(h + c0 + 32 * k);
+        gv[k] = __ldg(gamma + c0 + 32 * k);
+      }
+#pragma unroll
+    for (int k = 0; k < kLoadBatch; ++k) {
+      const int c = c0 + 32 * k;
+      if (c >= nvec) break;
+      float f[8], g[8];
+      unpack_bf16x8(hv[k], f);
+      unpack_bf16x8(gv[k], g);
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat16 lo = __float2bfloat16_rn((f[2 * i] * rstd) * g[2 * i]);
+        const __nv_bfloat16 hi = __float2bfloat16_rn((f[2 * i + 1] * rstd) * g[2 * i + 1]);
+        w[i] = static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
+               (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+      }
+      out[c] = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    out[c] = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
