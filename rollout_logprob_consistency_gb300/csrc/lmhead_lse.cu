@@ -122,14 +122,22 @@ struct GemmArgs {
 //               big*big + big*small + small*big per K step, 32 K-elements per
 //               stage row; a stage holds both parts of both operands, so the
 //               ring has half as many stages in the same shared memory.
-enum Prec : int { kPrecBf16 = 0, kPrecE4m3 = 1, kPrecTf32x3 = 2 };
+//   kPrecBf16x2 bf16 as kPrecBf16, but a work item is a pair of row tiles
+//               (2m, 2m + 1) against one W tile: a stage holds both y tiles and
+//               one W tile (64 KiB, 3 stages), and every K step issues the same
+//               M=128 MMA once per row tile into its own accumulator.  Each row
+//               sees the identical MMA sequence of the one-tile form; only the
+//               number of CTAs that stream a W tile at once changes (scoring
+//               mode only, for batches of a few row tiles).
+enum Prec : int { kPrecBf16 = 0, kPrecE4m3 = 1, kPrecTf32x3 = 2, kPrecBf16x2 = 3 };
 
 template <int kPrec>
 struct StageGeom {
   static constexpr int kParts = kPrec == kPrecTf32x3 ? 2 : 1;
-  static constexpr int kS = kStages / kParts;
-  static constexpr int kStageA = kParts * kABytes;
+  static constexpr int kRowTiles = kPrec == kPrecBf16x2 ? 2 : 1;  // row tiles per work item
+  static constexpr int kStageA = kParts * kRowTiles * kABytes;
   static constexpr int kStageB = kParts * kBBytes;
+  static constexpr int kS = kStages * (kABytes + kBBytes) / (kStageA + kStageB);
   static constexpr int kKElems = kPrec == kPrecE4m3 ? 2 * kBK : kPrec == kPrecTf32x3 ? kBK / 2 : kBK;
   // TMEM per tile: one 256-column fp32 accumulator, double-buffered; the tf32x3
   // path adds a second 256-column accumulator for the two correction products
@@ -137,9 +145,13 @@ struct StageGeom {
   // Keeping the corrections apart leaves the main sum with d/8 accumulation
   // steps instead of 3d/8 (each step of the tensor-core accumulation costs up to
   // one rounding of the running sum).
-  static constexpr int kAccCols = kPrec == kPrecTf32x3 ? 2 * kBN : kBN;
+  // The row-tile pair likewise takes all 512 columns: one accumulator per row tile.
+  static constexpr int kAccCols = (kPrec == kPrecTf32x3 || kPrec == kPrecBf16x2) ? 2 * kBN : kBN;
   static constexpr int kNumAcc = kTmemCols / kAccCols;
 };
+static_assert(StageGeom<kPrecBf16>::kS == kStages && StageGeom<kPrecTf32x3>::kS == 2 &&
+                  StageGeom<kPrecBf16x2>::kS == 3,
+              "stage rings fill the same shared memory");
 
 constexpr size_t kGemmSmemBytes =
     1024 /* alignment slack */ + kStages * (kABytes + kBBytes) + 256 /* barriers, flags */;
@@ -255,6 +267,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   using G = StageGeom<kPrec>;
   constexpr bool kFp8 = kPrec == kPrecE4m3;
   constexpr bool kX3 = kPrec == kPrecTf32x3;
+  constexpr int kRT = G::kRowTiles;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -313,19 +326,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // One stage of each operand: a K-major tile is one box (128-byte rows of K,
       // 8-row swizzle atoms); an MN-major tile (store mode) is boxes of 64 rows of
       // K x 64 elements of M or N, placed kMnChunkBytes apart.
-      auto load_a = [&](int st, int kb, int m) {
+      // mt: first row tile of the work item; two: the item's second row tile
+      // exists (row-tile pairs only)
+      auto load_a = [&](int st, int kb, int mt, bool two) {
         uint8_t* dst = sA + st * G::kStageA;
         if constexpr (kMode == 3) {
           if (a.a_mn) {
 #pragma unroll
             for (int c = 0; c < kBM / 64; ++c)
-              tma_load_2d(dst + c * kMnChunkBytes, &tmap_y, m * kBM + c * 64, kb * kKElems,
+              tma_load_2d(dst + c * kMnChunkBytes, &tmap_y, mt * kBM + c * 64, kb * kKElems,
                           &full[st]);
             return;
           }
         }
-        tma_load_2d(dst, &tmap_y, kb * kKElems, m * kBM, &full[st]);
-        if (kX3) tma_load_2d(dst + kABytes, &tmap_y2, kb * kKElems, m * kBM, &full[st]);
+        tma_load_2d(dst, &tmap_y, kb * kKElems, mt * kBM, &full[st]);
+        if (kX3) tma_load_2d(dst + kABytes, &tmap_y2, kb * kKElems, mt * kBM, &full[st]);
+        if (kRT == 2 && two)
+          tma_load_2d(dst + kABytes, &tmap_y, kb * kKElems, (mt + 1) * kBM, &full[st]);
       };
       auto load_b = [&](int st, int kb, int n) {
         uint8_t* dst = sB + st * G::kStageB;
@@ -348,19 +365,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int64_t tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
         int m, n;
         tile_coords(tile, a, m, n);
-        if (static_cast<int64_t>(m) * kBM >= t_rows) continue;  // no rows in this tile
+        const int mt = m * kRT;
+        if (static_cast<int64_t>(mt) * kBM >= t_rows) continue;  // no rows in this tile
+        const bool two = kRT == 2 && static_cast<int64_t>(mt + 1) * kBM < t_rows;
+        const uint32_t tx = (kRT == 1 || two) ? kTx : kTx - kABytes;
         int kb0 = 0;
         if (first) {
           // W does not depend on the RMSNorm kernel that precedes this one in the
           // stream: stream the first stages of W before waiting for y to be ready.
           const int pre = min(G::kS, a.num_kb);
           for (int s = 0; s < pre; ++s) {
-            mbar_arrive_expect_tx(&full[s], kTx);
+            mbar_arrive_expect_tx(&full[s], tx);
             load_b(s, s, n);
           }
           pdl_wait();
           for (int s = 0; s < pre; ++s) {
-            load_a(s, s, m);
+            load_a(s, s, mt, two);
             last_parity[s] = 0;
           }
           stage = pre % G::kS;
@@ -373,8 +393,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], kTx);
-          load_a(stage, kb, m);
+          mbar_arrive_expect_tx(&full[stage], tx);
+          load_a(stage, kb, mt, two);
           load_b(stage, kb, n);
           last_parity[stage] = ph;
           if (++stage == G::kS) {
@@ -403,6 +423,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           int m, n;
           tile_coords(tile, a, m, n);
           if (static_cast<int64_t>(m) * kBM >= t_rows) continue;
+        }
+        bool two = false;  // row-tile pairs: the item's second row tile exists
+        if constexpr (kRT == 2) {
+          int m, n;
+          tile_coords(tile, a, m, n);
+          two = static_cast<int64_t>(2 * m + 1) * kBM < t_rows;
         }
         if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1u, abort_flag, a.wait_limit_ns)) {
           ok = false;
@@ -440,6 +466,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (a.b_mn) bd = sw128_mnmajor_desc(b0 + k * 2048);
               }
               umma_bf16(d_tmem, ad, bd, idesc, acc_k);
+              if (kRT == 2 && two)  // same W slice, second row tile, own accumulator
+                umma_bf16(d_tmem + kBN, sw128_kmajor_desc(a0 + kABytes + k * 32), bd, idesc,
+                          acc_k);
             }
           }
           umma_commit(&empty[stage]);
@@ -465,8 +494,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int64_t tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
       int m, n;
       tile_coords(tile, a, m, n);
-      if (static_cast<int64_t>(m) * kBM >= t_rows) continue;
-      const int64_t row = static_cast<int64_t>(m) * kBM + q * 32 + lane;
+      const int mt = m * kRT;  // first row tile of the work item
+      if (static_cast<int64_t>(mt) * kBM >= t_rows) continue;
+      // row tiles in this item (2 only for a row-tile pair whose second tile exists)
+      const int nrt = (kRT == 2 && static_cast<int64_t>(mt + 1) * kBM < t_rows) ? 2 : 1;
+      const int64_t row = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
       const int x = (kMode != 3 && row < a.T) ? __ldg(a.ids + row) : -1;
       const int col_base = a.v0 + n * kBN;  // global vocabulary id of the tile's column 0
       const int rel = x - col_base;
@@ -481,37 +513,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       __syncwarp();
 
-      float m2 = -INFINITY, sum = 0.f, bz = -INFINITY, zt = 0.f;
-      int bi = col_base;
+      // scoring records, one per row tile of the item: row tile h of a pair is
+      // row + h * kBM, its accumulator h * kBN columns further on
+      float m2[kRT], sum[kRT], bz[kRT], zt[kRT];
+      int bi[kRT], relh[kRT];
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * G::kAccCols;
       if constexpr (kMode == 0) {
         const float srow = kFp8 ? __ldg(a.sy + row) : 1.f;
+#pragma unroll
+        for (int h = 0; h < kRT; ++h) {
+          m2[h] = -INFINITY;
+          sum[h] = 0.f;
+          bz[h] = -INFINITY;
+          zt[h] = 0.f;
+          bi[h] = col_base;
+          relh[h] = rel;
+          if (h >= nrt) continue;
+          if (h > 0) {
+            const int64_t rh = row + h * kBM;
+            relh[h] = (rh < a.T ? __ldg(a.ids + rh) : -1) - col_base;
+          }
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          const int col0 = col_base + c * 32;
-          if (col0 >= a.v_end) break;  // warp-uniform
-          uint32_t r[32];
-          tmem_ld32(tbase + c * 32, r);
-          const int nvalid = min(32, a.v_end - col0);
-          if constexpr (kFp8) {
+          for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = col_base + c * 32;
+            if (col0 >= a.v_end) break;  // warp-uniform
+            uint32_t r[32];
+            tmem_ld32(tbase + h * kBN + c * 32, r);
+            const int nvalid = min(32, a.v_end - col0);
+            if constexpr (kFp8) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float sc = srow * __ldg(a.sw + min(col0 + j, a.v_end - 1));
-              r[j] = __float_as_uint(__uint_as_float(r[j]) * sc);
+              for (int j = 0; j < 32; ++j) {
+                const float sc = srow * __ldg(a.sw + min(col0 + j, a.v_end - 1));
+                r[j] = __float_as_uint(__uint_as_float(r[j]) * sc);
+              }
             }
-          }
-          if constexpr (kX3) {
-            uint32_t rc[32];
-            tmem_ld32(tbase + kBN + c * 32, rc);
+            if constexpr (kX3) {
+              uint32_t rc[32];
+              tmem_ld32(tbase + kBN + c * 32, rc);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(rc[j]));
+              for (int j = 0; j < 32; ++j)
+                r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(rc[j]));
+            }
+            if (nvalid == 32)
+              epilogue_chunk<false>(r, 32, col0, relh[h] - c * 32, a.k2, m2[h], sum[h], bz[h],
+                                    bi[h], zt[h]);
+            else
+              epilogue_chunk<true>(r, nvalid, col0, relh[h] - c * 32, a.k2, m2[h], sum[h], bz[h],
+                                   bi[h], zt[h]);
           }
-          if (nvalid == 32)
-            epilogue_chunk<false>(r, 32, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
-          else
-            epilogue_chunk<true>(r, nvalid, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
         }
       } else if constexpr (kMode == 2) {
         const bool live = row < a.T;
@@ -644,10 +694,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
 
-      if (kMode == 0 && row < a.T) {
-        a.part[((row >> 5) * a.num_n + n) * 32 + (row & 31)] =
-            make_float4(m2, sum, bz, __int_as_float(bi));
-        if (static_cast<unsigned>(rel) < static_cast<unsigned>(kBN)) a.tgt[row] = zt * a.inv_temp;
+      if constexpr (kMode == 0) {
+#pragma unroll
+        for (int h = 0; h < kRT; ++h) {
+          const int64_t rh = row + h * kBM;
+          if (h < nrt && rh < a.T) {
+            a.part[((rh >> 5) * a.num_n + n) * 32 + (rh & 31)] =
+                make_float4(m2[h], sum[h], bz[h], __int_as_float(bi[h]));
+            if (static_cast<unsigned>(relh[h]) < static_cast<unsigned>(kBN))
+              a.tgt[rh] = zt[h] * a.inv_temp;
+          }
+        }
       }
       if (++acc == static_cast<uint32_t>(G::kNumAcc)) {
         acc = 0;
@@ -849,6 +906,21 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
   // (3 ms at 32768 rows), so larger batches are launched in stream order.  The
   // arithmetic is identical either way.
   const bool programmatic = a.num_m <= a.group_m;
+  // Batches of a few row tiles: the CTAs that share a W tile run side by side and
+  // only one of them streams each W k-slice from DRAM, so too few W bytes are in
+  // flight to cover DRAM latency.  With two or four row tiles each work item is a
+  // pair of row tiles (kPrecBf16x2) and every CTA streams its own W tile once for
+  // both; the per-row arithmetic is the same MMA sequence and epilogue as the
+  // one-tile form.  Measured on GB300 (d = 4096, V = 151936, whole calls): 200-256
+  // rows 249-250 -> 238-241 us, 448-512 rows 410-416 -> 387-392 us.  With three
+  // row tiles the pairs and the lone third tile split 2:1 between alternate CTAs
+  // (320-384 rows: 325 -> 407 us), so odd counts keep one row tile per item.
+  if (a.num_m == 2 || a.num_m == 4) {
+    a.num_m = (a.num_m + 1) / 2;  // work items along M: row-tile pairs
+    a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
+    return launch_gemm<0, kPrecBf16x2>(map_y, map_w, map_y, map_w, a, stream, num_sms,
+                                       programmatic);
+  }
   return launch_gemm<0, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, programmatic);
 }
 

@@ -37,6 +37,8 @@ SHAPES = [
     (129, 128, 1000, 0.5),
     (300, 256, 513, 1.3),
     (257, 192, 2048, 1.0),
+    (384, 128, 1000, 1.0),
+    (512, 256, 3001, 0.8),
     (513, 320, 4099, 0.9),
 ]
 
@@ -141,7 +143,7 @@ def test_batch_invariance_small(tim):
     """Targets scored inside batches of different sizes, positions and neighbours give
     bitwise identical (logprob, lse, top1)."""
     head = synth.make_custom(T=1, d=256, V=3000, tag="bi").head
-    plan = synth.make_sweep(Ms=(1, 7, 64, 129, 200, 513), n_targets=200, head=head)
+    plan = synth.make_sweep(Ms=(1, 7, 64, 129, 200, 384, 512, 513), n_targets=200, head=head)
     ref = None
     for M, batches in plan.batches.items():
         got = np.zeros((200, 3), dtype=np.uint32)
