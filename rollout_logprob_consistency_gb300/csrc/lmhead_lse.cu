@@ -333,9 +333,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if constexpr (kMode == 3) {
           if (a.a_mn) {
 #pragma unroll
-            for (int c = 0; c < kBM / 64; ++c)
-              tma_load_2d(dst + c * kMnChunkBytes, &tmap_y, mt * kBM + c * 64, kb * kKElems,
-                          &full[st]);
+            for (int h = 0; h < kRT; ++h) {
+              if (h > 0 && !two) break;
+#pragma unroll
+              for (int c = 0; c < kBM / 64; ++c)
+                tma_load_2d(dst + h * kABytes + c * kMnChunkBytes, &tmap_y,
+                            (mt + h) * kBM + c * 64, kb * kKElems, &full[st]);
+            }
             return;
           }
         }
@@ -461,14 +465,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             } else {
               uint64_t ad = sw128_kmajor_desc(a0 + k * 32);
               uint64_t bd = sw128_kmajor_desc(b0 + k * 32);
+              uint64_t ad2 = sw128_kmajor_desc(a0 + kABytes + k * 32);  // row-tile pairs
               if constexpr (kMode == 3) {  // 16 K-rows of an MN-major tile: 2 atoms
-                if (a.a_mn) ad = sw128_mnmajor_desc(a0 + k * 2048);
+                if (a.a_mn) {
+                  ad = sw128_mnmajor_desc(a0 + k * 2048);
+                  ad2 = sw128_mnmajor_desc(a0 + kABytes + k * 2048);
+                }
                 if (a.b_mn) bd = sw128_mnmajor_desc(b0 + k * 2048);
               }
               umma_bf16(d_tmem, ad, bd, idesc, acc_k);
-              if (kRT == 2 && two)  // same W slice, second row tile, own accumulator
-                umma_bf16(d_tmem + kBN, sw128_kmajor_desc(a0 + kABytes + k * 32), bd, idesc,
-                          acc_k);
+              if (kRT == 2 && two)  // same B slice, second row tile, own accumulator
+                umma_bf16(d_tmem + kBN, ad2, bd, idesc, acc_k);
             }
           }
           umma_commit(&empty[stage]);
@@ -614,13 +621,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       } else if constexpr (kMode == 3) {
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int hc = 0; hc < nrt * (kBN / 32); ++hc) {  // row tile hc / 8, chunk hc % 8
+          const int h = hc / (kBN / 32), c = hc % (kBN / 32);
+          const int64_t rh = row + h * kBM;
           const int col0 = col_base + c * 32;
-          if (col0 >= a.v_end) break;  // warp-uniform
+          if (col0 >= a.v_end) continue;  // warp-uniform
           uint32_t r[32];
-          tmem_ld32(tbase + c * 32, r);
-          if (row < a.T) {
-            float4* dst = reinterpret_cast<float4*>(a.c + row * a.ldc + col0);
+          tmem_ld32(tbase + h * kBN + c * 32, r);
+          if (rh < a.T) {
+            float4* dst = reinterpret_cast<float4*>(a.c + rh * a.ldc + col0);
 #pragma unroll
             for (int w = 0; w < 8; ++w) {
               float4 v = make_float4(__uint_as_float(r[4 * w]), __uint_as_float(r[4 * w + 1]),
@@ -1063,6 +1072,17 @@ cudaError_t launch_gemm_store(const void* A, int64_t rows_a, int64_t lda, int a_
   a.b_mn = b_mn;
   a.wait_limit_ns = kWaitLimitNs;
   a.stall_producer = 0;
+  // Two or more row tiles: work items are row-tile pairs sharing each B k-slice in
+  // shared memory (kPrecBf16x2), so the two tiles advance along K in lockstep and
+  // B is read from L2 once for both.  With K = V or K = T a tile's MMAs run for
+  // hundreds of microseconds, so the single accumulator buffer of a pair costs
+  // well under 1% in epilogue time.  The raster group is then one pair.
+  if (a.num_m >= 2) {
+    a.num_m = (a.num_m + 1) / 2;
+    a.group_m = 1;
+    a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
+    return launch_gemm<3, kPrecBf16x2>(map_a, map_b, map_a, map_b, a, stream, num_sms, false);
+  }
   return launch_gemm<3, kPrecBf16>(map_a, map_b, map_a, map_b, a, stream, num_sms, false);
 }
 
