@@ -25,6 +25,9 @@
 //                target's logit, and writes one 16-byte record per (row, tile).
 //   Double-buffered accumulators let the epilogue of tile i overlap the MMAs of
 //   tile i+1.
+//   Row-tile pairs (two 128-row tiles against one W tile, see kPrecBf16x2) use
+//   both accumulators for one work item and eight epilogue warps: warps 2..5
+//   read the first row tile's accumulator, warps 6..9 the second's.
 //
 // Batch invariance: every logit is the same sequence of MMAs (k-blocks in
 // order, 4 K=16 steps each) whatever T is; rows past T (zeros written by the
@@ -139,6 +142,10 @@ struct StageGeom {
   static constexpr int kStageB = kParts * kBBytes;
   static constexpr int kS = kStages * (kABytes + kBBytes) / (kStageA + kStageB);
   static constexpr int kKElems = kPrec == kPrecE4m3 ? 2 * kBK : kPrec == kPrecTf32x3 ? kBK / 2 : kBK;
+  // epilogue warps: one per TMEM lane quadrant and accumulator (a pair's two
+  // accumulators are read side by side by two warp groups)
+  static constexpr int kEpi = kRowTiles * kEpiWarps;
+  static constexpr int kThreads = 64 + 32 * kEpi;
   // TMEM per tile: one 256-column fp32 accumulator, double-buffered; the tf32x3
   // path adds a second 256-column accumulator for the two correction products
   // (big*small + small*big), so its tile takes all 512 columns, single-buffered.
@@ -259,7 +266,7 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], int nval
 // kPrec: operand precision (see Prec).  tmap_y2 / tmap_w2 are the remainder
 // parts for kPrecTf32x3 and unused otherwise.
 template <int kMode, int kPrec>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(StageGeom<kPrec>::kThreads, 1)
     lmhead_lse_kernel(const __grid_constant__ CUtensorMap tmap_y,
                       const __grid_constant__ CUtensorMap tmap_w,
                       const __grid_constant__ CUtensorMap tmap_y2,
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], kEpiWarps);
+      mbar_init(&acc_empty[b], G::kEpi);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -497,15 +504,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // row tile of the work item this warp reads: 0, or with row-tile pairs 0 for
+    // warps 2-5 and 1 for warps 6-9 (one accumulator each, kBN columns apart)
+    const int h = (warp - 2) / kEpiWarps;
     uint32_t acc = 0, acc_ph = 0;
     for (int64_t tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
       int m, n;
       tile_coords(tile, a, m, n);
       const int mt = m * kRT;  // first row tile of the work item
       if (static_cast<int64_t>(mt) * kBM >= t_rows) continue;
-      // row tiles in this item (2 only for a row-tile pair whose second tile exists)
-      const int nrt = (kRT == 2 && static_cast<int64_t>(mt + 1) * kBM < t_rows) ? 2 : 1;
-      const int64_t row = static_cast<int64_t>(mt) * kBM + q * 32 + lane;
+      // a pair's second row tile may not exist: its warps then only take part in
+      // the accumulator hand-off
+      const int nchunk = static_cast<int64_t>(mt + h) * kBM < t_rows ? kBN / 32 : 0;
+      const int64_t row = static_cast<int64_t>(mt + h) * kBM + q * 32 + lane;
       const int x = (kMode != 3 && row < a.T) ? __ldg(a.ids + row) : -1;
       const int col_base = a.v0 + n * kBN;  // global vocabulary id of the tile's column 0
       const int rel = x - col_base;
@@ -520,55 +531,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       __syncwarp();
 
-      // scoring records, one per row tile of the item: row tile h of a pair is
-      // row + h * kBM, its accumulator h * kBN columns further on
-      float m2[kRT], sum[kRT], bz[kRT], zt[kRT];
-      int bi[kRT], relh[kRT];
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * G::kAccCols;
+      float m2 = -INFINITY, sum = 0.f, bz = -INFINITY, zt = 0.f;
+      int bi = col_base;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             acc * G::kAccCols + h * kBN;
       if constexpr (kMode == 0) {
         const float srow = kFp8 ? __ldg(a.sy + row) : 1.f;
-#pragma unroll
-        for (int h = 0; h < kRT; ++h) {
-          m2[h] = -INFINITY;
-          sum[h] = 0.f;
-          bz[h] = -INFINITY;
-          zt[h] = 0.f;
-          bi[h] = col_base;
-          relh[h] = rel;
-          if (h >= nrt) continue;
-          if (h > 0) {
-            const int64_t rh = row + h * kBM;
-            relh[h] = (rh < a.T ? __ldg(a.ids + rh) : -1) - col_base;
-          }
 #pragma unroll 1
-          for (int c = 0; c < kBN / 32; ++c) {
-            const int col0 = col_base + c * 32;
-            if (col0 >= a.v_end) break;  // warp-uniform
-            uint32_t r[32];
-            tmem_ld32(tbase + h * kBN + c * 32, r);
-            const int nvalid = min(32, a.v_end - col0);
-            if constexpr (kFp8) {
+        for (int c = 0; c < nchunk; ++c) {
+          const int col0 = col_base + c * 32;
+          if (col0 >= a.v_end) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          const int nvalid = min(32, a.v_end - col0);
+          if constexpr (kFp8) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float sc = srow * __ldg(a.sw + min(col0 + j, a.v_end - 1));
-                r[j] = __float_as_uint(__uint_as_float(r[j]) * sc);
-              }
+            for (int j = 0; j < 32; ++j) {
+              const float sc = srow * __ldg(a.sw + min(col0 + j, a.v_end - 1));
+              r[j] = __float_as_uint(__uint_as_float(r[j]) * sc);
             }
-            if constexpr (kX3) {
-              uint32_t rc[32];
-              tmem_ld32(tbase + kBN + c * 32, rc);
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(rc[j]));
-            }
-            if (nvalid == 32)
-              epilogue_chunk<false>(r, 32, col0, relh[h] - c * 32, a.k2, m2[h], sum[h], bz[h],
-                                    bi[h], zt[h]);
-            else
-              epilogue_chunk<true>(r, nvalid, col0, relh[h] - c * 32, a.k2, m2[h], sum[h], bz[h],
-                                   bi[h], zt[h]);
           }
+          if constexpr (kX3) {
+            uint32_t rc[32];
+            tmem_ld32(tbase + kBN + c * 32, rc);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(rc[j]));
+          }
+          if (nvalid == 32)
+            epilogue_chunk<false>(r, 32, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
+          else
+            epilogue_chunk<true>(r, nvalid, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
         }
       } else if constexpr (kMode == 2) {
         const bool live = row < a.T;
@@ -583,7 +576,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint8_t* stg = grad_stage + q * (32 * 64);
         const int64_t row0 = row - lane;  // first row of this warp's 32
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = 0; c < nchunk; ++c) {
           const int col0 = col_base + c * 32;
           if (col0 >= a.v_end) break;  // warp-uniform
           uint32_t r[32];
@@ -621,15 +614,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       } else if constexpr (kMode == 3) {
 #pragma unroll 1
-        for (int hc = 0; hc < nrt * (kBN / 32); ++hc) {  // row tile hc / 8, chunk hc % 8
-          const int h = hc / (kBN / 32), c = hc % (kBN / 32);
-          const int64_t rh = row + h * kBM;
+        for (int c = 0; c < nchunk; ++c) {
           const int col0 = col_base + c * 32;
-          if (col0 >= a.v_end) continue;  // warp-uniform
+          if (col0 >= a.v_end) break;  // warp-uniform
           uint32_t r[32];
-          tmem_ld32(tbase + h * kBN + c * 32, r);
-          if (rh < a.T) {
-            float4* dst = reinterpret_cast<float4*>(a.c + rh * a.ldc + col0);
+          tmem_ld32(tbase + c * 32, r);
+          if (row < a.T) {
+            float4* dst = reinterpret_cast<float4*>(a.c + row * a.ldc + col0);
 #pragma unroll
             for (int w = 0; w < 8; ++w) {
               float4 v = make_float4(__uint_as_float(r[4 * w]), __uint_as_float(r[4 * w + 1]),
@@ -649,7 +640,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         float tv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         int ti[4] = {-1, -1, -1, -1};
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = 0; c < nchunk; ++c) {
           const int col0 = col_base + c * 32;
           if (col0 >= a.v_end) break;  // warp-uniform
           uint32_t r[32];
@@ -684,7 +675,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int64_t orow = (live && a.row_map != nullptr) ? __ldg(a.row_map + row) : row;
         const float thr = live ? __ldcg(a.thr + orow) : INFINITY;
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = 0; c < nchunk; ++c) {
           const int col0 = col_base + c * 32;
           if (col0 >= a.v_end) break;  // warp-uniform
           uint32_t r[32];
@@ -703,17 +694,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
 
-      if constexpr (kMode == 0) {
-#pragma unroll
-        for (int h = 0; h < kRT; ++h) {
-          const int64_t rh = row + h * kBM;
-          if (h < nrt && rh < a.T) {
-            a.part[((rh >> 5) * a.num_n + n) * 32 + (rh & 31)] =
-                make_float4(m2[h], sum[h], bz[h], __int_as_float(bi[h]));
-            if (static_cast<unsigned>(relh[h]) < static_cast<unsigned>(kBN))
-              a.tgt[rh] = zt[h] * a.inv_temp;
-          }
-        }
+      if (kMode == 0 && row < a.T) {
+        a.part[((row >> 5) * a.num_n + n) * 32 + (row & 31)] =
+            make_float4(m2, sum, bz, __int_as_float(bi));
+        if (static_cast<unsigned>(rel) < static_cast<unsigned>(kBN)) a.tgt[row] = zt * a.inv_temp;
       }
       if (++acc == static_cast<uint32_t>(G::kNumAcc)) {
         acc = 0;
@@ -831,7 +815,7 @@ static cudaError_t launch_gemm(const CUtensorMap& map_y, const CUtensorMap& map_
   // griddepcontrol.wait.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(StageGeom<kPrec>::kThreads);
   cfg.dynamicSmemBytes = gemm_smem_bytes(kMode);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -921,11 +905,12 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
   // pair of row tiles (kPrecBf16x2) and every CTA streams its own W tile once for
   // both; the per-row arithmetic is the same MMA sequence and epilogue as the
   // one-tile form.  Measured on GB300 (d = 4096, V = 151936, whole calls): 200-256
-  // rows 249-250 -> 238-241 us, 448-512 rows 410-416 -> 387-392 us.  With three
-  // row tiles the pairs and the lone third tile split 2:1 between alternate CTAs
-  // (320-384 rows: 325 -> 407 us), so odd counts keep one row tile per item.
+  // rows 252-256 -> 237-241 us, 448-512 rows 411-421 -> 381-388 us.  Three row
+  // tiles gain nothing (a pair and the lone third tile per W tile; 327-335 us
+  // either way, with an odd grid so that the two kinds of item rotate over the
+  // CTAs), so they keep one row tile per item.
   if (a.num_m == 2 || a.num_m == 4) {
-    a.num_m = (a.num_m + 1) / 2;  // work items along M: row-tile pairs
+    a.num_m /= 2;  // work items along M: row-tile pairs
     a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
     return launch_gemm<0, kPrecBf16x2>(map_y, map_w, map_y, map_w, a, stream, num_sms,
                                        programmatic);

@@ -22,7 +22,6 @@ constexpr int kStages = 4;        // smem pipeline depth
 constexpr int kABytes = kBM * kBK * 2;   // 16 KiB
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KiB
 constexpr int kEpiWarps = 4;             // one epilogue warp per TMEM lane quadrant
-constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;           // two 256-column fp32 accumulators
 constexpr int kRowGroup = 32;            // rows per partial-record group
 
