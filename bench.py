@@ -33,11 +33,11 @@ L2_NOTE = "inputs larger than L2 (W 1.245 GB + hidden 268 MB per step vs 129 MB 
 
 # DRAM bytes per lmhead_lse launch of this workload (T=32768, d=4096, V=151936),
 # measured by a one-pass ncu capture of the full-size launch
-# (profiles/lmhead_lse_T32768_dram.md): 8.902 GB read + 0.315 GB written.  Valid
+# (profiles/lmhead_lse_T32768_dram.md): 9.303 GB read + 0.316 GB written.  Valid
 # only for the kernel sources hashed here and for T = 32768.
-TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "d204a229d3244d06",
-                                "tim_common.cuh": "f67b058262e5bfe0"},
-                       T=32768, bytes=8.91e9 + 315.52e6)
+TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "6ce6d3c9489ad0fb",
+                                "tim_common.cuh": "b40069df5556ec34"},
+                       T=32768, bytes=9.3033088e9 + 315.502336e6)
 
 
 def traffic_per_launch(T):
