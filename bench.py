@@ -34,19 +34,32 @@ L2_NOTE = "inputs larger than L2 (W 1.245 GB + hidden 268 MB per step vs 129 MB 
 # DRAM bytes per lmhead_lse launch of this workload (T=32768, d=4096, V=151936),
 # measured by a one-pass ncu capture of the full-size launch
 # (profiles/lmhead_lse_T32768_dram.md): 9.303 GB read + 0.316 GB written.  Valid
-# only for the kernel sources hashed here and for T = 32768.
-TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "a90c21d5b612be8d",
-                                "tim_common.cuh": "b40069df5556ec34"},
+# only for the kernel sources hashed here (code lines only: comments and blank
+# lines do not enter the hash) and for T = 32768.
+TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "bb182d5442560f84",
+                                "tim_common.cuh": "7ff81004ca8e301b"},
                        T=32768, bytes=9.3033088e9 + 315.502336e6)
 
 
-def traffic_per_launch(T):
+def code_hash(path: str) -> str:
+    """sha256 (16 hex digits) of a C++ source with // comments and blank lines removed."""
     import hashlib
+    import re
+    with open(path) as f:
+        text = f.read()
+    lines = []
+    for line in text.splitlines():
+        line = re.sub(r"//.*$", "", line).rstrip()
+        if line:
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
+def traffic_per_launch(T):
     csrc = os.path.join(ROOT, "rollout_logprob_consistency_gb300", "csrc")
     for name, h in TRAFFIC_CAPTURE["sources"].items():
-        with open(os.path.join(csrc, name), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest()[:16] != h:
-                return None   # the kernel changed since the counters were taken
+        if code_hash(os.path.join(csrc, name)) != h:
+            return None   # the kernel changed since the counters were taken
     return TRAFFIC_CAPTURE["bytes"] if T == TRAFFIC_CAPTURE["T"] else None
 
 
