@@ -40,6 +40,7 @@ SHAPES = [
     (384, 128, 1000, 1.0),
     (512, 256, 3001, 0.8),
     (513, 320, 4099, 0.9),
+    (640, 64, 151936, 0.9),   # five row tiles as row-tile pairs with a lone last tile
 ]
 
 

@@ -113,9 +113,9 @@ def test_qwen3_8b_head_siblings(tim):
 
 def test_batch_invariance_sweep_8b_head(tim):
     """The 4096 target rows in batches of M = 1, 7, 64, 513, 4096 and 16384, plus
-    M = 200, 384 and 512: batches of two or four row tiles (M = 200, 512) are scored
-    as row-tile pairs, the others one row tile per work item, and every target keeps
-    its bits."""
+    M = 200, 384 and 512: M = 200, 512, 513 (an odd tile count) and 4096 are scored as
+    row-tile pairs, M = 1, 7, 64, 384 and 16384 one row tile per work item, and every
+    target keeps its bits."""
     import torch
     plan = synth.make_sweep(Ms=(1, 7, 64, 200, 384, 512, 513, 4096, 16384))
     head = plan.head
