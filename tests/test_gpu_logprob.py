@@ -41,6 +41,7 @@ SHAPES = [
     (512, 256, 3001, 0.8),
     (513, 320, 4099, 0.9),
     (640, 64, 151936, 0.9),   # five row tiles as row-tile pairs with a lone last tile
+    (256, 5120, 3001, 0.7),   # row-tile pairs at the long-rollout hidden size
 ]
 
 
