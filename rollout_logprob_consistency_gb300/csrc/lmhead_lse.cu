@@ -56,6 +56,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "tim_common.cuh"
@@ -731,15 +732,20 @@ __global__ void __launch_bounds__(StageGeom<kPrec>::kThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side
 
+// The driver's tensor-map encoder, resolved on first use and cached; host threads
+// may call concurrently (the cache is atomic, and a failed lookup is retried).
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cache{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = cache.load(std::memory_order_acquire);
   if (fn == nullptr) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      cache.store(fn, std::memory_order_release);
+    }
   }
   return fn;
 }
