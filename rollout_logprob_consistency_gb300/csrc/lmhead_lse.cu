@@ -888,6 +888,46 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   return cudaSuccess;
 }
 
+// Row-tile pairs for a scoring-type launch (one W pass per batch, light epilogue).
+// Batches that fit one raster group run as row-tile pairs (kPrecBf16x2): each
+// work item is two row tiles against one W tile, so every CTA streams its own W
+// tiles once for both (in the one-tile form the CTAs that share a W tile run
+// side by side and only one of them streams each k-slice from DRAM).  The
+// per-row arithmetic is the same MMA sequence and epilogue as the one-tile form.
+// An odd tile count leaves a lone last tile per W tile; that is paired only when
+// the items rotate over all CTAs (CTA count and number of pairs coprime: CTA c
+// meets pairs c, c + grid, c + 2 grid, ... modulo the pair count), otherwise some
+// CTAs would get a lone tile in every wave and others never.
+// Measured on GB300 (d = 4096, V = 151936, whole calls with L2 flushed, one-tile
+// -> pairs, medians of three alternating rounds on one box): 768 rows 575 -> 544
+// us, 1024 rows 771 -> 706 us, 1152 rows (9 tiles) 824 -> 799 us, 1536 rows
+// 1056 -> 1024 us, 2048 rows 1409 -> 1363 us, 3072 rows 2105 -> 2091 us, 4096
+// rows 2945 -> 2828 us, 6144 rows 4721 -> 4254 us; on other boxes 200-256 rows
+// 252-256 -> 237-241 us, 448-512 rows 411-421 -> 381-388 us, 513 rows (5 tiles)
+// 488-491 -> 478 us.  Odd counts without full rotation lost (7 tiles 666 -> 709
+// us, 11 tiles 996 -> 1053 us); 3 tiles tied even with an odd grid.  Batches of
+// more than one raster group stay in the one-tile form: 8192-16384 rows within
+// 1%, the benchmark batch of 32768 rows 1% slower with pairs under the power cap.
+static bool use_row_pairs(const GemmArgs& a, int num_sms) {
+  const int pairs = (a.num_m + 1) / 2;
+  const int64_t items = static_cast<int64_t>(pairs) * a.num_n;
+  const int grid = items < num_sms ? static_cast<int>(items) : num_sms;  // as launch_gemm
+  int g = grid, p = pairs;  // gcd(grid, pairs)
+  while (p != 0) {
+    const int r = g % p;
+    g = p;
+    p = r;
+  }
+  return a.num_m >= 2 && a.num_m <= a.group_m && (a.num_m % 2 == 0 || g == 1);
+}
+
+// Turns a one-tile schedule into the row-tile pair schedule.
+static void to_row_pairs(GemmArgs& a) {
+  a.num_m = (a.num_m + 1) / 2;  // work items along M: row-tile pairs
+  a.group_m = (a.group_m + 1) / 2;
+  a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
+}
+
 // W holds V vocabulary rows whose global ids start at v0 (a vocabulary shard when
 // v0 > 0 or V is not the whole vocabulary); records are written per local tile.
 cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t* ids, int64_t T,
@@ -905,38 +945,8 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
   // (3 ms at 32768 rows), so larger batches are launched in stream order.  The
   // arithmetic is identical either way.
   const bool programmatic = a.num_m <= a.group_m;
-  // Batches that fit one raster group run as row-tile pairs (kPrecBf16x2): each
-  // work item is two row tiles against one W tile, so every CTA streams its own W
-  // tiles once for both (in the one-tile form the CTAs that share a W tile run
-  // side by side and only one of them streams each k-slice from DRAM).  The
-  // per-row arithmetic is the same MMA sequence and epilogue as the one-tile form.
-  // An odd tile count leaves a lone last tile per W tile; that is paired only when
-  // the items rotate over all CTAs (CTA count and number of pairs coprime: CTA c
-  // meets pairs c, c + grid, c + 2 grid, ... modulo the pair count), otherwise some
-  // CTAs would get a lone tile in every wave and others never.
-  // Measured on GB300 (d = 4096, V = 151936, whole calls with L2 flushed, one-tile
-  // -> pairs, medians of three alternating rounds on one box): 768 rows 575 -> 544
-  // us, 1024 rows 771 -> 706 us, 1152 rows (9 tiles) 824 -> 799 us, 1536 rows
-  // 1056 -> 1024 us, 2048 rows 1409 -> 1363 us, 3072 rows 2105 -> 2091 us, 4096
-  // rows 2945 -> 2828 us, 6144 rows 4721 -> 4254 us; on other boxes 200-256 rows
-  // 252-256 -> 237-241 us, 448-512 rows 411-421 -> 381-388 us, 513 rows (5 tiles)
-  // 488-491 -> 478 us.  Odd counts without full rotation lost (7 tiles 666 -> 709
-  // us, 11 tiles 996 -> 1053 us); 3 tiles tied even with an odd grid.  Batches of
-  // more than one raster group stay in the one-tile form: 8192-16384 rows within
-  // 1%, the benchmark batch of 32768 rows 1% slower with pairs under the power cap.
-  const int pairs = (a.num_m + 1) / 2;
-  const int64_t items = static_cast<int64_t>(pairs) * a.num_n;
-  const int grid = items < num_sms ? static_cast<int>(items) : num_sms;  // as launch_gemm
-  int g = grid, p = pairs;  // gcd(grid, pairs)
-  while (p != 0) {
-    const int r = g % p;
-    g = p;
-    p = r;
-  }
-  if (a.num_m >= 2 && a.num_m <= a.group_m && (a.num_m % 2 == 0 || g == 1)) {
-    a.num_m = pairs;  // work items along M: row-tile pairs
-    a.group_m = (a.group_m + 1) / 2;
-    a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
+  if (use_row_pairs(a, num_sms)) {  // batches within one raster group (see use_row_pairs)
+    to_row_pairs(a);
     return launch_gemm<0, kPrecBf16x2>(map_y, map_w, map_y, map_w, a, stream, num_sms,
                                        programmatic);
   }
@@ -1017,6 +1027,10 @@ cudaError_t launch_lmhead_top4(const void* y, const void* W, const int32_t* ids,
   cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, 0, 1.0f, status);
   if (e != cudaSuccess) return e;
   a.top4 = top4;
+  if (use_row_pairs(a, num_sms)) {  // same schedule rule as the scoring GEMM
+    to_row_pairs(a);
+    return launch_gemm<4, kPrecBf16x2>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
+  }
   return launch_gemm<4, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }
 
