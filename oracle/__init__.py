@@ -12,10 +12,12 @@ Modules
 -------
 ``oracle.logprob``  the plain definition  logprob = log_softmax(z / tau)[x]
                     with z = bf16(RMSNorm(h)) . W^T, plus lse and top-1.
-``oracle.compare``  per-sequence A/B/C mismatch statistics, k3, TIS weights,
-                    and the single-pair ``compare`` summary.
+``oracle.compare``  per-sequence A/B/C mismatch statistics, k3, TIS weights.
 ``oracle.processed`` the processed (top-k, then top-p) selected-token logprob.
-``oracle.fp8``      the FP8 (e4m3, per-row power-of-two scales) head variant.
+``oracle.fp8``      the FP8 (e4m3, per-row power-of-two scales) head variant,
+                    and the set of its admissible results when the bf16
+                    rounding of y is within an implementation's error bound
+                    of a rounding midpoint.
 ``oracle.fp32head`` the FP32 head variant (fp32 y, fp32 W).
 ``oracle.backward`` the backward of the linear logprob (dL/dy, dL/dW).
 ``oracle.diag``     extended per-sequence diagnostics: |delta| quantiles,
@@ -33,15 +35,13 @@ from .logprob import (  # noqa: F401
 )
 from .compare import (  # noqa: F401
     OracleError, FLAG_EMPTY, FLAG_BAD_MASK, FLAG_NONFINITE, FLAG_BAD_OFFSETS,
-    FLAG_K3_OVERFLOW, PAIRS, oracle_compare, oracle_compare_lenient, compare_summary,
-    compare_bitwise,
+    FLAG_K3_OVERFLOW, PAIRS, oracle_compare, oracle_compare_lenient,
 )
 from .processed import oracle_processed_logprob, process_head, process_row  # noqa: F401
-from .fp8 import (e4m3_round, fp8_scale, oracle_logprob_fp8, quantize_rows,  # noqa: F401
-                  rmsnorm_fp32)
+from .fp8 import (bf16_choices, dequantized_weights, e4m3_round, fp8_scale,  # noqa: F401
+                  oracle_logprob_fp8, oracle_logprob_fp8_admissible, quantize_rows)
 from .fp32head import oracle_logprob_fp32, rmsnorm_unrounded  # noqa: F401
 from .backward import logit_grad, oracle_logprob_backward, rmsnorm_backward  # noqa: F401
 from .diag import (  # noqa: F401
-    FLAG_QUANTILE_SKIPPED, QUANTILE_MAX_TOKENS, QUANTILES, oracle_diag, oracle_diag_lenient,
-    quantile_linear,
+    QUANTILES, oracle_diag, oracle_diag_lenient, quantile_linear,
 )

@@ -220,57 +220,3 @@ def oracle_compare(lp_gen, lp_replay, lp_train, seq_offsets, mask, tis_cap: floa
     if errors:
         raise OracleError(errors[0], "input rule violated")
     return stats, tis_w
-
-
-def compare_summary(left, right, mask) -> Dict:
-    """The single-pair summary of "Debugging Logprob Mismatches ...", Case 1
-    ("Inspect this run's outlier and reproduce the comparison on CPU"):
-    count, signed mean, MAE, p95, p99 and maximum of |left - right| over active
-    tokens, with the page's input rules.  Restated, not copied.
-    """
-    left = np.asarray(left, dtype=np.float64)
-    right = np.asarray(right, dtype=np.float64)
-    mask = np.asarray(mask)
-    if left.ndim != 1 or left.shape != right.shape or left.shape != mask.shape:
-        raise OracleError("SHAPE", "expected equal-length, response-aligned 1-D arrays")
-    if not np.all((mask == 0) | (mask == 1)) or not np.any(mask == 1):
-        raise OracleError("BAD_MASK", "expected a binary mask with at least one active token")
-    active = mask == 1
-    if not (np.all(np.isfinite(left[active])) and np.all(np.isfinite(right[active]))):
-        raise OracleError("NONFINITE", "non-finite score on an active token")
-    delta = left[active] - right[active]
-    if not np.all(np.isfinite(delta)):
-        raise OracleError("NONFINITE", "non-finite difference")
-    err = np.abs(delta)
-    return dict(count=int(delta.size), signed_mean=float(delta.mean()), mae=float(err.mean()),
-                p95=float(np.quantile(err, 0.95)), p99=float(np.quantile(err, 0.99)),
-                maximum=float(err.max()))
-
-
-def compare_bitwise(a: Dict, b: Dict) -> Dict:
-    """Per-request bitwise compare ("Fault localization ...", Compare per-token
-    logprobs): ``a``/``b`` map request id -> (float32 scores, bool mask).
-    Request sets and masks must match.  Returns tokens, mismatched, first
-    (request, ordinal) and max_abs.
-    """
-    if set(a) != set(b):
-        raise OracleError("SHAPE", "request sets differ")
-    n = bad = 0
-    first = None
-    max_err = 0.0
-    for uid in sorted(a):
-        (x, mx), (y, my) = a[uid], b[uid]
-        mx = np.asarray(mx, dtype=bool)
-        my = np.asarray(my, dtype=bool)
-        if mx.shape != my.shape or not np.array_equal(mx, my):
-            raise OracleError("BAD_MASK", f"{uid}: masks differ")
-        xs = np.asarray(x, dtype=np.float32)[mx]
-        ys = np.asarray(y, dtype=np.float32)[my]
-        nz = np.flatnonzero(_bits(xs) != _bits(ys))
-        if nz.size and first is None:
-            first = (uid, int(nz[0]))
-        n += xs.size
-        bad += nz.size
-        if xs.size:
-            max_err = max(max_err, float(np.max(np.abs(xs.astype(np.float64) - ys.astype(np.float64)))))
-    return dict(tokens=n, mismatched=bad, first=first, max_abs=max_err)

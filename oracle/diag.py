@@ -32,9 +32,8 @@ valid sequence:
 * w2_mean = mean exp(2 d): the ratio-only second moment E_q[w^2] = exp D_2(p||q)
   -- "Rollout-Training Mismatch in LLM RL", section 5.3 (eq. 10 context).
 
-Flags follow ``oracle.compare``; sequences with more than QUANTILE_MAX_TOKENS
-active tokens get FLAG_QUANTILE_SKIPPED and NaN quantiles (the GPU kernel holds
-a sequence's keys in shared memory).
+Flags follow ``oracle.compare``.  The quantiles are defined, and computed here,
+for a sequence of any length.
 """
 from __future__ import annotations
 
@@ -46,8 +45,6 @@ import numpy as np
 from .compare import (FLAG_BAD_MASK, FLAG_BAD_OFFSETS, FLAG_EMPTY, FLAG_K3_OVERFLOW,
                       FLAG_NONFINITE, PAIRS, OracleError, _check_shapes)
 
-FLAG_QUANTILE_SKIPPED = 32
-QUANTILE_MAX_TOKENS = 16384
 QUANTILES = (0.5, 0.95, 0.99)
 
 
@@ -78,7 +75,6 @@ def _mis(d: np.ndarray, lo: float, hi: float):
 
 
 def _empty_diag(flags: int) -> Dict:
-    nan = float("nan")
     return dict(n_valid=0, abs_q50=[0.0] * 3, abs_q95=[0.0] * 3, abs_q99=[0.0] * 3,
                 prob_mae=[0.0] * 3, top1_flips=[-1] * 3, log_ratio_sum=0.0, k1_sum=0.0,
                 k3_sum=0.0, seq_tis=0.0, ratio_err_mean=0.0, mis_mean=0.0, mis_kept=0,
@@ -93,16 +89,11 @@ def _seq_diag(sets, tops, tis_cap, mis_lo, mis_hi) -> Dict:
     f64 = dict(A=A, B=B, C=C)
     for p, (l, r) in enumerate(PAIRS):
         a = np.abs(f64[l] - f64[r])
-        if n <= QUANTILE_MAX_TOKENS:
-            st["abs_q50"][p], st["abs_q95"][p], st["abs_q99"][p] = (
-                quantile_linear(a, q) for q in QUANTILES)
+        st["abs_q50"][p], st["abs_q95"][p], st["abs_q99"][p] = (
+            quantile_linear(a, q) for q in QUANTILES)
         st["prob_mae"][p] = _prob_mae(f64[l], f64[r])
         if tops[l] is not None and tops[r] is not None:
             st["top1_flips"][p] = int(np.sum(tops[l] != tops[r]))
-    if n > QUANTILE_MAX_TOKENS:
-        nan = float("nan")
-        st["abs_q50"], st["abs_q95"], st["abs_q99"] = [nan] * 3, [nan] * 3, [nan] * 3
-        st["flags"] |= FLAG_QUANTILE_SKIPPED
     d = C - A
     with np.errstate(over="ignore", invalid="ignore"):
         st["log_ratio_sum"] = float(np.sum(d))

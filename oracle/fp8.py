@@ -19,33 +19,31 @@ nor the scaling granularity; the readings taken here:
   from the codes when both scales are applied after accumulation -- then the
   same softmax definition as ``oracle.logprob``.
 
-Precision of y.  The e4m3 code of an element of y is an integer decided from
-y's bf16 value; one bf16 step of y moves that code across an e4m3 rounding
-boundary with probability about 1/16, and one code step moves a logit by up to
-~1e-2.  An fp64 RMSNorm and an fp32 one round a few y values per million to
-different bf16 neighbours, so the code decision is taken here in fp32, the
-precision the scoring kernel takes it in, with the RMSNorm reduction order
-fixed and stated ("Training and rollout stop disagreeing: vime and RL-Kernel
-...", Interpretation: the strict path pins the RMSNorm reduction domain, and a
-fixed order is what makes a reduction batch-invariant):
+y is the RMSNorm of ``oracle.logprob``: evaluated in fp64 and rounded once to
+bf16 (nearest even).
 
-* 32 partial sums; partial l adds h_i^2 for the 8-element chunks l, l+32,
-  l+64, ... of the row in increasing order (each square is exact in fp32: a
-  bf16 value has 8 significant bits), every addition rounded to fp32;
-* the partials combine by the butterfly s_l <- s_l + s_(l xor o) for
-  o = 16, 8, 4, 2, 1, rounded to fp32 (every partial ends equal);
-* rstd = 1 / sqrt(s / d + eps) and y = bf16((h * rstd) * gamma), each
-  operation rounded to fp32 (round to nearest even), then to bf16.
-
-``rmsnorm_fp32`` is that computation; ``oracle_logprob_fp8(...,
-y_precision="fp64")`` uses the fp64 RMSNorm of ``oracle.logprob`` instead.
+Admissible results.  An e4m3 code is an integer taken from y's bf16 value, and
+that bf16 value is itself a rounding decision.  An implementation that
+evaluates the RMSNorm in a narrower format (fp32) gets a value within a small
+relative distance ``margin`` of the exact one; where the exact value lies that
+close to a bf16 rounding midpoint, either bf16 neighbour is a correct rounding
+of a correct fp32 evaluation, and when the two neighbours give different e4m3
+codes (or a different row scale) the logits differ by a whole code step.
+``oracle_logprob_fp8_admissible`` lists, per row, the result of every such
+combination of choices.  Rounding is monotone, so the bf16 values reachable
+from the interval [x - margin |x|, x + margin |x|] are exactly the roundings of
+its two ends; with margin = 0 the list holds the one result of
+``oracle_logprob_fp8``.  The margin is the implementation's error bound, an
+input here.
 """
 from __future__ import annotations
 
+import itertools
 import math
 
 import numpy as np
 
+from .fp32head import rmsnorm_unrounded
 from .logprob import lse_stats, rmsnorm, round_to_bf16, widen_bf16, _top2_gap
 
 E4M3_MAX = 448.0
@@ -78,66 +76,118 @@ def quantize_rows(x: np.ndarray):
     return codes, scales
 
 
-def rmsnorm_fp32(h: np.ndarray, gamma: np.ndarray, eps: float, return_rstd: bool = False):
-    """y = bf16((h * rstd) * gamma) with every step in fp32 and the reduction order stated
-    in the module docstring.  h, gamma: fp64 arrays holding bf16 values.  Returns y as fp64
-    (and the fp32 rstd of each row with ``return_rstd``)."""
-    f32 = np.float32
-    h = np.asarray(h, dtype=np.float64)
-    T, d = h.shape
-    nvec = -(-d // 8)
-    nchunk = -(-nvec // 32)
-    hp = np.zeros((T, nchunk * 32 * 8))
-    hp[:, :d] = h
-    hp = hp.reshape(T, nchunk, 32, 8)            # [row, round, partial, element]
-    part = np.zeros((T, 32), dtype=f32)
-    for c in range(nchunk):
-        for i in range(8):
-            sq = hp[:, c, :, i] ** 2                 # exact
-            part = (part.astype(np.float64) + sq).astype(f32)
-    lanes = np.arange(32)
-    for o in (16, 8, 4, 2, 1):
-        part = part + part[:, lanes ^ o]             # fp32 additions
-    ss = part[:, 0]
-    rstd = f32(1.0) / np.sqrt(ss / f32(d) + f32(eps))
-    y32 = (h.astype(f32) * rstd[:, None]) * np.asarray(gamma, dtype=np.float64).astype(f32)[None, :]
-    y = round_to_bf16(y32.astype(np.float64))
-    return (y, rstd) if return_rstd else y
+def dequantized_weights(W_bits, vocab_block: int = 8192) -> np.ndarray:
+    """DQ(W) in fp64 [V, d], W quantised once by vocabulary row."""
+    V = W_bits.shape[0]
+    Wq = np.empty((V, W_bits.shape[1]))
+    for v0 in range(0, V, vocab_block):
+        c, s = quantize_rows(widen_bf16(W_bits[v0:v0 + vocab_block]))
+        Wq[v0:v0 + vocab_block] = c * s[:, None]
+    return Wq
+
+
+def _scores(z: np.ndarray, x: np.ndarray, V: int, temperature: float):
+    """(logprob, lse, top1, gap, zmax) of logit rows z for target ids x."""
+    s, lse = lse_stats(z, temperature)
+    ok = (x >= 0) & (x < V)
+    sx = np.full(z.shape[0], np.nan)
+    sx[ok] = s[np.flatnonzero(ok), x[ok]]
+    return sx - lse, lse, np.argmax(z, axis=1), _top2_gap(z), np.max(z, axis=1)
 
 
 def oracle_logprob_fp8(hidden_bits, gamma_bits, W_bits, token_ids, temperature: float,
-                       eps: float, row_block: int = 128, vocab_block: int = 8192,
-                       y_precision: str = "fp32"):
-    """Scores with FP8-quantised y and W.  Same output dict as oracle_logprob."""
-    if y_precision not in ("fp32", "fp64"):
-        raise ValueError("y_precision must be 'fp32' or 'fp64'")
-    norm = rmsnorm_fp32 if y_precision == "fp32" else rmsnorm
+                       eps: float, row_block: int = 128, vocab_block: int = 8192, Wq=None):
+    """Scores with FP8-quantised y and W.  Same output dict as oracle_logprob.
+    ``Wq``: DQ(W) from ``dequantized_weights``, to reuse across calls."""
     hidden_bits = np.asarray(hidden_bits, dtype=np.uint16)
     T = hidden_bits.shape[0]
     V = W_bits.shape[0]
     ids = np.asarray(token_ids, dtype=np.int64)
     gamma = widen_bf16(gamma_bits)
-    # W quantised once, by vocabulary row
-    Wq = np.empty((V, W_bits.shape[1]))
-    for v0 in range(0, V, vocab_block):
-        c, s = quantize_rows(widen_bf16(W_bits[v0:v0 + vocab_block]))
-        Wq[v0:v0 + vocab_block] = c * s[:, None]
+    if Wq is None:
+        Wq = dequantized_weights(W_bits, vocab_block)
     out = dict(logprob=np.empty(T), lse=np.empty(T), top1=np.empty(T, dtype=np.int64),
                gap=np.empty(T), zmax=np.empty(T), bad_token=(ids < 0) | (ids >= V),
                nonfinite=np.zeros(T, dtype=bool))
     for r0 in range(0, T, row_block):
         r1 = min(T, r0 + row_block)
-        y = norm(widen_bf16(hidden_bits[r0:r1]), gamma, eps)
+        y = rmsnorm(widen_bf16(hidden_bits[r0:r1]), gamma, eps)
         cy, sy = quantize_rows(y)
         z = (cy * sy[:, None]) @ Wq.T
-        s, lse = lse_stats(z, temperature)
-        x = ids[r0:r1]
-        ok = (x >= 0) & (x < V)
-        sx = np.full(r1 - r0, np.nan)
-        sx[ok] = s[np.flatnonzero(ok), x[ok]]
-        out["logprob"][r0:r1] = sx - lse
-        out["lse"][r0:r1] = lse
-        out["top1"][r0:r1] = np.argmax(z, axis=1)
-        out["zmax"][r0:r1] = np.max(z, axis=1)
-        out["gap"][r0:r1] = _top2_gap(z)
+        res = _scores(z, ids[r0:r1], V, temperature)
+        for k, v in zip(("logprob", "lse", "top1", "gap", "zmax"), res):
+            out[k][r0:r1] = v
     return out
+
+
+def bf16_choices(x: np.ndarray, margin: float):
+    """The bf16 roundings of every value within relative distance ``margin`` of x:
+    (lo, hi) arrays, equal where only one rounding is reachable.  Rounding is
+    monotone, so the two ends of the interval give them all (margin < 2^-10, far
+    below half a bf16 step, so the interval holds at most one midpoint)."""
+    if not 0.0 <= margin < 2.0 ** -10:
+        raise ValueError("margin must lie in [0, 2^-10)")
+    x = np.asarray(x, dtype=np.float64)
+    r = np.abs(x) * margin
+    return round_to_bf16(x - r), round_to_bf16(x + r)
+
+
+def _row_alternatives(x_row: np.ndarray, margin: float):
+    """For one row of exact (unrounded) y values: the base bf16 row, and the
+    elements whose bf16 choice can change the row's codes or its scale, each with
+    its other admissible value."""
+    base = round_to_bf16(x_row)
+    lo, hi = bf16_choices(x_row, margin)
+    amb = np.flatnonzero(lo != hi)
+    if amb.size == 0:
+        return base, amb, np.empty(0)
+    other = np.where(lo[amb] == base[amb], hi[amb], lo[amb])
+    fixed = np.ones(base.shape[0], dtype=bool)
+    fixed[amb] = False
+    amax_fixed = float(np.max(np.abs(base[fixed]))) if fixed.any() else 0.0
+    # every row maximum a choice can produce, hence every scale
+    cand = [amax_fixed] + [float(v) for v in np.abs(np.concatenate([base[amb], other]))
+                           if v > amax_fixed]
+    scales = sorted({fp8_scale(a) for a in cand})
+    keep = np.zeros(amb.size, dtype=bool)
+    for s in scales:
+        keep |= e4m3_round(base[amb] / s) != e4m3_round(other / s)
+    keep |= np.maximum(np.abs(base[amb]), np.abs(other)) > amax_fixed   # may set the scale
+    return base, amb[keep], other[keep]
+
+
+def oracle_logprob_fp8_admissible(hidden_bits, gamma_bits, W_bits, token_ids,
+                                  temperature: float, eps: float, margin: float,
+                                  max_choices: int = 8, Wq=None):
+    """Every FP8-head result reachable from the exact y by bf16 roundings of
+    values within relative distance ``margin`` (module docstring).
+
+    Returns a list with one entry per row: a list of dicts (logprob, lse, top1,
+    gap), the first being ``oracle_logprob_fp8``'s own result; or None when more
+    than ``max_choices`` elements of the row are ambiguous (2^k alternatives)."""
+    hidden_bits = np.asarray(hidden_bits, dtype=np.uint16)
+    V = W_bits.shape[0]
+    ids = np.asarray(token_ids, dtype=np.int64)
+    gamma = widen_bf16(gamma_bits)
+    if Wq is None:
+        Wq = dequantized_weights(W_bits)
+    x_all = rmsnorm_unrounded(widen_bf16(hidden_bits), gamma, eps)
+    rows = []
+    for t in range(hidden_bits.shape[0]):
+        base, idx, other = _row_alternatives(x_all[t], margin)
+        if idx.size > max_choices:
+            rows.append(None)
+            continue
+        ys = []
+        for pick in itertools.product((False, True), repeat=int(idx.size)):
+            y = base.copy()
+            sel = np.array(pick, dtype=bool)
+            y[idx[sel]] = other[sel]
+            ys.append(y)
+        Y = np.stack(ys)
+        cy, sy = quantize_rows(Y)
+        z = (cy * sy[:, None]) @ Wq.T
+        lp, lse, top1, gap, _ = _scores(z, np.full(Y.shape[0], ids[t]), V, temperature)
+        rows.append([dict(logprob=float(lp[i]), lse=float(lse[i]), top1=int(top1[i]),
+                          gap=float(gap[i])) for i in range(Y.shape[0])])
+    return rows

@@ -315,16 +315,20 @@ def _one_seq(A, B, C, mask=None, cap=2.0):
 
 
 def pin_recorded_token_summary():
-    """The Case 1 outlier token: compare() summaries reproduce the printed differences."""
+    """The Case 1 outlier token: the per-pair statistics of a one-token sequence reproduce the
+    printed differences (signed mean to 6 places, MAE and maximum equal to its size)."""
     gd = golden("recorded_token_case1.json")
-    s = gd["scores"]
+    sc = gd["scores"]
     for label, want in gd["signed_differences_6dp"].items():
         l, r = label.split("-")
-        res = oracle.compare_summary([s[l]], [s[r]], [1])
-        assert res["count"] == 1
-        assert round(res["signed_mean"], 6) == want, (label, res["signed_mean"], want)
-        assert round(res["mae"], 6) == abs(want)
-        assert res["maximum"] == res["p95"] == res["p99"] == res["mae"]
+        st, _ = _one_seq([sc[l]], [sc[r]], [sc[r]])
+        pr = st["pair"][0]
+        assert st["n_valid"] == 1
+        # A is printed with more digits than a float32 holds: the pair sees its float32 value
+        want_exact = float(np.float64(np.float32(sc[l])) - np.float64(np.float32(sc[r])))
+        assert pr["signed_mean"] == want_exact
+        assert round(pr["signed_mean"], 6) == want, (label, pr["signed_mean"], want)
+        assert pr["mae"] == pr["max_abs_diff"] == abs(want_exact)
 
 
 def pin_recorded_token_bitwise():
@@ -507,34 +511,26 @@ def pin_error_contract():
             assert e.code == code, (code, e.code)
         else:
             raise AssertionError(f"expected {code}")
-    for bad in (([1.0], [1.0, 2.0], [1, 1]), ([1.0, 2.0], [1.0, 2.0], [0, 0]),
-                ([1.0, 2.0], [1.0, 2.0], [1, 2]), ([np.inf, 2.0], [1.0, 2.0], [1, 1])):
-        try:
-            oracle.compare_summary(*bad)
-        except oracle.OracleError:
-            pass
-        else:
-            raise AssertionError("compare_summary must reject " + repr(bad))
 
 
 def pin_bitwise_requests():
-    """compare_logprobs semantics: request sets and masks must match; tokens, mismatched,
-    first (request, ordinal), max_abs."""
-    x1 = np.array([-1.0, -2.0, -3.0], np.float32)
-    y1 = np.array([-1.0, -2.5, -3.0], np.float32)
-    m1 = np.array([True, True, True])
-    x2 = np.array([-0.5, -0.25], np.float32)
-    m2 = np.array([False, True])
-    res = oracle.compare_bitwise({"r1": (x1, m1), "r2": (x2, m2)}, {"r1": (y1, m1), "r2": (x2, m2)})
-    assert res == dict(tokens=4, mismatched=1, first=("r1", 1), max_abs=0.5)
-    for a, b in (({"r1": (x1, m1)}, {"r2": (x1, m1)}),
-                 ({"r1": (x1, m1)}, {"r1": (x1, np.array([True, False, True]))})):
-        try:
-            oracle.compare_bitwise(a, b)
-        except oracle.OracleError:
-            pass
-        else:
-            raise AssertionError("must raise")
+    """Two responses scored twice, one token changed by 0.5 in the first and a masked
+    token changed in the second: per sequence the mismatch count, first divergence
+    (active ordinal) and maximum |difference| are the hand-counted values, and a change on
+    a masked token is not seen."""
+    x = np.array([-1.0, -2.0, -3.0, -0.5, -0.25], np.float32)
+    y = x.copy()
+    y[1] = -2.5                       # sequence 0, ordinal 1
+    y[3] = -7.0                       # sequence 1, masked out
+    mask = np.array([1, 1, 1, 0, 1], np.uint8)
+    offs = np.array([0, 3, 5], np.int64)
+    st, _ = oracle.oracle_compare(x, y, y, offs, mask, 2.0)
+    s0, s1 = st[0]["pair"][0], st[1]["pair"][0]
+    assert (st[0]["n_valid"], st[1]["n_valid"]) == (3, 1)
+    assert (s0["mismatch_count"], s0["first_div"], s0["longest_run"]) == (1, 1, 1)
+    assert s0["max_abs_diff"] == 0.5 and s0["signed_mean"] == 0.5 / 3
+    assert (s1["mismatch_count"], s1["first_div"], s1["max_abs_diff"]) == (0, -1, 0.0)
+    assert sum(q["pair"][0]["mismatch_count"] for q in st) == 1
 
 
 def pin_shift_fault_detected():
@@ -663,12 +659,26 @@ def pin_diag_recorded_token():
     assert round(want, 6) == gd["signed_differences_6dp"]["B0-B1"]
 
 
-def pin_diag_quantile_limit():
-    n = oracle.QUANTILE_MAX_TOKENS + 1
-    A = np.zeros(n, np.float32)
-    st = _diag1(A, A, A)
-    assert st["flags"] & oracle.FLAG_QUANTILE_SKIPPED and math.isnan(st["abs_q50"][0])
-    assert st["n_valid"] == n and st["k3_sum"] == 0.0
+def pin_diag_quantiles_long_sequence():
+    """Quantiles at any length: |A - B| = float32(k / 1000) for k = 0..40000 in a shuffled
+    order with masked tokens between them; type-7 interpolation lands on order statistics
+    k = 20000, 38000 and 39600 exactly (h = 40000 q is an integer)."""
+    n = 40001
+    g = np.random.default_rng(11)
+    vals = (np.arange(n) / 1000.0).astype(np.float32)
+    g.shuffle(vals)
+    A = np.zeros(2 * n, np.float32)
+    A[0::2] = vals
+    A[1::2] = np.float32(9.0)                      # masked: must not enter the statistics
+    mask = np.zeros(2 * n, np.uint8)
+    mask[0::2] = 1
+    B = np.zeros(2 * n, np.float32)
+    out = oracle.oracle_diag(A, B, B, np.array([0, 2 * n], np.int64), mask, 2.0, 0.5, 2.0)
+    st = out[0]
+    assert st["n_valid"] == n and st["flags"] == 0
+    for key, k in (("abs_q50", 20000), ("abs_q95", 38000), ("abs_q99", 39600)):
+        assert st[key][0] == float(np.float32(k / 1000.0)), (key, st[key][0])
+        assert st[key][1] == 0.0
 
 
 # ---------------------------------------------------------------------------
@@ -849,8 +859,7 @@ def pin_fp8_quantized_dot_product():
     """Random rows: z_fp8 = (Q(y) s_y) . (Q(W) s_W) written out term by term in exact rational
     arithmetic matches the oracle's logits to 1e-12."""
     b = synth.make_custom(T=2, d=64, V=12, tag="fp8dot")
-    y = oracle.rmsnorm_fp32(oracle.widen_bf16(b.hidden_gen), oracle.widen_bf16(b.head.gamma),
-                            b.eps)
+    y = oracle.rmsnorm(oracle.widen_bf16(b.hidden_gen), oracle.widen_bf16(b.head.gamma), b.eps)
     Wf = oracle.widen_bf16(b.head.W)
     out = oracle.oracle_logprob_fp8(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 1.0, b.eps)
     for t in range(2):
@@ -867,68 +876,110 @@ def pin_fp8_quantized_dot_product():
         assert abs(out["logprob"][t] - (zs[b.token_ids[t]] - lse)) < 1e-12
 
 
+def pin_fp8_y_is_the_bf16_heads_y():
+    """The FP8 head quantises the y of the bf16 head: fp64 RMSNorm (torch's rms_norm, a
+    routine the oracle does not call) rounded once to the nearest bf16 (table search).
+    Logits built from that y and the pinned quantiser give the oracle's lse to 1e-12."""
+    import torch
+    b = synth.make_custom(T=6, d=64, V=20, tag="fp8y")
+    h64 = torch.from_numpy(oracle.widen_bf16(b.hidden_gen))
+    g64 = torch.from_numpy(oracle.widen_bf16(b.head.gamma))
+    y = brute_nearest_bf16(torch.nn.functional.rms_norm(h64, (64,), g64, eps=b.eps).numpy())
+    cy, sy = oracle.quantize_rows(y)
+    cw, sw = oracle.quantize_rows(oracle.widen_bf16(b.head.W))
+    z = (cy * sy[:, None]) @ (cw * sw[:, None]).T
+    m = z.max(axis=1)
+    lse = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+    out = oracle.oracle_logprob_fp8(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 1.0, b.eps)
+    assert np.max(np.abs(out["lse"] - lse)) < 1e-12, np.max(np.abs(out["lse"] - lse))
+
+
 def _f32(x: float) -> float:
     """Round a Python float (fp64) to the nearest fp32 value, ties to even."""
     return struct.unpack("<f", struct.pack("<f", x))[0]
 
 
-def _rmsnorm_fp32_scalar(h_row, g_row, eps):
-    """The fixed-order fp32 RMSNorm of one row written as plain scalar steps: 32 partial
-    sums over interleaved 8-element chunks, a butterfly over the partials, then
-    rstd and y.  Rounding fp64 results of +, /, sqrt to fp32 equals the fp32 operation
-    itself (fp64 carries more than 2 x 24 + 2 bits, so the double rounding is harmless)."""
-    d = len(h_row)
-    part = [0.0] * 32
-    for c in range(0, -(-d // 8)):
-        lane = c % 32
-        for i in range(8):
-            k = 8 * c + i
-            if k < d:
-                sq = h_row[k] * h_row[k]
-                assert Fraction(part[lane]) + Fraction(sq) == Fraction(part[lane] + sq)
-                part[lane] = _f32(part[lane] + sq)
-    for o in (16, 8, 4, 2, 1):
-        part = [_f32(part[l] + part[l ^ o]) for l in range(32)]
-    assert len(set(part)) == 1
-    rstd = _f32(1.0 / _f32(math.sqrt(_f32(_f32(part[0] / d) + _f32(eps)))))
-    y = [_f32(_f32(h_row[k] * rstd) * g_row[k]) for k in range(d)]
-    return y, rstd
+def pin_bf16_choices_brute():
+    """bf16_choices against brute force: the set of nearest-bf16 roundings (table search)
+    of 64 points spread over [x - m|x|, x + m|x|] equals {lo, hi}, on values placed at,
+    near and away from rounding midpoints."""
+    vals, _ = _all_finite_bf16()
+    g = np.random.default_rng(5)
+    i = np.flatnonzero((np.abs(vals[:-1]) > 1e-30) & (np.abs(vals[1:]) < 1e30))
+    i = g.choice(i, 400)
+    a = vals[i]
+    mids = (vals[i] + vals[i + 1]) / 2                       # rounding midpoints
+    xs = np.concatenate([mids, mids * (1 + 3e-7), mids * (1 - 3e-7), a, g.standard_normal(200)])
+    for m in (0.0, 1e-7, 4.3e-6):
+        lo, hi = oracle.bf16_choices(xs, m)
+        for i, x in enumerate(xs):
+            pts = x + np.linspace(-1.0, 1.0, 65) * abs(x) * m
+            got = set(brute_nearest_bf16(pts).tolist())
+            assert got == {float(lo[i]), float(hi[i])}, (x, m, got, lo[i], hi[i])
+    lo, hi = oracle.bf16_choices(mids, 1e-6)
+    assert np.all(lo < hi)                                   # a midpoint is always ambiguous
 
 
-def pin_rmsnorm_fp32_scalar():
-    """The vectorised fixed-order fp32 RMSNorm equals the same steps written as scalar
-    Python arithmetic rounded to fp32 after every operation (rstd bit-exact, y bit-exact),
-    for d with a partial last round of chunks (320) and with fewer chunks than partials
-    (96)."""
-    for d, tag in ((320, "r320"), (96, "r96")):
-        b = synth.make_custom(T=12, d=d, V=4, tag=tag)
-        h = oracle.widen_bf16(b.hidden_gen)
-        g = oracle.widen_bf16(b.head.gamma)
-        y, rstd = oracle.rmsnorm_fp32(h, g, b.eps, return_rstd=True)
-        for t in range(h.shape[0]):
-            ys, rs = _rmsnorm_fp32_scalar([float(v) for v in h[t]], [float(v) for v in g], b.eps)
-            assert float(rstd[t]) == rs, (d, t)
-            assert np.array_equal(y[t], oracle.round_to_bf16(np.array(ys))), (d, t)
+def pin_fp8_admissible_margin_zero():
+    """With margin 0 the admissible set is the oracle's own result, alone."""
+    b = synth.make_custom(T=5, d=128, V=50, temperature=0.8, tag="adm0")
+    out = oracle.oracle_logprob_fp8(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, 0.8, b.eps)
+    adm = oracle.oracle_logprob_fp8_admissible(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids,
+                                               0.8, b.eps, 0.0)
+    for t, alts in enumerate(adm):
+        assert len(alts) == 1
+        assert alts[0]["logprob"] == out["logprob"][t] and alts[0]["top1"] == out["top1"][t]
 
 
-def pin_rmsnorm_fp32_against_fp64():
-    """The fp32 RMSNorm agrees with the fp64 one: rstd to 2^-18 relative, y within one bf16
-    step everywhere and equal in all but a few elements per 10^4; with |h| = 2 everywhere
-    and eps = 0 every step is exact and both equal (h / 2) * gamma rounded to bf16."""
-    b = synth.make_custom(T=64, d=2048, V=4, tag="r2048")
+def _rmsnorm_fp32_generic(h, g, eps, order):
+    """An fp32 RMSNorm in a generic summation order ('fwd': one running sum in element
+    order, 'rev': reversed, 'pair': numpy's float32 pairwise sum), every other step in fp32
+    as the textbook formula reads.  Not any kernel's order."""
+    f32 = np.float32
+    sq = (h * h).astype(f32)                                  # exact: 8-bit significands
+    if order == "pair":
+        ss = np.sum(sq, axis=1, dtype=f32)
+    else:
+        cols = range(h.shape[1]) if order == "fwd" else range(h.shape[1] - 1, -1, -1)
+        ss = np.zeros(h.shape[0], f32)
+        for k in cols:
+            ss = ss + sq[:, k]
+    rstd = f32(1.0) / np.sqrt(ss / f32(h.shape[1]) + f32(eps))
+    y32 = (h.astype(f32) * rstd[:, None]) * g.astype(f32)[None, :]
+    return oracle.round_to_bf16(y32.astype(np.float64))
+
+
+def pin_fp8_admissible_covers_fp32_evaluations():
+    """fp32 RMSNorms in three generic orders, each followed by the FP8 quantisation and an
+    fp64 head, land inside the admissible set taken with their error bound
+    ((d + 1) / 2 + 5) 2^-24 (sum of d squares, /d, + eps, sqrt, 1/x, two products), and
+    some of them really take the other rounding (so the set is not the base alone)."""
+    d, T, V = 512, 12000, 16
+    b = synth.make_custom(T=T, d=d, V=V, tag="adm32")
     h = oracle.widen_bf16(b.hidden_gen)
     g = oracle.widen_bf16(b.head.gamma)
-    y32, rstd = oracle.rmsnorm_fp32(h, g, b.eps, return_rstd=True)
-    rstd64 = 1.0 / np.sqrt(np.mean(h * h, axis=1) + b.eps)
-    assert np.max(np.abs(rstd / rstd64 - 1.0)) < 2.0 ** -18
-    y64 = oracle.rmsnorm(h, g, b.eps)
-    step = np.ldexp(1.0, np.frexp(np.maximum(np.abs(y32), np.abs(y64)))[1] - 8)
-    assert np.all(np.abs(y32 - y64) <= step)
-    assert np.mean(y32 != y64) < 1e-3
-    hh = np.where(np.arange(256) % 3 == 0, -2.0, 2.0)[None, :].repeat(3, axis=0)
-    gg = oracle.widen_bf16(b.head.gamma[:256])
-    assert np.array_equal(oracle.rmsnorm_fp32(hh, gg, 0.0), oracle.round_to_bf16(hh / 2 * gg))
-    assert np.array_equal(oracle.rmsnorm(hh, gg, 0.0), oracle.rmsnorm_fp32(hh, gg, 0.0))
+    margin = ((d + 1) / 2 + 5) * 2.0 ** -24
+    Wq = oracle.dequantized_weights(b.head.W)
+    base_y = oracle.rmsnorm(h, g, b.eps)
+    ys = {o: _rmsnorm_fp32_generic(h, g, b.eps, o) for o in ("fwd", "rev", "pair")}
+    moved = np.zeros(T, dtype=bool)
+    for y in ys.values():
+        cb, sb = oracle.quantize_rows(base_y)
+        cy, sy = oracle.quantize_rows(y)
+        moved |= np.any(cb * sb[:, None] != cy * sy[:, None], axis=1)
+    rows = np.flatnonzero(moved)
+    assert rows.size >= 3, rows.size                         # the pin has teeth
+    adm = oracle.oracle_logprob_fp8_admissible(b.hidden_gen[rows], b.head.gamma, b.head.W,
+                                               b.token_ids[rows], 1.0, b.eps, margin, Wq=Wq)
+    for y in ys.values():
+        cy, sy = oracle.quantize_rows(y[rows])
+        z = (cy * sy[:, None]) @ Wq.T
+        m = z.max(axis=1)
+        lse = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+        for i, t in enumerate(rows):
+            alts = adm[i]
+            assert alts is not None and len(alts) >= 2
+            assert min(abs(a["lse"] - lse[i]) for a in alts) < 1e-12, (t, lse[i])
 
 
 # ---------------------------------------------------------------------------

@@ -211,26 +211,26 @@ def _scale_max_over_448(amax):
     return amax / 448.0 if amax else 1.0
 
 
-_orig_rmsnorm_fp32 = of8.rmsnorm_fp32
+def _fp8_y_unrounded(h, gamma, eps):
+    return h * (1.0 / np.sqrt(np.mean(h * h, axis=1) + eps))[:, None] * gamma[None, :]
 
 
-def _rms32_in_fp64(h, gamma, eps, return_rstd=False):
-    h = np.asarray(h, dtype=np.float64)
-    rstd = 1.0 / np.sqrt(np.mean(h * h, axis=1) + eps)
-    y = ol.round_to_bf16(h * rstd[:, None] * np.asarray(gamma)[None, :])
-    return (y, rstd) if return_rstd else y
+def _choices_none(x, margin):
+    r = ol.round_to_bf16(x)
+    return r, r
 
 
-def _rms32_sequential_partials(h, gamma, eps, return_rstd=False):
-    f32 = np.float32
-    h = np.asarray(h, dtype=np.float64)
-    ss = np.zeros(h.shape[0], dtype=f32)
-    for k in range(h.shape[1]):                      # one running sum, element order
-        ss = (ss.astype(np.float64) + h[:, k] ** 2).astype(f32)
-    rstd = f32(1.0) / np.sqrt(ss / f32(h.shape[1]) + f32(eps))
-    y = ol.round_to_bf16(((h.astype(f32) * rstd[:, None]) *
-                          np.asarray(gamma).astype(f32)[None, :]).astype(np.float64))
-    return (y, rstd) if return_rstd else y
+def _choices_one_sided(x, margin):
+    x = np.asarray(x, dtype=np.float64)
+    return ol.round_to_bf16(x), ol.round_to_bf16(x + np.abs(x) * margin)
+
+
+_orig_row_alternatives = of8._row_alternatives
+
+
+def _alternatives_wrong_other(x_row, margin):
+    base, idx, other = _orig_row_alternatives(x_row, margin)
+    return base, idx, 2 * base[idx] - other                 # mirrored: not a rounding of x
 
 
 import oracle.fp32head as of32
@@ -323,10 +323,14 @@ MUTATIONS = [
     ("e4m3 with two mantissa bits", of8, "e4m3_round", _e4m3_two_mantissa_bits,
      ["pin_e4m3_rounding_exhaustive"]),
     ("non-power-of-two scale", of8, "fp8_scale", _scale_max_over_448, ["pin_fp8_scale_rule"]),
-    ("fp32 RMSNorm computed in fp64", of8, "rmsnorm_fp32", _rms32_in_fp64,
-     ["pin_rmsnorm_fp32_scalar"]),
-    ("fp32 RMSNorm with one running sum", of8, "rmsnorm_fp32", _rms32_sequential_partials,
-     ["pin_rmsnorm_fp32_scalar"]),
+    ("FP8 y not rounded to bf16", of8, "rmsnorm", _fp8_y_unrounded,
+     ["pin_fp8_y_is_the_bf16_heads_y"]),
+    ("admissible set without the other rounding", of8, "bf16_choices", _choices_none,
+     ["pin_bf16_choices_brute", "pin_fp8_admissible_covers_fp32_evaluations"]),
+    ("admissible set rounds one end only", of8, "bf16_choices", _choices_one_sided,
+     ["pin_bf16_choices_brute"]),
+    ("admissible alternative is not a rounding", of8, "_row_alternatives",
+     _alternatives_wrong_other, ["pin_fp8_admissible_covers_fp32_evaluations"]),
     ("FP32 head rounds y to bf16", of32, "rmsnorm_unrounded", _rms_unrounded_but_rounded,
      ["pin_fp32_head_mpmath", "pin_fp32_head_torch"]),
     ("FP32 head eps outside the sqrt", of32, "rmsnorm_unrounded", _rms_unrounded_eps_outside,
