@@ -32,8 +32,8 @@ WORKLOAD = ("Qwen3-8B-shaped head: T=32768 rows (8 samples x 4096: 1024 shared p
 L2_NOTE = "inputs larger than L2 (W 1.245 GB + hidden 268 MB per step vs 129 MB L2)"
 
 # DRAM bytes per lmhead_lse launch of this workload (T=32768, d=4096, V=151936),
-# measured by a one-pass ncu capture of the full-size launch
-# (profiles/lmhead_lse_T32768_dram.md): 9.310 GB read + 0.315 GB written.  Valid
+# measured by a one-pass ncu capture of the full-size launch: 9.310 GB read +
+# 0.315 GB written.  Valid
 # only for the kernel sources hashed here (code lines only: comments and blank
 # lines do not enter the hash) and for T = 32768.
 TRAFFIC_CAPTURE = dict(sources={"lmhead_lse.cu": "d5dfbf3dbdbd0d35",
@@ -101,6 +101,99 @@ def load_peaks():
 
 
 # ------------------------------------------------------------------------------ clocks
+
+class NvmlSampler:
+    """SM clock, power and clock-event reasons of this process's GPU, read through NVML
+    (queries only; no setting is changed) every ``period_s`` on a background thread
+    while the timed region runs."""
+
+    # nvmlClocksEventReason bits
+    REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
+               (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
+
+    def __init__(self, gpu_uuid, period_s=0.01):
+        import ctypes
+        import threading
+        self.ok = False
+        self.rows = []
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return
+        self.lib = lib
+        if lib.nvmlInit_v2() != 0:
+            return
+        self.dev = ctypes.c_void_p()
+        found = False
+        if gpu_uuid:
+            u = gpu_uuid if gpu_uuid.upper().startswith("GPU-") else "GPU-" + gpu_uuid
+            found = lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(self.dev)) == 0
+        if not found:
+            n = ctypes.c_uint()
+            if lib.nvmlDeviceGetCount_v2(ctypes.byref(n)) != 0 or n.value != 1 or \
+                    lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.dev)) != 0:
+                lib.nvmlShutdown()
+                return
+        self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        self.smax = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(
+            self.dev, 1, ctypes.byref(mx)) == 0 else None
+        self.ok = True
+        self.period = period_s
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def _sample(self):
+        import ctypes
+        clk, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(clk)) != 0:   # NVML_CLOCK_SM
+            return None
+        power = mw.value / 1e3 if self.lib.nvmlDeviceGetPowerUsage(self.dev, ctypes.byref(mw)) == 0 else 0.0
+        reasons = rs.value if self.reason_fn(self.dev, ctypes.byref(rs)) == 0 else 0
+        return dict(t=time.perf_counter(), sm=float(clk.value), power=power, reasons=reasons)
+
+    def _run(self):
+        while not self._stop.is_set():
+            r = self._sample()
+            if r is not None:
+                self.rows.append(r)
+            self._stop.wait(self.period)
+
+    def stop(self):
+        if not self.ok:
+            return None
+        self._stop.set()
+        self._thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+        rows = self.rows
+        if not rows:
+            return None
+        reasons = sorted({name for r in rows for bit, name in self.REASONS if r["reasons"] & bit})
+        bins = {}
+        for r in rows:
+            key = f"{int(r['sm'] // 100) * 100}-{int(r['sm'] // 100) * 100 + 99}"
+            bins[key] = bins.get(key, 0) + 1
+        span = rows[-1]["t"] - rows[0]["t"]
+        return dict(source="nvml", period_ms=1e3 * self.period,
+                    sm_mhz=statistics.median(r["sm"] for r in rows),
+                    sm_max_mhz=self.smax or max(r["sm"] for r in rows), reasons=reasons,
+                    samples=len(rows), samples_under_load=len(rows),
+                    sampled_span_s=round(span, 3),
+                    sm_mhz_bins=dict(sorted(bins.items())),
+                    sm_mhz_min=min(r["sm"] for r in rows), sm_mhz_max=max(r["sm"] for r in rows),
+                    power_w_max=max(r["power"] for r in rows),
+                    power_w_median=statistics.median(r["power"] for r in rows))
+
+
+def start_clock_record(torch, rank):
+    """In-process NVML sampling (10 ms) where NVML loads, else nvidia-smi (200 ms)."""
+    if rank != 0:
+        return None
+    s = NvmlSampler(gpu_uuid(torch))
+    return s if s.ok else ClockSampler(gpu_uuid(torch))
+
 
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples during the timed region."""
@@ -479,7 +572,7 @@ def main():
 
     ev_all = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(gpu_uuid(torch)) if rank == 0 else None
+    clocks = start_clock_record(torch, rank)
     barrier(dist, dev)
     torch.cuda.synchronize()
     start.record(stream)
@@ -500,7 +593,11 @@ def main():
 
     flops = 2.0 * T * d * V
     achieved_tflops = flops / (gemm_ms / 1e3) / 1e12
-    peak = peaks["bf16_sustained"]
+    # the burst peak (a GEMM timed alone for a short while) for a timed region under
+    # 2 s, the sustained one (seconds under the power cap) for longer regions
+    short_region = total_ms < 2000.0
+    peak = peaks["bf16"] if short_region else peaks["bf16_sustained"]
+    peak_other = peaks["bf16_sustained"] if short_region else peaks["bf16"]
 
     # ---------------------------------------------------------------- end to end (host buffers)
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -695,6 +792,41 @@ def main():
             rmsnorm_backward_ms=round(rms_ms, 3),
             rmsnorm_backward_GBps=round(rms_bytes / (rms_ms / 1e3) / 1e9, 1))
         del bws, dy_b, dW_b, rws, dh_b, dg_b
+        # the other two scoring workloads, whole tim_logprob calls: the Qwen3-1.7B-shaped
+        # head (T = 8192, d = 2048, tau = 1.0) and the long-rollout head (T = 131072,
+        # d = 5120, tau = 0.7).  Inputs are drawn on the device (seeded torch generator)
+        # with the workloads' shapes and value distributions; token ids are uniform here
+        # (the ids do not enter the time).
+        for name, (Tw, dw, tw) in (("qwen3_1p7b", (8192, 2048, 1.0)),
+                                   ("long_5120", (131072, 5120, 0.7))):
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(1234)
+            Ww = (torch.randn(V, dw, generator=gen, device=dev) * (2.0 / dw ** 0.5)).to(torch.bfloat16)
+            hw = torch.randn(Tw, dw, generator=gen, device=dev).to(torch.bfloat16)
+            gw = (1.0 + 0.05 ** 0.5 * torch.randn(dw, generator=gen, device=dev)).to(torch.bfloat16)
+            iw = torch.randint(0, V, (Tw,), generator=gen, device=dev, dtype=torch.int32)
+            wsw = tim.Workspace(tim.logprob_workspace_size(Tw, dw, V), dev)
+            ow = (torch.empty(Tw, device=dev), torch.empty(Tw, device=dev),
+                  torch.empty(Tw, dtype=torch.int32, device=dev))
+            for _ in range(2):
+                tim.logprob(hw, gw, Ww, iw, tw, eps, out=ow, workspace=wsw, check=False)
+            reps = 5 if Tw > 16384 else 20
+            e_a.record(stream)
+            for _ in range(reps):
+                tim.logprob(hw, gw, Ww, iw, tw, eps, out=ow, workspace=wsw, check=False)
+            e_b.record(stream)
+            torch.cuda.synchronize()
+            wsw.check(name)
+            wms = e_a.elapsed_time(e_b) / reps
+            wtf = 2.0 * Tw * dw * V / (wms / 1e3) / 1e12
+            extras[name] = dict(T=Tw, d=dw, V=V, temperature=tw, ms=round(wms, 3),
+                                tokens_per_s=round(Tw / (wms / 1e3), 1), TFLOPs=round(wtf, 1),
+                                frac_of_burst=round(wtf / peaks["bf16"], 3),
+                                frac_of_sustained=round(wtf / peaks["bf16_sustained"], 3),
+                                note="whole tim_logprob calls (RMSNorm, LM head, finalize); "
+                                     "inputs drawn on the device, seeded")
+            del Ww, hw, gw, iw, wsw, ow
+        torch.cuda.empty_cache()
         G = 8
         e_a.record(stream)
         for _ in range(2):
@@ -710,7 +842,7 @@ def main():
     decode = None
     if not args.no_decode and rank == 0 and world == 1:
         decode = {}
-        for M in (1, 7, 64):
+        for M in (1, 7, 64, 128, 200, 256, 320, 384, 448, 512, 513, 1024):
             wsm = tim.Workspace(tim.logprob_workspace_size(M, d, V), dev)
             outm = (torch.empty(M, device=dev), torch.empty(M, device=dev),
                     torch.empty(M, dtype=torch.int32, device=dev))
@@ -733,11 +865,17 @@ def main():
             call_us = 1e3 * t_a.elapsed_time(t_b) / iters
             gemm_us = 1e3 * statistics.median(e[1].elapsed_time(e[2]) for e in evs)
             nbytes = 2.0 * V * d + 2.0 * M * d
+            # roofline time: the larger of the W (+ hidden) read at the measured copy
+            # bandwidth and 2 M d V FLOP at the measured burst bf16 peak
+            roof_us = max(nbytes / peaks["hbm_gbs"] / 1e3, 2.0 * M * d * V / peaks["bf16"] / 1e6)
             decode[f"M{M}"] = dict(call_us=round(call_us, 2), gemm_us=round(gemm_us, 2),
                                    call_GBps=round(nbytes / call_us / 1e3, 1),
                                    gemm_GBps=round(nbytes / gemm_us / 1e3, 1),
                                    gemm_frac_of_hbm=round(nbytes / gemm_us / 1e3 / peaks["hbm_gbs"], 3),
-                                   call_frac_of_hbm=round(nbytes / call_us / 1e3 / peaks["hbm_gbs"], 3))
+                                   call_frac_of_hbm=round(nbytes / call_us / 1e3 / peaks["hbm_gbs"], 3),
+                                   roofline_us=round(roof_us, 2),
+                                   call_frac_of_roofline=round(roof_us / call_us, 3),
+                                   gemm_frac_of_roofline=round(roof_us / gemm_us, 3))
 
     # ---------------------------------------------------------------- CPU baseline (oracle)
     cpu = None
@@ -760,8 +898,15 @@ def main():
                           traffic_unit="DRAM bytes per launch (one-pass ncu capture of this launch)",
                           algorithmic_bytes=2.0 * V * d + 2.0 * T * d,
                           kernel="lmhead_lse_kernel",
-                          peak_source=f"{peaks['source']} bf16 sustained",
-                          frac_of_burst=achieved_tflops / peaks["bf16"],
+                          peak_source=(f"{peaks['source']} bf16 "
+                                       f"{'burst' if short_region else 'sustained'}"
+                                       f" (timed region {total_ms / 1e3:.2f} s)"),
+                          frac_secondary=achieved_tflops / peak_other,
+                          peak_secondary=peak_other,
+                          peak_secondary_source=(f"{peaks['source']} bf16 "
+                                                 f"{'sustained' if short_region else 'burst'}"),
+                          tflops_per_sm_ghz=(achieved_tflops / (clk["sm_mhz"] / 1e3)
+                                             if clk and clk.get("sm_mhz") else None),
                           step_frac=(value / world) * 2.0 * d * V / 1e12 / peak),
             stage_ms=dict(rmsnorm=norm_ms, lmhead_lse=gemm_ms, finalize=fin_ms,
                           compare=ms_per_step - norm_ms - gemm_ms - fin_ms),

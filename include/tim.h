@@ -487,8 +487,9 @@ tim_status tim_logprob_merge_shards(const void *recs, const float *tgts, const i
  *       test taken as ln(mis_lo) <= d <= ln(mis_hi); mis_kept = tokens inside
  *       ("Rollout-Training Mismatch in LLM RL", section 2.1, w_MIS);
  *   w2_mean = mean exp(2 d) (E_q[w^2] = exp D_2(p||q), same page, section 5.3).
- * Quantiles need at most TIM_DIAG_QUANTILE_MAX_TOKENS active tokens in a
- * sequence; longer sequences get NaN quantiles and TIM_SEQ_QUANTILE_SKIPPED.
+ * The quantiles are exact for a sequence of any length; a sequence with more
+ * than 16384 active tokens takes a slower select that re-reads its scores on
+ * every pass instead of holding its keys in shared memory.
  * Flags and errors as for tim_compare.
  *
  * Arguments: those of tim_compare, plus top1_gen / top1_replay / top1_train
@@ -496,8 +497,6 @@ tim_status tim_logprob_merge_shards(const void *recs, const float *tgts, const i
  * 0 < mis_lo <= mis_hi), out_diag (tim_seq_diag [n_seq], device memory).
  * The workspace holds only the status word (tim_compare_diag_workspace_size).
  * ------------------------------------------------------------------------ */
-#define TIM_SEQ_QUANTILE_SKIPPED 32
-#define TIM_DIAG_QUANTILE_MAX_TOKENS 16384
 
 typedef struct tim_seq_diag {
   int64_t n_valid;
@@ -552,9 +551,16 @@ tim_status tim_compare_diag(const float *lp_gen, const float *lp_replay, const f
  * data-dependent error code (0 = none; TIM_ERR_TOKEN_RANGE, TIM_ERR_NONFINITE,
  * TIM_ERR_TIMEOUT), or NULL to skip it.
  *
- * The first call on each device performs a one-time set-up (it looks up the
- * device address of the array with that device current); make that first call
- * before any stream capture.  All calls on a device share the one array and it
+ * The first call in each CUDA context (once per device in the usual case; again
+ * after a cudaDeviceReset) performs a one-time set-up with that context current:
+ * it looks up the device address of the array, which places the library's code
+ * and the array on the device, and loads every kernel this path launches (the
+ * CUDA runtime otherwise loads kernels lazily, at their first launch, and
+ * loading takes device memory).  That set-up is the only point where device
+ * memory is taken, so a caller that later claims the remaining free memory
+ * should make its first call (a warm-up at any accepted size) before doing so,
+ * and before any stream capture.  Later calls, at any accepted size, take no
+ * device memory.  All calls on a device share the one array and it
  * keeps the previous call's contents (each call clears the status word it
  * needs zeroed): calls whose work overlaps on the GPU -- on different streams,
  * or from different threads -- race on the array and must be serialised by the

@@ -36,7 +36,6 @@ SEQ_STATS_DTYPE = np.dtype([("n_valid", "<i8"), ("pair", PAIR_DTYPE, (3,)),
                             ("tis_clipped", "<i8"), ("flags", "<i4"), ("reserved", "<i4")])
 assert SEQ_STATS_DTYPE.itemsize == 208
 
-SEQ_QUANTILE_SKIPPED = 32
 # numpy mirror of struct tim_seq_diag (200 bytes)
 SEQ_DIAG_DTYPE = np.dtype([("n_valid", "<i8"), ("abs_q50", "<f8", (3,)), ("abs_q95", "<f8", (3,)),
                            ("abs_q99", "<f8", (3,)), ("prob_mae", "<f8", (3,)),

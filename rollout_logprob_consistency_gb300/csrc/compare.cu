@@ -18,8 +18,9 @@
 //    Mismatch in LLM RL", section 2.1, and "Diagnosing Training Inference
 //    Mismatch in LLM Reinforcement Learning", 3. TIS.
 //
-// Work split: sequence j is cut into P contiguous parts (P depends only on T
-// and the number of sequences); CTA (j, p) reduces part p to a 256-byte
+// Work split: sequence j is cut into P_j contiguous parts, P_j taken from the
+// sequence's own length (so its statistics do not depend on the batch it comes
+// in); CTA (j, p) reduces part p to a 256-byte
 // partial, and the last CTA of sequence j to finish (an atomic ticket) merges
 // the P partials in part order and writes the sequence's statistics.  Inside a
 // CTA each thread owns a 4-token vector (128-bit loads of each score array when

@@ -28,8 +28,9 @@
 // order) as 64-bit keys (the bit patterns of non-negative doubles order like
 // the values, so selection is integer work) and find the order statistics the
 // interpolation needs by a radix select; they are exact, and the interpolation
-// is the formula above.  Sequences with more than kQuantMax active tokens skip
-// the quantiles (flag, NaN).
+// is the formula above.  A sequence with more active tokens than the shared
+// key buffer holds (kQuantMax) runs the same select with its keys recomputed
+// from the score arrays on every pass instead of read from shared memory.
 #include <cmath>
 #include <cstring>
 
@@ -39,7 +40,7 @@ namespace tim {
 
 constexpr int kDiagThreads = 512;  // every CTA: quantile selects and per-token parts
 constexpr int kDiagWarps = kDiagThreads / 32;
-constexpr int kQuantMax = TIM_DIAG_QUANTILE_MAX_TOKENS;
+constexpr int kQuantMax = 16384;  // keys a quantile CTA holds in shared memory
 constexpr size_t kDiagSmemBytes = static_cast<size_t>(kQuantMax) * sizeof(unsigned long long);
 
 // per-part sums: prob[3], dsum, k3, rerr, mis, w2
@@ -218,7 +219,6 @@ __device__ void diag_fold(int j, bool ok_offs, const int32_t* __restrict__ tA,
     o->mis_kept = N[1];
     o->w2_mean = q[5];
     int flags = F;
-    if (n > kQuantMax) flags |= TIM_SEQ_QUANTILE_SKIPPED;
     if (!isfinite(S[4])) flags |= TIM_SEQ_K3_OVERFLOW;
     o->flags = flags;
     if (F & TIM_SEQ_NONFINITE) set_status(status, TIM_ERR_NONFINITE);
@@ -340,7 +340,37 @@ __device__ void diag_part(int b, unsigned long long* __restrict__ stage,
             out + j, status);
 }
 
-// Quantiles of pair p of sequence j (one CTA; keys: kQuantMax 64-bit slots).
+// The active keys of one pair of one sequence, visited by every thread of a
+// CTA with a uniform trip count: read from the shared copy when the sequence's
+// keys fit in it, else recomputed from the score arrays (L2-resident after the
+// first pass) on every visit.  Visit order is irrelevant to the selection.
+struct KeySource {
+  const unsigned long long* keys;
+  const float* L;
+  const float* R;
+  const uint8_t* mask;
+  int64_t s, e;
+  int n;
+  bool stream;
+
+  template <class F>
+  __device__ __forceinline__ void visit(int tid, F&& f) const {
+    if (!stream) {
+      const int n_round = (n + kDiagThreads - 1) / kDiagThreads * kDiagThreads;
+#pragma unroll 4
+      for (int i = tid; i < n_round; i += kDiagThreads)
+        if (i < n) f(keys[i]);
+    } else {
+      for (int64_t b = s; b < e; b += kDiagThreads) {
+        const int64_t t = b + tid;
+        if (t < e && __ldg(mask + t) == 1) f(abs_diff_key(__ldg(L + t), __ldg(R + t)));
+      }
+    }
+  }
+};
+
+// Quantiles of pair p of sequence j (one CTA; keys: kQuantMax 64-bit slots in
+// shared memory, used when the sequence's active tokens fit).
 __device__ void diag_quantiles(int j, int p, unsigned long long* __restrict__ keys,
                                const float* __restrict__ A, const float* __restrict__ B,
                                const float* __restrict__ C, const int64_t* __restrict__ offs,
@@ -396,15 +426,15 @@ __device__ void diag_quantiles(int j, int p, unsigned long long* __restrict__ ke
   }
   __syncthreads();
   const int n = s_fill;
-  if (s_bad || n == 0 || n > kQuantMax) {
+  if (s_bad || n == 0) {
     if (tid == 0) {
-      const double v = (s_bad || n == 0) ? 0.0 : NAN;
-      o->abs_q50[p] = v;
-      o->abs_q95[p] = v;
-      o->abs_q99[p] = v;
+      o->abs_q50[p] = 0.0;
+      o->abs_q95[p] = 0.0;
+      o->abs_q99[p] = 0.0;
     }
     return;
   }
+  const KeySource src{keys, L, R, mask, s, e, n, n > kQuantMax};
   // The three order statistics by an MSD radix select on the keys' bit
   // patterns.  Target q keeps the key prefix fixed so far (bits [fixed_from,
   // 64)), the rank it still seeks among the keys with that prefix (its
@@ -428,7 +458,6 @@ __device__ void diag_quantiles(int j, int p, unsigned long long* __restrict__ ke
     s_open[tid] = n > 1 && fixed_from > 0;
   }
   __syncthreads();
-  const int n_round = (n + kDiagThreads - 1) / kDiagThreads * kDiagThreads;
   while (fixed_from > 0) {
     bool open[3];
     bool any = false;
@@ -447,21 +476,17 @@ __device__ void diag_quantiles(int j, int p, unsigned long long* __restrict__ ke
       c_or[q] = 0ull;
       c_and[q] = ~0ull;
     }
-#pragma unroll 4
-    for (int i = tid; i < n_round; i += kDiagThreads) {  // uniform trip count
-      if (i < n) {
-        const unsigned long long k = keys[i];
-        const unsigned dig = static_cast<unsigned>(k >> sh) & 255u;
+    src.visit(tid, [&](unsigned long long k) {
+      const unsigned dig = static_cast<unsigned>(k >> sh) & 255u;
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          if (open[q] && (k & hmask) == pre[q]) {
-            atomicAdd(&s_hist[q * 256 + dig], 1u);
-            c_or[q] |= k;
-            c_and[q] &= k;
-          }
+      for (int q = 0; q < 3; ++q) {
+        if (open[q] && (k & hmask) == pre[q]) {
+          atomicAdd(&s_hist[q * 256 + dig], 1u);
+          c_or[q] |= k;
+          c_and[q] &= k;
         }
       }
-    }
+    });
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
       if (open[q]) {
@@ -536,16 +561,14 @@ __device__ void diag_quantiles(int j, int p, unsigned long long* __restrict__ ke
       msk[q] = s_mask[q];
       lo_min[q] = up_min[q] = ~0ull;
     }
-#pragma unroll 4
-    for (int i = tid; i < n; i += kDiagThreads) {
-      const unsigned long long k = keys[i];
+    src.visit(tid, [&](unsigned long long k) {
 #pragma unroll
       for (int q = 0; q < 3; ++q) {
         const unsigned long long km = k & msk[q];
         if (km == pre[q]) lo_min[q] = k < lo_min[q] ? k : lo_min[q];
         else if (km > pre[q]) up_min[q] = k < up_min[q] ? k : up_min[q];
       }
-    }
+    });
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
       lo_min[q] = warp_min_u64(lo_min[q]);

@@ -118,6 +118,13 @@ __global__ void __launch_bounds__(32 * kFinWarps)
   out_top1[row] = r.id;
 }
 
+// Loads lse_finalize_kernel on the current device now (the runtime loads kernels
+// lazily, and loading takes device memory).
+cudaError_t load_lse_finalize_kernel() {
+  cudaFuncAttributes attr;
+  return cudaFuncGetAttributes(&attr, lse_finalize_kernel);
+}
+
 cudaError_t launch_lse_finalize(const void* part, const float* tgt, const int32_t* ids, int64_t T,
                                 int V, float* out_lp, float* out_lse, int32_t* out_top1,
                                 int* status, cudaStream_t stream) {

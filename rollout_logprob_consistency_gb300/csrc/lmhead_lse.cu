@@ -1130,6 +1130,16 @@ cudaError_t launch_wait_selftest(const void* y, const void* W, const int32_t* id
   return launch_gemm<0, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }
 
+// Places the scoring path's two kernel forms (one row tile or a row-tile pair per
+// work item) on the current device now rather than at their first launch: the
+// CUDA runtime loads kernels lazily, and loading one takes device memory.
+cudaError_t load_scoring_gemm_kernels() {
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, lmhead_lse_kernel<0, kPrecBf16>);
+  if (e != cudaSuccess) return e;
+  return cudaFuncGetAttributes(&attr, lmhead_lse_kernel<0, kPrecBf16x2>);
+}
+
 cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T,
                               int d, int V, float temperature, void* part, float* tgt,
                               int* status, cudaStream_t stream, int num_sms) {

@@ -13,14 +13,24 @@
 // The array is a file-scope __device__ object: every GPU that loads the library
 // holds kNoAllocScratchBytes of it until the process exits.  Host code must not
 // hand the array's host-side name to a kernel (that name is a host stand-in,
-// not a device address); the device address is fetched once per device with
-// cudaGetSymbolAddress while that device is current, and cached.
+// not a device address).  Set-up, once per CUDA context with that context
+// current: fetch the device address with cudaGetSymbolAddress (this also places
+// the library's module, and with it the array, on the device) and load every
+// kernel the path can launch (the runtime loads kernels lazily, at first
+// launch, and loading takes device memory).  The address is cached under the
+// context's unique ID, so a context created after cudaDeviceReset gets its own
+// set-up instead of a stale address.
+#include <cuda.h>
+
 #include <cmath>
 #include <mutex>
 
 #include "tim_common.cuh"
 
 namespace tim {
+cudaError_t load_rmsnorm_rows_kernel();
+cudaError_t load_scoring_gemm_kernels();
+cudaError_t load_lse_finalize_kernel();
 cudaError_t launch_rmsnorm_rows(const void* hidden, const void* gamma, int64_t T, int d, float eps,
                                 void* y, int* status, cudaStream_t stream);
 cudaError_t launch_lmhead_lse(const void* y, const void* W, const int32_t* ids, int64_t T, int d,
@@ -39,20 +49,58 @@ __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_addr_mutex;
 void* g_addr[kMaxDevices] = {};
+unsigned long long g_ctx_id[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set-up done once
-// per device, with that device current).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique ID of the current CUDA context (0 when none is current yet).
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  if (get_current == nullptr || get_id == nullptr) {  // called under g_addr_mutex
+    void* p = nullptr;
+    void* q = nullptr;
+    cudaDriverEntryPointQueryResult r1, r2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &r1) !=
+            cudaSuccess ||
+        r1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) !=
+            cudaSuccess ||
+        r2 != cudaDriverEntryPointSuccess)
+      return false;
+    get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    get_id = reinterpret_cast<CtxGetIdFn>(q);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return false;
+  *id = 0;
+  return ctx == nullptr || get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current context, with the set-up
+// described above done the first time this context is seen on `dev`.
 tim_status scratch_address(int dev, void** out) {
   if (dev < 0 || dev >= kMaxDevices) return TIM_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_addr_mutex);
-  if (g_addr[dev] == nullptr) {
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) {
+    cudaGetLastError();
+    return TIM_ERR_CUDA;
+  }
+  if (id == 0 || g_addr[dev] == nullptr || g_ctx_id[dev] != id) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e == cudaSuccess) e = load_rmsnorm_rows_kernel();
+    if (e == cudaSuccess) e = load_scoring_gemm_kernels();
+    if (e == cudaSuccess) e = load_lse_finalize_kernel();
+    if (e != cudaSuccess || p == nullptr || !current_context_id(&id) || id == 0) {
       cudaGetLastError();
+      g_addr[dev] = nullptr;
       return TIM_ERR_CUDA;
     }
     g_addr[dev] = p;
+    g_ctx_id[dev] = id;
   }
   *out = g_addr[dev];
   return TIM_OK;

@@ -303,6 +303,13 @@ cudaError_t launch_split_tf32(const float* x, int64_t n, float* big, float* smal
   return cudaGetLastError();
 }
 
+// Loads rmsnorm_rows_kernel on the current device now (the runtime loads kernels
+// lazily, and loading takes device memory).
+cudaError_t load_rmsnorm_rows_kernel() {
+  cudaFuncAttributes attr;
+  return cudaFuncGetAttributes(&attr, rmsnorm_rows_kernel);
+}
+
 cudaError_t launch_rmsnorm_rows(const void* hidden, const void* gamma, int64_t T, int d,
                                 float eps, void* y, int* status, cudaStream_t stream) {
   const int64_t T_pad = rows_padded(T);

@@ -57,6 +57,51 @@ def assert_logprob_parity(gpu, orc, rows=None, what=""):
                 top1_checked=int(sel.sum()), rows=int(len(lse)))
 
 
+def fp8_y_margin(d: int) -> float:
+    """Relative error bound of y before its bf16 rounding, as the RMSNorm kernel computes
+    it in fp32 (u = 2^-24): each lane adds the squares of its 8-element chunks with fused
+    multiply-adds, n = 8 ceil(d / 256) rounded additions, then 5 butterfly additions
+    ((n + 5) u on the sum, all terms positive); the division by d and the + eps add u
+    each; the square root halves the argument's error and adds u; 1 / x adds u; h * rstd
+    and * gamma add u each: (n + 7) / 2 + 4 = n / 2 + 7.5 units, rounded up to n / 2 + 8
+    for the second-order terms."""
+    n = 8 * (-(-d // 256))
+    return (n / 2 + 8) * 2.0 ** -24
+
+
+def assert_fp8_admissible_parity(gpu, adm, ids, V, rows=None, what="", max_exempt=0.01):
+    """FP8-head parity: each row's GPU (logprob, lse) within LP_TOL of one of the row's
+    admissible oracle results (``oracle.oracle_logprob_fp8_admissible``), and top-1 equal to
+    that result's wherever its gap exceeds TOP1_GAP.  Rows with more ambiguous elements than
+    the oracle enumerates are exempt; at most ``max_exempt`` of the rows may be.  Returns the
+    counts (rows, rows with several admissible results, exempt rows)."""
+    lp, lse, top1 = gpu
+    if rows is not None:
+        lp, lse, top1, ids = lp[rows], lse[rows], top1[rows], np.asarray(ids)[rows]
+    multi = exempt = 0
+    for i, alts in enumerate(adm):
+        if alts is None:
+            exempt += 1
+            continue
+        multi += len(alts) > 1
+        bad_id = not (0 <= int(ids[i]) < V)
+        ok = False
+        for a in alts:
+            if abs(float(lse[i]) - a["lse"]) > LP_TOL:
+                continue
+            if bad_id:
+                ok = bool(np.isnan(lp[i]))
+            else:
+                ok = abs(float(lp[i]) - a["logprob"]) <= LP_TOL and (
+                    a["gap"] <= TOP1_GAP or int(top1[i]) == a["top1"])
+            if ok:
+                break
+        assert ok, (f"{what}: row {i} (lp {lp[i]!r}, lse {lse[i]!r}, top1 {top1[i]}) matches none "
+                    f"of {len(alts)} admissible results, e.g. {alts[0]}")
+    assert exempt <= max_exempt * max(1, len(adm)), f"{what}: {exempt} exempt rows"
+    return dict(rows=len(adm), several=multi, exempt=exempt)
+
+
 def _close(g, r, scale, extra=0.0):
     if g == r:
         return True
@@ -110,6 +155,29 @@ def sample_rows(T: int, n: int, seed: int = 1234, must=()) -> np.ndarray:
     rows = set(int(x) for x in must if 0 <= x < T)
     rows.update(g.choice(T, size=min(n, T), replace=False).tolist())
     rows.update([0, T - 1])
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+ROW_TILE = 128
+
+
+def raster_group_tiles(d: int) -> int:
+    """Row tiles per raster group of the scoring GEMM's one-tile schedule at hidden size d
+    (48 up to d = 4096, 36 above)."""
+    return 48 if d <= 4096 else 36
+
+
+def tile_rows(T: int, group_tiles: int, seed: int = 1234, must=()) -> np.ndarray:
+    """Rows for a one-by-one oracle check that reach every part of the schedule: one
+    seeded row inside every 128-row tile (the ragged last tile included), and the
+    first and last row of every raster group of ``group_tiles`` tiles."""
+    g = np.random.default_rng(seed)
+    rows = set(int(x) for x in must if 0 <= x < T)
+    for t0 in range(0, T, ROW_TILE):
+        rows.add(int(g.integers(t0, min(T, t0 + ROW_TILE))))
+    span = group_tiles * ROW_TILE
+    for r0 in range(0, T, span):
+        rows.update([r0, min(T, r0 + span) - 1])
     return np.array(sorted(rows), dtype=np.int64)
 
 

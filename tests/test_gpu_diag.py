@@ -114,14 +114,21 @@ def test_diag_parity(tim, T, seed):
     assert_diag_parity(g, r, d_abs(A, C, offs, mask), what=f"T={T}")
 
 
+# active tokens a quantile CTA holds in shared memory; longer sequences take the
+# streamed select (keys recomputed from the scores on every pass)
+SHARED_KEYS = 16384
+
+
 def test_diag_without_top1_and_long_sequence(tim):
-    n = oracle.QUANTILE_MAX_TOKENS + 5
+    """A sequence just past the shared-memory key capacity (16389 active tokens) next to a
+    short one: exact quantiles through the streamed select, no flag."""
+    n = SHARED_KEYS + 5
     A, B, C, _, _, _ = make_case(n + 100, 7)
     offs = np.array([0, 100, n + 100], dtype=np.int64)
     mask = np.ones(n + 100, np.uint8)
     g = run(tim, A, B, C, offs, mask, (None, None, None), cap=1.5, lo=0.9, hi=1.2)
     r, _ = oracle.oracle_diag_lenient(A, B, C, offs, mask, 1.5, 0.9, 1.2)
-    assert g[1]["flags"] & oracle.FLAG_QUANTILE_SKIPPED and g[1]["top1_flips"] == [-1, -1, -1]
+    assert g[1]["flags"] == 0 and g[1]["top1_flips"] == [-1, -1, -1]
     assert_diag_parity(g, r, d_abs(A, C, offs, mask), what="long")
 
 
@@ -191,8 +198,9 @@ def _eighths(g, n, lo, hi):
 def test_diag_quantiles_exact_on_ties_tiny_and_maximal_sequences(tim):
     """The order statistics are selected, not approximated: every quantile equals the
     oracle's sorted-array formula bit for bit, across tie groups that straddle the
-    interpolation ranks, all-equal sequences, 1-3 tokens, widely spread magnitudes
-    and a sequence of exactly the maximum quantile length."""
+    interpolation ranks, all-equal sequences, 1-3 tokens, widely spread magnitudes,
+    sequences at and past the shared-memory key capacity, and long sequences (65573 and
+    about 68000 active tokens) through the streamed select."""
     g = np.random.default_rng(31)
     parts = []
 
@@ -212,10 +220,13 @@ def test_diag_quantiles_exact_on_ties_tiny_and_maximal_sequences(tim):
         B = A.copy()
         B[zeros:] = A[zeros:] - (np.arange(202 - zeros) + 1) / 64.0
         add(A, B.astype(np.float32), B.astype(np.float32))
-    n = oracle.QUANTILE_MAX_TOKENS                                # maximal, spread exponents
-    A = (-np.abs(g.standard_normal(n)) * 4 - 1).astype(np.float32)
-    B = (A + g.standard_normal(n) * 10.0 ** g.uniform(-6, 1, n)).astype(np.float32)
-    add(A, B, (B + g.standard_normal(n) * 1e-3).astype(np.float32))
+    for n in (SHARED_KEYS, SHARED_KEYS + 1, 65536 + 37):         # both selects, spread exponents
+        A = (-np.abs(g.standard_normal(n)) * 4 - 1).astype(np.float32)
+        B = (A + g.standard_normal(n) * 10.0 ** g.uniform(-6, 1, n)).astype(np.float32)
+        add(A, B, (B + g.standard_normal(n) * 1e-3).astype(np.float32))
+    A = _eighths(g, 70001, -80, -8)                               # long, three tie groups
+    B = (A + g.choice([0.0, 0.5, 1.0], 70001, p=[0.5, 0.45, 0.05])).astype(np.float32)
+    add(A, B, B.copy(), (g.random(70001) < 0.97).astype(np.uint8))
     A = _eighths(g, 3000, -80, -8)                                # inactive tokens interleaved
     B = (A - g.integers(0, 4, 3000) / 16.0).astype(np.float32)
     add(A, B, A.copy(), (g.random(3000) < 0.5).astype(np.uint8))
@@ -233,8 +244,8 @@ def test_diag_quantiles_exact_on_ties_tiny_and_maximal_sequences(tim):
 
 def test_diag_and_compare_one_sequence_past_the_part_cap(tim):
     """A 300000-token sequence: its part count is capped at 256, so every part holds
-    more than 512 tokens (each thread loops, all warps reduce); the quantiles are
-    skipped (more than the maximum active tokens) and flagged."""
+    more than 512 tokens (each thread loops, all warps reduce); its quantiles (about
+    270000 active tokens) come from the streamed select, exact."""
     from parity import assert_compare_parity
     T = 300000
     A, B, C, _, _, tops = make_case(T, 41)
@@ -242,7 +253,7 @@ def test_diag_and_compare_one_sequence_past_the_part_cap(tim):
     mask = (np.random.default_rng(42).random(T) < 0.9).astype(np.uint8)
     g = run(tim, A, B, C, offs, mask, tops)
     r, errs = oracle.oracle_diag_lenient(A, B, C, offs, mask, 2.0, 0.5, 1.5, tops)
-    assert not errs and g[0]["flags"] & oracle.FLAG_QUANTILE_SKIPPED
+    assert not errs and g[0]["flags"] == 0
     assert_diag_parity(g, r, d_abs(A, C, offs, mask), what="past the cap")
     stats, w = tim.compare(cuda_tensor(A), cuda_tensor(B), cuda_tensor(C), cuda_tensor(offs),
                            cuda_tensor(mask), 2.0)

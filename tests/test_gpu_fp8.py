@@ -1,12 +1,20 @@
 """The FP8 (e4m3) head (tim_quantize_fp8_rows, tim_logprob_fp8) through the C ABI
 against the fp64 FP8 oracle: quantiser codes and scales bit-exact, scores within
-2e-3 nats, top-1 exact where the oracle's gap exceeds 1e-3, batch invariance."""
+2e-3 nats, top-1 exact where the oracle's gap exceeds 1e-3, batch invariance.
+
+y is the fp64 RMSNorm rounded to bf16, as for the bf16 head.  The kernel computes
+it in fp32, so where the exact value lies within the kernel's error bound
+(``parity.fp8_y_margin``) of a bf16 rounding midpoint it may round the other way,
+and when that changes an e4m3 code (or the row scale) the logits move by a code
+step.  Each row is therefore checked against its admissible oracle results
+(``oracle.oracle_logprob_fp8_admissible``): the oracle's own, plus one per
+combination of those roundings."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from parity import assert_logprob_parity, bf16_cuda, cuda_tensor
+from parity import assert_fp8_admissible_parity, bf16_cuda, cuda_tensor, fp8_y_margin
 
 pytestmark = pytest.mark.gpu
 
@@ -45,8 +53,10 @@ def test_fp8_parity(tim, T, d, V, tau):
     W8, sW = tim.quantize_fp8_rows(bf16_cuda(b.head.W))
     got = [x.cpu().numpy() for x in tim.logprob_fp8(bf16_cuda(b.hidden_gen), bf16_cuda(b.head.gamma),
                                                     W8, sW, cuda_tensor(b.token_ids), tau, b.eps)]
-    orc = oracle.oracle_logprob_fp8(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids, tau, b.eps)
-    assert_logprob_parity(got, orc, what=f"fp8 T={T} d={d} V={V}")
+    adm = oracle.oracle_logprob_fp8_admissible(b.hidden_gen, b.head.gamma, b.head.W, b.token_ids,
+                                               tau, b.eps, fp8_y_margin(d))
+    res = assert_fp8_admissible_parity(got, adm, b.token_ids, V, what=f"fp8 T={T} d={d} V={V}")
+    print(f"fp8 T={T} d={d} V={V}: {res}")
 
 
 def test_fp8_full_head_and_batch_invariance(tim):
@@ -55,9 +65,11 @@ def test_fp8_full_head_and_batch_invariance(tim):
     hid, gam, ids = bf16_cuda(b.hidden_gen), bf16_cuda(b.head.gamma), cuda_tensor(b.token_ids)
     full = [x.cpu().numpy() for x in tim.logprob_fp8(hid, gam, W8, sW, ids, 0.7, b.eps)]
     rows = np.arange(0, 200, 5)
-    orc = oracle.oracle_logprob_fp8(b.hidden_gen[rows], b.head.gamma, b.head.W, b.token_ids[rows],
-                                    0.7, b.eps)
-    assert_logprob_parity(full, orc, rows=rows, what="fp8 full head")
+    adm = oracle.oracle_logprob_fp8_admissible(b.hidden_gen[rows], b.head.gamma, b.head.W,
+                                               b.token_ids[rows], 0.7, b.eps, fp8_y_margin(4096))
+    res = assert_fp8_admissible_parity(full, adm, b.token_ids, 151936, rows=rows,
+                                       what="fp8 full head")
+    print(f"fp8 full head: {res}")
     part = [x.cpu().numpy() for x in tim.logprob_fp8(hid[13:77].contiguous(), gam, W8, sW,
                                                      cuda_tensor(b.token_ids[13:77]), 0.7, b.eps)]
     for x, y in zip(part, full):

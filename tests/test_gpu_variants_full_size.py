@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 import synth
-from parity import assert_logprob_parity, bf16_cuda, cuda_tensor, sample_rows
+from parity import (assert_fp8_admissible_parity, assert_logprob_parity, bf16_cuda, cuda_tensor,
+                    fp8_y_margin, sample_rows)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -52,10 +53,11 @@ def test_fp8_head_full_size(tim, work):
     W8, sW = tim.quantize_fp8_rows(dv["W"])
     got = [x.cpu().numpy() for x in tim.logprob_fp8(dv["hid"], dv["gam"], W8, sW, dv["ids"], 0.7,
                                                     b.eps)]
-    rows = sample_rows(b.T, 24)
-    orc = oracle.oracle_logprob_fp8(b.hidden_train[rows], b.head.gamma, b.head.W,
-                                    b.token_ids[rows], 0.7, b.eps)
-    assert_logprob_parity(got, orc, rows=rows, what="fp8 T=32768")
+    rows = sample_rows(b.T, 64)
+    adm = oracle.oracle_logprob_fp8_admissible(b.hidden_train[rows], b.head.gamma, b.head.W,
+                                               b.token_ids[rows], 0.7, b.eps, fp8_y_margin(4096))
+    res = assert_fp8_admissible_parity(got, adm, b.token_ids, b.V, rows=rows, what="fp8 T=32768")
+    print(f"fp8 T=32768: {res}")
 
 
 def test_fp32_head_full_size(tim, work):

@@ -1,19 +1,18 @@
 """Full-size scoring workloads on the GPU, through the C ABI, in the launch
-configuration the benchmark times.  The fp64 oracle checks a seeded sample of
-rows one by one; properties that hold at any size (bitwise replay equality,
-same-prefix siblings, batch invariance, the eq. (1) split) are checked on all
-rows."""
+configuration the benchmark times.  The fp64 oracle checks rows one by one: one
+seeded row inside every 128-row tile and both ends of every raster group of the
+GEMM's schedule (``parity.tile_rows``); properties that hold at any size
+(bitwise replay equality, same-prefix siblings, batch invariance, the eq. (1)
+split) are checked on all rows."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
 from parity import (assert_compare_parity, assert_logprob_parity, assert_tis_parity,
-                    bf16_cuda, covered_rows, cuda_tensor, sample_rows)
+                    bf16_cuda, covered_rows, cuda_tensor, raster_group_tiles, tile_rows)
 
 pytestmark = pytest.mark.gpu
-
-N_ORACLE_ROWS = 64
 
 
 @pytest.fixture(scope="module")
@@ -50,7 +49,7 @@ def same_bits(x, y):
                for a, b in zip(x, y))
 
 
-def three_way(tim, b, W_train_bits=None, oracle_rows=N_ORACLE_ROWS):
+def three_way(tim, b, W_train_bits=None):
     hid = bf16_cuda(b.hidden_gen)
     hid_c = bf16_cuda(b.hidden_train)
     gam = bf16_cuda(b.head.gamma)
@@ -64,7 +63,7 @@ def three_way(tim, b, W_train_bits=None, oracle_rows=N_ORACLE_ROWS):
               splits=[np.sort(perm[cuts[i]:cuts[i + 1]]) for i in range(3)])
     C = score(tim, hid_c, gam, Wc, ids, b.temperature, b.eps)
     assert same_bits(A, B), "replay in another batch split must be bitwise identical"
-    rows = sample_rows(b.T, oracle_rows)
+    rows = tile_rows(b.T, raster_group_tiles(b.head.d))
     oA = oracle.oracle_logprob(b.hidden_gen[rows], b.head.gamma, b.head.W, b.token_ids[rows],
                                b.temperature, b.eps)
     assert_logprob_parity(A, oA, rows=rows, what=f"{b.name} A")
@@ -137,7 +136,7 @@ def test_batch_invariance_sweep_8b_head(tim):
         ws.check(f"M={M}")
         if ref is None:
             ref = got
-            rows = sample_rows(got.shape[0], N_ORACLE_ROWS)
+            rows = tile_rows(got.shape[0], raster_group_tiles(head.d))
             orc = oracle.oracle_logprob(plan.targets_hidden[rows], head.gamma, head.W,
                                         plan.targets_ids[rows], plan.temperature, plan.eps)
             assert_logprob_parity((got[:, 0].view(np.float32), got[:, 1].view(np.float32),
@@ -149,6 +148,6 @@ def test_batch_invariance_sweep_8b_head(tim):
 
 def test_long_rollout_5120_stale_weights(tim):
     b = synth.make_long_5120()
-    A, C, gs = three_way(tim, b, W_train_bits=b.W_train, oracle_rows=32)
+    A, C, gs = three_way(tim, b, W_train_bits=b.W_train)
     # a stale weight version moves every active token (Case 3 pattern: A == B, C differs)
     assert all(st["pair"][1]["mismatch_count"] > 0.9 * st["n_valid"] for st in gs)

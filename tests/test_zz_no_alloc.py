@@ -6,8 +6,11 @@ fixed 8 MiB array inside the library instead of a caller workspace.
 
 Checked through the C ABI against tim_logprob on two calls in a row (the second
 call finds the first call's bytes still in the shared array), within the
-parity tolerance of the other tests, and for the size limit.  This file is
-collected last so that a failure here comes after every other test has run.
+parity tolerance of the other tests, and for the size limit at its exact edges.
+After the first call (the set-up), calls at sizes not seen before take no device
+memory: the free device memory reported by cudaMemGetInfo does not move.  This
+file is collected last so that a failure here comes after every other test has
+run.
 """
 import ctypes
 
@@ -50,6 +53,71 @@ def call_noalloc(torch, f, hidden, gamma, W, ids, tau, eps):
              top1.data_ptr(), st.data_ptr(), torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     return code, (lp.cpu().numpy(), lse.cpu().numpy(), top1.cpu().numpy()), int(st.item())
+
+
+def call_into(torch, f, hidden, gamma, W, ids, tau, eps, out):
+    """The entry point with outputs allocated beforehand (nothing allocated here)."""
+    lp, lse, top1, st = out
+    T = hidden.shape[0]
+    return f(hidden.data_ptr(), gamma.data_ptr(), W.data_ptr(), ids.data_ptr(), T,
+             hidden.shape[1], W.shape[0], tau, eps, lp[:T].data_ptr(), lse[:T].data_ptr(),
+             top1[:T].data_ptr(), st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+def test_noalloc_takes_no_device_memory_after_setup(env):
+    """First call (the set-up) at one row and d = 4096, then calls at sizes not seen
+    before -- 129, 300 and 416 rows (one-tile and row-tile-pair GEMM forms) and 384 rows
+    at d = 5120 -- leave cudaMemGetInfo's free memory exactly where it was, and give the
+    bits of tim_logprob."""
+    torch, tim, f = env
+    b4 = synth.make_custom(T=416, d=4096, V=151936, temperature=0.7, tag="noalloc_mem4")
+    b5 = synth.make_custom(T=384, d=5120, V=151936, temperature=0.7, tag="noalloc_mem5")
+    dev = {}
+    for key, b in (("4", b4), ("5", b5)):
+        dev[key] = (bf16_cuda(b.hidden_gen), bf16_cuda(b.head.gamma), bf16_cuda(b.head.W),
+                    cuda_tensor(b.token_ids))
+    out = (torch.empty(416, dtype=torch.float32, device="cuda"),
+           torch.empty(416, dtype=torch.float32, device="cuda"),
+           torch.empty(416, dtype=torch.int32, device="cuda"),
+           torch.full((1,), -1, dtype=torch.int32, device="cuda"))
+    h, g, W, ids = dev["4"]
+    assert call_into(torch, f, h[:1], g, W, ids[:1], 0.7, b4.eps, out) == 0      # set-up
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    results = []
+    for key, T, eps in (("4", 129, b4.eps), ("4", 300, b4.eps), ("4", 416, b4.eps),
+                        ("5", 384, b5.eps)):
+        h, g, W, ids = dev[key]
+        assert call_into(torch, f, h[:T], g, W, ids[:T], 0.7, eps, out) == 0
+        torch.cuda.synchronize()
+        assert int(out[3].item()) == 0
+        results.append((key, T, [x[:T].cpu().numpy().copy() for x in out[:3]]))
+    free1 = torch.cuda.mem_get_info()[0]
+    assert free1 == free0, f"free device memory moved by {free0 - free1} bytes"
+    for key, T, got in results:
+        h, g, W, ids = dev[key]
+        eps = b4.eps if key == "4" else b5.eps
+        ref = [x.cpu().numpy() for x in tim.logprob(h[:T], g, W, ids[:T], 0.7, eps)]
+        assert all(x.tobytes() == y.tobytes() for x, y in zip(got, ref)), (key, T)
+
+
+def test_noalloc_size_limit_at_its_edges(env):
+    """The header's limits: 416 rows at d = 4096 and 384 rows at d = 5120 (V = 151936) are
+    accepted, one row more is rejected with TIM_ERR_WORKSPACE and nothing enqueued; each
+    answer agrees with tim_logprob_workspace_size against the 8 MiB array."""
+    torch, tim, f = env
+    for d, T_max in ((4096, 416), (5120, 384)):
+        b = synth.make_custom(T=T_max + 1, d=d, V=151936, temperature=0.7, tag=f"noalloc_edge{d}")
+        hid, gam, W = bf16_cuda(b.hidden_gen), bf16_cuda(b.head.gamma), bf16_cuda(b.head.W)
+        ids = cuda_tensor(b.token_ids)
+        assert tim.logprob_workspace_size(T_max, d, 151936) <= SCRATCH_BYTES
+        assert tim.logprob_workspace_size(T_max + 1, d, 151936) > SCRATCH_BYTES
+        code, got, status = call_noalloc(torch, f, hid[:T_max], gam, W, ids[:T_max], 0.7, b.eps)
+        assert code == 0 and status == 0, (d, code, status)
+        ref = [x.cpu().numpy() for x in tim.logprob(hid[:T_max], gam, W, ids[:T_max], 0.7, b.eps)]
+        assert all(x.tobytes() == y.tobytes() for x, y in zip(got, ref)), d
+        code, _, status = call_noalloc(torch, f, hid, gam, W, ids, 0.7, b.eps)
+        assert code == tim.STATUS["TIM_ERR_WORKSPACE"] and status == -1, (d, code, status)
 
 
 def test_noalloc_matches_workspace_path_twice(env):
