@@ -106,6 +106,11 @@ struct GemmArgs {
   // sets stall_producer so that no load is ever issued
   uint64_t wait_limit_ns;
   int stall_producer;
+  // scoring-type launches within one raster group: the CTA that works on a W
+  // tile's first work item prefetches that tile's W k-blocks into L2 this many
+  // k-blocks ahead of its loads (0 = none); the other CTAs on the tile then find
+  // them in L2
+  int w_prefetch;
   // top-4 mode only: per-(row, tile) records of the four largest logits
   void* top4;
   // collect mode only: when dyn_T is set, only row tiles below *dyn_T (a row
@@ -400,7 +405,15 @@ __global__ void __launch_bounds__(StageGeom<kPrec>::kThreads, 1)
           kb0 = pre;
           first = false;
         }
+        // the CTA on the W tile's first work item of the raster group prefetches
+        const bool leader = a.w_prefetch > 0 && (m % a.group_m) == 0;
+        if (leader) {
+          for (int k = kb0 + 1; k < min(a.num_kb, kb0 + a.w_prefetch); ++k)
+            tma_prefetch_2d(&tmap_w, k * kKElems, n * kBN);
+        }
         for (int kb = kb0; kb < a.num_kb; ++kb) {
+          if (leader && kb + a.w_prefetch < a.num_kb)
+            tma_prefetch_2d(&tmap_w, (kb + a.w_prefetch) * kKElems, n * kBN);
           if (!mbar_wait(&empty[stage], ph ^ 1u, abort_flag, a.wait_limit_ns)) {
             ok = false;
             break;
@@ -536,7 +549,35 @@ __global__ void __launch_bounds__(StageGeom<kPrec>::kThreads, 1)
       int bi = col_base;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              acc * G::kAccCols + h * kBN;
-      if constexpr (kMode == 0) {
+      if constexpr (kMode == 0 && !kFp8 && !kX3) {
+        // bf16 operands: the load of chunk c + 1 is in flight while chunk c is
+        // reduced (same chunks, same order, same arithmetic as one load at a time)
+        const int nch = min(nchunk, max(0, (a.v_end - col_base + 31) / 32));
+        auto reduce = [&](const uint32_t(&r)[32], int c) {
+          const int col0 = col_base + c * 32;
+          const int nvalid = min(32, a.v_end - col0);
+          if (nvalid == 32)
+            epilogue_chunk<false>(r, 32, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
+          else
+            epilogue_chunk<true>(r, nvalid, col0, rel - c * 32, a.k2, m2, sum, bz, bi, zt);
+        };
+        uint32_t ra[32], rb[32];
+        if (nch > 0) {
+          tmem_ld32_async(tbase, ra);
+          tmem_ld_wait(ra);
+        }
+#pragma unroll 1
+        for (int c = 0; c < nch; c += 2) {
+          if (c + 1 < nch) tmem_ld32_async(tbase + (c + 1) * 32, rb);
+          reduce(ra, c);
+          if (c + 1 < nch) {
+            tmem_ld_wait(rb);
+            if (c + 2 < nch) tmem_ld32_async(tbase + (c + 2) * 32, ra);
+            reduce(rb, c + 1);
+            if (c + 2 < nch) tmem_ld_wait(ra);
+          }
+        }
+      } else if constexpr (kMode == 0) {
         const float srow = kFp8 ? __ldg(a.sy + row) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < nchunk; ++c) {
@@ -858,6 +899,7 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   // e4m3 operands do as well with 48 as with 96.
   a.group_m = d <= 4096 ? 48 : 36;
   if (prec == kPrecTf32x3) a.group_m /= 4;
+  a.w_prefetch = 0;
   a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
   a.k2 = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   a.inv_temp = static_cast<float>(1.0 / static_cast<double>(temperature));
@@ -888,44 +930,42 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   return cudaSuccess;
 }
 
-// Row-tile pairs for a scoring-type launch (one W pass per batch, light epilogue).
-// Batches that fit one raster group run as row-tile pairs (kPrecBf16x2): each
-// work item is two row tiles against one W tile, so every CTA streams its own W
-// tiles once for both (in the one-tile form the CTAs that share a W tile run
-// side by side and only one of them streams each k-slice from DRAM).  The
-// per-row arithmetic is the same MMA sequence and epilogue as the one-tile form.
-// An odd tile count leaves a lone last tile per W tile; that is paired only when
-// the items rotate over all CTAs (CTA count and number of pairs coprime: CTA c
-// meets pairs c, c + grid, c + 2 grid, ... modulo the pair count), otherwise some
-// CTAs would get a lone tile in every wave and others never.
-// Measured on GB300 (d = 4096, V = 151936, whole calls with L2 flushed, one-tile
-// -> pairs, medians of three alternating rounds on one box): 768 rows 575 -> 544
-// us, 1024 rows 771 -> 706 us, 1152 rows (9 tiles) 824 -> 799 us, 1536 rows
-// 1056 -> 1024 us, 2048 rows 1409 -> 1363 us, 3072 rows 2105 -> 2091 us, 4096
-// rows 2945 -> 2828 us, 6144 rows 4721 -> 4254 us; on other boxes 200-256 rows
-// 252-256 -> 237-241 us, 448-512 rows 411-421 -> 381-388 us, 513 rows (5 tiles)
-// 488-491 -> 478 us.  Odd counts without full rotation lost (7 tiles 666 -> 709
-// us, 11 tiles 996 -> 1053 us); 3 tiles tied even with an odd grid.  Batches of
-// more than one raster group stay in the one-tile form: 8192-16384 rows within
-// 1%, the benchmark batch of 32768 rows 1% slower with pairs under the power cap.
-static bool use_row_pairs(const GemmArgs& a, int num_sms) {
-  const int pairs = (a.num_m + 1) / 2;
-  const int64_t items = static_cast<int64_t>(pairs) * a.num_n;
-  const int grid = items < num_sms ? static_cast<int>(items) : num_sms;  // as launch_gemm
-  int g = grid, p = pairs;  // gcd(grid, pairs)
-  while (p != 0) {
-    const int r = g % p;
-    g = p;
-    p = r;
-  }
-  return a.num_m >= 2 && a.num_m <= a.group_m && (a.num_m % 2 == 0 || g == 1);
-}
+// Schedule of a scoring-type launch (scoring records, or the top-4 records of the
+// processed score): one W pass per batch and a light epilogue.
+//
+// Batches of an even number of row tiles that fit one raster group (2 to 48 row
+// tiles) run as row-tile pairs (kPrecBf16x2): each work item is two row tiles
+// against one W tile, so a W tile is streamed by half as many CTAs, and every row
+// still sees the MMA sequence and epilogue of the one-tile form.  Odd counts run
+// one row tile per item (a lone last tile per W tile would hand some CTAs half the
+// work of others).  When several work items share a W tile inside one raster
+// group, the CTA on the tile's first item prefetches the tile's W k-blocks into
+// L2 kLeaderPrefetch k-blocks ahead of its own loads, so that the other CTAs on
+// the tile, which request the same k-blocks, are not held to one ring's depth of
+// DRAM requests in flight.  Batches of more than one raster group keep one row
+// tile per item and no prefetch.
+// Measured on GB300 (d = 4096, V = 151936, whole calls; the previous schedule
+// and this one, with the bf16 epilogue's overlapped TMEM loads, built side by
+// side and timed in one process, alternating in random order over ten rounds,
+// bitwise equal outputs): 448 rows 411 -> 395 us, 512 rows 429 -> 416, 513 rows
+// 533 -> 516, 640 rows 546 -> 531, 768 rows 613 -> 602, 1024 rows 794 -> 779,
+// 2048 rows 1523 -> 1496; 128, 256, 384, 1408 and 4096 rows within 0.3%; 6144
+// rows +0.5% and 32768 rows +0.7% (noise level).  Prefetching 8 k-blocks ahead
+// was no better than 4; prefetching where each CTA streams its own W tile
+// (256 rows) or in batches of several raster groups (32768 rows: +10%) was
+// slower.
+constexpr int kLeaderPrefetch = 4;
 
-// Turns a one-tile schedule into the row-tile pair schedule.
-static void to_row_pairs(GemmArgs& a) {
-  a.num_m = (a.num_m + 1) / 2;  // work items along M: row-tile pairs
-  a.group_m = (a.group_m + 1) / 2;
-  a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
+static bool plan_scoring_schedule(GemmArgs& a) {
+  const bool one_group = a.num_m <= a.group_m;
+  const bool pairs = one_group && a.num_m >= 2 && a.num_m % 2 == 0;
+  if (pairs) {
+    a.num_m /= 2;  // work items along M: row-tile pairs
+    a.group_m = (a.group_m + 1) / 2;
+    a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
+  }
+  a.w_prefetch = (one_group && a.num_m >= 2) ? kLeaderPrefetch : 0;
+  return pairs;
 }
 
 // W holds V vocabulary rows whose global ids start at v0 (a vocabulary shard when
@@ -945,11 +985,9 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
   // (3 ms at 32768 rows), so larger batches are launched in stream order.  The
   // arithmetic is identical either way.
   const bool programmatic = a.num_m <= a.group_m;
-  if (use_row_pairs(a, num_sms)) {  // batches within one raster group (see use_row_pairs)
-    to_row_pairs(a);
+  if (plan_scoring_schedule(a))
     return launch_gemm<0, kPrecBf16x2>(map_y, map_w, map_y, map_w, a, stream, num_sms,
                                        programmatic);
-  }
   return launch_gemm<0, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, programmatic);
 }
 
@@ -1027,10 +1065,8 @@ cudaError_t launch_lmhead_top4(const void* y, const void* W, const int32_t* ids,
   cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, 0, 1.0f, status);
   if (e != cudaSuccess) return e;
   a.top4 = top4;
-  if (use_row_pairs(a, num_sms)) {  // same schedule rule as the scoring GEMM
-    to_row_pairs(a);
+  if (plan_scoring_schedule(a))  // the scoring GEMM's schedule
     return launch_gemm<4, kPrecBf16x2>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
-  }
   return launch_gemm<4, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }
 

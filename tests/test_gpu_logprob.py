@@ -40,7 +40,8 @@ SHAPES = [
     (384, 128, 1000, 1.0),
     (512, 256, 3001, 0.8),
     (513, 320, 4099, 0.9),
-    (640, 64, 151936, 0.9),   # five row tiles as row-tile pairs with a lone last tile
+    (640, 64, 151936, 0.9),   # five row tiles, one per item, the leader prefetching W
+    (1024, 64, 151936, 0.9),  # eight row tiles as four pairs per W tile, with the prefetch
     (256, 5120, 3001, 0.7),   # row-tile pairs at the long-rollout hidden size
 ]
 

@@ -74,6 +74,8 @@ def targets(b, tau):
     (50, 128, 1000, 1.0, 1, 1.0), (50, 128, 1000, 1.0, 2, 1.0), (50, 128, 1000, 0.7, 17, 0.9),
     (33, 192, 2048, 1.3, 64, 0.5), (40, 256, 20000, 0.8, 40, 0.95), (9, 64, 5000, 1.0, 5, 1.0),
     (256, 128, 3000, 0.9, 10, 0.9),   # two row tiles: the top-4 pass runs as a row-tile pair
+    (384, 128, 3000, 0.9, 10, 0.9),   # three row tiles, one per item, the leader prefetching W
+    (512, 128, 3000, 0.9, 10, 0.9),   # four row tiles: two pairs per W tile, with the prefetch
 ])
 def test_processed_parity(tim, T, d, V, tau, k, p):
     b = synth.make_custom(T=T, d=d, V=V, temperature=tau, tag=f"pr{T}_{d}_{V}")

@@ -112,11 +112,15 @@ def test_qwen3_8b_head_siblings(tim):
 
 def test_batch_invariance_sweep_8b_head(tim):
     """The 4096 target rows in batches of M = 1, 7, 64, 513, 4096 and 16384, plus
-    M = 200, 384 and 512: M = 200, 512, 513 (an odd tile count) and 4096 are scored as
-    row-tile pairs, M = 1, 7, 64, 384 and 16384 one row tile per work item, and every
-    target keeps its bits."""
+    M = 200, 256, 384, 512, 768, 1152, 6144 and 6145, covering every schedule form of
+    the GEMM: one row tile (M <= 128); a row-tile pair per W tile (200, 256); pairs
+    with several items per W tile and the leader's L2 prefetch (512, 768, 4096, and
+    6144 = the 48-tile raster group); odd tile counts, one row tile per item with the
+    prefetch (384, 513, 1152); and batches of several raster groups (6145, 16384).
+    Every target keeps its bits."""
     import torch
-    plan = synth.make_sweep(Ms=(1, 7, 64, 200, 384, 512, 513, 4096, 16384))
+    plan = synth.make_sweep(Ms=(1, 7, 64, 200, 256, 384, 512, 513, 768, 1152, 4096, 6144, 6145,
+                                16384))
     head = plan.head
     gam, W = bf16_cuda(head.gamma), bf16_cuda(head.W)
     ref = None
