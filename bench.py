@@ -110,15 +110,16 @@ class NvmlSampler:
     REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
                (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
 
-    def __init__(self, gpu_uuid, period_s=0.01):
+    def __init__(self, gpu_uuid, period_s=0.01, lib=None):
         import ctypes
         import threading
         self.ok = False
         self.rows = []
-        try:
-            lib = ctypes.CDLL("libnvidia-ml.so.1")
-        except OSError:
-            return
+        if lib is None:
+            try:
+                lib = ctypes.CDLL("libnvidia-ml.so.1")
+            except OSError:
+                return
         self.lib = lib
         if lib.nvmlInit_v2() != 0:
             return
@@ -166,18 +167,23 @@ class NvmlSampler:
         self._stop.set()
         self._thread.join(timeout=5)
         self.lib.nvmlShutdown()
-        rows = self.rows
+        return self.summarize(self.rows, self.smax, self.period)
+
+    @classmethod
+    def summarize(cls, rows, smax, period):
+        """Median / min / max SM clock, 100 MHz histogram, clock-event reasons seen and
+        power of the samples (all taken inside the timed region)."""
         if not rows:
             return None
-        reasons = sorted({name for r in rows for bit, name in self.REASONS if r["reasons"] & bit})
+        reasons = sorted({name for r in rows for bit, name in cls.REASONS if r["reasons"] & bit})
         bins = {}
         for r in rows:
             key = f"{int(r['sm'] // 100) * 100}-{int(r['sm'] // 100) * 100 + 99}"
             bins[key] = bins.get(key, 0) + 1
         span = rows[-1]["t"] - rows[0]["t"]
-        return dict(source="nvml", period_ms=1e3 * self.period,
+        return dict(source="nvml", period_ms=1e3 * period,
                     sm_mhz=statistics.median(r["sm"] for r in rows),
-                    sm_max_mhz=self.smax or max(r["sm"] for r in rows), reasons=reasons,
+                    sm_max_mhz=smax or max(r["sm"] for r in rows), reasons=reasons,
                     samples=len(rows), samples_under_load=len(rows),
                     sampled_span_s=round(span, 3),
                     sm_mhz_bins=dict(sorted(bins.items())),
