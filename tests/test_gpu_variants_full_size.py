@@ -1,6 +1,8 @@
 """The next-row paths at the benchmark's full size and launch configuration
 (Qwen3-8B-shaped head, T = 32768, d = 4096, V = 151936, trainer hidden states, as
-bench.py times them), checked against the fp64 oracle on seeded samples of rows,
+bench.py times them), checked against the fp64 oracle row by row -- one seeded row
+inside every 128-row tile and both ends of every raster group (``parity.tile_rows``)
+for every path --
 with each path's own tolerance (see the per-path test files), and by properties
 that hold at any size."""
 import math
@@ -10,8 +12,8 @@ import pytest
 
 import oracle
 import synth
-from parity import (assert_fp8_admissible_parity, assert_logprob_parity, bf16_cuda, cuda_tensor,
-                    fp8_y_margin, sample_rows)
+from parity import (assert_fp8_admissible_parity, bf16_cuda, cuda_tensor, fp8_y_margin,
+                    raster_group_tiles, tile_rows)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -40,7 +42,7 @@ def test_processed_full_size(tim, work):
     b, dv = work
     got = [x.cpu().numpy() for x in tim.processed_logprob(dv["hid"], dv["gam"], dv["W"],
                                                           dv["ids"], 0.7, b.eps, 50, 0.95)]
-    rows = sample_rows(b.T, 24)
+    rows = tile_rows(b.T, raster_group_tiles(b.head.d))
     orc = oracle.oracle_processed_logprob(b.hidden_train[rows], b.head.gamma, b.head.W,
                                           b.token_ids[rows], float(np.float32(0.7)), b.eps, 50,
                                           float(np.float32(0.95)))
@@ -53,7 +55,7 @@ def test_fp8_head_full_size(tim, work):
     W8, sW = tim.quantize_fp8_rows(dv["W"])
     got = [x.cpu().numpy() for x in tim.logprob_fp8(dv["hid"], dv["gam"], W8, sW, dv["ids"], 0.7,
                                                     b.eps)]
-    rows = sample_rows(b.T, 64)
+    rows = tile_rows(b.T, raster_group_tiles(b.head.d))
     adm = oracle.oracle_logprob_fp8_admissible(b.hidden_train[rows], b.head.gamma, b.head.W,
                                                b.token_ids[rows], 0.7, b.eps, fp8_y_margin(4096))
     res = assert_fp8_admissible_parity(got, adm, b.token_ids, b.V, rows=rows, what="fp8 T=32768")
@@ -69,7 +71,7 @@ def test_fp32_head_full_size(tim, work):
                                                      b.eps)]
     del Wb, Ws
     torch.cuda.empty_cache()
-    rows = sample_rows(b.T, 16)
+    rows = tile_rows(b.T, raster_group_tiles(b.head.d))
     W32 = oracle.widen_bf16(b.head.W).astype(np.float32)
     orc = oracle.oracle_logprob_fp32(b.hidden_train[rows], b.head.gamma, W32, b.token_ids[rows],
                                      0.7, b.eps)
@@ -90,7 +92,7 @@ def test_backward_full_size(tim, work):
     _, lse, _ = tim.logprob(dv["hid"], dv["gam"], dv["W"], dv["ids"], 0.7, b.eps)
     dy, dW = tim.logprob_backward(dv["hid"], dv["gam"], dv["W"], dv["ids"], lse,
                                   torch.from_numpy(g).cuda(), 0.7, b.eps)
-    rows = sample_rows(b.T, 12, must=[b.meta["prefix"] + 3])
+    rows = tile_rows(b.T, raster_group_tiles(b.head.d), must=[b.meta["prefix"] + 3])
     orc = oracle.oracle_logprob_backward(b.hidden_train[rows], b.head.gamma, b.head.W,
                                          b.token_ids[rows], 0.7, b.eps, g[rows], dW_rows=[0])
     dyr = dy.cpu().numpy()[rows].astype(np.float64)
