@@ -54,28 +54,38 @@ unsigned long long g_ctx_id[kMaxDevices] = {};
 using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Unique ID of the current CUDA context (0 when none is current yet).
+// Unique ID of the current CUDA context (0 when none is current yet).  Drivers
+// without cuCtxGetId get the context handle as the key instead (a new context may
+// reuse a freed handle's value there, so the ID is preferred).
 bool current_context_id(unsigned long long* id) {
   static CtxGetCurrentFn get_current = nullptr;
   static CtxGetIdFn get_id = nullptr;
-  if (get_current == nullptr || get_id == nullptr) {  // called under g_addr_mutex
+  static bool looked_up = false;
+  if (!looked_up) {  // called under g_addr_mutex
     void* p = nullptr;
     void* q = nullptr;
     cudaDriverEntryPointQueryResult r1, r2;
     if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &r1) !=
             cudaSuccess ||
-        r1 != cudaDriverEntryPointSuccess ||
-        cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) !=
-            cudaSuccess ||
-        r2 != cudaDriverEntryPointSuccess)
+        r1 != cudaDriverEntryPointSuccess)
       return false;
     get_current = reinterpret_cast<CtxGetCurrentFn>(p);
-    get_id = reinterpret_cast<CtxGetIdFn>(q);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) ==
+            cudaSuccess &&
+        r2 == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(q);
+    cudaGetLastError();
+    looked_up = true;
   }
   CUcontext ctx = nullptr;
   if (get_current(&ctx) != CUDA_SUCCESS) return false;
   *id = 0;
-  return ctx == nullptr || get_id(ctx, id) == CUDA_SUCCESS;
+  if (ctx == nullptr) return true;
+  if (get_id == nullptr) {
+    *id = static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(ctx));
+    return true;
+  }
+  return get_id(ctx, id) == CUDA_SUCCESS;
 }
 
 // Device address of the scratch array in the current context, with the set-up
