@@ -653,7 +653,7 @@ def main():
     for k in range(3):
         e2e_step(k)
     torch.cuda.synchronize()
-    e2e_steps = max(3, args.steps // 2)
+    e2e_steps = max(3, args.steps)
     barrier(dist, dev)
     start.record(stream)
     copy_stream.wait_event(start)
