@@ -931,6 +931,40 @@ def pin_fp8_admissible_margin_zero():
         assert alts[0]["logprob"] == out["logprob"][t] and alts[0]["top1"] == out["top1"][t]
 
 
+def pin_fp8_admissible_scale_flip():
+    """A row whose maximum lies on a bf16 rounding midpoint (7.015625, between 7.0 and
+    7.03125) whose two neighbours give different row scales (2^-6 and 2^-5): the codes of
+    the maximum agree, but a tiny element (1.8358e-5, in e4m3's subnormal range) becomes
+    2^-15 under one scale and 0 under the other.  The admissible set must hold both
+    results, computed here by hand: logits (7 + 64 * 2^-15, 7, 0, 0) and (7, 7, 0, 0)."""
+    d = 64
+    h = np.zeros(d)
+    h[0], h[2] = 7.0, 2.0 ** -16
+    g = np.ones(d)
+    g[2] = 1.203125
+    eps = 1.0 / (7.015625 / 7.0) ** 2 - float(np.mean(h * h))     # rstd = 7.015625 / 7
+    W = np.zeros((4, d))
+    W[0, 0], W[0, 2], W[1, 0] = 1.0, 64.0, 1.0
+    bits = lambda a: np.array([[trunc_bf16_bits(v) for v in r] for r in np.atleast_2d(a)],
+                              dtype=np.uint16)
+    hb, gb, Wb = bits(h), bits(g)[0], bits(W)
+    assert np.array_equal(oracle.widen_bf16(hb)[0], h) and np.array_equal(oracle.widen_bf16(Wb), W)
+    adm = oracle.oracle_logprob_fp8_admissible(hb, gb, Wb, np.array([0], np.int32), 1.0, eps,
+                                               1e-6)[0]
+    assert adm is not None and len(adm) == 2, adm
+    want = []
+    for z0 in (7.0 + 64 * 2.0 ** -15, 7.0):
+        z = np.array([z0, 7.0, 0.0, 0.0])
+        lse = math.log(sum(math.exp(v) for v in z))
+        want.append((z0 - lse, lse))
+    got = sorted((a["logprob"], a["lse"]) for a in adm)
+    for (lp_g, lse_g), (lp_w, lse_w) in zip(got, sorted(want)):
+        assert abs(lp_g - lp_w) < 1e-12 and abs(lse_g - lse_w) < 1e-12, (got, want)
+    # the oracle's own result is one of them (the tie rounds to the even 7.0: scale 2^-6)
+    base = oracle.oracle_logprob_fp8(hb, gb, Wb, np.array([0], np.int32), 1.0, eps)
+    assert abs(base["lse"][0] - want[0][1]) < 1e-12
+
+
 def _rmsnorm_fp32_generic(h, g, eps, order):
     """An fp32 RMSNorm in a generic summation order ('fwd': one running sum in element
     order, 'rev': reversed, 'pair': numpy's float32 pairwise sum), every other step in fp32

@@ -228,6 +228,17 @@ def _choices_one_sided(x, margin):
 _orig_row_alternatives = of8._row_alternatives
 
 
+def _alternatives_codes_only(x_row, margin):
+    # keep only elements whose codes differ under the base scale (ignores the row scale)
+    base = ol.round_to_bf16(x_row)
+    lo, hi = of8.bf16_choices(x_row, margin)
+    amb = np.flatnonzero(lo != hi)
+    other = np.where(lo[amb] == base[amb], hi[amb], lo[amb])
+    s = of8.fp8_scale(float(np.max(np.abs(base))))
+    keep = of8.e4m3_round(base[amb] / s) != of8.e4m3_round(other / s)
+    return base, amb[keep], other[keep]
+
+
 def _alternatives_wrong_other(x_row, margin):
     base, idx, other = _orig_row_alternatives(x_row, margin)
     return base, idx, 2 * base[idx] - other                 # mirrored: not a rounding of x
@@ -331,6 +342,8 @@ MUTATIONS = [
      ["pin_bf16_choices_brute"]),
     ("admissible alternative is not a rounding", of8, "_row_alternatives",
      _alternatives_wrong_other, ["pin_fp8_admissible_covers_fp32_evaluations"]),
+    ("admissible set ignores a flip of the row scale", of8, "_row_alternatives",
+     _alternatives_codes_only, ["pin_fp8_admissible_scale_flip"]),
     ("FP32 head rounds y to bf16", of32, "rmsnorm_unrounded", _rms_unrounded_but_rounded,
      ["pin_fp32_head_mpmath", "pin_fp32_head_torch"]),
     ("FP32 head eps outside the sqrt", of32, "rmsnorm_unrounded", _rms_unrounded_eps_outside,
