@@ -196,7 +196,7 @@ tim_status tim_lse_finalize(const int32_t *token_ids, int64_t T, int32_t d, int3
  *                0 <= seq_offsets[j] <= seq_offsets[j+1] <= T.
  *   n_seq        >= 1.
  *   mask         uint8 [T], values 0 or 1.
- *   T            >= 1.
+ *   T            1 <= T <= 2^31 - 1.
  *   tis_cap      finite and > 0.
  *   out_stats    tim_seq_stats [n_seq] (device memory).
  *   out_tis_w    float32 [T] or NULL.

@@ -367,7 +367,7 @@ tim_status tim_compare(const float* lp_gen, const float* lp_replay, const float*
       !aligned(seq_offsets, 8) || !aligned(out_stats, 8) ||
       (out_tis_w != nullptr && !aligned(out_tis_w, 4)))
     return TIM_ERR_INVALID_ARG;
-  if (T < 1 || n_seq < 1) return TIM_ERR_SHAPE;
+  if (T < 1 || T > INT32_MAX || n_seq < 1) return TIM_ERR_SHAPE;
   if (!(std::isfinite(tis_cap) && tis_cap > 0.f)) return TIM_ERR_INVALID_ARG;
   tim_status s = check_workspace(workspace, workspace_bytes, tim_compare_workspace_size(T, n_seq));
   if (s != TIM_OK) return s;
@@ -771,7 +771,7 @@ tim_status tim_compare_diag(const float* lp_gen, const float* lp_replay, const f
       (top1_replay != nullptr && !aligned(top1_replay, 4)) ||
       (top1_train != nullptr && !aligned(top1_train, 4)))
     return TIM_ERR_INVALID_ARG;
-  if (T < 1 || n_seq < 1) return TIM_ERR_SHAPE;
+  if (T < 1 || T > INT32_MAX || n_seq < 1) return TIM_ERR_SHAPE;
   if (!(std::isfinite(tis_cap) && tis_cap > 0.f)) return TIM_ERR_INVALID_ARG;
   if (!(std::isfinite(mis_lo) && std::isfinite(mis_hi) && mis_lo > 0.f && mis_lo <= mis_hi))
     return TIM_ERR_INVALID_ARG;

@@ -92,6 +92,12 @@ def test_argument_errors_need_no_gpu(lib):
                            None) == STATUS["TIM_ERR_SHAPE"]
     assert lib.tim_compare(fake, None, fake, fake, 1, fake, 8, 2.0, fake, None, ws, 4096,
                            None) == STATUS["TIM_ERR_INVALID_ARG"]
+    # more than 2^31 - 1 tokens: rejected (per-sequence token counts are 32-bit inside)
+    big = 1 << 31
+    assert lib.tim_compare(fake, fake, fake, fake, 1, fake, big, 2.0, fake, None, ws, 1 << 62,
+                           None) == STATUS["TIM_ERR_SHAPE"]
+    assert lib.tim_compare_diag(fake, fake, fake, None, None, None, fake, 1, fake, big, 2.0, 0.5,
+                                2.0, fake, ws, 1 << 62, None) == STATUS["TIM_ERR_SHAPE"]
     assert lib.tim_workspace_init(None, 0, None) == STATUS["TIM_ERR_WORKSPACE"]
 
 
