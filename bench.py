@@ -717,6 +717,23 @@ def main():
         torch.cuda.synchronize()
         dws.check("diag")
         extras["compare_diag_us"] = round(1e3 * e_a.elapsed_time(e_b) / 10, 2)
+        # the whole batch as one sequence: 24576 active tokens, more than a quantile CTA
+        # holds in shared memory, so the quantiles take the streamed select
+        offs1 = torch.tensor([0, T], dtype=torch.int64, device=dev)
+        dws1 = tim.Workspace(int(tim.lib().tim_compare_diag_workspace_size(T, 1)), dev)
+        dout1 = torch.empty(tim.SEQ_DIAG_DTYPE.itemsize, dtype=torch.uint8, device=dev)
+        tim.compare_diag(A[0], Bo[0], C[0], offs1, mask, b.tis_cap, 0.5, 2.0, top1=tops, out=dout1,
+                         workspace=dws1, check=False, to_host=False)
+        e_a.record(stream)
+        for _ in range(10):
+            tim.compare_diag(A[0], Bo[0], C[0], offs1, mask, b.tis_cap, 0.5, 2.0, top1=tops,
+                             out=dout1, workspace=dws1, check=False, to_host=False)
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        dws1.check("diag one sequence")
+        extras["compare_diag_one_sequence_us"] = dict(
+            us=round(1e3 * e_a.elapsed_time(e_b) / 10, 2), active_tokens=int(b.mask.sum()),
+            note="quantiles by the streamed select (keys recomputed from the scores each pass)")
         # FP8 (e4m3) head: W quantised once per weight version (untimed), then whole calls
         W8, sW8 = tim.quantize_fp8_rows(W)
         fws = tim.Workspace(int(tim.lib().tim_logprob_fp8_workspace_size(T, d, V)), dev)
