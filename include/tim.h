@@ -495,7 +495,10 @@ tim_status tim_logprob_merge_shards(const void *recs, const float *tgts, const i
  * Arguments: those of tim_compare, plus top1_gen / top1_replay / top1_train
  * (int32 [T] device arrays or NULL), mis_lo / mis_hi (finite,
  * 0 < mis_lo <= mis_hi), out_diag (tim_seq_diag [n_seq], device memory).
- * The workspace holds only the status word (tim_compare_diag_workspace_size).
+ * The workspace (tim_compare_diag_workspace_size(T, n_seq) bytes, zero-
+ * initialised once) holds the status word, the per-sequence part bookkeeping
+ * and, for sequences with more than 16384 active tokens, the quantile keys past
+ * the first 16384 (24 bytes per token of T).
  * ------------------------------------------------------------------------ */
 
 typedef struct tim_seq_diag {

@@ -29,8 +29,9 @@
 // the values, so selection is integer work) and find the order statistics the
 // interpolation needs by a radix select; they are exact, and the interpolation
 // is the formula above.  A sequence with more active tokens than the shared
-// key buffer holds (kQuantMax) runs the same select with its keys recomputed
-// from the score arrays on every pass instead of read from shared memory.
+// key buffer holds (kQuantMax) keeps the keys past the first kQuantMax in a
+// workspace region (8 bytes per token and pair) and runs the same select over
+// both.
 #include <cmath>
 #include <cstring>
 
@@ -341,37 +342,32 @@ __device__ void diag_part(int b, unsigned long long* __restrict__ stage,
 }
 
 // The active keys of one pair of one sequence, visited by every thread of a
-// CTA with a uniform trip count: read from the shared copy when the sequence's
-// keys fit in it, else recomputed from the score arrays (L2-resident after the
-// first pass) on every visit.  Visit order is irrelevant to the selection.
+// CTA with a uniform trip count: the first kQuantMax from shared memory, the
+// rest (sequences longer than that) from the workspace region the gather wrote
+// them to (read through L2: this CTA wrote them during this launch).  Visit
+// order is irrelevant to the selection.
 struct KeySource {
   const unsigned long long* keys;
-  const float* L;
-  const float* R;
-  const uint8_t* mask;
-  int64_t s, e;
+  const unsigned long long* spill;
   int n;
-  bool stream;
 
   template <class F>
   __device__ __forceinline__ void visit(int tid, F&& f) const {
-    if (!stream) {
-      const int n_round = (n + kDiagThreads - 1) / kDiagThreads * kDiagThreads;
+    const int n_round = (n + kDiagThreads - 1) / kDiagThreads * kDiagThreads;
+    const int n_smem = n < kQuantMax ? n : kQuantMax;
 #pragma unroll 4
-      for (int i = tid; i < n_round; i += kDiagThreads)
-        if (i < n) f(keys[i]);
-    } else {
-      for (int64_t b = s; b < e; b += kDiagThreads) {
-        const int64_t t = b + tid;
-        if (t < e && __ldg(mask + t) == 1) f(abs_diff_key(__ldg(L + t), __ldg(R + t)));
-      }
+    for (int i = tid; i < n_round; i += kDiagThreads) {
+      if (i < n_smem) f(keys[i]);
+      else if (i < n) f(__ldcg(spill + (i - kQuantMax)));
     }
   }
 };
 
 // Quantiles of pair p of sequence j (one CTA; keys: kQuantMax 64-bit slots in
-// shared memory, used when the sequence's active tokens fit).
+// shared memory; spill: the workspace region for pair p's keys past those,
+// indexed from the sequence's first token).
 __device__ void diag_quantiles(int j, int p, unsigned long long* __restrict__ keys,
+                               unsigned long long* __restrict__ spill,
                                const float* __restrict__ A, const float* __restrict__ B,
                                const float* __restrict__ C, const int64_t* __restrict__ offs,
                                const uint8_t* __restrict__ mask, int64_t T,
@@ -416,6 +412,7 @@ __device__ void diag_quantiles(int j, int p, unsigned long long* __restrict__ ke
       k_and &= k;
       const int slot = slot0 + __popc(bal & ((1u << lane) - 1u));
       if (slot < kQuantMax) keys[slot] = k;
+      else spill[s + (slot - kQuantMax)] = k;  // slot < e - s: inside the sequence's range
     }
   }
   k_or = warp_or_u64(k_or);
@@ -434,7 +431,7 @@ __device__ void diag_quantiles(int j, int p, unsigned long long* __restrict__ ke
     }
     return;
   }
-  const KeySource src{keys, L, R, mask, s, e, n, n > kQuantMax};
+  const KeySource src{keys, spill + s, n};
   // The three order statistics by an MSD radix select on the keys' bit
   // patterns.  Target q keeps the key prefix fixed so far (bits [fixed_from,
   // 64)), the rank it still seeks among the keys with that prefix (its
@@ -618,11 +615,13 @@ __global__ void __launch_bounds__(kDiagThreads)
                     const int64_t* __restrict__ offs, const uint8_t* __restrict__ mask, int64_t T,
                     int n_seq, const int* __restrict__ base, double ln_lo, double ln_hi,
                     double cap, double ln_cap, DiagPart* __restrict__ parts,
-                    int* __restrict__ cnt_seq, tim_seq_diag* __restrict__ out, int* status) {
+                    int* __restrict__ cnt_seq, unsigned long long* __restrict__ spill,
+                    tim_seq_diag* __restrict__ out, int* status) {
   extern __shared__ unsigned long long keys[];
   const int b = static_cast<int>(blockIdx.x);
   if (b < 3 * n_seq) {
-    diag_quantiles(b / 3, b % 3, keys, A, B, C, offs, mask, T, out);
+    diag_quantiles(b / 3, b % 3, keys, spill + static_cast<int64_t>(b % 3) * T, A, B, C, offs,
+                   mask, T, out);
   } else {
     pdl_wait();  // the partition kernel's bases and zeroed counters
     diag_part(b - 3 * n_seq, keys, A, B, C, tA, tB, tC, offs, mask, T, n_seq, base, ln_lo, ln_hi, cap,
@@ -631,7 +630,8 @@ __global__ void __launch_bounds__(kDiagThreads)
 }
 
 // Diagnostics workspace: status | part bases int32 [S + 1] | per-sequence part
-// counters int32 [S] (zeroed by the partition kernel of each call) | parts.
+// counters int32 [S] (zeroed by the partition kernel of each call) | parts |
+// quantile keys past the shared-memory ones, uint64 [3][T] (pair p, token t).
 size_t diag_base_offset() { return 1024; }
 size_t diag_counter_offset(int n_seq) {
   return align_up(diag_base_offset() + static_cast<size_t>(n_seq + 1) * 4, 256);
@@ -639,10 +639,13 @@ size_t diag_counter_offset(int n_seq) {
 size_t diag_parts_offset(int n_seq) {
   return align_up(diag_counter_offset(n_seq) + static_cast<size_t>(n_seq) * 4, 1024);
 }
-size_t diag_workspace_bytes(int64_t T, int n_seq) {
+size_t diag_spill_offset(int64_t T, int n_seq) {
   return align_up(diag_parts_offset(n_seq) +
                       static_cast<size_t>(seq_parts_bound(T, n_seq)) * sizeof(DiagPart),
                   1024);
+}
+size_t diag_workspace_bytes(int64_t T, int n_seq) {
+  return align_up(diag_spill_offset(T, n_seq) + 3 * static_cast<size_t>(T) * 8, 1024);
 }
 
 cudaError_t launch_seg_diag(const float* A, const float* B, const float* C, const int32_t* tA,
@@ -657,6 +660,8 @@ cudaError_t launch_seg_diag(const float* A, const float* B, const float* C, cons
       reinterpret_cast<DiagPart*>(static_cast<uint8_t*>(workspace) + diag_parts_offset(n_seq));
   int* cnt_seq =
       reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + diag_counter_offset(n_seq));
+  unsigned long long* spill = reinterpret_cast<unsigned long long*>(
+      static_cast<uint8_t*>(workspace) + diag_spill_offset(T, n_seq));
   cudaError_t err = launch_seq_partition(offs, n_seq, T, base, cnt_seq, stream);
   if (err != cudaSuccess) return err;
   err = cudaFuncSetAttribute(seg_diag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -676,7 +681,7 @@ cudaError_t launch_seg_diag(const float* A, const float* B, const float* C, cons
   return cudaLaunchKernelEx(&cfg, seg_diag_kernel, A, B, C, tA, tB, tC, offs, mask, T, n_seq,
                             static_cast<const int*>(base), std::log(static_cast<double>(mis_lo)),
                             std::log(static_cast<double>(mis_hi)), cap, std::log(cap), parts,
-                            cnt_seq, out, status);
+                            cnt_seq, spill, out, status);
 }
 
 }  // namespace tim
