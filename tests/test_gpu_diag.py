@@ -115,13 +115,13 @@ def test_diag_parity(tim, T, seed):
 
 
 # active tokens a quantile CTA holds in shared memory; longer sequences take the
-# streamed select (keys recomputed from the scores on every pass)
+# select over the shared-memory keys plus the rest kept in the workspace
 SHARED_KEYS = 16384
 
 
 def test_diag_without_top1_and_long_sequence(tim):
     """A sequence just past the shared-memory key capacity (16389 active tokens) next to a
-    short one: exact quantiles through the streamed select, no flag."""
+    short one: exact quantiles with the keys past the shared-memory ones in the workspace, no flag."""
     n = SHARED_KEYS + 5
     A, B, C, _, _, _ = make_case(n + 100, 7)
     offs = np.array([0, 100, n + 100], dtype=np.int64)
@@ -200,7 +200,7 @@ def test_diag_quantiles_exact_on_ties_tiny_and_maximal_sequences(tim):
     oracle's sorted-array formula bit for bit, across tie groups that straddle the
     interpolation ranks, all-equal sequences, 1-3 tokens, widely spread magnitudes,
     sequences at and past the shared-memory key capacity, and long sequences (65573 and
-    about 68000 active tokens) through the streamed select."""
+    about 68000 active tokens) with keys kept in the workspace."""
     g = np.random.default_rng(31)
     parts = []
 
@@ -245,7 +245,7 @@ def test_diag_quantiles_exact_on_ties_tiny_and_maximal_sequences(tim):
 def test_diag_and_compare_one_sequence_past_the_part_cap(tim):
     """A 300000-token sequence: its part count is capped at 256, so every part holds
     more than 512 tokens (each thread loops, all warps reduce); its quantiles (about
-    270000 active tokens) come from the streamed select, exact."""
+    270000 active tokens) come from the select over shared-memory and workspace keys, exact."""
     from parity import assert_compare_parity
     T = 300000
     A, B, C, _, _, tops = make_case(T, 41)
