@@ -933,35 +933,56 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
 // Schedule of a scoring-type launch (scoring records, or the top-4 records of the
 // processed score): one W pass per batch and a light epilogue.
 //
-// Batches of an even number of row tiles that fit one raster group (2 to 48 row
-// tiles) run as row-tile pairs (kPrecBf16x2): each work item is two row tiles
-// against one W tile, so a W tile is streamed by half as many CTAs, and every row
-// still sees the MMA sequence and epilogue of the one-tile form.  Odd counts run
-// one row tile per item (a lone last tile per W tile would hand some CTAs half the
-// work of others).  When several work items share a W tile inside one raster
-// group, the CTA on the tile's first item prefetches the tile's W k-blocks into
-// L2 kLeaderPrefetch k-blocks ahead of its own loads, so that the other CTAs on
-// the tile, which request the same k-blocks, are not held to one ring's depth of
-// DRAM requests in flight.  Batches of more than one raster group keep one row
-// tile per item and no prefetch.
-// Measured on GB300 (d = 4096, V = 151936, whole calls; the previous schedule
-// and this one, with the bf16 epilogue's overlapped TMEM loads, built side by
-// side and timed in one process, alternating in random order over ten rounds,
-// bitwise equal outputs): 448 rows 411 -> 395 us, 512 rows 429 -> 416, 513 rows
-// 533 -> 516, 640 rows 546 -> 531, 768 rows 613 -> 602, 1024 rows 794 -> 779,
-// 2048 rows 1523 -> 1496; 128, 256, 384, 1408 and 4096 rows within 0.3%; 6144
-// rows +0.5% and 32768 rows +0.7% (noise level).  Prefetching 8 k-blocks ahead
-// was no better than 4; prefetching where each CTA streams its own W tile
-// (256 rows) or in batches of several raster groups (32768 rows: +10%) was
-// slower.
+// Row-tile pairs (kPrecBf16x2): each work item is two row tiles against one W
+// tile, so a W tile is streamed by half as many CTAs and every W k-slice in shared
+// memory feeds two row tiles (a third fewer L2 reads per MMA), while every row
+// still sees the MMA sequence and epilogue of the one-tile form.  A pair holds
+// all of TMEM, so its epilogue is exposed once per item; that fixed cost weighs
+// against MMAs that last 2 d / 16 K steps, so the pairs pay off at d >= 4096 for
+// every even tile count, and below that only for batches of 2-4 row tiles (the
+// bandwidth-bound knee).  Odd counts run one row tile per item (a lone last tile
+// per W tile would hand some CTAs half the work of others).  Beyond one raster
+// group the pairs' group at d = 4096 is 20 pairs (40 row tiles): the pairs keep
+// twice as many W tiles in flight beside the group's y panel, and a 48-tile
+// group let the panel spill (11.2 GB of DRAM reads per 32768-row launch against
+// 9.3 GB with 40 tiles).  When several work items share a W tile inside one
+// raster group (batches of up to one group), the CTA on the tile's first item
+// prefetches the tile's W k-blocks into L2 kLeaderPrefetch k-blocks ahead of its
+// own loads, so that the other CTAs on the tile, which request the same
+// k-blocks, are not held to one ring's depth of DRAM requests in flight.  The
+// top-4 pass keeps one row tile per item beyond one raster group (its heavier
+// epilogue is exposed once per pair item).
+// Measured on GB300 (V = 151936, whole calls; builds or variants side by side in
+// one process, alternating in random order, bitwise equal outputs):
+//  * d = 4096 within one raster group, against the previous schedule (pairs for
+//    even counts and for odd counts whose pair count is coprime with the CTA
+//    count, no prefetch) and with the epilogue's overlapped TMEM loads: 448 rows
+//    411 -> 395 us, 512 rows 429 -> 416, 513 rows 533 -> 516, 640 rows 546 ->
+//    531, 768 rows 613 -> 602, 1024 rows 794 -> 779, 2048 rows 1523 -> 1496; 128,
+//    256, 384, 1408 and 4096 rows within 0.3%.  Prefetching 8 k-blocks ahead was
+//    no better than 4; prefetching where each CTA streams its own W tile (64-256
+//    rows: +5-10%) or in batches of several raster groups (32768 rows: +10%) was
+//    slower;
+//  * d = 4096 beyond one raster group, one tile per item -> pairs in groups of
+//    24 / 20 / 16 pairs (20 back-to-back calls per sample, 8 rounds): 32768 rows
+//    23575 -> 23377 / 23061 / 23226 us (28 pairs: 23987), 16384 rows 11766 ->
+//    11571 / 11538 us;
+//  * d = 5120: one tile per item -> pairs, 256-4096 rows 311 -> 285, 574 -> 506,
+//    1107 -> 950, 2061 -> 1927, 3854 -> 3786 us; 131072 rows 118.6 -> 115.9 ms
+//    (groups of 18 pairs);
+//  * d = 2048: one tile per item -> pairs, 256 rows 130 -> 130 us, 512 rows 231
+//    -> 224, 768 rows 309 -> 329, 1024 rows 440 -> 429, 2048 rows 776 -> 839,
+//    4096 rows 1456 -> 1653, 6144 rows 2254 -> 2373, 8192 rows 2917 -> 3041-3092.
 constexpr int kLeaderPrefetch = 4;
 
-static bool plan_scoring_schedule(GemmArgs& a) {
+static bool plan_scoring_schedule(GemmArgs& a, bool pairs_beyond_one_group) {
   const bool one_group = a.num_m <= a.group_m;
-  const bool pairs = one_group && a.num_m >= 2 && a.num_m % 2 == 0;
+  const bool long_k = a.d >= 4096;
+  const bool pairs = a.num_m >= 2 && a.num_m % 2 == 0 &&
+                     (long_k ? (one_group || pairs_beyond_one_group) : a.num_m <= 4);
   if (pairs) {
     a.num_m /= 2;  // work items along M: row-tile pairs
-    a.group_m = (a.group_m + 1) / 2;
+    a.group_m = (!one_group && a.d <= 4096) ? 20 : (a.group_m + 1) / 2;
     a.num_tiles = static_cast<int64_t>(a.num_m) * a.num_n;
   }
   a.w_prefetch = (one_group && a.num_m >= 2) ? kLeaderPrefetch : 0;
@@ -985,7 +1006,7 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
   // (3 ms at 32768 rows), so larger batches are launched in stream order.  The
   // arithmetic is identical either way.
   const bool programmatic = a.num_m <= a.group_m;
-  if (plan_scoring_schedule(a))
+  if (plan_scoring_schedule(a, true))
     return launch_gemm<0, kPrecBf16x2>(map_y, map_w, map_y, map_w, a, stream, num_sms,
                                        programmatic);
   return launch_gemm<0, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, programmatic);
@@ -1065,7 +1086,7 @@ cudaError_t launch_lmhead_top4(const void* y, const void* W, const int32_t* ids,
   cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, 0, 1.0f, status);
   if (e != cudaSuccess) return e;
   a.top4 = top4;
-  if (plan_scoring_schedule(a))  // the scoring GEMM's schedule
+  if (plan_scoring_schedule(a, false))  // the scoring GEMM's schedule up to one raster group
     return launch_gemm<4, kPrecBf16x2>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
   return launch_gemm<4, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }

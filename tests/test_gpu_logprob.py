@@ -41,7 +41,8 @@ SHAPES = [
     (512, 256, 3001, 0.8),
     (513, 320, 4099, 0.9),
     (640, 64, 151936, 0.9),   # five row tiles, one per item, the leader prefetching W
-    (1024, 64, 151936, 0.9),  # eight row tiles as four pairs per W tile, with the prefetch
+    (1024, 4096, 20000, 0.9), # eight row tiles as four pairs per W tile, with the prefetch
+    (1024, 64, 151936, 0.9),  # the same at d < 4096: one row tile per item, with the prefetch
     (256, 5120, 3001, 0.7),   # row-tile pairs at the long-rollout hidden size
 ]
 

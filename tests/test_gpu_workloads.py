@@ -116,8 +116,8 @@ def test_batch_invariance_sweep_8b_head(tim):
     the GEMM: one row tile (M <= 128); a row-tile pair per W tile (200, 256); pairs
     with several items per W tile and the leader's L2 prefetch (512, 768, 4096, and
     6144 = the 48-tile raster group); odd tile counts, one row tile per item with the
-    prefetch (384, 513, 1152); and batches of several raster groups (6145, 16384).
-    Every target keeps its bits."""
+    prefetch (384, 513, 1152); and batches of several raster groups, as pairs (16384)
+    and one row tile per item (6145, 49 tiles).  Every target keeps its bits."""
     import torch
     plan = synth.make_sweep(Ms=(1, 7, 64, 200, 256, 384, 512, 513, 768, 1152, 4096, 6144, 6145,
                                 16384))
