@@ -930,8 +930,7 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
   return cudaSuccess;
 }
 
-// Schedule of a scoring-type launch (scoring records, or the top-4 records of the
-// processed score): one W pass per batch and a light epilogue.
+// Schedule of the scoring launch: one W pass per batch and a light epilogue.
 //
 // Row-tile pairs (kPrecBf16x2): each work item is two row tiles against one W
 // tile, so a W tile is streamed by half as many CTAs and every W k-slice in shared
@@ -949,9 +948,7 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
 // raster group (batches of up to one group), the CTA on the tile's first item
 // prefetches the tile's W k-blocks into L2 kLeaderPrefetch k-blocks ahead of its
 // own loads, so that the other CTAs on the tile, which request the same
-// k-blocks, are not held to one ring's depth of DRAM requests in flight.  The
-// top-4 pass keeps one row tile per item beyond one raster group (its heavier
-// epilogue is exposed once per pair item).
+// k-blocks, are not held to one ring's depth of DRAM requests in flight.
 // Measured on GB300 (V = 151936, whole calls; builds or variants side by side in
 // one process, alternating in random order, bitwise equal outputs):
 //  * d = 4096 within one raster group, against the previous schedule (pairs for
@@ -975,11 +972,10 @@ static cudaError_t make_args(GemmArgs& a, CUtensorMap& map_y, CUtensorMap& map_w
 //    4096 rows 1456 -> 1653, 6144 rows 2254 -> 2373, 8192 rows 2917 -> 3041-3092.
 constexpr int kLeaderPrefetch = 4;
 
-static bool plan_scoring_schedule(GemmArgs& a, bool pairs_beyond_one_group) {
+static bool plan_scoring_schedule(GemmArgs& a) {
   const bool one_group = a.num_m <= a.group_m;
   const bool long_k = a.d >= 4096;
-  const bool pairs = a.num_m >= 2 && a.num_m % 2 == 0 &&
-                     (long_k ? (one_group || pairs_beyond_one_group) : a.num_m <= 4);
+  const bool pairs = a.num_m >= 2 && a.num_m % 2 == 0 && (long_k || a.num_m <= 4);
   if (pairs) {
     a.num_m /= 2;  // work items along M: row-tile pairs
     a.group_m = (!one_group && a.d <= 4096) ? 20 : (a.group_m + 1) / 2;
@@ -1006,7 +1002,7 @@ cudaError_t launch_lmhead_lse_shard(const void* y, const void* W, const int32_t*
   // (3 ms at 32768 rows), so larger batches are launched in stream order.  The
   // arithmetic is identical either way.
   const bool programmatic = a.num_m <= a.group_m;
-  if (plan_scoring_schedule(a, true))
+  if (plan_scoring_schedule(a))
     return launch_gemm<0, kPrecBf16x2>(map_y, map_w, map_y, map_w, a, stream, num_sms,
                                        programmatic);
   return launch_gemm<0, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, programmatic);
@@ -1086,8 +1082,13 @@ cudaError_t launch_lmhead_top4(const void* y, const void* W, const int32_t* ids,
   cudaError_t e = make_args(a, map_y, map_w, y, W, ids, T, d, V, 0, 1.0f, status);
   if (e != cudaSuccess) return e;
   a.top4 = top4;
-  if (plan_scoring_schedule(a, false))  // the scoring GEMM's schedule up to one raster group
-    return launch_gemm<4, kPrecBf16x2>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
+  // One row tile per item at every size: the top-4 epilogue (an insertion per
+  // logit) is heavy enough that a row-tile pair's exposed epilogue costs more than
+  // the shared W saves (GB300, processed score k = 50, p = 0.95, d = 4096, same-
+  // process A/B, bitwise equal outputs: 256-32768 rows 5-25% slower with pairs,
+  // e.g. 4096 rows 3.16 -> 3.94 ms).  The leader's L2 prefetch of W is kept for
+  // batches within one raster group, as in the scoring launch.
+  a.w_prefetch = (a.num_m <= a.group_m && a.num_m >= 2) ? kLeaderPrefetch : 0;
   return launch_gemm<4, kPrecBf16>(map_y, map_w, map_y, map_w, a, stream, num_sms, false);
 }
 

@@ -73,9 +73,9 @@ def targets(b, tau):
 @pytest.mark.parametrize("T,d,V,tau,k,p", [
     (50, 128, 1000, 1.0, 1, 1.0), (50, 128, 1000, 1.0, 2, 1.0), (50, 128, 1000, 0.7, 17, 0.9),
     (33, 192, 2048, 1.3, 64, 0.5), (40, 256, 20000, 0.8, 40, 0.95), (9, 64, 5000, 1.0, 5, 1.0),
-    (256, 128, 3000, 0.9, 10, 0.9),   # two row tiles: the top-4 pass runs as a row-tile pair
-    (384, 128, 3000, 0.9, 10, 0.9),   # three row tiles, one per item, the leader prefetching W
-    (512, 128, 3000, 0.9, 10, 0.9),   # four row tiles: two pairs per W tile, with the prefetch
+    (256, 128, 3000, 0.9, 10, 0.9),   # two row tiles per W tile, the leader prefetching W
+    (384, 128, 3000, 0.9, 10, 0.9),   # three row tiles
+    (512, 128, 3000, 0.9, 10, 0.9),   # four row tiles
 ])
 def test_processed_parity(tim, T, d, V, tau, k, p):
     b = synth.make_custom(T=T, d=d, V=V, temperature=tau, tag=f"pr{T}_{d}_{V}")
@@ -112,7 +112,7 @@ def test_processed_full_head_and_batch_invariance(tim):
             hid[7:40].contiguous(), gam, W, cuda_tensor(ids[7:40]), 0.7, b.eps, k, p)]
         for x, y in zip(part, full):
             assert x.tobytes() == y[7:40].tobytes()
-        # and inside a 256-row batch (two row tiles, scored as a row-tile pair)
+        # and inside a 256-row batch (two row tiles against each W tile)
         fill = synth.make_custom(T=160, d=4096, V=151936, tag="pr_fill")
         big_h = torch.cat([hid, bf16_cuda(fill.hidden_gen)])
         big_ids = cuda_tensor(np.concatenate([ids, fill.token_ids]).astype(np.int32))
