@@ -233,15 +233,13 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], int nval
     v[j] = __uint_as_float(r[j]);
     if (kPartial) v[j] = (j < nvalid) ? v[j] : -INFINITY;
   }
+  // chunk maximum; its first index is looked up only when it beats the row's best
+  // so far (the arg-max is then the first index of the largest logit, as a
+  // sequential scan gives; outputs bitwise equal to the scan with an index per
+  // logit, which took three instructions a logit instead of one)
   float cmax = v[0];
-  int cidx = 0;
 #pragma unroll
-  for (int j = 1; j < 32; ++j) {
-    if (v[j] > cmax) {
-      cmax = v[j];
-      cidx = j;
-    }
-  }
+  for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
   const float mnew = fmaxf(m2, cmax * k2);
   float cs = 0.f;
 #pragma unroll
@@ -249,6 +247,10 @@ __device__ __forceinline__ void epilogue_chunk(const uint32_t (&r)[32], int nval
   sum = sum * ex2_approx(m2 - mnew) + cs;
   m2 = mnew;
   if (cmax > bz) {
+    int cidx = 31;
+#pragma unroll
+    for (int j = 30; j >= 0; --j)
+      if (v[j] == cmax) cidx = j;
     bz = cmax;
     bi = col0 + cidx;
   }
