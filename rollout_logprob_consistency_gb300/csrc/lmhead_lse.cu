@@ -136,8 +136,8 @@ struct GemmArgs {
 //               one W tile (64 KiB, 3 stages), and every K step issues the same
 //               M=128 MMA once per row tile into its own accumulator.  Each row
 //               sees the identical MMA sequence of the one-tile form; only the
-//               number of CTAs that stream a W tile at once changes (scoring
-//               mode only, for batches of a few row tiles).
+//               number of CTAs that stream a W tile at once changes (the scoring
+//               mode, see plan_scoring_schedule, and the backward products).
 enum Prec : int { kPrecBf16 = 0, kPrecE4m3 = 1, kPrecTf32x3 = 2, kPrecBf16x2 = 3 };
 
 template <int kPrec>
